@@ -1,0 +1,453 @@
+#!/usr/bin/env python3
+"""Benchmark of the ReplaySSM decode path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mamba2_serving|mamba2_spec|gdn_serving|mamba2_bf16_read|mamba2_tiny]
+    python bench.py --mode profile --steps 3 --warmup 1      # a few calls, no timing (for ncu)
+
+A step is one decode step of one layer over the whole batch: one
+``rssm_mamba2_step`` call (the append, the output-only read of the checkpoint
+and window, the flush fused into every sequence's L-th step, the cursor
+advance). Inputs are resident in HBM before the timed region; the 1 GiB
+checkpoint streamed each step is larger than L2, so no flush is needed. The
+same steps also run through the in-house conventional kernel (read + write of
+the full state every step) for the speedup.
+
+Prints ONE JSON line (rank 0). Under torchrun every rank runs its own replica
+(sequences shard with no exchange: weak scaling), timing is the max over
+ranks, and value/tokens are whole-job figures.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Mamba2 ReplaySSM decode µs/step/layer & HBM GB/s at B=256,L=16 vs conventional"
+UNIT = "us/step/layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- plumbing
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mamba2_serving")
+    ap.add_argument("--mode", choices=["bench", "profile"], default="bench")
+    ap.add_argument("--out-dtype", choices=["bf16", "f32"], default="bf16")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU time budget of the oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")  # host-side coordination only: no data-path collective
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([float(v)], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([float(v)], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        load = [v for v in sm if smax and v >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_file, kernel_sources):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", profile_file)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != source_hash(kernel_sources):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+KERNEL_SOURCES = ["recurrent_state_decode_gb300/csrc/mamba2.cu", "recurrent_state_decode_gb300/csrc/common.cuh"]
+
+
+# ----------------------------------------------------------------------------- oracle (CPU baseline / reference arm)
+
+class OracleRunner:
+    """The oracle's conventional fp64 decode of a sample of `nseq` sequences of a
+    Mamba-2 workload, one decode step per call (inputs drawn beforehand, on the
+    GPU when there is one, and cycled)."""
+
+    def __init__(self, w, nseq, pool=32):
+        import torch
+
+        from oracle import sessions
+        from recurrent_state_decode_gb300 import inputs as I
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        self.w, self.nseq = w, nseq
+        seqs = list(range(nseq))
+        A, D = I.mamba2_params(w, dev)
+        h0 = I.to_f64(I.mamba2_checkpoint(w, dev)[seqs])
+        pre = {k: I.to_f64(v[seqs]) for k, v in I.mamba2_prefill(w, dev).items()}
+        starts, counts = (t[seqs].cpu().numpy() for t in I.initial_cursors(w, dev))
+        recs = [{k: I.to_f64(v[seqs]) for k, v in I.mamba2_step_inputs(w, t, dev).items()} for t in range(pool)]
+
+        def cycle():
+            t = 0
+            while True:
+                yield recs[t % pool]
+                t += 1
+
+        self.sess = sessions.mamba2_ar_session(h0, pre, starts, counts, cycle(), I.to_f64(A), I.to_f64(D),
+                                               w.buf_len)
+        next(self.sess)  # the prefill replay and the first step stay outside any timing
+
+    def step(self):
+        next(self.sess)
+
+    def describe(self, n, seconds):
+        return (f"oracle conventional fp64 decode (numpy, one thread) of {self.nseq} of {self.w.batch} sequences, "
+                f"{n} steps in {seconds:.1f} s, scaled to the full batch")
+
+
+def oracle_time_per_step(w, budget_s, nseq=4):
+    """µs per full-batch decode step of the oracle, from as many steps of an
+    `nseq`-sequence sample as fit in `budget_s` seconds."""
+    r = OracleRunner(w, nseq)
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s:
+        r.step()
+        n += 1
+    dt = time.perf_counter() - t0
+    return dt / n * (w.batch / nseq) * 1e6, r.describe(n, dt)
+
+
+def run_reference(args, dist):
+    """The reference arm: the oracle as it stands, on the host cores. Each bench
+    step is one oracle decode step of a one-sequence sample, scaled to the batch."""
+    if dist.rank != 0:
+        return None
+    from recurrent_state_decode_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    r = OracleRunner(w, 1)
+    for _ in range(args.warmup):
+        r.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r.step()
+    dt = time.perf_counter() - t0
+    value = dt / args.steps * w.batch * 1e6
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": r.describe(args.steps, dt)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def workload_config(w, args):
+    cfg = {"workload": w.name}
+    for k in ("batch", "nheads", "headdim", "dstate", "ngroups", "dk", "dv", "buf_len", "drafts"):
+        if hasattr(w, k):
+            cfg[k] = getattr(w, k)
+    cfg["state"] = "fp32 checkpoint" + (" + bf16 read copy" if getattr(w, "read_copy", False) else "")
+    cfg["io_dtype"] = "bf16 records, " + args.out_dtype + " outputs"
+    cfg["l2"] = "working set larger than L2: the full checkpoint is streamed every step"
+    return cfg
+
+
+# ----------------------------------------------------------------------------- GPU timing
+
+def time_calls(fn, n, stream):
+    """Run fn(i) n times on `stream` with an event after each call; returns
+    (total ms, per-call ms list)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(stream)
+    for i in range(n):
+        fn(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+    return ev[0].elapsed_time(ev[n]), per
+
+
+def bench_mamba2_ar(args, dist):
+    import torch
+
+    from recurrent_state_decode_gb300 import binding as bd
+    from recurrent_state_decode_gb300 import bytes_model as bm
+    from recurrent_state_decode_gb300 import inputs as I
+    from recurrent_state_decode_gb300.state import mamba2_from_workload
+
+    w = I.WORKLOADS[args.workload]
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    out = bd.RSSM_BF16 if args.out_dtype == "bf16" else bd.RSSM_F32
+    out_bytes = 2 if out == bd.RSSM_BF16 else 4
+    st, A, D, _, _, counts0 = mamba2_from_workload(w, dev, out)
+    W_, K = args.warmup, args.steps
+    recs = [I.mamba2_step_inputs(w, t, dev) for t in range(W_ + K)]
+    y = st.new_output()
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2  # step kernel + cursor advance
+
+    if args.mode == "profile":
+        for t in range(W_ + K):
+            st.step(recs[t], A, D, y)
+        torch.cuda.synchronize()
+        return None
+
+    # --- ReplaySSM step
+    for t in range(W_):
+        st.step(recs[t], A, D, y)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    total_ms, per = time_calls(lambda i: st.step(recs[W_ + i], A, D, y), K, stream)
+    clk = clocks.stop()
+    dist.barrier()
+    bd.check(int(st.status.item()), "device status")
+    c0 = counts0.cpu().tolist()
+    L = w.buf_len
+    alg_bytes = sum(bm.mamba2_step_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, L,
+                                         [(c + W_ + i) % L for c in c0], w.read_copy, out_bytes) for i in range(K))
+    us_step = dist.max(total_ms * 1e3 / K)
+    mean_call_ms = total_ms / K
+    achieved_gbs = (alg_bytes / K) / (mean_call_ms * 1e-3) / 1e9
+
+    # --- conventional comparator over the same steps
+    state = st.ckpt.clone()
+    yc = st.new_output()
+    desc = st.desc
+
+    def conv(i):
+        r = recs[W_ + i] if i >= 0 else recs[0]
+        bd.check(bd.rssm_mamba2_conventional_step(desc, state, r["x"], r["z"], r["B"], r["C"], r["dt"], A, D, yc))
+
+    for _ in range(W_):
+        conv(-1)
+    torch.cuda.synchronize()
+    dist.barrier()
+    conv_ms, _ = time_calls(conv, K, stream)
+    conv_us = dist.max(conv_ms * 1e3 / K)
+    conv_bytes = bm.mamba2_conventional_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.batch, out_bytes)
+    del state
+
+    # --- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_mamba2(st, A, D, w, dev, K, W_, y.dtype)
+        e2e["value"] = dist.max(e2e["value"])
+
+    peak, peak_kind = measured_peak()
+    tokens = dist.sum(w.batch * K) / (dist.max(total_ms) * 1e-3)
+    res = {
+        "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": W_,
+        "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
+        "tokens_per_s": tokens,
+        "hbm_gbs": achieved_gbs,
+        "conventional_us_per_step": conv_us,
+        "conventional_hbm_gbs": conv_bytes / (conv_us * 1e-6) / 1e9,
+        "speedup_vs_conventional": conv_us / us_step,
+        "algorithmic_bytes_per_step": alg_bytes / K,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "peak_source": peak_kind,
+                     "traffic": profiled_traffic("mamba2_step_serving.txt", KERNEL_SOURCES),
+                     "kernel": "m2_step_kernel (+ cursor advance, timed per call)"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    return res
+
+
+def e2e_mamba2(st, A, D, w, dev, K, W_, y_dtype):
+    """µs/step through rssm_mamba2_step with each step's record copied from pinned
+    host memory and its output copied back, pipelined on two copy streams."""
+    import torch
+
+    from recurrent_state_decode_gb300 import inputs as I
+    pool = 8
+    host = []
+    for t in range(pool):
+        r = I.mamba2_step_inputs(w, 10_000 + t, dev)
+        host.append({k: v.cpu().pin_memory() for k, v in r.items()})
+    dbuf = [{k: torch.empty_like(v, device=dev) for k, v in host[0].items()} for _ in range(2)]
+    ybuf = [st.new_output() for _ in range(2)]
+    yhost = torch.empty(ybuf[0].shape, dtype=y_dtype).pin_memory()
+    comp = torch.cuda.current_stream(dev)
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    h2d_bytes = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h_bytes = ybuf[0].numel() * ybuf[0].element_size()
+
+    def one(i):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(done[b])
+            for k, v in host[i % pool].items():
+                dbuf[b][k].copy_(v, non_blocking=True)
+            loaded[b].record(h2d)
+        comp.wait_event(loaded[b])
+        if i >= 2:
+            comp.wait_event(copied[b])
+        st.step(dbuf[b], A, D, ybuf[b], stream=comp.cuda_stream)
+        done[b].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(done[b])
+            yhost.copy_(ybuf[b], non_blocking=True)
+            copied[b].record(d2h)
+
+    for i in range(W_):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        one(i)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": dt * 1e6 / K, "unit": UNIT, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "how": "wall clock around K pipelined steps: H2D of the step's record from pinned host memory, "
+                   "rssm_mamba2_step, D2H of y; two copy streams overlap the copies with compute"}
+
+
+def main(argv=None):
+    args = parse(argv)
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, dist)
+        else:
+            from recurrent_state_decode_gb300 import binding
+            binding.load()
+            if args.workload.startswith("mamba2") and "spec" not in args.workload:
+                res = bench_mamba2_ar(args, dist)
+            else:
+                raise SystemExit(f"workload {args.workload} is not benchmarked by this script yet")
+            if res is not None and dist.rank == 0 and not args.no_cpu_baseline and dist.world == 1:
+                from recurrent_state_decode_gb300 import inputs as I
+                v, sample = oracle_time_per_step(I.WORKLOADS[args.workload], args.cpu_seconds)
+                res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+        if res is not None and dist.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,261 @@
+/*
+ * rssm.h -- C ABI of librssm, ReplaySSM decode kernels for GB300 (sm_103a).
+ *
+ * ReplaySSM keeps each sequence's SSM state as a high-precision checkpoint
+ * plus a ring buffer of the last L input records ("ReplaySSM Caches Inputs
+ * Instead of State to Speed Up Hybrid-Model Decoding", section "How ReplaySSM
+ * works"). A non-flush step appends the current record and computes the
+ * output from the read-only checkpoint and the window, storing no state; the
+ * L-th step folds the window into the checkpoint and writes it once.
+ * Speculative decoding appends draft records and rolls rejected ones back by
+ * moving a cursor ("ReplaySSM", code repository, introduction: "Cheap
+ * rollback").
+ *
+ * Conventions shared by every call:
+ *  - All tensor arguments are DEVICE pointers to memory the caller owns.
+ *    Tensors are dense, row-major (C order) with the shapes given below, and
+ *    every base pointer must be 16-byte aligned (RSSM_ERR_MISALIGNED).
+ *  - bf16 tensors hold IEEE bfloat16 bit patterns (rssm_bf16).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream). The library allocates no memory and never
+ *    synchronises.
+ *  - Host-side checks run first; on failure the call returns a negative
+ *    RSSM_ERR_* code and launches nothing. RSSM_ERR_CUDA reports a launch
+ *    error (cudaGetLastError after the launch).
+ *  - Errors that depend on device data (a cursor out of range, a commit of
+ *    more drafts than are pending) are written to the optional device word
+ *    `dev_status` (int32, caller-zeroed; the first error code wins). The
+ *    affected sequence is skipped: its checkpoint, ring and cursor are left
+ *    as they were and its outputs are not written. Pass NULL to ignore them.
+ *  - batch == 0 is a valid empty call: nothing is launched.
+ *
+ * Cursor: int32 [batch, 4] = {start, count, pending, flags} per sequence.
+ *  start   ring slot of the oldest record since the checkpoint, [0, L)
+ *  count   committed records in the window, [0, L]
+ *  pending draft records appended by the last verify, not yet committed
+ *  flags   bit 0: that verify folded the committed window into the checkpoint
+ * Record j of the window (j = 0 oldest) lives in ring slot (start + j) mod L.
+ */
+#ifndef RSSM_H
+#define RSSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RSSM_API __attribute__((visibility("default")))
+#else
+#define RSSM_API
+#endif
+
+typedef struct CUstream_st* rssm_stream_t; /* identical to cudaStream_t */
+typedef uint16_t rssm_bf16;                /* bfloat16 bit pattern */
+
+/* Return codes of every call. */
+enum {
+  RSSM_OK = 0,
+  RSSM_ERR_INVALID_ARG = -1, /* null pointer, bad dimension, bad n_new */
+  RSSM_ERR_UNSUPPORTED = -2, /* valid but outside this build's limits */
+  RSSM_ERR_MISALIGNED = -3,  /* a base pointer is not 16-byte aligned */
+  RSSM_ERR_CUDA = -4         /* a CUDA launch failed */
+};
+
+/* Codes written to dev_status. */
+enum {
+  RSSM_DEV_OK = 0,
+  RSSM_DEV_BAD_CURSOR = 1,  /* start or count out of range */
+  RSSM_DEV_WINDOW_FULL = 2, /* AR step on a window holding L records */
+  RSSM_DEV_PENDING = 3,     /* step, verify or flush before the last verify was committed */
+  RSSM_DEV_BAD_KEPT = 4,    /* commit with kept < 0 or kept > pending */
+  RSSM_DEV_BAD_SLOT = 5,    /* reset of a slot outside [0, batch) */
+  RSSM_DEV_TIMEOUT = 6      /* a bounded wait for an asynchronous copy expired */
+};
+
+/* Output element types. */
+enum { RSSM_F32 = 0, RSSM_BF16 = 1 };
+
+/* Limits of this build. */
+#define RSSM_MAX_BUF_LEN 32 /* L in [1, 32] */
+#define RSSM_MAX_DIM 256    /* headdim, dstate, dk, dv: multiples of 8 in [8, 256] */
+
+/* ----------------------------------------------------------------------------
+ * Mamba-2
+ *
+ * Recurrence per (sequence b, head h), group g = floor(h * ngroups / nheads),
+ * state h[headdim, dstate] (the published selective_state_update decode step;
+ * the pages name the Mamba-2 layer in "Why SSM layers slow down hybrid models"):
+ *   dA = exp(dt * A[h]);  h = dA * h + dt * x B^T;  y = (h C + D[h] x) * silu(z)
+ * A record is (x, z [headdim] bf16; B, C [dstate] bf16 per group; dt fp32 > 0).
+ */
+typedef struct {
+  int batch, nheads, headdim, dstate, ngroups;
+  int buf_len;   /* L, the window length */
+  int out_dtype; /* RSSM_F32 or RSSM_BF16: element type of y */
+} rssm_mamba2_desc;
+
+/* Ring buffer of window records, head- (or group-) major so that one
+ * (sequence, head) tile's history is contiguous. Each step stores the whole
+ * record of its token. */
+typedef struct {
+  rssm_bf16* x;  /* [batch, nheads, buf_len, headdim] */
+  rssm_bf16* z;  /* [batch, nheads, buf_len, headdim] */
+  rssm_bf16* B;  /* [batch, ngroups, buf_len, dstate] */
+  rssm_bf16* C;  /* [batch, ngroups, buf_len, dstate] */
+  float* dt;     /* [batch, nheads, buf_len] */
+} rssm_mamba2_ring;
+
+/* Bytes of each ring field, in the order x, z, B, C, dt. Returns RSSM_OK or
+ * RSSM_ERR_INVALID_ARG. */
+RSSM_API int rssm_mamba2_ring_bytes(const rssm_mamba2_desc* desc, size_t bytes[5]);
+
+/* Conventional decode step (the comparison point): reads and writes the full
+ * state every step ("Why SSM layers slow down hybrid models", first cause).
+ *  state [batch, nheads, headdim, dstate] fp32, updated in place
+ *  x, z [batch, nheads, headdim]; B, C [batch, ngroups, dstate] (bf16)
+ *  dt [batch, nheads] fp32; A, D [nheads] fp32
+ *  y [batch, nheads, headdim] of desc->out_dtype (written) */
+RSSM_API int rssm_mamba2_conventional_step(const rssm_mamba2_desc* desc, float* state,
+                                  const rssm_bf16* x, const rssm_bf16* z,
+                                  const rssm_bf16* B, const rssm_bf16* C,
+                                  const float* dt, const float* A,
+                                  const float* D, void* y,
+                                  rssm_stream_t stream);
+
+/* One ReplaySSM AR decode step ("How ReplaySSM works"). For each sequence
+ * with window count c (needs c < L and pending == 0):
+ *  - c + 1 < L (non-flush): stores the record in ring slot (start + c) mod L
+ *    and computes y from the checkpoint and the c + 1 window records without
+ *    writing any state; count becomes c + 1.
+ *  - c + 1 == L (flush): folds the L records into the checkpoint, writes it
+ *    (and ckpt_read, if given) once, computes y; count becomes 0.
+ *  ckpt      [batch, nheads, headdim, dstate] fp32 recurrence checkpoint
+ *  ckpt_read same shape in bf16, or NULL. When given, non-flush steps read
+ *            it instead of ckpt (the low-precision read copy of "ReplaySSM",
+ *            introduction, "Separate state precisions"); flushes read ckpt
+ *            and write both.
+ *  ring      window records (see rssm_mamba2_ring), cursors [batch, 4]
+ *  x .. D, y as in rssm_mamba2_conventional_step.
+ * Cursors advance by a second kernel in stream order after the step. */
+RSSM_API int rssm_mamba2_step(const rssm_mamba2_desc* desc, float* ckpt,
+                     rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
+                     int32_t* cursors, const rssm_bf16* x, const rssm_bf16* z,
+                     const rssm_bf16* B, const rssm_bf16* C, const float* dt,
+                     const float* A, const float* D, void* y,
+                     int32_t* dev_status, rssm_stream_t stream);
+
+/* Standalone flush: for every sequence with count > 0 and pending == 0,
+ * folds its window into ckpt (and ckpt_read, if given); start moves past the
+ * folded records and count becomes 0. Produces no output. */
+RSSM_API int rssm_mamba2_flush(const rssm_mamba2_desc* desc, float* ckpt,
+                      rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
+                      int32_t* cursors, const float* A, int32_t* dev_status,
+                      rssm_stream_t stream);
+
+/* Speculative verify ("How ReplaySSM works": drafts are appended to the
+ * buffer instead of snapshotting state; "Core implementation files":
+ * speculative decode on a circular buffer). Appends n_new = K records per
+ * sequence (the bonus token and K-1 drafts) at ring slots
+ * (start + count + i) mod L and computes, output-only, y_i for i < K: the
+ * output after committed records plus new records 0..i. If count + K > L the
+ * committed window is first folded into the checkpoint (written once).
+ * Needs pending == 0; sets pending = K and flags = folded. Must be followed
+ * by one rssm_commit_cursors.
+ *  x, z [batch, K, nheads, headdim]; B, C [batch, K, ngroups, dstate] (bf16)
+ *  dt [batch, K, nheads] fp32; y [batch, K, nheads, headdim]
+ *  1 <= n_new <= buf_len (else RSSM_ERR_INVALID_ARG). */
+RSSM_API int rssm_mamba2_spec_verify(const rssm_mamba2_desc* desc, int n_new,
+                            float* ckpt, rssm_bf16* ckpt_read,
+                            const rssm_mamba2_ring* ring, int32_t* cursors,
+                            const rssm_bf16* x, const rssm_bf16* z,
+                            const rssm_bf16* B, const rssm_bf16* C,
+                            const float* dt, const float* A, const float* D,
+                            void* y, int32_t* dev_status,
+                            rssm_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Cursors (shared by Mamba-2 and Gated DeltaNet)
+ */
+
+/* Commit after a verify ("ReplaySSM", introduction, "Cheap rollback";
+ * "Core implementation files": the commit call of the speculative path).
+ * kept [batch] int32: records of the last verify to keep, 0 <= kept <=
+ * pending. If that verify folded: start += count (mod L), count = 0. Then
+ * count += kept, pending = 0, flags = 0. Rejected drafts are dropped by this
+ * cursor move alone. */
+RSSM_API int rssm_commit_cursors(int32_t* cursors, const int32_t* kept, int batch,
+                        int buf_len, int32_t* dev_status,
+                        rssm_stream_t stream);
+
+/* Reset the cursors of the listed sequences to {0, 0, 0, 0} (a new request in
+ * that slot; "Core implementation files": the reset call). slots [n_slots]
+ * int32 in [0, batch). The checkpoint is not touched: the caller writes it,
+ * then calls rssm_checkpoint_downcast if it keeps a read copy. */
+RSSM_API int rssm_reset_cursors(int32_t* cursors, const int32_t* slots, int n_slots,
+                       int batch, int32_t* dev_status, rssm_stream_t stream);
+
+/* fp32 -> bf16 read copy, round to nearest even ("ReplaySSM", introduction,
+ * "Separate state precisions"). src [n] fp32, dst [n] bf16. */
+RSSM_API int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n,
+                             rssm_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Gated DeltaNet
+ *
+ * Recurrence per (sequence, head), state S[dv, dk], alpha = exp(g) (the
+ * published gated delta rule; Gated DeltaNet is named in "Why SSM layers slow
+ * down hybrid models"):
+ *   S = alpha * S (I - beta k k^T) + beta v k^T;   o = S q
+ * A record is (q, k [dk] bf16; v [dv] bf16; g, beta fp32).
+ */
+typedef struct {
+  int batch, nheads, dk, dv;
+  int buf_len;
+  int out_dtype; /* element type of o */
+} rssm_gdn_desc;
+
+typedef struct {
+  rssm_bf16* q;  /* [batch, nheads, buf_len, dk] */
+  rssm_bf16* k;  /* [batch, nheads, buf_len, dk] */
+  rssm_bf16* v;  /* [batch, nheads, buf_len, dv] */
+  float* g;      /* [batch, nheads, buf_len] */
+  float* beta;   /* [batch, nheads, buf_len] */
+} rssm_gdn_ring;
+
+/* Bytes of each ring field, in the order q, k, v, g, beta. */
+RSSM_API int rssm_gdn_ring_bytes(const rssm_gdn_desc* desc, size_t bytes[5]);
+
+/* Conventional step: S [batch, nheads, dv, dk] fp32 updated in place;
+ * q, k [batch, nheads, dk], v [batch, nheads, dv] bf16; g, beta
+ * [batch, nheads] fp32; o [batch, nheads, dv] of desc->out_dtype. */
+RSSM_API int rssm_gdn_conventional_step(const rssm_gdn_desc* desc, float* S,
+                               const rssm_bf16* q, const rssm_bf16* k,
+                               const rssm_bf16* v, const float* g,
+                               const float* beta, void* o,
+                               rssm_stream_t stream);
+
+/* ReplaySSM AR step for Gated DeltaNet: same protocol as rssm_mamba2_step
+ * (non-flush steps write no state; the L-th step folds and writes S once). */
+RSSM_API int rssm_gdn_step(const rssm_gdn_desc* desc, float* S, const rssm_gdn_ring* ring,
+                  int32_t* cursors, const rssm_bf16* q, const rssm_bf16* k,
+                  const rssm_bf16* v, const float* g, const float* beta,
+                  void* o, int32_t* dev_status, rssm_stream_t stream);
+
+/* Standalone flush for Gated DeltaNet (as rssm_mamba2_flush). */
+RSSM_API int rssm_gdn_flush(const rssm_gdn_desc* desc, float* S, const rssm_gdn_ring* ring,
+                   int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Misc
+ */
+RSSM_API const char* rssm_status_string(int code); /* text for RSSM_* and RSSM_DEV_* codes */
+RSSM_API int rssm_version(void);                   /* major * 10000 + minor * 100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSSM_H */

@@ -1,0 +1,77 @@
+"""Algorithmic HBM bytes of each call, from the sizes and the window counts.
+
+These are the bytes the method must move (what a perfect kernel reads and
+writes once), the denominator of the roofline fraction: the checkpoint is
+read every step (bf16 read copy on non-flush steps when present) and written
+only on a flush; the current record is read once and appended to the ring;
+past records contribute the fields later steps read (Mamba-2 x, B, dt;
+Gated DeltaNet k, v, g, beta); outputs are written once; each cursor is read
+and written (16 + 16 bytes).
+"""
+
+CURSOR = 32
+
+
+def mamba2_parts(H, P, N, G, out_bytes):
+    tile32 = H * P * N * 4                              # fp32 checkpoint of one sequence
+    rec = 2 * H * P * 2 + 2 * G * N * 2 + H * 4        # x, z, B, C, dt of one token
+    past = H * P * 2 + G * N * 2 + H * 4               # x, B, dt of one window record
+    y = H * P * out_bytes
+    return tile32, rec, past, y
+
+
+def mamba2_step_bytes(H, P, N, G, L, counts, read_copy=False, out_bytes=2):
+    """One AR step; counts = each sequence's window count before the step."""
+    tile32, rec, past, y = mamba2_parts(H, P, N, G, out_bytes)
+    total = 0
+    for c in counts:
+        if c + 1 == L:  # flush: read fp32, write fp32 (+ bf16 copy); the record is folded, not stored
+            total += 2 * tile32 + (tile32 // 2 if read_copy else 0) + rec
+        else:
+            total += (tile32 // 2 if read_copy else tile32) + 2 * rec
+        total += c * past + y + CURSOR
+    return total
+
+
+def mamba2_conventional_bytes(H, P, N, G, batch, out_bytes=2):
+    tile32, rec, past, y = mamba2_parts(H, P, N, G, out_bytes)
+    return batch * (2 * tile32 + rec + y)
+
+
+def mamba2_verify_bytes(H, P, N, G, L, K, counts, read_copy=False, out_bytes=2):
+    """One verify + commit; counts = committed window counts before the verify."""
+    tile32, rec, past, y = mamba2_parts(H, P, N, G, out_bytes)
+    total = 0
+    for c in counts:
+        fold = c + K > L
+        if fold:
+            total += 2 * tile32 + (tile32 // 2 if read_copy else 0)
+        else:
+            total += tile32 // 2 if read_copy else tile32
+        total += 2 * K * rec + c * past + K * y + 2 * CURSOR + 4
+    return total
+
+
+def gdn_parts(H, DK, DV, out_bytes):
+    tile = H * DV * DK * 4
+    rec = H * (2 * DK * 2 + DV * 2 + 8)                # q, k, v, g, beta
+    past = H * (DK * 2 + DV * 2 + 8)                   # k, v, g, beta
+    o = H * DV * out_bytes
+    return tile, rec, past, o
+
+
+def gdn_step_bytes(H, DK, DV, L, counts, out_bytes=2):
+    tile, rec, past, o = gdn_parts(H, DK, DV, out_bytes)
+    total = 0
+    for c in counts:
+        if c + 1 == L:
+            total += 2 * tile + rec
+        else:
+            total += tile + 2 * rec
+        total += c * past + o + CURSOR
+    return total
+
+
+def gdn_conventional_bytes(H, DK, DV, batch, out_bytes=2):
+    tile, rec, past, o = gdn_parts(H, DK, DV, out_bytes)
+    return batch * (2 * tile + rec + o)

@@ -1,0 +1,324 @@
+// C ABI of librssm: host-side argument checks, then kernel launches on the
+// caller's stream. Nothing here allocates, synchronises or reads device data.
+#include <climits>
+#include <cstdint>
+
+#include "kernels.h"
+#include "rssm.h"
+
+using namespace rssm;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_ok(int v) { return v >= 8 && v <= RSSM_MAX_DIM && v % 8 == 0; }
+
+// All pointers non-null and 16-byte aligned.
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p) return RSSM_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return RSSM_ERR_MISALIGNED;
+  return RSSM_OK;
+}
+
+int check_opt(const void* p) { return (p && !aligned16(p)) ? RSSM_ERR_MISALIGNED : RSSM_OK; }
+
+int check_m2(const rssm_mamba2_desc* d) {
+  if (!d) return RSSM_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->nheads < 1 || d->ngroups < 1 || d->nheads % d->ngroups != 0) return RSSM_ERR_INVALID_ARG;
+  if (!dim_ok(d->headdim) || !dim_ok(d->dstate)) return RSSM_ERR_INVALID_ARG;
+  if (d->buf_len < 1 || d->buf_len > RSSM_MAX_BUF_LEN) return RSSM_ERR_INVALID_ARG;
+  if (d->out_dtype != RSSM_F32 && d->out_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
+  const int pb = rows_per_block(d->headdim, d->dstate);
+  const long long grid = (long long)d->batch * d->nheads * ((d->headdim + pb - 1) / pb);
+  if (grid > INT_MAX) return RSSM_ERR_UNSUPPORTED;
+  return RSSM_OK;
+}
+
+int check_gdn(const rssm_gdn_desc* d) {
+  if (!d) return RSSM_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->nheads < 1) return RSSM_ERR_INVALID_ARG;
+  if (!dim_ok(d->dk) || !dim_ok(d->dv)) return RSSM_ERR_INVALID_ARG;
+  if (d->buf_len < 1 || d->buf_len > RSSM_MAX_BUF_LEN) return RSSM_ERR_INVALID_ARG;
+  if (d->out_dtype != RSSM_F32 && d->out_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
+  const long long grid = (long long)d->batch * d->nheads * ((d->dv + 63) / 64);
+  if (grid > INT_MAX) return RSSM_ERR_UNSUPPORTED;
+  return RSSM_OK;
+}
+
+M2Args m2_args(const rssm_mamba2_desc* d) {
+  M2Args a{};
+  a.Bt = d->batch;
+  a.H = d->nheads;
+  a.P = d->headdim;
+  a.N = d->dstate;
+  a.G = d->ngroups;
+  a.L = d->buf_len;
+  a.PB = rows_per_block(a.P, a.N);
+  a.nPB = (a.P + a.PB - 1) / a.PB;
+  a.K = 1;
+  return a;
+}
+
+void set_ring(M2Args& a, const rssm_mamba2_ring* r) {
+  a.rx = r->x;
+  a.rz = r->z;
+  a.rB = r->B;
+  a.rC = r->C;
+  a.rdt = r->dt;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA; }
+
+GdnArgs gdn_args(const rssm_gdn_desc* d) {
+  GdnArgs a{};
+  a.Bt = d->batch;
+  a.H = d->nheads;
+  a.DK = d->dk;
+  a.DV = d->dv;
+  a.L = d->buf_len;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rssm_version(void) { return 100; }
+
+const char* rssm_status_string(int code) {
+  switch (code) {
+    case RSSM_OK: return "ok";
+    case RSSM_ERR_INVALID_ARG: return "invalid argument (null pointer, bad dimension or bad count)";
+    case RSSM_ERR_UNSUPPORTED: return "unsupported by this build (size limit)";
+    case RSSM_ERR_MISALIGNED: return "a base pointer is not 16-byte aligned";
+    case RSSM_ERR_CUDA: return "CUDA launch error";
+    case RSSM_DEV_BAD_CURSOR: return "device: cursor start/count out of range";
+    case RSSM_DEV_WINDOW_FULL: return "device: AR step on a full window (flush or commit first)";
+    case RSSM_DEV_PENDING: return "device: previous verify not committed";
+    case RSSM_DEV_BAD_KEPT: return "device: kept outside [0, pending]";
+    case RSSM_DEV_BAD_SLOT: return "device: reset slot outside [0, batch)";
+    case RSSM_DEV_TIMEOUT: return "device: bounded wait for a bulk copy expired";
+    default: return "unknown status code";
+  }
+}
+
+int rssm_mamba2_ring_bytes(const rssm_mamba2_desc* d, size_t bytes[5]) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (!bytes) return RSSM_ERR_INVALID_ARG;
+  const size_t Bt = d->batch, H = d->nheads, L = d->buf_len, G = d->ngroups;
+  bytes[0] = bytes[1] = Bt * H * L * d->headdim * 2;
+  bytes[2] = bytes[3] = Bt * G * L * d->dstate * 2;
+  bytes[4] = Bt * H * L * 4;
+  return RSSM_OK;
+}
+
+int rssm_gdn_ring_bytes(const rssm_gdn_desc* d, size_t bytes[5]) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (!bytes) return RSSM_ERR_INVALID_ARG;
+  const size_t Bt = d->batch, H = d->nheads, L = d->buf_len;
+  bytes[0] = bytes[1] = Bt * H * L * d->dk * 2;
+  bytes[2] = Bt * H * L * d->dv * 2;
+  bytes[3] = bytes[4] = Bt * H * L * 4;
+  return RSSM_OK;
+}
+
+int rssm_mamba2_conventional_step(const rssm_mamba2_desc* d, float* state, const rssm_bf16* x, const rssm_bf16* z,
+                                  const rssm_bf16* B, const rssm_bf16* C, const float* dt, const float* A,
+                                  const float* D, void* y, rssm_stream_t stream) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if ((rc = check_ptrs({state, x, z, B, C, dt, A, D, y}))) return rc;
+  M2Args a = m2_args(d);
+  a.ckpt = state;
+  a.x = x;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.dt = dt;
+  a.A = A;
+  a.D = D;
+  a.y = y;
+  return cuda_rc(m2_launch(M2_CONVENTIONAL, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
+}
+
+int rssm_mamba2_step(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
+                     int32_t* cursors, const rssm_bf16* x, const rssm_bf16* z, const rssm_bf16* B,
+                     const rssm_bf16* C, const float* dt, const float* A, const float* D, void* y,
+                     int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({ckpt, ring->x, ring->z, ring->B, ring->C, ring->dt, cursors, x, z, B, C, dt, A, D, y})))
+    return rc;
+  if ((rc = check_opt(ckpt_read)) || (rc = check_opt(dev_status))) return rc;
+  M2Args a = m2_args(d);
+  a.ckpt = ckpt;
+  a.ckpt_read = ckpt_read;
+  set_ring(a, ring);
+  a.cursors = cursors;
+  a.x = x;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.dt = dt;
+  a.A = A;
+  a.D = D;
+  a.y = y;
+  a.status = dev_status;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = cuda_rc(m2_launch(M2_STEP, a, d->out_dtype == RSSM_BF16, st)))) return rc;
+  return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+int rssm_mamba2_flush(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
+                      int32_t* cursors, const float* A, int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({ckpt, ring->x, ring->B, ring->dt, cursors, A}))) return rc;
+  if ((rc = check_opt(ckpt_read)) || (rc = check_opt(dev_status))) return rc;
+  M2Args a = m2_args(d);
+  a.ckpt = ckpt;
+  a.ckpt_read = ckpt_read;
+  set_ring(a, ring);
+  a.cursors = cursors;
+  a.A = A;
+  a.status = dev_status;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = cuda_rc(m2_launch(M2_FLUSH, a, 0, st)))) return rc;
+  return cuda_rc(cursor_launch(CUR_FLUSH, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+int rssm_mamba2_spec_verify(const rssm_mamba2_desc* d, int n_new, float* ckpt, rssm_bf16* ckpt_read,
+                            const rssm_mamba2_ring* ring, int32_t* cursors, const rssm_bf16* x, const rssm_bf16* z,
+                            const rssm_bf16* B, const rssm_bf16* C, const float* dt, const float* A,
+                            const float* D, void* y, int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (n_new < 1 || n_new > d->buf_len) return RSSM_ERR_INVALID_ARG;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({ckpt, ring->x, ring->z, ring->B, ring->C, ring->dt, cursors, x, z, B, C, dt, A, D, y})))
+    return rc;
+  if ((rc = check_opt(ckpt_read)) || (rc = check_opt(dev_status))) return rc;
+  M2Args a = m2_args(d);
+  a.K = n_new;
+  a.ckpt = ckpt;
+  a.ckpt_read = ckpt_read;
+  set_ring(a, ring);
+  a.cursors = cursors;
+  a.x = x;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.dt = dt;
+  a.A = A;
+  a.D = D;
+  a.y = y;
+  a.status = dev_status;
+  return cuda_rc(m2_launch(M2_VERIFY, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
+}
+
+int rssm_commit_cursors(int32_t* cursors, const int32_t* kept, int batch, int buf_len, int32_t* dev_status,
+                        rssm_stream_t stream) {
+  if (batch < 0 || buf_len < 1 || buf_len > RSSM_MAX_BUF_LEN) return RSSM_ERR_INVALID_ARG;
+  if (batch == 0) return RSSM_OK;
+  int rc;
+  if ((rc = check_ptrs({cursors, kept})) || (rc = check_opt(dev_status))) return rc;
+  return cuda_rc(cursor_launch(CUR_COMMIT, cursors, kept, batch, buf_len, dev_status, (cudaStream_t)stream));
+}
+
+int rssm_reset_cursors(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* dev_status,
+                       rssm_stream_t stream) {
+  if (n_slots < 0 || batch < 0) return RSSM_ERR_INVALID_ARG;
+  if (n_slots == 0) return RSSM_OK;
+  int rc;
+  if ((rc = check_ptrs({cursors, slots})) || (rc = check_opt(dev_status))) return rc;
+  return cuda_rc(reset_launch(cursors, slots, n_slots, batch, dev_status, (cudaStream_t)stream));
+}
+
+int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, rssm_stream_t stream) {
+  if (n == 0) return RSSM_OK;
+  int rc;
+  if ((rc = check_ptrs({src, dst}))) return rc;
+  return cuda_rc(downcast_launch(src, dst, n, (cudaStream_t)stream));
+}
+
+int rssm_gdn_conventional_step(const rssm_gdn_desc* d, float* S, const rssm_bf16* q, const rssm_bf16* k,
+                               const rssm_bf16* v, const float* g, const float* beta, void* o,
+                               rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if ((rc = check_ptrs({S, q, k, v, g, beta, o}))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.S = S;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.o = o;
+  return cuda_rc(gdn_launch(GDN_CONVENTIONAL, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
+}
+
+int rssm_gdn_step(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, int32_t* cursors, const rssm_bf16* q,
+                  const rssm_bf16* k, const rssm_bf16* v, const float* g, const float* beta, void* o,
+                  int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, cursors, q, k, v, g, beta, o}))) return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.S = S;
+  a.rq = ring->q;
+  a.rk = ring->k;
+  a.rv = ring->v;
+  a.rg = ring->g;
+  a.rbeta = ring->beta;
+  a.cursors = cursors;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.o = o;
+  a.status = dev_status;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = cuda_rc(gdn_launch(GDN_STEP, a, d->out_dtype == RSSM_BF16, st)))) return rc;
+  return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+int rssm_gdn_flush(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, int32_t* cursors, int32_t* dev_status,
+                   rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->k, ring->v, ring->g, ring->beta, cursors}))) return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.S = S;
+  a.rq = ring->q;
+  a.rk = ring->k;
+  a.rv = ring->v;
+  a.rg = ring->g;
+  a.rbeta = ring->beta;
+  a.cursors = cursors;
+  a.status = dev_status;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = cuda_rc(gdn_launch(GDN_FLUSH, a, 0, st)))) return rc;
+  return cuda_rc(cursor_launch(CUR_FLUSH, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+}  // extern "C"

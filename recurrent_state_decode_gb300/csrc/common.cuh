@@ -1,0 +1,177 @@
+// Device helpers shared by the librssm kernels: bf16 packing, warp
+// reductions, mbarrier + bulk-copy (TMA, non-tensor) wrappers and the
+// bounded waits every kernel uses on them.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rssm.h"
+
+namespace rssm {
+
+constexpr unsigned FULL = 0xffffffffu;
+// A bounded wait gives up after this many nanoseconds and reports
+// RSSM_DEV_TIMEOUT; a healthy bulk copy lands in microseconds.
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+
+// ---------------------------------------------------------------- bf16 packing
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ float4 bf4_to_f4(uint2 u) {
+  return make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // RNE, a in the low half
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint2 f4_to_bf4(float4 v) {
+  return make_uint2(pack_bf2(v.x, v.y), pack_bf2(v.z, v.w));
+}
+
+__device__ __forceinline__ uint16_t f_to_bf(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ float bf_to_f(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
+
+__device__ __forceinline__ float4 load_bf4(const uint16_t* p) {
+  return bf4_to_f4(*reinterpret_cast<const uint2*>(p));
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ float4 fma4(float s, float4 a, float4 c) {
+  return make_float4(fmaf(s, a.x, c.x), fmaf(s, a.y, c.y), fmaf(s, a.z, c.z), fmaf(s, a.w, c.w));
+}
+
+__device__ __forceinline__ float4 scale4(float s, float4 a) {
+  return make_float4(s * a.x, s * a.y, s * a.z, s * a.w);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ---------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+// Sum eight per-lane partials v[0..7] over the warp. Afterwards v[0] of a
+// lane holds the total of partial index reduce8_row(lane); the four lanes
+// that share bits 4..2 of the lane id hold the same total. 9 shuffles
+// instead of 40 for eight separate butterflies.
+__device__ __forceinline__ int reduce8_row(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+
+__device__ __forceinline__ void reduce8(float (&v)[8], int lane) {
+  const bool b16 = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    float send = b16 ? v[i] : v[i + 4];
+    float keep = b16 ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(FULL, send, 16);
+  }
+  const bool b8 = lane & 8;
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    float send = b8 ? v[i] : v[i + 2];
+    float keep = b8 ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(FULL, send, 8);
+  }
+  const bool b4 = lane & 4;
+  {
+    float send = b4 ? v[0] : v[1];
+    float keep = b4 ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(FULL, send, 4);
+  }
+  v[0] += __shfl_xor_sync(FULL, v[0], 2);
+  v[0] += __shfl_xor_sync(FULL, v[0], 1);
+}
+
+// ---------------------------------------------------------------- status
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy (TMA, non-tensor form) completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; i++)
+      if (mbar_test(bar, parity)) return true;
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
+// Wait for a bulk copy; on timeout report it, wait once more (bounded) so the
+// copy is not left writing into shared memory of an exited block, and
+// return false so the caller can skip the tile.
+__device__ __forceinline__ bool mbar_wait_or_report(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_wait(bar, parity)) return true;
+  report(status, RSSM_DEV_TIMEOUT);
+  mbar_wait(bar, parity);
+  return false;
+}
+
+}  // namespace rssm

@@ -1,0 +1,65 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rssm {
+
+// Mamba-2 launch arguments (device pointers, dense row-major layouts of rssm.h).
+struct M2Args {
+  int Bt, H, P, N, G, L;
+  int PB, nPB;  // rows per block, row blocks per (sequence, head) tile
+  int K;        // records per verify (1 for the AR step)
+  float* ckpt;
+  uint16_t* ckpt_read;
+  uint16_t *rx, *rz, *rB, *rC;
+  float* rdt;
+  int32_t* cursors;
+  const uint16_t *x, *z, *B, *C;
+  const float *dt, *A, *D;
+  void* y;
+  int32_t* status;
+};
+
+enum { M2_CONVENTIONAL = 0, M2_STEP = 1, M2_FLUSH = 2, M2_VERIFY = 3 };
+
+cudaError_t m2_launch(int kind, const M2Args& a, int out_bf16, cudaStream_t st);
+size_t m2_smem_bytes(int kind, const M2Args& a);
+
+// Gated DeltaNet launch arguments.
+struct GdnArgs {
+  int Bt, H, DK, DV, L;
+  float* S;
+  uint16_t *rq, *rk, *rv;
+  float *rg, *rbeta;
+  int32_t* cursors;
+  const uint16_t *q, *k, *v;
+  const float *g, *beta;
+  void* o;
+  int32_t* status;
+};
+
+enum { GDN_CONVENTIONAL = 0, GDN_STEP = 1, GDN_FLUSH = 2 };
+
+cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st);
+
+// Cursor kernels (one thread per sequence).
+enum { CUR_AR = 0, CUR_FLUSH = 1, CUR_COMMIT = 2 };
+
+cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status,
+                          cudaStream_t st);
+cudaError_t reset_launch(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* status,
+                         cudaStream_t st);
+cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, cudaStream_t st);
+
+// Rows per block for a tile of `rows` x `cols` fp32 elements: at most 32 KiB of
+// tile per block, a multiple of 8 rows.
+inline int rows_per_block(int rows, int cols) {
+  int pb = (8192 / cols) & ~7;
+  if (pb < 8) pb = 8;
+  return pb < rows ? pb : rows;
+}
+
+}  // namespace rssm

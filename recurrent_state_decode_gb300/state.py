@@ -1,0 +1,136 @@
+"""Device buffers of a decode session, allocated with torch, and thin methods
+that pass them to the C-ABI calls.
+
+Plumbing only: torch owns the memory and the stream, every step runs in
+librssm's kernels. Layouts follow ``include/rssm.h``.
+"""
+import torch
+
+from . import binding as bd
+
+
+class Mamba2State:
+    """Checkpoint (+ optional bf16 read copy), ring buffer, cursors and a
+    device status word for one Mamba-2 layer of `batch` sequences."""
+
+    def __init__(self, batch, nheads, headdim, dstate, ngroups, buf_len, device="cuda",
+                 read_copy=False, out_dtype=bd.RSSM_F32):
+        self.batch, self.nheads, self.headdim, self.dstate = batch, nheads, headdim, dstate
+        self.ngroups, self.buf_len, self.out_dtype = ngroups, buf_len, out_dtype
+        self.desc = bd.mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype)
+        dev = torch.device(device)
+        self.ckpt = torch.zeros((batch, nheads, headdim, dstate), dtype=torch.float32, device=dev)
+        self.ckpt_read = (torch.zeros((batch, nheads, headdim, dstate), dtype=torch.bfloat16, device=dev)
+                          if read_copy else None)
+        self.rx = torch.zeros((batch, nheads, buf_len, headdim), dtype=torch.bfloat16, device=dev)
+        self.rz = torch.zeros_like(self.rx)
+        self.rB = torch.zeros((batch, ngroups, buf_len, dstate), dtype=torch.bfloat16, device=dev)
+        self.rC = torch.zeros_like(self.rB)
+        self.rdt = torch.zeros((batch, nheads, buf_len), dtype=torch.float32, device=dev)
+        self.ring = bd.mamba2_ring(self.rx, self.rz, self.rB, self.rC, self.rdt)
+        self.cursors = torch.zeros((batch, 4), dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    @property
+    def y_dtype(self):
+        return torch.bfloat16 if self.out_dtype == bd.RSSM_BF16 else torch.float32
+
+    def new_output(self, n_new=0):
+        shape = (self.batch, self.nheads, self.headdim) if n_new == 0 else (self.batch, n_new, self.nheads, self.headdim)
+        return torch.empty(shape, dtype=self.y_dtype, device=self.ckpt.device)
+
+    def downcast(self, stream=None):
+        bd.check(bd.rssm_checkpoint_downcast(self.ckpt, self.ckpt_read, self.ckpt.numel(), stream),
+                 "rssm_checkpoint_downcast")
+
+    def step(self, rec, A, D, y, stream=None):
+        bd.check(bd.rssm_mamba2_step(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors,
+                                     rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
+                                     self.status, stream), "rssm_mamba2_step")
+
+    def flush(self, A, stream=None):
+        bd.check(bd.rssm_mamba2_flush(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors, A,
+                                      self.status, stream), "rssm_mamba2_flush")
+
+    def verify(self, rec, A, D, y, stream=None):
+        n_new = rec["x"].shape[1]
+        bd.check(bd.rssm_mamba2_spec_verify(self.desc, n_new, self.ckpt, self.ckpt_read, self.ring, self.cursors,
+                                            rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
+                                            self.status, stream), "rssm_mamba2_spec_verify")
+
+    def commit(self, kept, stream=None):
+        bd.check(bd.rssm_commit_cursors(self.cursors, kept, self.batch, self.buf_len, self.status, stream),
+                 "rssm_commit_cursors")
+
+    def reset(self, slots, stream=None):
+        bd.check(bd.rssm_reset_cursors(self.cursors, slots, slots.numel(), self.batch, self.status, stream),
+                 "rssm_reset_cursors")
+
+
+class GDNState:
+    """Checkpoint S, ring buffer, cursors and status word for one Gated DeltaNet layer."""
+
+    def __init__(self, batch, nheads, dk, dv, buf_len, device="cuda", out_dtype=bd.RSSM_F32):
+        self.batch, self.nheads, self.dk, self.dv, self.buf_len = batch, nheads, dk, dv, buf_len
+        self.out_dtype = out_dtype
+        self.desc = bd.gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype)
+        dev = torch.device(device)
+        self.S = torch.zeros((batch, nheads, dv, dk), dtype=torch.float32, device=dev)
+        self.rq = torch.zeros((batch, nheads, buf_len, dk), dtype=torch.bfloat16, device=dev)
+        self.rk = torch.zeros_like(self.rq)
+        self.rv = torch.zeros((batch, nheads, buf_len, dv), dtype=torch.bfloat16, device=dev)
+        self.rg = torch.zeros((batch, nheads, buf_len), dtype=torch.float32, device=dev)
+        self.rbeta = torch.zeros_like(self.rg)
+        self.ring = bd.gdn_ring(self.rq, self.rk, self.rv, self.rg, self.rbeta)
+        self.cursors = torch.zeros((batch, 4), dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    @property
+    def o_dtype(self):
+        return torch.bfloat16 if self.out_dtype == bd.RSSM_BF16 else torch.float32
+
+    def new_output(self):
+        return torch.empty((self.batch, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
+
+    def step(self, rec, o, stream=None):
+        bd.check(bd.rssm_gdn_step(self.desc, self.S, self.ring, self.cursors, rec["q"], rec["k"], rec["v"],
+                                  rec["g"], rec["beta"], o, self.status, stream), "rssm_gdn_step")
+
+    def flush(self, stream=None):
+        bd.check(bd.rssm_gdn_flush(self.desc, self.S, self.ring, self.cursors, self.status, stream),
+                 "rssm_gdn_flush")
+
+
+def mamba2_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32, read_copy=None):
+    """A Mamba2State at the start of workload ``w`` (see ``inputs``): checkpoint,
+    pre-filled windows and cursors; the read copy is downcast if present.
+    Returns (state, A, D, prefill records, starts, counts)."""
+    from . import inputs as I
+    read_copy = w.read_copy if read_copy is None else read_copy
+    st = Mamba2State(w.batch, w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len, device,
+                     read_copy=read_copy, out_dtype=out_dtype)
+    A, D = I.mamba2_params(w, device)
+    st.ckpt.copy_(I.mamba2_checkpoint(w, device))
+    starts, counts = I.initial_cursors(w, device)
+    pre = I.mamba2_prefill(w, device)
+    for field, ring in (("x", st.rx), ("z", st.rz), ("B", st.rB), ("C", st.rC), ("dt", st.rdt)):
+        I.place_window(ring, pre[field], starts, counts, w.buf_len)
+    st.cursors[:, 0] = starts
+    st.cursors[:, 1] = counts
+    if read_copy:
+        st.downcast()
+    return st, A, D, pre, starts, counts
+
+
+def gdn_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32):
+    """A GDNState at the start of workload ``w``. Returns (state, prefill, starts, counts)."""
+    from . import inputs as I
+    st = GDNState(w.batch, w.nheads, w.dk, w.dv, w.buf_len, device, out_dtype=out_dtype)
+    st.S.copy_(I.gdn_checkpoint(w, device))
+    starts, counts = I.initial_cursors(w, device)
+    pre = I.gdn_prefill(w, device)
+    for field, ring in (("q", st.rq), ("k", st.rk), ("v", st.rv), ("g", st.rg), ("beta", st.rbeta)):
+        I.place_window(ring, pre[field], starts, counts, w.buf_len)
+    st.cursors[:, 0] = starts
+    st.cursors[:, 1] = counts
+    return st, pre, starts, counts

@@ -1,0 +1,147 @@
+"""CPU tests of the C-ABI boundary: the library loads, exports exactly the calls
+include/rssm.h declares, and rejects bad arguments on the host before any
+launch (no GPU is touched by any of these)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from recurrent_state_decode_gb300 import binding as bd
+from recurrent_state_decode_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rssm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return bd.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return set(re.findall(r"RSSM_API\s+(?:const\s+)?\w+\*?\s+(rssm_\w+)\s*\(", text))
+
+
+def test_exports_match_header(lib):
+    declared = header_functions()
+    assert len(declared) == 14
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == declared
+    assert set(bd.EXPORTED) == declared
+    for name in declared:
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "rssm.h"\nint main(void){ rssm_mamba2_desc d; (void)d; return RSSM_OK; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c", str(src),
+                    "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_status_strings(lib):
+    assert bd.rssm_version() == 100
+    for code in (0, -1, -2, -3, -4, 1, 2, 3, 4, 5, 6):
+        assert bd.status_string(code) != "unknown status code"
+    assert bd.status_string(999) == "unknown status code"
+
+
+def test_ring_bytes(lib):
+    d = bd.mamba2_desc(256, 128, 64, 128, 8, 16)
+    assert bd.rssm_mamba2_ring_bytes(d) == [256 * 128 * 16 * 64 * 2] * 2 + [256 * 8 * 16 * 128 * 2] * 2 + [256 * 128 * 16 * 4]
+    g = bd.gdn_desc(256, 32, 128, 128, 16)
+    assert bd.rssm_gdn_ring_bytes(g) == [256 * 32 * 16 * 128 * 2] * 3 + [256 * 32 * 16 * 4] * 2
+
+
+ALIGNED = 1 << 20  # a fake, 16-byte aligned address: never dereferenced because validation fails first
+ARGS9 = [ALIGNED] * 9  # cursors, x, z, B, C, dt, A, D, y
+
+
+@pytest.mark.parametrize("desc", [
+    (4, 8, 64, 128, 3, 16),    # H % G != 0
+    (4, 8, 60, 128, 1, 16),    # headdim not a multiple of 8
+    (4, 8, 64, 264, 1, 16),    # dstate > 256
+    (4, 8, 64, 128, 1, 0),     # L < 1
+    (4, 8, 64, 128, 1, 33),    # L > 32
+    (-1, 8, 64, 128, 1, 16),   # negative batch
+    (4, 8, 64, 128, 1, 16, 7),  # bad out_dtype
+])
+def test_mamba2_desc_validation(lib, desc):
+    d = bd.mamba2_desc(*desc)
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, None, ctypes.byref(ring), *ARGS9, None, None) == \
+        bd.RSSM_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_noop(lib):
+    d = bd.mamba2_desc(0, 8, 64, 128, 1, 16)
+    assert lib.rssm_mamba2_step(ctypes.byref(d), None, None, None, *([None] * 9), None, None) == bd.RSSM_OK
+    assert lib.rssm_mamba2_flush(ctypes.byref(d), None, None, None, None, None, None, None) == bd.RSSM_OK
+    assert lib.rssm_mamba2_conventional_step(ctypes.byref(d), *([None] * 9), None) == bd.RSSM_OK
+
+
+def test_mamba2_pointer_checks(lib):
+    d = bd.mamba2_desc(4, 8, 64, 128, 1, 16)
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    rb = ctypes.byref(ring)
+    assert lib.rssm_mamba2_step(ctypes.byref(d), None, None, rb, *ARGS9, None, None) == bd.RSSM_ERR_INVALID_ARG
+    bad = list(ARGS9)
+    bad[-1] = ALIGNED + 4  # misaligned y
+    assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, None, rb, *bad, None, None) == bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, ALIGNED + 2, rb, *ARGS9, None, None) == bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, None, rb, *ARGS9, ALIGNED + 8, None) == bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, None, None, *ARGS9, None, None) == bd.RSSM_ERR_INVALID_ARG
+    ring0 = bd.rssm_mamba2_ring(ALIGNED, ALIGNED, None, ALIGNED, ALIGNED)
+    assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, None, ctypes.byref(ring0), *ARGS9, None, None) == \
+        bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_mamba2_step(None, ALIGNED, None, rb, *ARGS9, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_mamba2_conventional_step(ctypes.byref(d), ALIGNED, *([ALIGNED] * 7), ALIGNED + 4, None) == \
+        bd.RSSM_ERR_MISALIGNED
+
+
+def test_verify_n_new_range(lib):
+    d = bd.mamba2_desc(4, 8, 64, 128, 1, 16)
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    for n_new in (0, 17, -1):
+        rc = lib.rssm_mamba2_spec_verify(ctypes.byref(d), n_new, ALIGNED, None, ctypes.byref(ring), *ARGS9,
+                                         None, None)
+        assert rc == bd.RSSM_ERR_INVALID_ARG
+
+
+def test_cursor_call_validation(lib):
+    assert lib.rssm_commit_cursors(ALIGNED, ALIGNED, 4, 0, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_commit_cursors(ALIGNED, ALIGNED, 4, 33, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_commit_cursors(ALIGNED, None, 4, 16, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_commit_cursors(ALIGNED + 4, ALIGNED, 4, 16, None, None) == bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_commit_cursors(None, None, 0, 16, None, None) == bd.RSSM_OK
+    assert lib.rssm_reset_cursors(None, None, 0, 4, None, None) == bd.RSSM_OK
+    assert lib.rssm_reset_cursors(ALIGNED, None, 2, 4, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_reset_cursors(ALIGNED, ALIGNED, -1, 4, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_checkpoint_downcast(None, None, 0, None) == bd.RSSM_OK
+    assert lib.rssm_checkpoint_downcast(ALIGNED, ALIGNED + 2, 8, None) == bd.RSSM_ERR_MISALIGNED
+
+
+def test_gdn_validation(lib):
+    ring = bd.rssm_gdn_ring(*([ALIGNED] * 5))
+    for desc in ((4, 2, 60, 128, 16), (4, 2, 128, 512, 16), (4, 0, 128, 128, 16), (4, 2, 128, 128, 40)):
+        d = bd.gdn_desc(*desc)
+        assert lib.rssm_gdn_step(ctypes.byref(d), ALIGNED, ctypes.byref(ring), *([ALIGNED] * 7), None, None) == \
+            bd.RSSM_ERR_INVALID_ARG
+    d = bd.gdn_desc(4, 2, 128, 128, 16)
+    assert lib.rssm_gdn_step(ctypes.byref(d), ALIGNED + 4, ctypes.byref(ring), *([ALIGNED] * 7), None, None) == \
+        bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_gdn_flush(ctypes.byref(d), ALIGNED, None, ALIGNED, None, None) == bd.RSSM_ERR_INVALID_ARG
+    d0 = bd.gdn_desc(0, 2, 128, 128, 16)
+    assert lib.rssm_gdn_flush(ctypes.byref(d0), None, None, None, None, None) == bd.RSSM_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(bd, "_lib", None)
+    monkeypatch.setattr(bd, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        bd.load()

@@ -1,0 +1,109 @@
+"""Gated DeltaNet parity on the GPU, through the C ABI, against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+from oracle import gdn as og
+from oracle import sessions
+from recurrent_state_decode_gb300 import binding as bd
+from recurrent_state_decode_gb300 import inputs as I
+from recurrent_state_decode_gb300.inputs import GDNWorkload as GW
+
+pytestmark = pytest.mark.gpu
+
+TOL_Y32, TOL_CKPT, TOL_BF16_EXCESS = 1e-4, 1e-5, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from recurrent_state_decode_gb300 import build
+    build.build()
+    bd.load()
+
+
+def run_gdn(w, out_dtype=bd.RSSM_F32, seqs=None, steps=None):
+    dev = "cuda"
+    st, pre, starts, counts = H.gdn_setup(w, dev, out_dtype)
+    seqs = list(range(w.batch)) if seqs is None else list(seqs)
+    feed = H.Feed()
+    sess = sessions.gdn_ar_session(H.F64(st.S[seqs]), H.sub(pre, seqs), starts[seqs].cpu().numpy(),
+                                   counts[seqs].cpu().numpy(), feed, w.buf_len)
+    o = st.new_output()
+    flushes = 0
+    for t in range(w.steps if steps is None else steps):
+        rec = I.gdn_step_inputs(w, t, dev)
+        feed.rec = H.sub(rec, seqs)
+        st.step(rec, o)
+        exp = next(sess)
+        og_ = H.F64(o[seqs])
+        if out_dtype == bd.RSSM_F32:
+            err = H.rel_l2(og_, exp["o"])
+            assert err <= TOL_Y32, (t, err)
+        else:
+            ex = H.bf16_excess(og_, exp["o"])
+            assert ex <= TOL_BF16_EXCESS, (t, ex)
+        np.testing.assert_array_equal(st.cursors[seqs].cpu().numpy(), exp["cursors"])
+        for i, b in enumerate(seqs):
+            if exp["flushed"][i]:
+                flushes += 1
+                e = H.rel_l2(H.F64(st.S[b]), exp["state"][i])
+                assert e <= TOL_CKPT, (t, b, e)
+    assert H.status(st) == 0
+    return flushes
+
+
+GSHAPES = [
+    GW("gdn_small", 3, 2, 64, 64, 16, 40, seed=71),
+    GW("gdn_ragged", 3, 3, 40, 24, 5, 17, seed=72),          # dk, dv off the chunk sizes
+    GW("gdn_L1", 2, 2, 32, 32, 1, 5, seed=73),
+    GW("gdn_L32", 2, 2, 32, 48, 32, 70, seed=74),
+    GW("gdn_big_tile", 2, 1, 256, 256, 4, 9, seed=75),       # 4 row blocks, 16 chunks per thread
+    GW("gdn_128", 2, 4, 128, 128, 16, 34, seed=76),          # the serving tile
+]
+
+
+@pytest.mark.parametrize("w", GSHAPES, ids=lambda w: w.name)
+@pytest.mark.parametrize("out", [bd.RSSM_F32, bd.RSSM_BF16], ids=["f32", "bf16"])
+def test_gdn_shapes(w, out):
+    run_gdn(w, out)
+
+
+def test_gdn_conventional_kernel():
+    w = GW("gconv", 3, 3, 40, 24, 16, 20, seed=77)
+    dev = "cuda"
+    S = I.gdn_checkpoint(w, dev)
+    Sh = H.F64(S)
+    o = torch.empty((w.batch, w.nheads, w.dv), device=dev)
+    desc = bd.gdn_desc(w.batch, w.nheads, w.dk, w.dv, w.buf_len)
+    for t in range(w.steps):
+        rec = I.gdn_step_inputs(w, t, dev)
+        bd.check(bd.rssm_gdn_conventional_step(desc, S, rec["q"], rec["k"], rec["v"], rec["g"], rec["beta"], o))
+        r = {k: H.F64(v) for k, v in rec.items()}
+        Sh, oe = og.conventional_step(Sh, r["q"], r["k"], r["v"], r["g"], r["beta"])
+        assert H.rel_l2(H.F64(o), oe) <= TOL_Y32
+        assert H.rel_l2(H.F64(S), Sh) <= TOL_CKPT
+
+
+def test_gdn_standalone_flush():
+    w = GW("gflush", 3, 2, 32, 40, 8, 5, seed=78)
+    dev = "cuda"
+    st, pre, starts, counts = H.gdn_setup(w, dev)
+    feed = H.Feed()
+    sess = sessions.gdn_ar_session(H.F64(st.S), H.sub(pre, slice(None)), starts.cpu().numpy(), counts.cpu().numpy(),
+                                   feed, w.buf_len)
+    o = st.new_output()
+    for t in range(w.steps):
+        rec = I.gdn_step_inputs(w, t, dev)
+        feed.rec = H.sub(rec, slice(None))
+        st.step(rec, o)
+        exp = next(sess)
+    before = st.cursors.cpu().numpy()
+    st.flush()
+    cur = st.cursors.cpu().numpy()
+    np.testing.assert_array_equal(cur[:, 0], (before[:, 0] + before[:, 1]) % w.buf_len)
+    np.testing.assert_array_equal(cur[:, 1:], 0)
+    for b in range(w.batch):
+        assert H.rel_l2(H.F64(st.S[b]), exp["state"][b]) <= TOL_CKPT
+    assert H.status(st) == 0
