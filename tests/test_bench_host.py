@@ -1,0 +1,68 @@
+"""CPU tests of bench.py's host logic: multi-rank coordination over gloo
+(world size 2, replicas: max/sum over ranks, rank-0 output only) and the
+algorithmic bytes model."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from recurrent_state_decode_gb300 import bytes_model as bm
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "WORLD_SIZE": str(world),
+                       "RANK": str(rank), "LOCAL_RANK": str(rank)})
+    d = bench.Dist()
+    try:
+        d.barrier()
+        q.put((rank, d.max(10.0 + rank), d.sum(1.0 + rank)))
+    finally:
+        d.close()
+
+
+def test_dist_max_sum_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 11.0, 3.0), (1, 11.0, 3.0)]
+
+
+def test_reference_arm_other_ranks_exit(monkeypatch):
+    class Fake:
+        rank = 1
+    assert bench.run_reference(bench.parse(["--impl", "reference"]), Fake()) is None
+
+
+def test_bytes_model_serving_cycle():
+    """Average over a full L-cycle of staggered windows at the serving shape:
+    4 MiB read every step, 4 MiB written on 1 step in 16, 2 x 37,376 B of
+    record in + append on the 15 non-flush steps (one read on the flush),
+    7.5 window records of 18,944 B on average, 16,384 B of bf16 y, 32 B of cursor."""
+    H, P, N, G, L = 128, 64, 128, 8, 16
+    per_seq = sum(bm.mamba2_step_bytes(H, P, N, G, L, [c]) for c in range(L)) / L
+    expect = 4194304 + 4194304 / 16 + (15 * 2 * 37376 + 37376) / 16 + 7.5 * 18944 + 16384 + 32
+    assert per_seq == pytest.approx(expect)
+    conv = bm.mamba2_conventional_bytes(H, P, N, G, 1)
+    assert conv == 2 * 4194304 + 37376 + 16384
+    # GDN serving shape: 2 MiB state per sequence
+    g = sum(bm.gdn_step_bytes(32, 128, 128, 16, [c]) for c in range(16)) / 16
+    rec = 32 * (2 * 256 + 256 + 8)
+    past = 32 * (256 + 256 + 8)
+    assert g == pytest.approx(2097152 * 17 / 16 + (15 * 2 * rec + rec) / 16 + 7.5 * past + 32 * 128 * 2 + 32)
