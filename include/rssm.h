@@ -105,7 +105,8 @@ typedef struct {
   rssm_bf16* z;  /* [batch, nheads, buf_len, headdim] */
   rssm_bf16* B;  /* [batch, ngroups, buf_len, dstate] */
   rssm_bf16* C;  /* [batch, ngroups, buf_len, dstate] */
-  float* dt;     /* [batch, nheads, buf_len] */
+  float* dt;     /* [batch, nheads, Lp], Lp = buf_len rounded up to a
+                    multiple of 4 (slots >= buf_len unused) */
 } rssm_mamba2_ring;
 
 /* Bytes of each ring field, in the order x, z, B, C, dt. Returns RSSM_OK or
@@ -221,8 +222,8 @@ typedef struct {
   rssm_bf16* q;  /* [batch, nheads, buf_len, dk] */
   rssm_bf16* k;  /* [batch, nheads, buf_len, dk] */
   rssm_bf16* v;  /* [batch, nheads, buf_len, dv] */
-  float* g;      /* [batch, nheads, buf_len] */
-  float* beta;   /* [batch, nheads, buf_len] */
+  float* g;      /* [batch, nheads, Lp], Lp as in rssm_mamba2_ring.dt */
+  float* beta;   /* [batch, nheads, Lp] */
 } rssm_gdn_ring;
 
 /* Bytes of each ring field, in the order q, k, v, g, beta. */

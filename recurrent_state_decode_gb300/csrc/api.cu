@@ -112,7 +112,7 @@ int rssm_mamba2_ring_bytes(const rssm_mamba2_desc* d, size_t bytes[5]) {
   const size_t Bt = d->batch, H = d->nheads, L = d->buf_len, G = d->ngroups;
   bytes[0] = bytes[1] = Bt * H * L * d->headdim * 2;
   bytes[2] = bytes[3] = Bt * G * L * d->dstate * 2;
-  bytes[4] = Bt * H * L * 4;
+  bytes[4] = Bt * H * pad4(d->buf_len) * 4;
   return RSSM_OK;
 }
 
@@ -123,7 +123,7 @@ int rssm_gdn_ring_bytes(const rssm_gdn_desc* d, size_t bytes[5]) {
   const size_t Bt = d->batch, H = d->nheads, L = d->buf_len;
   bytes[0] = bytes[1] = Bt * H * L * d->dk * 2;
   bytes[2] = Bt * H * L * d->dv * 2;
-  bytes[3] = bytes[4] = Bt * H * L * 4;
+  bytes[3] = bytes[4] = Bt * H * pad4(d->buf_len) * 4;
   return RSSM_OK;
 }
 

@@ -99,6 +99,31 @@ __device__ __forceinline__ void reduce8(float (&v)[8], int lane) {
   v[0] += __shfl_xor_sync(FULL, v[0], 1);
 }
 
+// Sum V per-lane partials p[0..V) (V = 8, 16 or 32) over the warp by a
+// transposed butterfly: V-1 shuffles in all instead of 5V. Afterwards p[0] of
+// lane l holds the total of partial index idx(l): for V = 32, idx(l) = l; for
+// V = 16, idx(l) = l >> 1; for V = 8, idx(l) = reduce8_row(l).
+template <int V>
+__device__ __forceinline__ float reduce_transpose(float (&p)[V], int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 5; lvl++) {
+    const int off = 16 >> lvl;
+    const int n = V >> lvl;  // partials still held before this level
+    if (n > 1) {
+      const bool hi = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; i++) {
+        const float send = hi ? p[i] : p[i + n / 2];
+        const float keep = hi ? p[i + n / 2] : p[i];
+        p[i] = keep + __shfl_xor_sync(FULL, send, off);
+      }
+    } else {
+      p[0] += __shfl_xor_sync(FULL, p[0], off);
+    }
+  }
+  return p[0];
+}
+
 // ---------------------------------------------------------------- status
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
@@ -138,6 +163,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {

@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
   if (tid < m) {
     const bool ring = tid < count;
     const size_t slot = bh * L + (start + tid) % L;
-    s.sg[tid] = ring ? a.rg[slot] : a.g[bh];
-    s.sb[tid] = ring ? a.rbeta[slot] : a.beta[bh];
+    const size_t sslot = bh * pad4(L) + (start + tid) % L;
+    s.sg[tid] = ring ? a.rg[sslot] : a.g[bh];
+    s.sb[tid] = ring ? a.rbeta[sslot] : a.beta[bh];
   }
   if (!FLUSH_ONLY && !flush) {  // append the current record
     const size_t slot = bh * L + (start + count) % L;
@@ -220,8 +221,9 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
         *reinterpret_cast<uint4*>(a.rq + slot * DK + i * 8) = *reinterpret_cast<const uint4*>(a.q + bh * DK + i * 8);
       }
       if (tid == 0) {
-        a.rg[slot] = a.g[bh];
-        a.rbeta[slot] = a.beta[bh];
+        const size_t sslot = bh * pad4(L) + (start + count) % L;
+        a.rg[sslot] = a.g[bh];
+        a.rbeta[sslot] = a.beta[bh];
       }
     }
   }

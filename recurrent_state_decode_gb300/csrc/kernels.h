@@ -26,6 +26,8 @@ struct M2Args {
 enum { M2_CONVENTIONAL = 0, M2_STEP = 1, M2_FLUSH = 2, M2_VERIFY = 3 };
 
 cudaError_t m2_launch(int kind, const M2Args& a, int out_bf16, cudaStream_t st);
+// The persistent, warp-specialised AR step (mamba2_step.cu).
+cudaError_t m2_step_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 size_t m2_smem_bytes(int kind, const M2Args& a);
 
 // Gated DeltaNet launch arguments.
@@ -53,6 +55,10 @@ cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int b
 cudaError_t reset_launch(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* status,
                          cudaStream_t st);
 cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, cudaStream_t st);
+
+// Row stride of the per-record scalar rings (dt; g, beta): L rounded up to a
+// multiple of 4 slots, so that a row is a whole number of 16-byte units.
+inline __host__ __device__ int pad4(int L) { return (L + 3) & ~3; }
 
 // Rows per block for a tile of `rows` x `cols` fp32 elements: at most 32 KiB of
 // tile per block, a multiple of 8 rows.

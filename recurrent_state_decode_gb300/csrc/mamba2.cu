@@ -1,6 +1,6 @@
 // Mamba-2 decode kernels for sm_103a: the conventional read-modify-write step
-// (comparison point), the ReplaySSM AR step with the flush fused into its
-// L-th step, the standalone flush, and the speculative verify.
+// (comparison point), the standalone flush and the speculative verify. The
+// AR step with its fused flush lives in mamba2_step.cu.
 //
 // Work unit: one CTA of 128 threads per (sequence b, head h, row block) of the
 // [headdim, dstate] state tile; a row block holds PB rows (PB*dstate*4 <= 32
@@ -269,130 +269,6 @@ __global__ void __launch_bounds__(128) m2_conventional_kernel(M2Args a) {
   }
 }
 
-// ------------------------------------------------------------------ ReplaySSM AR step
-
-template <int NCH, bool OUT_BF16>
-__global__ void __launch_bounds__(128) m2_step_kernel(M2Args a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int blk = blockIdx.x;
-  const int pb = blk % a.nPB;
-  blk /= a.nPB;
-  const int h = blk % a.H, b = blk / a.H;
-  const int g = (h * a.G) / a.H;
-  const int L = a.L, N = a.N, P = a.P, PB = a.PB, H = a.H;
-  const int p0 = pb * PB, R = min(PB, P - p0);
-  const size_t bh = (size_t)b * H + h, bg = (size_t)b * a.G + g;
-
-  const int4 cur = load_cursor(a.cursors, b);
-  const int start = cur.x, count = cur.y;
-  if (start < 0 || start >= L || count < 0 || count >= L || cur.z != 0) return;  // reported by the cursor kernel
-  const int m = count + 1;
-  const bool flush = (m == L);
-  const bool rd16 = (a.ckpt_read != nullptr) && !flush;
-
-  M2Smem s;
-  m2_smem_layout(PB, N, L, L, 1, smem_raw, &s);
-  init_bars(s);
-  const size_t tile_off = (bh * P + p0) * N;
-  if (tid == 0) {
-    const char* src = rd16 ? (const char*)(a.ckpt_read + tile_off) : (const char*)(a.ckpt + tile_off);
-    issue_tile(s, src, R, N, rd16 ? 2 : 4);
-  }
-
-  // window records: k < count from ring slot (start + k) mod L, k == count is the input
-  if (tid < m) s.sdt[tid] = (tid < count) ? a.rdt[bh * L + (start + tid) % L] : a.dt[bh];
-  const int xv = R >> 3;
-  for (int i = tid; i < m * xv; i += 128) {
-    const int k = i / xv, v = i - k * xv;
-    const uint16_t* src = (k < count) ? a.rx + (bh * L + (start + k) % L) * P + p0 + v * 8 : a.x + bh * P + p0 + v * 8;
-    bf8_to_smem(s.xs + (size_t)k * PB + v * 8, src);
-  }
-  float4 cm[NCH];
-#pragma unroll
-  for (int j = 0; j < NCH; j++) {
-    const int c = lane + 32 * j;
-    cm[j] = (c * 4 < N) ? load_bf4(a.C + bg * N + c * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int k = warp; k < m; k += 4) {
-    const uint16_t* Bk = (k < count) ? a.rB + (bg * L + (start + k) % L) * N : a.B + bg * N;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < NCH; j++) {
-      const int c = lane + 32 * j;
-      if (c * 4 < N) {
-        const float4 bv = load_bf4(Bk + c * 4);
-        acc += dot4(bv, cm[j]);
-        if (flush) reinterpret_cast<float4*>(s.Bs + (size_t)k * N)[c] = bv;
-      }
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) s.sc[k] = acc;
-  }
-  if (!flush) {  // append the record; the flush folds it instead
-    const int slot = (start + count) % L;
-    for (int i = tid; i < xv; i += 128) {
-      copy8(a.rx + (bh * L + slot) * P + p0 + i * 8, a.x + bh * P + p0 + i * 8);
-      copy8(a.rz + (bh * L + slot) * P + p0 + i * 8, a.z + bh * P + p0 + i * 8);
-    }
-    if (pb == 0) {
-      if (tid == 0) a.rdt[bh * L + slot] = a.dt[bh];
-      if (h == g * (H / a.G)) {  // first head of the group stores the group rows
-        for (int i = tid; i < (N >> 3); i += 128) {
-          copy8(a.rB + (bg * L + slot) * N + i * 8, a.B + bg * N + i * 8);
-          copy8(a.rC + (bg * L + slot) * N + i * 8, a.C + bg * N + i * 8);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) window_weights(s.sdt, m, a.A[h], lane, s.sw, s.sc, s.scoef, &s.sP[0]);
-  __syncthreads();
-  for (int r = tid; r < R; r += 128) {
-    float acc = 0.f;
-    for (int k = 0; k < m; k++) acc = fmaf(s.scoef[k], s.xs[(size_t)k * PB + r], acc);
-    s.xsum[r] = acc;
-  }
-  if (flush) {
-    __syncthreads();
-    for (int i = tid; i < m * R; i += 128) {
-      const int k = i / R, r = i - k * R;
-      s.xs[(size_t)k * PB + r] *= s.sw[k];
-    }
-  }
-  __syncthreads();
-
-  const float Pm = s.sP[0], Dh = a.D[h];
-  int r0w, r1w;
-  warp_rows(R, warp, r0w, r1w);
-  if (r1w <= r0w) return;
-  if (!mbar_wait_or_report(&s.bars[warp], 0, a.status)) return;
-  for (int r0 = r0w; r0 < r1w; r0 += 8) {
-    float4 hv[8][NCH];
-    float v[8];
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++) {
-      v[rr] = 0.f;
-#pragma unroll
-      for (int j = 0; j < NCH; j++) {
-        const int c = lane + 32 * j;
-        hv[rr][j] = (c * 4 < N) ? tile_chunk<NCH>(s, rd16, r0 + rr, N, c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[rr] += dot4(hv[rr][j], cm[j]);
-      }
-    }
-    reduce8(v, lane);
-    if ((lane & 3) == 0) {
-      const int r = r0 + reduce8_row(lane);
-      const size_t oi = bh * P + p0 + r;
-      const float xm = bf_to_f(a.x[oi]), zm = bf_to_f(a.z[oi]);
-      store_out<OUT_BF16>(a.y, oi, (Pm * v[0] + s.xsum[r] + Dh * xm) * silu(zm));
-    }
-    if (flush)
-      fold_group<NCH>(hv, s, r0, PB, N, m, Pm, lane, a.ckpt + tile_off,
-                      a.ckpt_read ? a.ckpt_read + tile_off : nullptr, nullptr);
-  }
-}
-
 // ------------------------------------------------------------------ standalone flush
 
 template <int NCH>
@@ -418,7 +294,7 @@ __global__ void __launch_bounds__(128) m2_flush_kernel(M2Args a) {
   const size_t tile_off = (bh * P + p0) * N;
   if (tid == 0) issue_tile(s, (const char*)(a.ckpt + tile_off), R, N, 4);
 
-  if (tid < m) s.sdt[tid] = a.rdt[bh * L + (start + tid) % L];
+  if (tid < m) s.sdt[tid] = a.rdt[bh * pad4(L) + (start + tid) % L];
   const int xv = R >> 3;
   for (int i = tid; i < m * xv; i += 128) {
     const int k = i / xv, v = i - k * xv;
@@ -493,7 +369,7 @@ __global__ void __launch_bounds__(128) m2_verify_kernel(M2Args a) {
 
   // new record i of this sequence: x/z at ((b*K + i)*H + h)*P, B/C at ((b*K + i)*G + g)*N
   for (int k = tid; k < W; k += 128)
-    s.sdt[k] = (k < count) ? a.rdt[bh * L + (start + k) % L] : a.dt[((size_t)b * K + (k - count)) * H + h];
+    s.sdt[k] = (k < count) ? a.rdt[bh * pad4(L) + (start + k) % L] : a.dt[((size_t)b * K + (k - count)) * H + h];
   const int xv = R >> 3;
   for (int i = tid; i < W * xv; i += 128) {
     const int k = i / xv, v = i - k * xv;
@@ -630,7 +506,7 @@ __global__ void __launch_bounds__(128) m2_verify_epilogue_kernel(M2Args a) {
   for (int q = tid; q < K * H; q += 128) {
     const int i = q / H, h = q - i * H;
     const int slot = (start + count + i) % L;
-    a.rdt[((size_t)b * H + h) * L + slot] = a.dt[((size_t)b * K + i) * H + h];
+    a.rdt[((size_t)b * H + h) * pad4(L) + slot] = a.dt[((size_t)b * K + i) * H + h];
   }
   if (tid == 0) {
     int4 nc = cur;
@@ -689,11 +565,7 @@ cudaError_t m2_launch(int kind, const M2Args& a, int out_bf16, cudaStream_t st) 
       })
       return e;
     case M2_STEP:
-      RSSM_DISPATCH_NCH(NCH, {
-        e = out_bf16 ? launch(m2_step_kernel<NCH, true>, grid, smem, st, a)
-                     : launch(m2_step_kernel<NCH, false>, grid, smem, st, a);
-      })
-      return e;
+      return m2_step_launch(a, out_bf16, st);
     case M2_FLUSH:
       RSSM_DISPATCH_NCH(NCH, { e = launch(m2_flush_kernel<NCH>, grid, smem, st, a); })
       return e;

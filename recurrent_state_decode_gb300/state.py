@@ -26,7 +26,7 @@ class Mamba2State:
         self.rz = torch.zeros_like(self.rx)
         self.rB = torch.zeros((batch, ngroups, buf_len, dstate), dtype=torch.bfloat16, device=dev)
         self.rC = torch.zeros_like(self.rB)
-        self.rdt = torch.zeros((batch, nheads, buf_len), dtype=torch.float32, device=dev)
+        self.rdt = torch.zeros((batch, nheads, (buf_len + 3) // 4 * 4), dtype=torch.float32, device=dev)
         self.ring = bd.mamba2_ring(self.rx, self.rz, self.rB, self.rC, self.rdt)
         self.cursors = torch.zeros((batch, 4), dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -79,7 +79,7 @@ class GDNState:
         self.rq = torch.zeros((batch, nheads, buf_len, dk), dtype=torch.bfloat16, device=dev)
         self.rk = torch.zeros_like(self.rq)
         self.rv = torch.zeros((batch, nheads, buf_len, dv), dtype=torch.bfloat16, device=dev)
-        self.rg = torch.zeros((batch, nheads, buf_len), dtype=torch.float32, device=dev)
+        self.rg = torch.zeros((batch, nheads, (buf_len + 3) // 4 * 4), dtype=torch.float32, device=dev)
         self.rbeta = torch.zeros_like(self.rg)
         self.ring = bd.gdn_ring(self.rq, self.rk, self.rv, self.rg, self.rbeta)
         self.cursors = torch.zeros((batch, 4), dtype=torch.int32, device=dev)
