@@ -175,7 +175,7 @@ def profiled_traffic(profile_file, kernel_sources):
         return None
 
 
-KERNEL_SOURCES = ["recurrent_state_decode_gb300/csrc/mamba2.cu", "recurrent_state_decode_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["recurrent_state_decode_gb300/csrc/mamba2_step.cu", "recurrent_state_decode_gb300/csrc/common.cuh"]
 
 
 # ----------------------------------------------------------------------------- oracle (CPU baseline / reference arm)
@@ -327,6 +327,46 @@ def bench_mamba2_ar(args, dist):
     achieved_gbs = (alg_bytes / K) / (mean_call_ms * 1e-3) / 1e9
 
     # --- conventional comparator over the same steps
+    conv_us, conv_gbs = time_mamba2_conventional(st, A, D, recs, W_, K, stream, dist, w, out_bytes)
+
+    # --- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_mamba2(st, A, D, w, dev, K, W_, y.dtype)
+        e2e["value"] = dist.max(e2e["value"])
+    del recs, st
+    torch.cuda.empty_cache()
+
+    peak, peak_kind = measured_peak()
+    tokens = dist.sum(w.batch * K) / (dist.max(total_ms) * 1e-3)
+    res = {
+        "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": W_,
+        "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
+        "tokens_per_s": tokens,
+        "hbm_gbs": achieved_gbs,
+        "conventional_us_per_step": conv_us,
+        "conventional_hbm_gbs": conv_gbs,
+        "speedup_vs_conventional": conv_us / us_step,
+        "algorithmic_bytes_per_step": alg_bytes / K,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "peak_source": peak_kind,
+                     "traffic": profiled_traffic("mamba2_step_serving.txt", KERNEL_SOURCES),
+                     "kernel": "m2_step_kernel (+ cursor advance, timed per call)"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if args.workload == "mamba2_serving" and dist.world == 1:
+        res["workloads"] = other_workloads(args, dev, out, out_bytes, min(K, 256), W_, dist, stream)
+    return res
+
+
+def time_mamba2_conventional(st, A, D, recs, W_, K, stream, dist, w, out_bytes):
+    import torch
+
+    from recurrent_state_decode_gb300 import binding as bd
+    from recurrent_state_decode_gb300 import bytes_model as bm
     state = st.ckpt.clone()
     yc = st.new_output()
     desc = st.desc
@@ -343,33 +383,110 @@ def bench_mamba2_ar(args, dist):
     conv_us = dist.max(conv_ms * 1e3 / K)
     conv_bytes = bm.mamba2_conventional_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.batch, out_bytes)
     del state
+    return conv_us, conv_bytes / (conv_us * 1e-6) / 1e9
 
-    # --- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    e2e = None
-    if not args.no_e2e:
-        e2e = e2e_mamba2(st, A, D, w, dev, K, W_, y.dtype)
-        e2e["value"] = dist.max(e2e["value"])
 
-    peak, peak_kind = measured_peak()
-    tokens = dist.sum(w.batch * K) / (dist.max(total_ms) * 1e-3)
-    res = {
-        "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": W_,
-        "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
-        "tokens_per_s": tokens,
-        "hbm_gbs": achieved_gbs,
-        "conventional_us_per_step": conv_us,
-        "conventional_hbm_gbs": conv_bytes / (conv_us * 1e-6) / 1e9,
-        "speedup_vs_conventional": conv_us / us_step,
-        "algorithmic_bytes_per_step": alg_bytes / K,
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": achieved_gbs / peak, "peak_source": peak_kind,
-                     "traffic": profiled_traffic("mamba2_step_serving.txt", KERNEL_SOURCES),
-                     "kernel": "m2_step_kernel (+ cursor advance, timed per call)"},
-        "gpu_launches": launches_per_step * K,
-        "clocks": clk,
-        "e2e": e2e,
-    }
+def other_workloads(args, dev, out, out_bytes, K, W_, dist, stream):
+    """The other hot-path workloads, each timed like the main one on K steps."""
+    import torch
+
+    from recurrent_state_decode_gb300 import binding as bd
+    from recurrent_state_decode_gb300 import bytes_model as bm
+    from recurrent_state_decode_gb300 import inputs as I
+    from recurrent_state_decode_gb300.state import gdn_from_workload, mamba2_from_workload
+    peak, _ = measured_peak()
+    res = {}
+
+    # bf16 read copy of the checkpoint (non-flush steps read 2 bytes per state element)
+    w = I.WORKLOADS["mamba2_bf16_read"]
+    st, A, D, _, _, counts0 = mamba2_from_workload(w, dev, out)
+    recs = [I.mamba2_step_inputs(w, t, dev) for t in range(W_ + K)]
+    y = st.new_output()
+    for t in range(W_):
+        st.step(recs[t], A, D, y)
+    torch.cuda.synchronize()
+    ms, _ = time_calls(lambda i: st.step(recs[W_ + i], A, D, y), K, stream)
+    bd.check(int(st.status.item()), "device status")
+    c0 = counts0.cpu().tolist()
+    nbytes = sum(bm.mamba2_step_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len,
+                                      [(c + W_ + i) % w.buf_len for c in c0], True, out_bytes) for i in range(K)) / K
+    us = ms * 1e3 / K
+    res[w.name] = {"us_per_step": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
+                   "frac": nbytes / (us * 1e-6) / 1e9 / peak, "algorithmic_bytes_per_step": nbytes, "steps": K}
+    del st, recs
+    torch.cuda.empty_cache()
+
+    # speculative verify + commit, K = T + 1 records per sequence per step
+    w = I.WORKLOADS["mamba2_spec"]
+    st, A, D, _, _, counts0 = mamba2_from_workload(w, dev, out)
+    recs = [I.mamba2_verify_inputs(w, t, dev) for t in range(W_ + K)]
+    kepts = [I.accepted_kept(w, t, dev) for t in range(W_ + K)]
+    y = st.new_output(w.n_new)
+
+    def spec(i):
+        st.verify(recs[i], A, D, y)
+        st.commit(kepts[i])
+
+    for t in range(W_):
+        spec(t)
+    torch.cuda.synchronize()
+    ms, _ = time_calls(lambda i: spec(W_ + i), K, stream)
+    bd.check(int(st.status.item()), "device status")
+    # cursor trace on the host for the bytes model (fold when count + K > L)
+    counts = counts0.cpu().tolist()
+    kl = [k.cpu().tolist() for k in kepts]
+    nbytes = 0
+    accepted = 0
+    for t in range(W_ + K):
+        if t >= W_:
+            nbytes += bm.mamba2_verify_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len, w.n_new, counts,
+                                             False, out_bytes)
+            accepted += sum(kl[t])
+        counts = [(0 if c + w.n_new > w.buf_len else c) + k for c, k in zip(counts, kl[t])]
+    nbytes /= K
+    us = ms * 1e3 / K
+    tile32 = w.nheads * w.headdim * w.dstate * 4
+    conv_spec_bytes = w.batch * tile32 * (1 + w.drafts)  # one state read + T snapshot writes per verify
+    res[w.name] = {"us_per_step": us, "accepted_tokens_per_s": accepted / (ms * 1e-3),
+                   "hbm_gbs": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                   "algorithmic_bytes_per_step": nbytes,
+                   "conventional_snapshot_bytes_per_step": conv_spec_bytes,
+                   "bytes_ratio_vs_snapshot_spec": conv_spec_bytes / nbytes, "steps": K}
+    del st, recs, kepts
+    torch.cuda.empty_cache()
+
+    # Gated DeltaNet AR step vs its conventional kernel
+    w = I.WORKLOADS["gdn_serving"]
+    st, _, _, counts0 = gdn_from_workload(w, dev, out)
+    recs = [I.gdn_step_inputs(w, t, dev) for t in range(W_ + K)]
+    o = st.new_output()
+    for t in range(W_):
+        st.step(recs[t], o)
+    torch.cuda.synchronize()
+    ms, _ = time_calls(lambda i: st.step(recs[W_ + i], o), K, stream)
+    bd.check(int(st.status.item()), "device status")
+    c0 = counts0.cpu().tolist()
+    nbytes = sum(bm.gdn_step_bytes(w.nheads, w.dk, w.dv, w.buf_len, [(c + W_ + i) % w.buf_len for c in c0],
+                                   out_bytes) for i in range(K)) / K
+    us = ms * 1e3 / K
+    S = st.S.clone()
+    oc = st.new_output()
+
+    def conv(i):
+        r = recs[W_ + i]
+        bd.check(bd.rssm_gdn_conventional_step(st.desc, S, r["q"], r["k"], r["v"], r["g"], r["beta"], oc))
+
+    conv(0)
+    torch.cuda.synchronize()
+    cms, _ = time_calls(conv, K, stream)
+    cus = cms * 1e3 / K
+    cbytes = bm.gdn_conventional_bytes(w.nheads, w.dk, w.dv, w.batch, out_bytes)
+    res[w.name] = {"us_per_step": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                   "algorithmic_bytes_per_step": nbytes, "conventional_us_per_step": cus,
+                   "conventional_hbm_gbs": cbytes / (cus * 1e-6) / 1e9, "speedup_vs_conventional": cus / us,
+                   "steps": K}
+    del st, recs, S
+    torch.cuda.empty_cache()
     return res
 
 
@@ -426,6 +543,34 @@ def e2e_mamba2(st, A, D, w, dev, K, W_, y_dtype):
                    "rssm_mamba2_step, D2H of y; two copy streams overlap the copies with compute"}
 
 
+def profile_other(args, dist):
+    """A few calls of the speculative or GDN workload, untimed (for ncu)."""
+    import torch
+
+    from recurrent_state_decode_gb300 import binding as bd
+    from recurrent_state_decode_gb300 import inputs as I
+    from recurrent_state_decode_gb300.state import gdn_from_workload, mamba2_from_workload
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    out = bd.RSSM_BF16 if args.out_dtype == "bf16" else bd.RSSM_F32
+    w = I.WORKLOADS[args.workload]
+    n = args.warmup + args.steps
+    if args.workload == "gdn_serving":
+        st, _, _, _ = gdn_from_workload(w, dev, out)
+        o = st.new_output()
+        for t in range(n):
+            st.step(I.gdn_step_inputs(w, t, dev), o)
+    else:
+        st, A, D, _, _, _ = mamba2_from_workload(w, dev, out)
+        y = st.new_output(w.n_new)
+        for t in range(n):
+            st.verify(I.mamba2_verify_inputs(w, t, dev), A, D, y)
+            st.commit(I.accepted_kept(w, t, dev))
+    torch.cuda.synchronize()
+    bd.check(int(st.status.item()), "device status")
+    return None
+
+
 def main(argv=None):
     args = parse(argv)
     dist = Dist()
@@ -435,10 +580,13 @@ def main(argv=None):
         else:
             from recurrent_state_decode_gb300 import binding
             binding.load()
-            if args.workload.startswith("mamba2") and "spec" not in args.workload:
+            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec"):
+                res = profile_other(args, dist)
+            elif args.workload.startswith("mamba2") and "spec" not in args.workload:
                 res = bench_mamba2_ar(args, dist)
             else:
-                raise SystemExit(f"workload {args.workload} is not benchmarked by this script yet")
+                raise SystemExit(f"workload {args.workload}: run it with --mode profile, or read the "
+                                 "'workloads' object of the default run")
             if res is not None and dist.rank == 0 and not args.no_cpu_baseline and dist.world == 1:
                 from recurrent_state_decode_gb300 import inputs as I
                 v, sample = oracle_time_per_step(I.WORKLOADS[args.workload], args.cpu_seconds)
