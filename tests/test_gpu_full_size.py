@@ -152,7 +152,7 @@ def test_bf16_read_copy_4096_steps():
     dev = "cuda"
     st, A, D, pre, starts, counts = H.mamba2_setup(w, dev, bd.RSSM_F32)
     assert st.ckpt_read is not None
-    seqs = spread(counts, 3)
+    seqs = spread(counts, 2)
     feed = H.Feed()
     sess = sessions.mamba2_ar_session(H.F64(st.ckpt[seqs]), H.sub(pre, seqs), starts[seqs].cpu().numpy(),
                                       counts[seqs].cpu().numpy(), feed, H.F64(A), H.F64(D), w.buf_len)
