@@ -181,14 +181,26 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or the hint (ns) runs out, so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete; false after WAIT_LIMIT_NS.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; i++)
-      if (mbar_test(bar, parity)) return true;
+    if (mbar_test_sleep(bar, parity)) return true;
     if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
   }
 }

@@ -205,7 +205,6 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
   if (!FLUSH_ONLY) bf_row_to_smem(s.qv, a.q + bh * DK, DK, tid, GDN_THREADS);
   if (tid < m) {
     const bool ring = tid < count;
-    const size_t slot = bh * L + (start + tid) % L;
     const size_t sslot = bh * pad4(L) + (start + tid) % L;
     s.sg[tid] = ring ? a.rg[sslot] : a.g[bh];
     s.sb[tid] = ring ? a.rbeta[sslot] : a.beta[bh];

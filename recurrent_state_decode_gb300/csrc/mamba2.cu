@@ -331,152 +331,7 @@ __global__ void __launch_bounds__(128) m2_flush_kernel(M2Args a) {
   }
 }
 
-// ------------------------------------------------------------------ speculative verify
-
-// Window records of a verify, index k in [0, count + K): k < count are the
-// committed records (ring slot (start + k) mod L), k >= count the new ones.
-// Output i covers records [first, count + i] with first = count if the
-// committed window is folded first, else 0.
-template <int NCH, bool OUT_BF16>
-__global__ void __launch_bounds__(128) m2_verify_kernel(M2Args a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int blk = blockIdx.x;
-  const int pb = blk % a.nPB;
-  blk /= a.nPB;
-  const int h = blk % a.H, b = blk / a.H;
-  const int g = (h * a.G) / a.H;
-  const int L = a.L, N = a.N, P = a.P, PB = a.PB, H = a.H, K = a.K, G = a.G;
-  const int p0 = pb * PB, R = min(PB, P - p0);
-  const size_t bh = (size_t)b * H + h, bg = (size_t)b * G + g;
-
-  const int4 cur = load_cursor(a.cursors, b);
-  const int start = cur.x, count = cur.y;
-  if (start < 0 || start >= L || count < 0 || count > L || cur.z != 0) return;
-  const bool fold = count + K > L;
-  const int first = fold ? count : 0;
-  const int W = count + K;
-  const bool rd16 = (a.ckpt_read != nullptr) && !fold;
-
-  M2Smem s;
-  m2_smem_layout(PB, N, 2 * L, L, K, smem_raw, &s);
-  init_bars(s);
-  const size_t tile_off = (bh * P + p0) * N;
-  if (tid == 0) {
-    const char* src = rd16 ? (const char*)(a.ckpt_read + tile_off) : (const char*)(a.ckpt + tile_off);
-    issue_tile(s, src, R, N, rd16 ? 2 : 4);
-  }
-
-  // new record i of this sequence: x/z at ((b*K + i)*H + h)*P, B/C at ((b*K + i)*G + g)*N
-  for (int k = tid; k < W; k += 128)
-    s.sdt[k] = (k < count) ? a.rdt[bh * pad4(L) + (start + k) % L] : a.dt[((size_t)b * K + (k - count)) * H + h];
-  const int xv = R >> 3;
-  for (int i = tid; i < W * xv; i += 128) {
-    const int k = i / xv, v = i - k * xv;
-    const uint16_t* src = (k < count) ? a.rx + (bh * L + (start + k) % L) * P + p0 + v * 8
-                                      : a.x + (((size_t)b * K + (k - count)) * H + h) * P + p0 + v * 8;
-    bf8_to_smem(s.xs + (size_t)k * PB + v * 8, src);
-  }
-  if (fold) {
-    for (int i = tid; i < count * (N >> 3); i += 128) {
-      const int k = i / (N >> 3), v = i - k * (N >> 3);
-      bf8_to_smem(s.Bs + (size_t)k * N + v * 8, a.rB + (bg * L + (start + k) % L) * N + v * 8);
-    }
-  }
-  // dots B_k . C_i for every output i and record k in [first, count + i]
-  const int span = W - first;  // records that any output can reach
-  for (int q = warp; q < K * span; q += 4) {
-    const int i = q / span, kk = q - i * span, k = first + kk;
-    if (k > count + i) continue;
-    const uint16_t* Bk = (k < count) ? a.rB + (bg * L + (start + k) % L) * N
-                                     : a.B + (((size_t)b * K + (k - count)) * G + g) * N;
-    const uint16_t* Ci = a.C + (((size_t)b * K + i) * G + g) * N;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < NCH; j++) {
-      const int c = lane + 32 * j;
-      if (c * 4 < N) acc += dot4(load_bf4(Bk + c * 4), load_bf4(Ci + c * 4));
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) s.sc[i * 2 * L + kk] = acc;
-  }
-  __syncthreads();
-  // decay weights: one warp per output window, and the fold window in row K
-  for (int i = warp; i <= K; i += 4) {
-    if (i < K) {
-      window_weights(s.sdt + first, count + i + 1 - first, a.A[h], lane, s.sw + i * 2 * L, s.sc + i * 2 * L,
-                     s.scoef + i * 2 * L, &s.sP[i]);
-    } else if (fold) {
-      window_weights(s.sdt, count, a.A[h], lane, s.sw + K * 2 * L, nullptr, nullptr, &s.sP[K]);
-    }
-  }
-  __syncthreads();
-  for (int q = tid; q < K * R; q += 128) {
-    const int i = q / R, r = q - i * R;
-    float acc = 0.f;
-    const int mi = count + i + 1 - first;
-    for (int kk = 0; kk < mi; kk++) acc = fmaf(s.scoef[i * 2 * L + kk], s.xs[(size_t)(first + kk) * PB + r], acc);
-    s.xsum[(size_t)i * PB + r] = acc;
-  }
-  __syncthreads();
-  if (fold) {  // x rows of the folded records scaled by the fold weights
-    for (int q = tid; q < count * R; q += 128) {
-      const int k = q / R, r = q - k * R;
-      s.xs[(size_t)k * PB + r] *= s.sw[K * 2 * L + k];
-    }
-  }
-  // append x, z rows of the new records (the group rows and dt go in the epilogue kernel:
-  // on a fold their slots can alias committed records other blocks still read)
-  for (int q = tid; q < K * xv; q += 128) {
-    const int i = q / xv, v = q - i * xv;
-    const int slot = (start + count + i) % L;
-    copy8(a.rx + (bh * L + slot) * P + p0 + v * 8, a.x + (((size_t)b * K + i) * H + h) * P + p0 + v * 8);
-    copy8(a.rz + (bh * L + slot) * P + p0 + v * 8, a.z + (((size_t)b * K + i) * H + h) * P + p0 + v * 8);
-  }
-  __syncthreads();
-
-  const float Dh = a.D[h];
-  int r0w, r1w;
-  warp_rows(R, warp, r0w, r1w);
-  if (r1w <= r0w) return;
-  if (!mbar_wait_or_report(&s.bars[warp], 0, a.status)) return;
-  for (int r0 = r0w; r0 < r1w; r0 += 8) {
-    float4 hv[8][NCH];
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++)
-#pragma unroll
-      for (int j = 0; j < NCH; j++) {
-        const int c = lane + 32 * j;
-        hv[rr][j] = (c * 4 < N) ? tile_chunk<NCH>(s, rd16, r0 + rr, N, c) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    if (fold)
-      fold_group<NCH>(hv, s, r0, PB, N, count, s.sP[K], lane, a.ckpt + tile_off,
-                      a.ckpt_read ? a.ckpt_read + tile_off : nullptr, nullptr);
-    // hv now holds the (possibly folded) checkpoint rows
-    for (int i = 0; i < K; i++) {
-      const uint16_t* Ci = a.C + (((size_t)b * K + i) * G + g) * N;
-      float v[8];
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++) v[rr] = 0.f;
-#pragma unroll
-      for (int j = 0; j < NCH; j++) {
-        const int c = lane + 32 * j;
-        if (c * 4 < N) {
-          const float4 ci = load_bf4(Ci + c * 4);
-#pragma unroll
-          for (int rr = 0; rr < 8; rr++) v[rr] += dot4(hv[rr][j], ci);
-        }
-      }
-      reduce8(v, lane);
-      if ((lane & 3) == 0) {
-        const int r = r0 + reduce8_row(lane);
-        const size_t xi = (((size_t)b * K + i) * H + h) * P + p0 + r;
-        const float xm = bf_to_f(a.x[xi]), zm = bf_to_f(a.z[xi]);
-        store_out<OUT_BF16>(a.y, xi, (s.sP[i] * v[0] + s.xsum[(size_t)i * PB + r] + Dh * xm) * silu(zm));
-      }
-    }
-  }
-}
+// ------------------------------------------------------------------ speculative verify epilogue
 
 // Verify epilogue, one block per sequence (runs after the verify kernel in
 // stream order): checks the cursor as the verify did, appends the group rows
@@ -533,14 +388,7 @@ cudaError_t launch(Kern k, int grid, size_t smem, cudaStream_t st, const M2Args&
 }  // namespace
 
 size_t m2_smem_bytes(int kind, const M2Args& a) {
-  switch (kind) {
-    case M2_STEP:
-    case M2_FLUSH:
-      return m2_smem_layout(a.PB, a.N, a.L, a.L, 1, nullptr, nullptr);
-    case M2_VERIFY:
-      return m2_smem_layout(a.PB, a.N, 2 * a.L, a.L, a.K, nullptr, nullptr);
-  }
-  return 0;
+  return kind == M2_FLUSH ? m2_smem_layout(a.PB, a.N, a.L, a.L, 1, nullptr, nullptr) : 0;
 }
 
 #define RSSM_DISPATCH_NCH(NCH_, ...)       \
@@ -570,11 +418,7 @@ cudaError_t m2_launch(int kind, const M2Args& a, int out_bf16, cudaStream_t st) 
       RSSM_DISPATCH_NCH(NCH, { e = launch(m2_flush_kernel<NCH>, grid, smem, st, a); })
       return e;
     case M2_VERIFY:
-      RSSM_DISPATCH_NCH(NCH, {
-        e = out_bf16 ? launch(m2_verify_kernel<NCH, true>, grid, smem, st, a)
-                     : launch(m2_verify_kernel<NCH, false>, grid, smem, st, a);
-      })
-      if (e != cudaSuccess) return e;
+      if ((e = m2_verify_launch(a, out_bf16, st)) != cudaSuccess) return e;
       m2_verify_epilogue_kernel<<<a.Bt, 128, 0, st>>>(a);
       return cudaGetLastError();
   }

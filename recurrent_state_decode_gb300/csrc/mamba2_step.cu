@@ -26,17 +26,13 @@
 //      holds in registers and streams them out (and the bf16 read copy);
 //   5. otherwise appends the current record to its ring slot;
 // and releases the stage on its `empty` mbarrier. All waits are bounded.
-#include "common.cuh"
-#include "kernels.h"
+#include "persistent.cuh"
 
 namespace rssm {
 
 namespace {
 
-constexpr int NCONS = 4;                  // consumer warps
-constexpr int THREADS = 32 * (NCONS + 1);  // + one producer warp
-constexpr int MAX_STAGES = 8;
-constexpr uint32_t BAR_BYTES = 2 * MAX_STAGES * 8;
+using namespace persistent;
 
 struct Meta {
   int start, count, b, h;
@@ -48,30 +44,18 @@ struct Layout {  // byte offsets inside one stage, 128-byte aligned
   uint32_t tile, xw, zc, Bw, Cc, dtr, meta, bytes;
 };
 
-__host__ __device__ inline Layout make_layout(int PB, int N, int L) {
+inline Layout make_layout(int PB, int N, int L) {
   Layout s{};
-  uint32_t off = 0;
-  auto take = [&](uint32_t b) {
-    const uint32_t o = off;
-    off = (off + b + 127u) & ~127u;
-    return o;
-  };
-  s.tile = take(PB * N * 4);     // checkpoint rows (fp32; bf16 uses the first half)
-  s.xw = take(L * PB * 2);       // x rows of the window records, window order (bf16)
-  s.zc = take(PB * 2);           // z rows of the current record
-  s.Bw = take(L * N * 2);        // B rows of the window records, window order
-  s.Cc = take(N * 2);            // C of the current record
-  s.dtr = take(pad4(L) * 4);     // dt ring row (slot order)
-  s.meta = take(sizeof(Meta));
-  s.bytes = off;
+  Carver c;
+  s.tile = c.take(PB * N * 4);     // checkpoint rows (fp32; bf16 uses the first half)
+  s.xw = c.take(L * PB * 2);       // x rows of the window records, window order (bf16)
+  s.zc = c.take(PB * 2);           // z rows of the current record
+  s.Bw = c.take(L * N * 2);        // B rows of the window records, window order
+  s.Cc = c.take(N * 2);            // C of the current record
+  s.dtr = c.take(pad4(L) * 4);     // dt ring row (slot order)
+  s.meta = c.take(sizeof(Meta));
+  s.bytes = c.off;
   return s;
-}
-
-__device__ __forceinline__ void decode_tile(const M2Args& a, int t, int& b, int& h, int& pb) {
-  pb = t % a.nPB;
-  t /= a.nPB;
-  h = t % a.H;
-  b = t / a.H;
 }
 
 // Copy q of a stage fill; returns false if copy q moves nothing.
@@ -242,11 +226,7 @@ __device__ __forceinline__ void consume_tile(const M2Args& a, const Layout& lay,
   const float coef = (lane < m) ? wk * ck + (lane == count ? mt.D : 0.f) : 0.f;
 
   int r0w, r1w;
-  {
-    const int ngrp = R >> 3;
-    r0w = ((warp * ngrp) / NCONS) * 8;
-    r1w = (((warp + 1) * ngrp) / NCONS) * 8;
-  }
+  consumer_rows(R, warp, r0w, r1w);
   for (int r0 = r0w; r0 < r1w; r0 += 8) {
     // 3. outputs of rows r0..r0+7
     float xl[8];
@@ -352,20 +332,13 @@ __global__ void __launch_bounds__(THREADS, 1) m2_step_kernel(M2Args a, Layout la
   uint64_t* empty = full + MAX_STAGES;
   unsigned char* stages = smem + BAR_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; s++) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCONS);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (warp == NCONS) {
+  init_ring(full, S);
+  if (warp == NCW) {
     producer(a, lay, S, stages, full, empty, ntiles, lane);
     return;
   }
-  int j = 0;
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x, j++) {
+  const int group = warp / NCONS, wg = warp % NCONS;
+  for (int j = group, t = blockIdx.x + group * gridDim.x; t < ntiles; j += NGROUPS, t += NGROUPS * gridDim.x) {
     const int stage = j % S;
     const unsigned char* st = stages + (size_t)stage * lay.bytes;
     if (!__all_sync(FULL, mbar_wait(&full[stage], (j / S) & 1))) {
@@ -373,35 +346,18 @@ __global__ void __launch_bounds__(THREADS, 1) m2_step_kernel(M2Args a, Layout la
       return;
     }
     const Meta mt = *reinterpret_cast<const Meta*>(st + lay.meta);
-    if (!mt.skip) consume_tile<LM, NCH, OUT_BF16>(a, lay, st, mt, warp, lane);
+    if (!mt.skip) consume_tile<LM, NCH, OUT_BF16>(a, lay, st, mt, wg, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
-}
-
-struct DeviceInfo {
-  int sms = 0, smem_optin = 0;
-};
-
-DeviceInfo device_info() {
-  static DeviceInfo cache[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  DeviceInfo& d = cache[dev & 63];
-  if (d.sms == 0) {
-    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  }
-  return d;
 }
 
 template <int LM, int NCH, bool OUT_BF16>
 cudaError_t launch_step(const M2Args& a, cudaStream_t st) {
   const DeviceInfo di = device_info();
   const Layout lay = make_layout(a.PB, a.N, a.L);
-  int S = (int)((di.smem_optin - BAR_BYTES) / lay.bytes);
-  if (S > MAX_STAGES) S = MAX_STAGES;
-  if (S < 2) return cudaErrorInvalidConfiguration;
+  const int S = stages_for(lay.bytes);
+  if (S == 0) return cudaErrorInvalidConfiguration;
   const size_t smem = BAR_BYTES + (size_t)S * lay.bytes;
   const int ntiles = a.Bt * a.H * a.nPB;
   const int grid = ntiles < di.sms ? ntiles : di.sms;
