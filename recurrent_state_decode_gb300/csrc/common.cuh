@@ -124,6 +124,25 @@ __device__ __forceinline__ float reduce_transpose(float (&p)[V], int lane) {
   return p[0];
 }
 
+// ---------------------------------------------------------------- warp-level tensor-core pieces
+
+// Four 8x8 bf16 matrices from shared memory; lane l gives the address of row
+// (l & 7) of matrix (l >> 3). Rows are 16 bytes, 16-byte aligned.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_row))));
+}
+
+// d += A (16x16 bf16, row-major fragment) * B (16x8 bf16, column fragment), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // ---------------------------------------------------------------- status
 
 __device__ __forceinline__ void report(int32_t* status, int code) {

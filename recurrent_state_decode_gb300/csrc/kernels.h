@@ -62,11 +62,12 @@ cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, cudaStrea
 // multiple of 4 slots, so that a row is a whole number of 16-byte units.
 inline __host__ __device__ int pad4(int L) { return (L + 3) & ~3; }
 
-// Rows per block for a tile of `rows` x `cols` fp32 elements: at most 32 KiB of
-// tile per block, a multiple of 8 rows.
+// Rows per block of a Mamba-2 state tile of `rows` (headdim) x `cols` (dstate)
+// fp32 elements: 64 rows when a row fits one float4 per lane (dstate <= 128),
+// 32 rows otherwise, so a block is at most 32 KiB and a consumer warp holds its
+// quarter of the rows in 64 registers.
 inline int rows_per_block(int rows, int cols) {
-  int pb = (8192 / cols) & ~7;
-  if (pb < 8) pb = 8;
+  const int pb = cols <= 128 ? 64 : 32;
   return pb < rows ? pb : rows;
 }
 
