@@ -2,27 +2,31 @@
 // non-flush steps read the checkpoint and the window and store no state; the
 // L-th step folds the window into the checkpoint and writes it once).
 //
-// One CTA of four warps per (sequence, head, row block); each warp owns up to
-// 16 rows (8 when dstate > 128) and each lane a float4 column chunk of them.
-// The kernel is shaped like a streaming copy: every thread first issues the
-// 16-byte loads of its checkpoint rows straight into registers (the bf16
-// read copy on non-flush steps when there is one), so a resident CTA keeps its
-// whole 32 KiB tile in flight, and only then does the latency-bound window
-// work:
-//   1. lane k of every warp takes record k's dt and one warp suffix scan gives
+// One CTA of eight warps per (sequence, head, row block); each warp owns 8
+// rows and each lane a float4 column chunk of them (two when dstate > 128).
+// The kernel is shaped like a streaming copy: at launch every thread issues
+// the 16-byte loads of its checkpoint rows straight into registers, and, in
+// the same breath, lane s loads ring slot s (its dt and its x rows for the
+// warp) and the current record, none of which waits on the cursor. Once the
+// cursor arrives, lane k takes record k from lane (start + k) mod L by a
+// shuffle. Then:
+//   1. one warp suffix scan over the window (lane k = record k) gives
 //      w_k = dt_k exp(A sum_{j>k} dt_j) and P = exp(A sum_j dt_j);
-//   2. warp w forms c_k = B_k . C for records k = w, w+4, ... (per-lane
-//      partials over the lane's column chunk, one transposed butterfly
-//      reduction for all of them) and shares them through shared memory;
-//   3. lane k holds x_k of the warp's rows; per 8-row group each lane adds its
-//      record's term (w_k c_k [+ D on the current record]) x_k[r] to its
-//      P (h0 . C) partials, so one transposed 8-row reduction gives
-//      P (h0 C)[r] + sum_k w_k c_k x_k[r] + D x[r]; the gate silu(z) and the
-//      store run on one lane per row;
+//   2. the warps form c_s = B_s . C for every ring slot and the current record
+//      (per-lane partials over the lane's column chunk, one transposed
+//      butterfly reduction per warp) and share them through shared memory;
+//   3. each lane adds its record's term (w_k c_k [+ D on the current record])
+//      x_k[r] to its P (h0 . C) partials, so one transposed 8-row reduction
+//      gives P (h0 C)[r] + sum_k w_k c_k x_k[r] + D x[r]; the gate silu(z)
+//      and the store run on one lane per row;
 //   4. on the L-th step the window is folded into the rows held in registers
 //      and written once (with the bf16 read copy); otherwise the record is
 //      appended to its ring slot.
-// The cursor is only read here; a trailing kernel advances it.
+// Loading every ring slot's x rows rather than only the window's costs the
+// unused slots' bytes (a few percent of the step) and removes a dependent
+// round trip from every block. The cursor is only read; a trailing kernel
+// advances it. With a bf16 read copy the checkpoint load waits for the
+// cursor, which decides between the copy and the fp32 rows.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,21 +34,25 @@ namespace rssm {
 
 namespace {
 
-constexpr int THREADS = 128;
+constexpr int WARPS = 8;
+constexpr int THREADS = 32 * WARPS;
 
-// Rows [r0, r1) of warp w: R rows (a multiple of 8) in 8-row groups dealt out
-// contiguously to the four warps.
-__device__ __forceinline__ void warp_rows(int R, int w, int& r0, int& r1) {
-  const int ngrp = R >> 3;
-  r0 = ((w * ngrp) >> 2) * 8;
-  r1 = (((w + 1) * ngrp) >> 2) * 8;
+__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
+  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
 }
 
+__device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
+  return make_uint4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
+                    __shfl_sync(FULL, v.w, src));
+}
+
+// KW = ring slots (plus the current record) whose B.C dot one warp forms:
+// warp w takes slots w, w + 8, ...; slot L stands for the current record.
 template <int LM, int NCH, bool OUT_BF16>
-__global__ void __launch_bounds__(THREADS, 4) m2_step_kernel(M2Args a) {
-  constexpr int G8 = 2 / NCH;   // 8-row groups per warp at most
-  constexpr int KW = LM / 4;    // records whose B.C dot one warp forms
-  __shared__ float sc[LM];      // c_k = B_k . C
+__global__ void __launch_bounds__(THREADS, NCH == 1 ? 3 : 2) m2_step_kernel(M2Args a) {
+  constexpr int KW = LM == 16 ? 4 : 8;  // 8 warps x KW >= L + 1
+  __shared__ float sc[WARPS * KW];      // c_s = B_s . C by ring slot; [L] = current record
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int blk = blockIdx.x;
   const int pb = blk % a.nPB;
@@ -54,100 +62,90 @@ __global__ void __launch_bounds__(THREADS, 4) m2_step_kernel(M2Args a) {
   const int g = (h * G) / H;
   const int p0 = pb * a.PB, R = min(a.PB, P - p0);
   const size_t bh = (size_t)b * H + h, bg = (size_t)b * G + g;
-  int r0w, r1w;
-  warp_rows(R, warp, r0w, r1w);
-  const int nrows = r1w - r0w;
-  const size_t toff = (bh * P + p0) * N;
-
-  // 0. checkpoint rows into registers first (fp32 unless a read copy is used)
-  float4 hv[G8][8][NCH];
+  const int r0 = warp * 8;
+  const bool rows = r0 < R;  // R is a multiple of 8
+  const size_t toff = (bh * P + p0 + r0) * N;
   const bool has_copy = a.ckpt_read != nullptr;
+
+  // 0. loads that do not depend on the cursor
+  float4 hv[8][NCH];
   if (!has_copy) {
 #pragma unroll
-    for (int gg = 0; gg < G8; gg++)
+    for (int rr = 0; rr < 8; rr++)
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++)
-#pragma unroll
-        for (int jj = 0; jj < NCH; jj++) {
-          const int c = lane + 32 * jj;
-          hv[gg][rr][jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (gg * 8 < nrows && c * 4 < N)
-            hv[gg][rr][jj] =
-                __ldcs(reinterpret_cast<const float4*>(a.ckpt + toff + (size_t)(r0w + gg * 8 + rr) * N) + c);
-        }
+      for (int jj = 0; jj < NCH; jj++) {
+        const int c = lane + 32 * jj;
+        hv[rr][jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rows && c * 4 < N) hv[rr][jj] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + toff + (size_t)rr * N) + c);
+      }
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
-  const int start = cur.x, count = cur.y;
-  if (start < 0 || start >= L || count < 0 || count >= L || cur.z != 0) return;  // reported by the cursor kernel
-  const int m = count + 1;
-  const bool flush = (m == L);
-  if (has_copy) {
-#pragma unroll
-    for (int gg = 0; gg < G8; gg++)
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++)
-#pragma unroll
-        for (int jj = 0; jj < NCH; jj++) {
-          const int c = lane + 32 * jj;
-          const size_t row = toff + (size_t)(r0w + gg * 8 + rr) * N;
-          hv[gg][rr][jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (gg * 8 < nrows && c * 4 < N)
-            hv[gg][rr][jj] = flush ? __ldcs(reinterpret_cast<const float4*>(a.ckpt + row) + c)
-                                   : load_bf4(a.ckpt_read + row + c * 4);
-        }
+  const float dts = lane < L ? a.rdt[bh * pad4(L) + lane] : 0.f;   // ring slot `lane`
+  const float dtc = a.dt[bh];                                     // current record
+  uint4 xs = make_uint4(0, 0, 0, 0), xc = make_uint4(0, 0, 0, 0);
+  if (rows) {
+    if (lane < L) xs = *reinterpret_cast<const uint4*>(a.rx + (bh * L + lane) * P + p0 + r0);
+    xc = *reinterpret_cast<const uint4*>(a.x + bh * P + p0 + r0);
   }
-
-  // window record k: ring slot (start + k) mod L for k < count, the input for k == count
-  const int kl = lane;
-  int sl = start + kl;
-  sl = sl < L ? sl : sl - L;
-  const float dtk = kl < count ? a.rdt[bh * pad4(L) + sl] : (kl == count ? a.dt[bh] : 0.f);
-  const float Ah = a.A[h];
   float4 cm[NCH];
 #pragma unroll
   for (int jj = 0; jj < NCH; jj++) {
     const int c = lane + 32 * jj;
     cm[jj] = (c * 4 < N) ? load_bf4(a.C + bg * N + c * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // x_k of this warp's rows, lane k (16 rows: two 16-byte loads)
-  float xl[G8][8];
-#pragma unroll
-  for (int gg = 0; gg < G8; gg++) {
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++) xl[gg][rr] = 0.f;
-    if (kl < m && gg * 8 < nrows) {
-      const uint16_t* xs = kl < count ? a.rx + (bh * L + sl) * P : a.x + bh * P;
-      const uint4 u = *reinterpret_cast<const uint4*>(xs + p0 + r0w + gg * 8);
-      xl[gg][0] = bf_lo(u.x); xl[gg][1] = bf_hi(u.x); xl[gg][2] = bf_lo(u.y); xl[gg][3] = bf_hi(u.y);
-      xl[gg][4] = bf_lo(u.z); xl[gg][5] = bf_hi(u.z); xl[gg][6] = bf_lo(u.w); xl[gg][7] = bf_hi(u.w);
-    }
-  }
-  // 2. c_k = B_k . C for k = warp + 4 i
-  {
+  {  // 2. c_s = B_s . C for slots s = warp + 8 i (s == L: the current record)
     float pk[KW];
 #pragma unroll
     for (int i = 0; i < KW; i++) {
       pk[i] = 0.f;
-      const int k = warp + 4 * i;
-      if (k < m) {
-        int s = start + k;
-        s = s < L ? s : s - L;
-        const uint16_t* Bk = k < count ? a.rB + (bg * L + s) * N : a.B + bg * N;
+      const int s = warp + WARPS * i;
+      if (s <= L) {
+        const uint16_t* Bs = s < L ? a.rB + (bg * L + s) * N : a.B + bg * N;
 #pragma unroll
         for (int jj = 0; jj < NCH; jj++) {
           const int c = lane + 32 * jj;
-          if (c * 4 < N) pk[i] += dot4(load_bf4(Bk + c * 4), cm[jj]);
+          if (c * 4 < N) pk[i] += dot4(load_bf4(Bs + c * 4), cm[jj]);
         }
       }
     }
     const float red = reduce_transpose<KW>(pk, lane);
-    // lanes whose low bits are zero hold partial index idx(lane) (see reduce_transpose)
     const int idx = KW == 4 ? ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1) : reduce8_row(lane);
     const bool rep = KW == 4 ? (lane & 7) == 0 : (lane & 3) == 0;
-    if (rep && warp + 4 * idx < LM) sc[warp + 4 * idx] = red;
+    if (rep) sc[warp + WARPS * idx] = red;
   }
-  // 1. decay weights (every warp, lane k = record k)
-  float sfx = dtk * Ah;
+
+  // the cursor decides the window: record k < count is ring slot (start + k) mod L
+  const int start = cur.x, count = cur.y;
+  if (start < 0 || start >= L || count < 0 || count >= L || cur.z != 0) return;  // reported by the cursor kernel
+  const int m = count + 1;
+  const bool flush = (m == L);
+  if (has_copy) {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++)
+#pragma unroll
+      for (int jj = 0; jj < NCH; jj++) {
+        const int c = lane + 32 * jj;
+        const size_t row = toff + (size_t)rr * N;
+        hv[rr][jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rows && c * 4 < N)
+          hv[rr][jj] = flush ? __ldcs(reinterpret_cast<const float4*>(a.ckpt + row) + c)
+                             : load_bf4(a.ckpt_read + row + c * 4);
+      }
+  }
+  int sl = start + lane;
+  sl = sl < L ? sl : sl - L;
+  const int slot_of_lane = lane < count ? sl : L;  // L = the current record
+  const float dtr = __shfl_sync(FULL, dts, sl);
+  const float dtk = lane < count ? dtr : (lane == count ? dtc : 0.f);
+  const uint4 xr = shfl_u4(xs, sl);
+  float xl[8];
+  unpack8(lane < count ? xr : xc, xl);
+  if (lane >= m) {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
+  }
+  // 1. decay weights (lane k = record k)
+  float sfx = dtk * a.A[h];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float v = __shfl_down_sync(FULL, sfx, o);
@@ -158,32 +156,25 @@ __global__ void __launch_bounds__(THREADS, 4) m2_step_kernel(M2Args a) {
   const float Pm = expf(__shfl_sync(FULL, sfx, 0));
   const float wk = dtk * expf(ex);
   __syncthreads();
-  const float coef = kl < m ? fmaf(wk, sc[kl], kl == count ? a.D[h] : 0.f) : 0.f;
+  const float coef = lane < m ? fmaf(wk, sc[slot_of_lane], lane == count ? a.D[h] : 0.f) : 0.f;
+  if (!rows) return;
 
-  // 3. pre-gate outputs
-  float tot[G8];
+  // 3. pre-gate outputs of the warp's 8 rows
+  float v[8];
 #pragma unroll
-  for (int gg = 0; gg < G8; gg++) {
-    float v[8];
+  for (int rr = 0; rr < 8; rr++) {
+    float d = 0.f;
 #pragma unroll
-    for (int rr = 0; rr < 8; rr++) {
-      float d = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < NCH; jj++) d += dot4(hv[gg][rr][jj], cm[jj]);
-      v[rr] = fmaf(Pm, d, coef * xl[gg][rr]);
-    }
-    tot[gg] = reduce_transpose<8>(v, lane);
+    for (int jj = 0; jj < NCH; jj++) d += dot4(hv[rr][jj], cm[jj]);
+    v[rr] = fmaf(Pm, d, coef * xl[rr]);
   }
-  {  // lane r < nrows gathers row r's total, gates and stores it
+  reduce_transpose<8>(v, lane);
+  {
     const int rr = lane & 7;
     const int src = ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
-    float mine = __shfl_sync(FULL, tot[0], src);
-    if (G8 > 1) {
-      const float t1 = __shfl_sync(FULL, tot[G8 - 1], src);
-      if (lane & 8) mine = t1;
-    }
-    if (lane < nrows) {
-      const size_t oi = bh * P + p0 + r0w + lane;
+    const float mine = __shfl_sync(FULL, v[0], src);
+    if (lane < 8) {
+      const size_t oi = bh * P + p0 + r0 + lane;
       const float zm = bf_to_f(a.z[oi]);
       const float yv = mine * __fdividef(zm, 1.f + __expf(-zm));
       if (OUT_BF16)
@@ -195,53 +186,45 @@ __global__ void __launch_bounds__(THREADS, 4) m2_step_kernel(M2Args a) {
 
   if (flush) {  // 4a. fold the window into the rows in registers, write them once
 #pragma unroll
-    for (int gg = 0; gg < G8; gg++) {
-      if (gg * 8 >= nrows) continue;
+    for (int rr = 0; rr < 8; rr++)
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++)
+      for (int jj = 0; jj < NCH; jj++) hv[rr][jj] = scale4(Pm, hv[rr][jj]);
+    for (int k = 0; k < m; k++) {
+      const float w = __shfl_sync(FULL, wk, k);
+      float wx[8];
 #pragma unroll
-        for (int jj = 0; jj < NCH; jj++) hv[gg][rr][jj] = scale4(Pm, hv[gg][rr][jj]);
-      for (int k = 0; k < m; k++) {
-        const float w = __shfl_sync(FULL, wk, k);
-        float wx[8];
+      for (int rr = 0; rr < 8; rr++) wx[rr] = w * __shfl_sync(FULL, xl[rr], k);
+      int s = start + k;
+      s = s < L ? s : s - L;
+      const uint16_t* Bk = k < count ? a.rB + (bg * L + s) * N : a.B + bg * N;
 #pragma unroll
-        for (int rr = 0; rr < 8; rr++) wx[rr] = w * __shfl_sync(FULL, xl[gg][rr], k);
-        int s = start + k;
-        s = s < L ? s : s - L;
-        const uint16_t* Bk = k < count ? a.rB + (bg * L + s) * N : a.B + bg * N;
+      for (int jj = 0; jj < NCH; jj++) {
+        const int c = lane + 32 * jj;
+        if (c * 4 < N) {
+          const float4 bk = load_bf4(Bk + c * 4);
 #pragma unroll
-        for (int jj = 0; jj < NCH; jj++) {
-          const int c = lane + 32 * jj;
-          if (c * 4 < N) {
-            const float4 bk = load_bf4(Bk + c * 4);
-#pragma unroll
-            for (int rr = 0; rr < 8; rr++) hv[gg][rr][jj] = fma4(wx[rr], bk, hv[gg][rr][jj]);
-          }
+          for (int rr = 0; rr < 8; rr++) hv[rr][jj] = fma4(wx[rr], bk, hv[rr][jj]);
         }
       }
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++)
-#pragma unroll
-        for (int jj = 0; jj < NCH; jj++) {
-          const int c = lane + 32 * jj;
-          if (c * 4 < N) {
-            const size_t o = toff + (size_t)(r0w + gg * 8 + rr) * N + c * 4;
-            __stcs(reinterpret_cast<float4*>(a.ckpt + o), hv[gg][rr][jj]);
-            if (has_copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), f4_to_bf4(hv[gg][rr][jj]));
-          }
-        }
     }
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++)
+#pragma unroll
+      for (int jj = 0; jj < NCH; jj++) {
+        const int c = lane + 32 * jj;
+        if (c * 4 < N) {
+          const size_t o = toff + (size_t)rr * N + c * 4;
+          __stcs(reinterpret_cast<float4*>(a.ckpt + o), hv[rr][jj]);
+          if (has_copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), f4_to_bf4(hv[rr][jj]));
+        }
+      }
   } else {  // 4b. append the current record: x, z rows of this warp; dt, B, C once
     const int slot = start + count < L ? start + count : start + count - L;
-    const size_t rrow = (bh * L + slot) * P + p0;
-    if (lane < 2 * (nrows >> 3)) {
-      const int f = lane & 1, r = r0w + (lane >> 1) * 8;
-      const uint16_t* src = (f ? a.z : a.x) + bh * P + p0 + r;
-      uint16_t* dst = (f ? a.rz : a.rx) + rrow + r;
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-    }
+    const size_t rrow = (bh * L + slot) * P + p0 + r0;
+    if (lane == 0) *reinterpret_cast<uint4*>(a.rx + rrow) = xc;
+    if (lane == 1) *reinterpret_cast<uint4*>(a.rz + rrow) = *reinterpret_cast<const uint4*>(a.z + bh * P + p0 + r0);
     if (warp == 0 && pb == 0) {
-      if (lane == 0) a.rdt[bh * pad4(L) + slot] = a.dt[bh];
+      if (lane == 2) a.rdt[bh * pad4(L) + slot] = dtc;
       if (h == g * (H / G)) {  // the group's first head stores the group rows
         const size_t brow = (bg * L + slot) * N;
         for (int i = lane; i < (N >> 3); i += 32) {
