@@ -80,6 +80,7 @@ enum { RSSM_F32 = 0, RSSM_BF16 = 1 };
 
 /* Limits of this build. */
 #define RSSM_MAX_BUF_LEN 32 /* L in [1, 32] */
+#define RSSM_MAX_BATCH 65535 /* Mamba-2 batch (RSSM_ERR_UNSUPPORTED above) */
 #define RSSM_MAX_DIM 256    /* headdim, dstate, dk, dv: multiples of 8 in [8, 256] */
 
 /* ----------------------------------------------------------------------------

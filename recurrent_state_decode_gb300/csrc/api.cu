@@ -33,7 +33,7 @@ int check_m2(const rssm_mamba2_desc* d) {
   if (d->out_dtype != RSSM_F32 && d->out_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
   const int pb = rows_per_block(d->headdim, d->dstate);
   const long long grid = (long long)d->batch * d->nheads * ((d->headdim + pb - 1) / pb);
-  if (grid > INT_MAX) return RSSM_ERR_UNSUPPORTED;
+  if (grid > INT_MAX || d->batch > 65535) return RSSM_ERR_UNSUPPORTED;
   return RSSM_OK;
 }
 
