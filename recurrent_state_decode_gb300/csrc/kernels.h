@@ -28,6 +28,9 @@ enum { M2_CONVENTIONAL = 0, M2_STEP = 1, M2_FLUSH = 2, M2_VERIFY = 3 };
 cudaError_t m2_launch(int kind, const M2Args& a, int out_bf16, cudaStream_t st);
 // The persistent, warp-specialised AR step (mamba2_step.cu).
 cudaError_t m2_step_launch(const M2Args& a, int out_bf16, cudaStream_t st);
+// Shape-specialised AR step (dstate 128, headdim a multiple of 64; mamba2_step_fast.cu).
+bool m2_step_fast_applies(const M2Args& a);
+cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // The persistent speculative verify (mamba2_verify.cu); its epilogue kernel is in mamba2.cu.
 cudaError_t m2_verify_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 size_t m2_smem_bytes(int kind, const M2Args& a);
