@@ -197,8 +197,10 @@ __global__ void __launch_bounds__(FT, CPS) m2_step_fast_kernel(M2Args a, int nti
       }
       // this slab's window x rows, lane k = record k
       float xl[SR];
-      unpack8(lane < count ? shfl_u4(rec.xs0, sl) : rec.xc0, xl);
-      unpack8(lane < count ? shfl_u4(rec.xs1, sl) : rec.xc1, xl + 8);
+      // every lane takes part in the shuffles; the choice comes after
+      const uint4 xr0 = shfl_u4(rec.xs0, sl), xr1 = shfl_u4(rec.xs1, sl);
+      unpack8(lane < count ? xr0 : rec.xc0, xl);
+      unpack8(lane < count ? xr1 : rec.xc1, xl + 8);
       if (lane >= m) {
 #pragma unroll
         for (int r = 0; r < SR; r++) xl[r] = 0.f;
