@@ -4,31 +4,27 @@
 // non-flush steps read the checkpoint and the window and store no state; the
 // L-th step folds the window into the checkpoint and writes it once).
 //
-// Persistent warps, each working alone: warp gw of the grid takes the
-// (sequence, head, 64-row block) tiles gw, gw + W, ... (W = warps in the grid),
-// so the tiles of a flushing sequence spread over all warps. A tile streams
-// through the warp in four slabs of 16 rows (8 KiB fp32, 4 KiB from the bf16
-// read copy), each one bulk copy (TMA, non-tensor; never multicast) into the
-// warp's double buffer on the warp's own mbarriers: while the warp computes
-// slab n the copy of slab n+1 -- possibly the first slab of its next tile -- is
-// in flight. The next tile's cursor, dts, A and D are loaded a tile ahead and
-// each slab's x records a slab ahead, so no warp ever waits on them. Nothing is
-// shared between warps.
-//
-// Per tile (lane k = window record k; ring slots are fetched by slot and the
-// window picked by shuffles once the cursor is known):
-//   * one warp suffix scan: w_k = dt_k exp(A sum_{j>k} dt_j), P = exp(A sum dt);
-//   * c_k = B_k . C for all ring slots by per-lane partials over the lane's
-//     float4 column chunk and one transposed butterfly reduction, plus the
-//     current record's dot;
-//   * coef_k = w_k c_k (+ D on the current record).
-// Per 8-row group of a slab: lane l holds the float4 chunk 4l..4l+3 of each
-// row; its partial P (h0 . C) plus coef_l x_l[r] goes through one transposed
-// 8-row reduction, giving y[r] before the gate; the gate silu(z) and the store
-// run one lane per row. On the L-th step the window is folded into each row
-// (re-read from the buffer) and written once, with the bf16 read copy;
-// otherwise the record is appended to its ring slot. The cursor is only read;
-// a trailing kernel advances it.
+// One CTA of four warps per (sequence, head, 64-row block). The block's 32 KiB
+// of checkpoint is fetched at launch through both of the SM's buffers at once:
+// rows 0..31 by the threads' own 16-byte loads straight into registers (warp w
+// rows 8w..8w+7, lane l the float4 column chunk 4l..4l+3), rows 32..63 by one
+// bulk copy (TMA, non-tensor; never multicast) into shared memory on an
+// mbarrier (warp w reads rows 32+8w..32+8w+7 from there). That keeps about 80
+// registers and 16 KiB of shared memory per block, so six blocks -- 192 KiB of
+// checkpoint -- are in flight per SM. Also at launch and without waiting on the
+// cursor, lane s loads ring slot s (its dt and its x rows) and the current
+// record; warp w forms the B.C dots of ring slots w, w+4, ... (per-lane partials
+// over the lane's column chunk, one transposed butterfly reduction) and of the
+// current record, shared through shared memory. Once the cursor is known lane k
+// takes record k from lane (start + k) mod L by a shuffle, one warp suffix scan
+// gives w_k = dt_k exp(A sum_{j>k} dt_j) and P = exp(A sum dt), and per 8-row
+// group each lane's partial (h0 . P C) plus its record's term (w_k c_k [+ D on
+// the current record]) x_k[r] goes through one transposed 8-row reduction,
+// yielding y[r] before the gate; the gate silu(z) and the store run one lane
+// per row. On the L-th step the window is folded into the rows and written
+// once, with the bf16 read copy; otherwise
+// the record is appended to its ring slot. The cursor is only read; a trailing
+// kernel advances it.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -36,15 +32,12 @@ namespace rssm {
 
 namespace {
 
-constexpr int FN = 128;                   // dstate
-constexpr int FPB = 64;                   // rows per tile
-constexpr int SR = 16;                    // rows per slab
-constexpr int NSLAB = FPB / SR;
-constexpr int WPC = 4;                    // warps per block
-constexpr int FT = 32 * WPC;
-constexpr int CPS = 3;                    // blocks per SM
-constexpr int SLAB = SR * FN;             // floats of one slab
-constexpr int SMEM = WPC * 2 * SLAB * 4;  // per-warp double buffer: 64 KiB per block
+constexpr int FN = 128;            // dstate
+constexpr int FPB = 64;            // rows per block
+constexpr int FW = 4;              // warps
+constexpr int FT = 32 * FW;
+constexpr int HALF = 32;           // rows loaded into registers; the rest by bulk copy
+constexpr int KW = 8;              // 4 warps x 8 >= L + 1 dots for L <= 31
 
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
@@ -58,265 +51,215 @@ __device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
                     __shfl_sync(FULL, v.w, src));
 }
 
-// What a tile needs before its first slab: where it is, its cursor, its scalars.
-struct TileHead {
-  int t;          // tile index, >= ntiles when there is none
-  int bh, h, pb;  // bh = b * H + h
-  int b, g;
-  int4 cur;
-  float dts, dtc, A, D;  // dt of ring slot `lane`, current dt, A[h], D[h]
-};
-
-__device__ __forceinline__ void load_head(TileHead& th, const M2Args& a, int t, int ntiles, int lane) {
-  th.t = t;
-  if (t >= ntiles) return;
-  const int pb = t % a.nPB, bh = t / a.nPB;
-  th.pb = pb;
-  th.bh = bh;
-  th.h = bh % a.H;
-  th.b = bh / a.H;
-  th.g = th.h / (a.H / a.G);
-  th.cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)th.b);
-  th.dts = lane < a.L ? a.rdt[(size_t)bh * pad4(a.L) + lane] : 0.f;
-  th.dtc = a.dt[bh];
-  th.A = a.A[th.h];
-  th.D = a.D[th.h];
+// y[r] before the gate for 8 rows: sum over lanes of (h . PC) + coef * x[r]
+__device__ __forceinline__ float rows8(const float4 (&hv)[8], float4 pc, float coef, const float (&xl)[8],
+                                       int lane) {
+  float v[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++)
+    v[rr] = fmaf(hv[rr].x, pc.x, fmaf(hv[rr].y, pc.y, fmaf(hv[rr].z, pc.z, fmaf(hv[rr].w, pc.w, coef * xl[rr]))));
+  return reduce_transpose<8>(v, lane);
 }
 
-__device__ __forceinline__ bool head_valid(const TileHead& th, int L) {
-  const int4 c = th.cur;
-  return c.x >= 0 && c.x < L && c.y >= 0 && c.y < L && c.z == 0;
-}
-
-// x rows of one slab: ring slot `lane` and the current record.
-struct SlabRec {
-  uint4 xs0, xs1, xc0, xc1;
-};
-
-__device__ __forceinline__ void load_slab_rec(SlabRec& r, const M2Args& a, int bh, int row0, int lane) {
-  const int L = a.L, P = a.P;
-  r.xs0 = r.xs1 = make_uint4(0, 0, 0, 0);
-  if (lane < L) {
-    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P + row0;
-    r.xs0 = ldg16(xp);
-    r.xs1 = ldg16(xp + 8);
+template <bool OUT_BF16>
+__device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float tot, int lane) {
+  const int rr = lane & 7;
+  const int src = ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
+  const float t = __shfl_sync(FULL, tot, src);
+  if (lane < 8) {
+    const float zm = bf_to_f(a.z[obase + lane]);
+    const float yv = t * __fdividef(zm, 1.f + __expf(-zm));
+    if (OUT_BF16)
+      reinterpret_cast<uint16_t*>(a.y)[obase + lane] = f_to_bf(yv);
+    else
+      reinterpret_cast<float*>(a.y)[obase + lane] = yv;
   }
-  const uint16_t* xcp = a.x + (size_t)bh * P + row0;
-  r.xc0 = ldg16(xcp);
-  r.xc1 = ldg16(xcp + 8);
 }
 
-template <int LM, bool OUT_BF16>
-__global__ void __launch_bounds__(FT, CPS) m2_step_fast_kernel(M2Args a, int ntiles) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t bars[WPC * 2];
+// h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the bf16 copy).
+__device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm, float wk, const float (&xl)[8],
+                                      int m, int count, int start, int bg, size_t off, int lane) {
+  const int L = a.L;
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pm, hv[rr]);
+  const uint16_t* rB = a.rB + (size_t)bg * L * FN + lane * 4;
+  for (int k = 0; k < m; k++) {
+    const float w = __shfl_sync(FULL, wk, k);
+    int s = start + k;
+    s = s < L ? s : s - L;
+    const float4 bk = load_bf4(k < count ? rB + s * FN : a.B + (size_t)bg * FN + lane * 4);
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[rr], k), bk, hv[rr]);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) {
+    __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
+    if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
+  }
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
+  __shared__ __align__(128) float tile2[(FPB - HALF) * FN];  // rows 32..63 (fp32, or bf16 in the first half)
+  __shared__ float sc[FW * KW];                              // c_s = B_s . C by ring slot; [L] = current
+  __shared__ uint64_t bar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.y;
+  const int h = blockIdx.x / a.nPB, pb = blockIdx.x - h * a.nPB;
   const int L = a.L, P = a.P, H = a.H;
-  const int W = gridDim.x * WPC;
-  float* buf = reinterpret_cast<float*>(smem) + warp * 2 * SLAB;
-  uint64_t* bar = bars + warp * 2;
+  const int g = h / (H / a.G);
+  const int bh = b * H + h, bg = b * a.G + g;
+  const int p0 = pb * FPB;
   const bool copy = a.ckpt_read != nullptr;
-  if (lane == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
+  const size_t tbase = ((size_t)bh * P + p0) * FN;    // element offset of the block's row 0
+  const size_t offA = tbase + (size_t)(warp * 8) * FN + lane * 4;  // the warp's register rows
 
-  // slab q of a tile into buffer n & 1
-  auto issue = [&](const TileHead& th, int q, uint32_t n) {
-    if (lane != 0) return;
-    const bool rd16 = copy && (th.cur.y + 1 < L);
-    const size_t off = ((size_t)th.bh * P + th.pb * FPB + q * SR) * FN;
-    const uint32_t bytes = rd16 ? SLAB * 2 : SLAB * 4;
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&bar[n & 1], bytes);
-    bulk_load(buf + (n & 1) * SLAB, rd16 ? (const void*)(a.ckpt_read + off) : (const void*)(a.ckpt + off), bytes,
-              &bar[n & 1]);
+  // the checkpoint: half into registers, half by one bulk copy. Without a read
+  // copy the rows are fp32 whatever the cursor says, so they are requested
+  // before the cursor is looked at; with one the cursor decides first.
+  auto fetch = [&](bool bf16) {
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      const uint32_t bytes = (FPB - HALF) * FN * (bf16 ? 2 : 4);
+      const size_t off2 = tbase + (size_t)HALF * FN;
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_load(tile2, bf16 ? (const void*)(a.ckpt_read + off2) : (const void*)(a.ckpt + off2), bytes, &bar);
+    }
   };
-  // the next valid tile from t on (invalid cursors are skipped and reported by the cursor kernel)
-  auto next_valid = [&](TileHead& th, int t) {
-    load_head(th, a, t, ntiles, lane);
-    while (th.t < ntiles && !head_valid(th, L)) load_head(th, a, th.t + W, ntiles, lane);
-  };
-
-  TileHead cur;
-  next_valid(cur, blockIdx.x * WPC + warp);
-  if (cur.t >= ntiles) return;
-  uint32_t n = 0;  // slabs consumed by this warp
-  issue(cur, 0, n);
-  SlabRec rec;
-  load_slab_rec(rec, a, cur.bh, cur.pb * FPB, lane);
-
-  while (cur.t < ntiles) {
-    TileHead nxt;
-    next_valid(nxt, cur.t + W);  // a whole tile ahead
-
-    // ---- per-tile setup
-    const int start = cur.cur.x, count = cur.cur.y, m = count + 1;
-    const bool flush = (m == L), rd16 = copy && !flush;
-    const int bg = cur.b * a.G + cur.g;
-    int sl = start + lane;
-    sl = sl < L ? sl : sl - L;
-    const float dtr = __shfl_sync(FULL, cur.dts, sl);
-    const float dtk = lane < count ? dtr : (lane == count ? cur.dtc : 0.f);
-    float sfx = dtk * cur.A;
+  float4 hv[8];
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
+  if (!copy) {
+    fetch(false);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_down_sync(FULL, sfx, o);
-      if (lane + o < 32) sfx += v;
-    }
-    float ex = __shfl_down_sync(FULL, sfx, 1);
-    if (lane == 31) ex = 0.f;
-    const float Pm = expf(__shfl_sync(FULL, sfx, 0));
-    const float wk = dtk * expf(ex);
-    const float4 cm = load_bf4(a.C + (size_t)bg * FN + lane * 4);
-    float coef;
-    {
-      const uint16_t* rB = a.rB + (size_t)bg * L * FN + lane * 4;
-      float pk[LM];
-#pragma unroll
-      for (int s = 0; s < LM; s++) pk[s] = s < L ? dot4(load_bf4(rB + s * FN), cm) : 0.f;
-      const float cc = warp_sum(dot4(load_bf4(a.B + (size_t)bg * FN + lane * 4), cm));
-      const float red = reduce_transpose<LM>(pk, lane);  // slot s at lane idx^-1(s)
-      const float cs = __shfl_sync(FULL, red, LM == 16 ? (2 * sl) & 31 : sl);
-      coef = lane < count ? wk * cs : (lane == count ? fmaf(wk, cc, cur.D) : 0.f);
-    }
-    const int appl = start + count < L ? start + count : start + count - L;
-
-    for (int q = 0; q < NSLAB; q++, n++) {
-      const int row0 = cur.pb * FPB + q * SR;  // first row of the slab within the head
-      // next slab in flight, its records into registers
-      SlabRec nrec;
-      if (q + 1 < NSLAB) {
-        issue(cur, q + 1, n + 1);
-        load_slab_rec(nrec, a, cur.bh, row0 + SR, lane);
-      } else if (nxt.t < ntiles) {
-        issue(nxt, 0, n + 1);
-        load_slab_rec(nrec, a, nxt.bh, nxt.pb * FPB, lane);
-      }
-      // this slab's window x rows, lane k = record k
-      float xl[SR];
-      // every lane takes part in the shuffles; the choice comes after
-      const uint4 xr0 = shfl_u4(rec.xs0, sl), xr1 = shfl_u4(rec.xs1, sl);
-      unpack8(lane < count ? xr0 : rec.xc0, xl);
-      unpack8(lane < count ? xr1 : rec.xc1, xl + 8);
-      if (lane >= m) {
-#pragma unroll
-        for (int r = 0; r < SR; r++) xl[r] = 0.f;
-      }
-      if (!__all_sync(FULL, mbar_wait(&bar[n & 1], (n >> 1) & 1))) {
-        if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
-        mbar_wait(&bar[(n + 1) & 1], ((n + 1) >> 1) & 1);  // let the next copy land before leaving
-        return;
-      }
-      const float* s32 = buf + (n & 1) * SLAB;
-      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(s32);
-      auto row_chunk = [&](int r) -> float4 {
-        return rd16 ? load_bf4(s16 + r * FN + lane * 4) : reinterpret_cast<const float4*>(s32 + r * FN)[lane];
-      };
-      float tot[2];
-#pragma unroll
-      for (int gg = 0; gg < 2; gg++) {
-        float v[8];
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++) v[rr] = fmaf(Pm, dot4(row_chunk(gg * 8 + rr), cm), coef * xl[gg * 8 + rr]);
-        tot[gg] = reduce_transpose<8>(v, lane);
-      }
-      {
-        const int rr = lane & 7;
-        const int src = ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
-        const float t0 = __shfl_sync(FULL, tot[0], src), t1 = __shfl_sync(FULL, tot[1], src);
-        if (lane < SR) {
-          const size_t oi = (size_t)cur.bh * P + row0 + lane;
-          const float zm = bf_to_f(a.z[oi]);
-          const float yv = (lane & 8 ? t1 : t0) * __fdividef(zm, 1.f + __expf(-zm));
-          if (OUT_BF16)
-            reinterpret_cast<uint16_t*>(a.y)[oi] = f_to_bf(yv);
-          else
-            reinterpret_cast<float*>(a.y)[oi] = yv;
-        }
-      }
-      const size_t soff = ((size_t)cur.bh * P + row0) * FN + lane * 4;
-      if (flush) {  // fold the window into the slab's rows, write them once
-        const uint16_t* rB = a.rB + (size_t)bg * L * FN + lane * 4;
-#pragma unroll
-        for (int gg = 0; gg < 2; gg++) {
-          float4 hv[8];
-#pragma unroll
-          for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pm, row_chunk(gg * 8 + rr));
-          for (int k = 0; k < m; k++) {
-            const float w = __shfl_sync(FULL, wk, k);
-            int s = start + k;
-            s = s < L ? s : s - L;
-            const float4 bk = load_bf4(k < count ? rB + s * FN : a.B + (size_t)bg * FN + lane * 4);
-#pragma unroll
-            for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[gg * 8 + rr], k), bk, hv[rr]);
-          }
-#pragma unroll
-          for (int rr = 0; rr < 8; rr++) {
-            const size_t o = soff + (size_t)(gg * 8 + rr) * FN;
-            __stcs(reinterpret_cast<float4*>(a.ckpt + o), hv[rr]);
-            if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), f4_to_bf4(hv[rr]));
-          }
-        }
-      } else {  // append the current record's x, z rows of this slab (dt, B, C once per tile)
-        const size_t rrow = ((size_t)cur.bh * L + appl) * P + row0;
-        if (lane < 2) *reinterpret_cast<uint4*>(a.rx + rrow + lane * 8) = lane ? rec.xc1 : rec.xc0;
-        if (lane == 2 || lane == 3) {
-          const int o = (lane - 2) * 8;
-          *reinterpret_cast<uint4*>(a.rz + rrow + o) = ldg16(a.z + (size_t)cur.bh * P + row0 + o);
-        }
-        if (q == 0 && cur.pb == 0) {
-          if (lane == 4) a.rdt[(size_t)cur.bh * pad4(L) + appl] = cur.dtc;
-          if (cur.h == cur.g * (H / a.G) && lane >= 8 && lane < 8 + FN / 8) {  // the group's first head
-            const int c8 = (lane - 8) * 8;
-            const size_t brow = ((size_t)bg * L + appl) * FN + c8;
-            *reinterpret_cast<uint4*>(a.rB + brow) = ldg16(a.B + (size_t)bg * FN + c8);
-            *reinterpret_cast<uint4*>(a.rC + brow) = ldg16(a.C + (size_t)bg * FN + c8);
-          }
-        }
-      }
-      __syncwarp();  // the buffer may be refilled from here on
-      rec = nrec;
-    }
-    cur = nxt;
+    for (int rr = 0; rr < 8; rr++) hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + offA + (size_t)rr * FN));
   }
-}
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
+  if (!valid) {  // reported by the cursor kernel (uniform over the block)
+    if (!copy && threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
+    return;
+  }
+  const int start = cur.x, count = cur.y, m = count + 1;
+  const bool flush = (m == L), rd16 = copy && !flush;
+  if (copy) {
+    fetch(rd16);
+    if (rd16) {
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(a.ckpt_read + offA + (size_t)rr * FN);
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++)
+        hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + offA + (size_t)rr * FN));
+    }
+  }
+  // records: ring slot `lane` and the current record, for the warp's two row groups
+  const int rA = p0 + warp * 8, rB2 = p0 + HALF + warp * 8;  // first rows (within the head)
+  const float dts = lane < L ? a.rdt[(size_t)bh * pad4(L) + lane] : 0.f;
+  const float dtc = a.dt[bh];
+  uint4 xsA = make_uint4(0, 0, 0, 0), xsB = xsA;
+  if (lane < L) {
+    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P;
+    xsA = ldg16(xp + rA);
+    xsB = ldg16(xp + rB2);
+  }
+  const uint4 xcA = ldg16(a.x + (size_t)bh * P + rA), xcB = ldg16(a.x + (size_t)bh * P + rB2);
+  const float4 cm = load_bf4(a.C + (size_t)bg * FN + lane * 4);
+  {  // c_s = B_s . C for slots s = warp + 4 i (s == L: the current record)
+    const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
+    float pk[KW];
+#pragma unroll
+    for (int i = 0; i < KW; i++) {
+      const int s = warp + FW * i;
+      pk[i] = s < L ? dot4(load_bf4(rBp + s * FN), cm)
+                    : (s == L ? dot4(load_bf4(a.B + (size_t)bg * FN + lane * 4), cm) : 0.f);
+    }
+    const float red = reduce_transpose<KW>(pk, lane);
+    if ((lane & 3) == 0) sc[warp + FW * reduce8_row(lane)] = red;
+  }
+  // window, lane k = record k
+  int sl = start + lane;
+  sl = sl < L ? sl : sl - L;
+  const float dtr = __shfl_sync(FULL, dts, sl);
+  const float dtk = lane < count ? dtr : (lane == count ? dtc : 0.f);
+  float sfx = dtk * a.A[h];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_down_sync(FULL, sfx, o);
+    if (lane + o < 32) sfx += v;
+  }
+  float ex = __shfl_down_sync(FULL, sfx, 1);
+  if (lane == 31) ex = 0.f;
+  const float Pm = expf(__shfl_sync(FULL, sfx, 0));
+  const float wk = dtk * expf(ex);
+  const float4 pc = scale4(Pm, cm);
+  const uint4 xrA = shfl_u4(xsA, sl), xrB = shfl_u4(xsB, sl);
+  __syncthreads();
+  const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? a.D[h] : 0.f) : 0.f;
 
-struct DeviceSMs {
-  int sms = 0;
-};
+  // rows of the register half
+  float xl[8];
+  unpack8(lane < count ? xrA : xcA, xl);
+  if (lane >= m) {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
+  }
+  gate_store<OUT_BF16>(a, (size_t)bh * P + rA, rows8(hv, pc, coef, xl, lane), lane);
+  if (flush) fold8(a, hv, Pm, wk, xl, m, count, start, bg, offA, lane);  // hv holds the fp32 rows here
+  // rows of the bulk-copied half
+  unpack8(lane < count ? xrB : xcB, xl);
+  if (lane >= m) {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
+  }
+  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
+    if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
+    mbar_wait(&bar, 0);
+    return;
+  }
+  const int rl = warp * 8;  // row within the copied half
+  if (rd16) {
+    const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile2) + lane * 4;
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
+  } else {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile2 + (rl + rr) * FN)[lane];
+  }
+  gate_store<OUT_BF16>(a, (size_t)bh * P + rB2, rows8(hv, pc, coef, xl, lane), lane);
+  if (flush) fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)(HALF + rl) * FN + lane * 4, lane);
 
-int sm_count() {
-  static DeviceSMs cache[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  DeviceSMs& d = cache[dev & 63];
-  if (d.sms == 0) cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-  return d.sms;
-}
-
-template <int LM, bool OUT_BF16>
-cudaError_t launch_fast(const M2Args& a, cudaStream_t st) {
-  auto k = m2_step_fast_kernel<LM, OUT_BF16>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  if (e != cudaSuccess) return e;
-  const int ntiles = a.Bt * a.H * a.nPB;
-  int grid = sm_count() * CPS;
-  const int need = (ntiles + WPC - 1) / WPC;
-  if (grid > need) grid = need;
-  k<<<grid, FT, SMEM, st>>>(a, ntiles);
-  return cudaGetLastError();
+  if (!flush) {  // append the current record: x, z rows of this warp's groups; dt, B, C once
+    const int slot = start + count < L ? start + count : start + count - L;
+    const size_t rrow = ((size_t)bh * L + slot) * P;
+    if (lane == 0) *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xcA;
+    if (lane == 1) *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xcB;
+    if (lane == 2) *reinterpret_cast<uint4*>(a.rz + rrow + rA) = ldg16(a.z + (size_t)bh * P + rA);
+    if (lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + rB2) = ldg16(a.z + (size_t)bh * P + rB2);
+    if (warp == 0 && pb == 0) {
+      if (lane == 4) a.rdt[(size_t)bh * pad4(L) + slot] = dtc;
+      if (h == g * (H / a.G) && lane >= 8 && lane < 8 + FN / 8) {  // the group's first head
+        const int c8 = (lane - 8) * 8;
+        const size_t brow = ((size_t)bg * L + slot) * FN + c8;
+        *reinterpret_cast<uint4*>(a.rB + brow) = ldg16(a.B + (size_t)bg * FN + c8);
+        *reinterpret_cast<uint4*>(a.rC + brow) = ldg16(a.C + (size_t)bg * FN + c8);
+      }
+    }
+  }
 }
 
 }  // namespace
 
-bool m2_step_fast_applies(const M2Args& a) { return a.N == FN && a.P % FPB == 0 && a.PB == FPB; }
+bool m2_step_fast_applies(const M2Args& a) {
+  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.L <= FW * KW - 1;
+}
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
-  if (a.L <= 16) return out_bf16 ? launch_fast<16, true>(a, st) : launch_fast<16, false>(a, st);
-  return out_bf16 ? launch_fast<32, true>(a, st) : launch_fast<32, false>(a, st);
+  const dim3 grid(a.H * a.nPB, a.Bt);
+  if (out_bf16)
+    m2_step_fast_kernel<true><<<grid, FT, 0, st>>>(a);
+  else
+    m2_step_fast_kernel<false><<<grid, FT, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace rssm
