@@ -4,27 +4,25 @@
 // non-flush steps read the checkpoint and the window and store no state; the
 // L-th step folds the window into the checkpoint and writes it once).
 //
-// One CTA of four warps per (sequence, head, 64-row block). The block's 32 KiB
-// of checkpoint is fetched at launch through both of the SM's buffers at once:
-// rows 0..31 by the threads' own 16-byte loads straight into registers (warp w
-// rows 8w..8w+7, lane l the float4 column chunk 4l..4l+3), rows 32..63 by one
-// bulk copy (TMA, non-tensor; never multicast) into shared memory on an
-// mbarrier (warp w reads rows 32+8w..32+8w+7 from there). That keeps about 80
-// registers and 16 KiB of shared memory per block, so six blocks -- 192 KiB of
-// checkpoint -- are in flight per SM. Also at launch and without waiting on the
-// cursor, lane s loads ring slot s (its dt and its x rows) and the current
-// record; warp w forms the B.C dots of ring slots w, w+4, ... (per-lane partials
-// over the lane's column chunk, one transposed butterfly reduction) and of the
-// current record, shared through shared memory. Once the cursor is known lane k
+// One CTA of four warps per (sequence, head, 64-row block). Every global load
+// the block needs is issued at launch, none of them waiting on the cursor, so a
+// block's life is one memory round trip plus its arithmetic: thread 0 starts one
+// bulk copy (TMA, non-tensor; never multicast) of the block's 64 checkpoint rows
+// into shared memory (32 KiB fp32, or 16 KiB from the bf16 read copy), and every
+// lane loads, for its warp's two 8-row groups, ring slot `lane` (its dt and x
+// rows), the current record, the gate z, and the B rows of the ring slots whose
+// B.C dots the warp forms (per-lane partials over the lane's column chunk, one
+// transposed butterfly reduction; shared through shared memory). Six blocks --
+// 192 KiB of checkpoint -- are in flight per SM. Once the cursor is known lane k
 // takes record k from lane (start + k) mod L by a shuffle, one warp suffix scan
 // gives w_k = dt_k exp(A sum_{j>k} dt_j) and P = exp(A sum dt), and per 8-row
 // group each lane's partial (h0 . P C) plus its record's term (w_k c_k [+ D on
 // the current record]) x_k[r] goes through one transposed 8-row reduction,
-// yielding y[r] before the gate; the gate silu(z) and the store run one lane
-// per row. On the L-th step the window is folded into the rows and written
-// once, with the bf16 read copy; otherwise
-// the record is appended to its ring slot. The cursor is only read; a trailing
-// kernel advances it.
+// yielding y[r] before the gate; the gate silu(z) and the store run one lane per
+// row. On the L-th step the window is folded into the rows and written once,
+// with the bf16 read copy (a block reading the bf16 copy takes its fp32 rows
+// from global memory on that step); otherwise the record is appended to its
+// ring slot. The cursor is only read; a trailing kernel advances it.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -36,7 +34,7 @@ constexpr int FN = 128;            // dstate
 constexpr int FPB = 64;            // rows per block
 constexpr int FW = 4;              // warps
 constexpr int FT = 32 * FW;
-constexpr int HALF = 32;           // rows loaded into registers; the rest by bulk copy
+constexpr int HALF = 32;           // a warp's second row group starts here
 constexpr int KW = 8;              // 4 warps x 8 >= L + 1 dots for L <= 31
 
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
@@ -62,12 +60,11 @@ __device__ __forceinline__ float rows8(const float4 (&hv)[8], float4 pc, float c
 }
 
 template <bool OUT_BF16>
-__device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float tot, int lane) {
+__device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float zm, float tot, int lane) {
   const int rr = lane & 7;
   const int src = ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
   const float t = __shfl_sync(FULL, tot, src);
   if (lane < 8) {
-    const float zm = bf_to_f(a.z[obase + lane]);
     const float yv = t * __fdividef(zm, 1.f + __expf(-zm));
     if (OUT_BF16)
       reinterpret_cast<uint16_t*>(a.y)[obase + lane] = f_to_bf(yv);
@@ -100,8 +97,8 @@ __device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm
 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
-  __shared__ __align__(128) float tile2[(FPB - HALF) * FN];  // rows 32..63 (fp32, or bf16 in the first half)
-  __shared__ float sc[FW * KW];                              // c_s = B_s . C by ring slot; [L] = current
+  __shared__ __align__(128) float tile[FPB * FN];  // the block's rows (fp32, or bf16 in the first half)
+  __shared__ float sc[FW * KW];                    // c_s = B_s . C by ring slot; [L] = current
   __shared__ uint64_t bar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
@@ -111,77 +108,59 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const int bh = b * H + h, bg = b * a.G + g;
   const int p0 = pb * FPB;
   const bool copy = a.ckpt_read != nullptr;
-  const size_t tbase = ((size_t)bh * P + p0) * FN;    // element offset of the block's row 0
-  const size_t offA = tbase + (size_t)(warp * 8) * FN + lane * 4;  // the warp's register rows
+  const size_t tbase = ((size_t)bh * P + p0) * FN;  // element offset of the block's row 0
 
-  // the checkpoint: half into registers, half by one bulk copy. Without a read
-  // copy the rows are fp32 whatever the cursor says, so they are requested
-  // before the cursor is looked at; with one the cursor decides first.
-  auto fetch = [&](bool bf16) {
-    if (threadIdx.x == 0) {
-      mbar_init(&bar, 1);
-      fence_mbar_init();
-      const uint32_t bytes = (FPB - HALF) * FN * (bf16 ? 2 : 4);
-      const size_t off2 = tbase + (size_t)HALF * FN;
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_load(tile2, bf16 ? (const void*)(a.ckpt_read + off2) : (const void*)(a.ckpt + off2), bytes, &bar);
-    }
-  };
-  float4 hv[8];
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = FPB * FN * (copy ? 2 : 4);
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_load(tile, copy ? (const void*)(a.ckpt_read + tbase) : (const void*)(a.ckpt + tbase), bytes, &bar);
+  }
+  // everything else, at launch: cursor, window records, current record, gate
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
-  if (!copy) {
-    fetch(false);
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++) hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + offA + (size_t)rr * FN));
-  }
-  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
-  if (!valid) {  // reported by the cursor kernel (uniform over the block)
-    if (!copy && threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
-    return;
-  }
-  const int start = cur.x, count = cur.y, m = count + 1;
-  const bool flush = (m == L), rd16 = copy && !flush;
-  if (copy) {
-    fetch(rd16);
-    if (rd16) {
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(a.ckpt_read + offA + (size_t)rr * FN);
-    } else {
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++)
-        hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + offA + (size_t)rr * FN));
-    }
-  }
-  // records: ring slot `lane` and the current record, for the warp's two row groups
-  const int rA = p0 + warp * 8, rB2 = p0 + HALF + warp * 8;  // first rows (within the head)
+  const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's two row groups (within the block)
+  const int rA = p0 + rl0, rB2 = p0 + rl1;          // ... within the head
+  const size_t xrow = (size_t)bh * P;
   const float dts = lane < L ? a.rdt[(size_t)bh * pad4(L) + lane] : 0.f;
-  const float dtc = a.dt[bh];
+  const float dtc = a.dt[bh], Ah = a.A[h], Dh = a.D[h];
   uint4 xsA = make_uint4(0, 0, 0, 0), xsB = xsA;
   if (lane < L) {
     const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P;
     xsA = ldg16(xp + rA);
     xsB = ldg16(xp + rB2);
   }
-  const uint4 xcA = ldg16(a.x + (size_t)bh * P + rA), xcB = ldg16(a.x + (size_t)bh * P + rB2);
-  const float4 cm = load_bf4(a.C + (size_t)bg * FN + lane * 4);
+  const uint4 xcA = ldg16(a.x + xrow + rA), xcB = ldg16(a.x + xrow + rB2);
+  const float zA = bf_to_f(a.z[xrow + rA + (lane & 7)]), zB = bf_to_f(a.z[xrow + rB2 + (lane & 7)]);
+  const uint4 zap = ldg16(a.z + xrow + ((lane & 1) ? rB2 : rA));  // the append's z rows (lanes 2, 3)
+  const uint2 craw = *reinterpret_cast<const uint2*>(a.C + (size_t)bg * FN + lane * 4);
+  const uint2 braw = *reinterpret_cast<const uint2*>(a.B + (size_t)bg * FN + lane * 4);
+  const float4 cm = bf4_to_f4(craw);
   {  // c_s = B_s . C for slots s = warp + 4 i (s == L: the current record)
     const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
+    const float4 bc = bf4_to_f4(braw);
     float pk[KW];
 #pragma unroll
     for (int i = 0; i < KW; i++) {
       const int s = warp + FW * i;
-      pk[i] = s < L ? dot4(load_bf4(rBp + s * FN), cm)
-                    : (s == L ? dot4(load_bf4(a.B + (size_t)bg * FN + lane * 4), cm) : 0.f);
+      pk[i] = s < L ? dot4(load_bf4(rBp + s * FN), cm) : (s == L ? dot4(bc, cm) : 0.f);
     }
     const float red = reduce_transpose<KW>(pk, lane);
     if ((lane & 3) == 0) sc[warp + FW * reduce8_row(lane)] = red;
   }
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
+  if (!valid) {  // reported by the cursor kernel (uniform over the block)
+    if (threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
+    return;
+  }
+  const int start = cur.x, count = cur.y, m = count + 1;
+  const bool flush = (m == L);
   // window, lane k = record k
   int sl = start + lane;
   sl = sl < L ? sl : sl - L;
   const float dtr = __shfl_sync(FULL, dts, sl);
   const float dtk = lane < count ? dtr : (lane == count ? dtc : 0.f);
-  float sfx = dtk * a.A[h];
+  float sfx = dtk * Ah;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float v = __shfl_down_sync(FULL, sfx, o);
@@ -194,54 +173,52 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const float4 pc = scale4(Pm, cm);
   const uint4 xrA = shfl_u4(xsA, sl), xrB = shfl_u4(xsB, sl);
   __syncthreads();
-  const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? a.D[h] : 0.f) : 0.f;
-
-  // rows of the register half
-  float xl[8];
-  unpack8(lane < count ? xrA : xcA, xl);
-  if (lane >= m) {
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
-  }
-  gate_store<OUT_BF16>(a, (size_t)bh * P + rA, rows8(hv, pc, coef, xl, lane), lane);
-  if (flush) fold8(a, hv, Pm, wk, xl, m, count, start, bg, offA, lane);  // hv holds the fp32 rows here
-  // rows of the bulk-copied half
-  unpack8(lane < count ? xrB : xcB, xl);
-  if (lane >= m) {
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
-  }
+  const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? Dh : 0.f) : 0.f;
   if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar, 0);
     return;
   }
-  const int rl = warp * 8;  // row within the copied half
-  if (rd16) {
-    const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile2) + lane * 4;
+  // A block that reads the bf16 copy folds from the fp32 rows in global memory.
+  const bool from_tile = !(copy && flush);
 #pragma unroll
-    for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
-  } else {
+  for (int half = 0; half < 2; half++) {
+    const int rl = half ? rl1 : rl0;
+    float4 hv[8];
+    if (!from_tile) {
 #pragma unroll
-    for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile2 + (rl + rr) * FN)[lane];
+      for (int rr = 0; rr < 8; rr++)
+        hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + tbase + (size_t)(rl + rr) * FN) + lane);
+    } else if (copy) {
+      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
+    }
+    float xl[8];
+    unpack8(lane < count ? (half ? xrB : xrA) : (half ? xcB : xcA), xl);
+    if (lane >= m) {
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
+    }
+    gate_store<OUT_BF16>(a, xrow + p0 + rl, half ? zB : zA, rows8(hv, pc, coef, xl, lane), lane);
+    if (flush) fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)rl * FN + lane * 4, lane);
   }
-  gate_store<OUT_BF16>(a, (size_t)bh * P + rB2, rows8(hv, pc, coef, xl, lane), lane);
-  if (flush) fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)(HALF + rl) * FN + lane * 4, lane);
 
   if (!flush) {  // append the current record: x, z rows of this warp's groups; dt, B, C once
     const int slot = start + count < L ? start + count : start + count - L;
     const size_t rrow = ((size_t)bh * L + slot) * P;
     if (lane == 0) *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xcA;
     if (lane == 1) *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xcB;
-    if (lane == 2) *reinterpret_cast<uint4*>(a.rz + rrow + rA) = ldg16(a.z + (size_t)bh * P + rA);
-    if (lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + rB2) = ldg16(a.z + (size_t)bh * P + rB2);
+    if (lane == 2 || lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + (lane == 3 ? rB2 : rA)) = zap;
     if (warp == 0 && pb == 0) {
       if (lane == 4) a.rdt[(size_t)bh * pad4(L) + slot] = dtc;
-      if (h == g * (H / a.G) && lane >= 8 && lane < 8 + FN / 8) {  // the group's first head
-        const int c8 = (lane - 8) * 8;
-        const size_t brow = ((size_t)bg * L + slot) * FN + c8;
-        *reinterpret_cast<uint4*>(a.rB + brow) = ldg16(a.B + (size_t)bg * FN + c8);
-        *reinterpret_cast<uint4*>(a.rC + brow) = ldg16(a.C + (size_t)bg * FN + c8);
+      if (h == g * (H / a.G)) {  // the group's first head
+        const size_t brow = ((size_t)bg * L + slot) * FN + lane * 4;
+        *reinterpret_cast<uint2*>(a.rB + brow) = braw;
+        *reinterpret_cast<uint2*>(a.rC + brow) = craw;
       }
     }
   }
@@ -255,10 +232,12 @@ bool m2_step_fast_applies(const M2Args& a) {
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
   const dim3 grid(a.H * a.nPB, a.Bt);
-  if (out_bf16)
-    m2_step_fast_kernel<true><<<grid, FT, 0, st>>>(a);
-  else
-    m2_step_fast_kernel<false><<<grid, FT, 0, st>>>(a);
+  auto k = out_bf16 ? m2_step_fast_kernel<true> : m2_step_fast_kernel<false>;
+  // six 32 KiB tiles per SM need the largest shared-memory split of the unified L1
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  k<<<grid, FT, 0, st>>>(a);
   return cudaGetLastError();
 }
 
