@@ -1,0 +1,56 @@
+// Pieces shared by the shape-specialised Mamba-2 kernels (dstate 128, rows in
+// blocks of 64): a block of four warps holds a (sequence, head) tile's 64
+// checkpoint rows, warp w the rows 8w..8w+7 and 32+8w..32+8w+7, lane l the
+// float4 column chunk 4l..4l+3 of each.
+#pragma once
+#include "common.cuh"
+
+namespace rssm {
+namespace fastrows {
+
+constexpr int FN = 128;     // dstate
+constexpr int FPB = 64;     // rows per block
+constexpr int FW = 4;       // warps
+constexpr int FT = 32 * FW;
+constexpr int HALF = 32;    // a warp's second row group starts here
+
+__device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ void unpack8(uint4 u, float* f) {
+  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
+}
+
+// Every lane must call this (a full-warp shuffle).
+__device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
+  return make_uint4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
+                    __shfl_sync(FULL, v.w, src));
+}
+
+// y[r] before the gate for 8 rows: sum over lanes of (h . PC) + t[r], where
+// t[r] is the lane's window term. The total of row rr ends in lane row_src(rr).
+__device__ __forceinline__ float rows8(const float4 (&hv)[8], float4 pc, const float (&t)[8], int lane) {
+  float v[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++)
+    v[rr] = fmaf(hv[rr].x, pc.x, fmaf(hv[rr].y, pc.y, fmaf(hv[rr].z, pc.z, fmaf(hv[rr].w, pc.w, t[rr]))));
+  return reduce_transpose<8>(v, lane);
+}
+
+__device__ __forceinline__ int row_src(int rr) {
+  return ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
+}
+
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_y(void* y, size_t i, float v) {
+  if (OUT_BF16)
+    reinterpret_cast<uint16_t*>(y)[i] = f_to_bf(v);
+  else
+    reinterpret_cast<float*>(y)[i] = v;
+}
+
+// silu(z) = z sigmoid(z)
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
+}  // namespace fastrows
+}  // namespace rssm

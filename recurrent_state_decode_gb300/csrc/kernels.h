@@ -33,6 +33,9 @@ bool m2_step_fast_applies(const M2Args& a);
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // The persistent speculative verify (mamba2_verify.cu); its epilogue kernel is in mamba2.cu.
 cudaError_t m2_verify_launch(const M2Args& a, int out_bf16, cudaStream_t st);
+// Shape-specialised verify (dstate 128, headdim a multiple of 64, K <= 4; mamba2_verify_fast.cu).
+bool m2_verify_fast_applies(const M2Args& a);
+cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 size_t m2_smem_bytes(int kind, const M2Args& a);
 
 // Gated DeltaNet launch arguments.

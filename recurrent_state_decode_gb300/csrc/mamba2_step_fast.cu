@@ -23,54 +23,22 @@
 // with the bf16 read copy (a block reading the bf16 copy takes its fp32 rows
 // from global memory on that step); otherwise the record is appended to its
 // ring slot. The cursor is only read; a trailing kernel advances it.
-#include "common.cuh"
+#include "fast_rows.cuh"
 #include "kernels.h"
 
 namespace rssm {
 
 namespace {
 
-constexpr int FN = 128;            // dstate
-constexpr int FPB = 64;            // rows per block
-constexpr int FW = 4;              // warps
-constexpr int FT = 32 * FW;
-constexpr int HALF = 32;           // a warp's second row group starts here
-constexpr int KW = 8;              // 4 warps x 8 >= L + 1 dots for L <= 31
+using namespace fastrows;
 
-__device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 
-__device__ __forceinline__ void unpack8(uint4 u, float* f) {
-  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
-  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
-}
-
-__device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
-  return make_uint4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
-                    __shfl_sync(FULL, v.w, src));
-}
-
-// y[r] before the gate for 8 rows: sum over lanes of (h . PC) + coef * x[r]
-__device__ __forceinline__ float rows8(const float4 (&hv)[8], float4 pc, float coef, const float (&xl)[8],
-                                       int lane) {
-  float v[8];
-#pragma unroll
-  for (int rr = 0; rr < 8; rr++)
-    v[rr] = fmaf(hv[rr].x, pc.x, fmaf(hv[rr].y, pc.y, fmaf(hv[rr].z, pc.z, fmaf(hv[rr].w, pc.w, coef * xl[rr]))));
-  return reduce_transpose<8>(v, lane);
-}
-
+// gate: silu(z) of row (lane & 7), computed before the rows land
 template <bool OUT_BF16>
-__device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float zm, float tot, int lane) {
-  const int rr = lane & 7;
-  const int src = ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
-  const float t = __shfl_sync(FULL, tot, src);
-  if (lane < 8) {
-    const float yv = t * __fdividef(zm, 1.f + __expf(-zm));
-    if (OUT_BF16)
-      reinterpret_cast<uint16_t*>(a.y)[obase + lane] = f_to_bf(yv);
-    else
-      reinterpret_cast<float*>(a.y)[obase + lane] = yv;
-  }
+__device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float gate, float tot, int lane) {
+  const float t = __shfl_sync(FULL, tot, row_src(lane & 7));
+  if (lane < 8) store_y<OUT_BF16>(a.y, obase + lane, t * gate);
 }
 
 // h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the bf16 copy).
@@ -174,6 +142,9 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const uint4 xrA = shfl_u4(xsA, sl), xrB = shfl_u4(xsB, sl);
   __syncthreads();
   const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? Dh : 0.f) : 0.f;
+  // the gates do not need the checkpoint rows: computed before waiting for them
+  const uint4 xq[2] = {lane < count ? xrA : xcA, lane < count ? xrB : xcB};  // lane k: x_k, both groups
+  const float gA = silu_fast(zA), gB = silu_fast(zB);
   if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar, 0);
@@ -197,14 +168,14 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
     }
-    float xl[8];
-    unpack8(lane < count ? (half ? xrB : xrA) : (half ? xcB : xcA), xl);
-    if (lane >= m) {
+    float xl[8], tx[8];
+    unpack8(xq[half], xl);
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) xl[rr] = 0.f;
+    for (int rr = 0; rr < 8; rr++) tx[rr] = lane < m ? coef * xl[rr] : 0.f;
+    gate_store<OUT_BF16>(a, xrow + p0 + rl, half ? gB : gA, rows8(hv, pc, tx, lane), lane);
+    if (flush) {
+      fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)rl * FN + lane * 4, lane);
     }
-    gate_store<OUT_BF16>(a, xrow + p0 + rl, half ? zB : zA, rows8(hv, pc, coef, xl, lane), lane);
-    if (flush) fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)rl * FN + lane * 4, lane);
   }
 
   if (!flush) {  // append the current record: x, z rows of this warp's groups; dt, B, C once

@@ -1,0 +1,259 @@
+// Speculative verify for Mamba-2, shape-specialised fast path: dstate 128,
+// headdim a multiple of 64, at most 4 new records and L + K <= 32 ("How
+// ReplaySSM works": drafts go into the buffer instead of a state snapshot and
+// are verified output-only; "ReplaySSM" repository, introduction: rollback by
+// moving a pointer). Same results as the persistent verify in
+// mamba2_verify.cu, built like the AR step's fast path.
+//
+// One CTA of four warps per (sequence, head, 64-row block); warp w owns rows
+// 8w..8w+7 and 32+8w..32+8w+7. Everything is requested at launch, none of it
+// waiting on the cursor: thread 0 starts one bulk copy (TMA, non-tensor, never
+// multicast) of the block's checkpoint rows into shared memory; lane s loads
+// ring slot s (dt, x rows), lane j new record j (dt, x rows), lane 8i + r the
+// gate z of new record i at row r, and every lane its column chunk of the new
+// records' C. Records are indexed k in [0, count + K): k < count the committed
+// window (ring slot (start + k) mod L), then the K new ones. Entry e of the
+// B.C table is ring slot e (e < L) or new record e - L; warp w forms the dots
+// of entries w, w+4, ... against all four C_i (two batches of 16 partials per
+// lane, one transposed reduction each), shared through shared memory.
+//
+// Once the cursor is known lane k takes record k by a shuffle and one
+// inclusive warp scan gives S_k = A sum_{j<=k} dt_j. If count + K > L the
+// committed window is folded first, h' = e^{S_{count-1}} h0 + sum_{k<count}
+// dt_k e^{S_{count-1}-S_k} x_k B_k^T, written once (with the bf16 read copy),
+// and output i covers records [count, count+i]; otherwise h' = h0 and output i
+// covers [0, count+i]. Output i: y_i[r] = (e^{S_last - S_first-1} (h' . C_i)[r]
+// + sum_k dt_k e^{S_last - S_k} (B_k . C_i) x_k[r] + D x_last[r]) silu(z_i[r]),
+// last = count + i, one transposed 8-row reduction per output and row group.
+// The new records' x and z rows go to the ring here (these rows are read by
+// this block alone); their B, C and dt rows, which other blocks read, go in the
+// epilogue kernel that follows in stream order.
+#include "fast_rows.cuh"
+#include "kernels.h"
+
+namespace rssm {
+
+namespace {
+
+using namespace fastrows;
+
+constexpr int KMAX = 4;  // new records per verify on this path
+constexpr int EW = 8;    // B.C entries per warp: 4 warps x 8 = 32 >= L + K
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
+  __shared__ __align__(128) float tile[FPB * FN];  // the block's rows (fp32, or bf16 in the first half)
+  __shared__ float sc[KMAX][FW * EW];              // B_e . C_i
+  __shared__ uint64_t bar;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.y;
+  const int h = blockIdx.x / a.nPB, pb = blockIdx.x - h * a.nPB;
+  const int L = a.L, P = a.P, H = a.H, G = a.G, K = a.K;
+  const int g = h / (H / G);
+  const int bh = b * H + h, bg = b * G + g;
+  const int p0 = pb * FPB;
+  const bool copy = a.ckpt_read != nullptr;
+  const size_t tbase = ((size_t)bh * P + p0) * FN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = FPB * FN * (copy ? 2 : 4);
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_load(tile, copy ? (const void*)(a.ckpt_read + tbase) : (const void*)(a.ckpt + tbase), bytes, &bar);
+  }
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
+  const int rl0 = warp * 8, rl1 = HALF + warp * 8;
+  const int rA = p0 + rl0, rB2 = p0 + rl1;
+  // ring slot `lane`
+  const float dts = lane < L ? a.rdt[(size_t)bh * pad4(L) + lane] : 0.f;
+  uint4 xsA = make_uint4(0, 0, 0, 0), xsB = xsA, xnA = xsA, xnB = xsA;
+  if (lane < L) {
+    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P;
+    xsA = ldg16(xp + rA);
+    xsB = ldg16(xp + rB2);
+  }
+  // new record `lane`
+  const size_t nrow = ((size_t)b * K + lane) * H + h;
+  float dtn = 0.f;
+  if (lane < K) {
+    dtn = a.dt[nrow];
+    xnA = ldg16(a.x + nrow * P + rA);
+    xnB = ldg16(a.x + nrow * P + rB2);
+  }
+  // gate z of new record gi at row gr of each row group
+  const int gi = lane >> 3, gr = lane & 7;
+  uint16_t zbA = 0, zbB = 0;
+  if (gi < K) {
+    const size_t zrow = (((size_t)b * K + gi) * H + h) * P;
+    zbA = a.z[zrow + rA + gr];
+    zbB = a.z[zrow + rB2 + gr];
+  }
+  const float Ah = a.A[h], Dh = a.D[h];
+  float4 ci[KMAX];  // the lane's column chunk of C_i
+#pragma unroll
+  for (int i = 0; i < KMAX; i++)
+    ci[i] = i < K ? load_bf4(a.C + (((size_t)b * K + i) * G + g) * FN + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  {  // sc[i][e] = B_e . C_i for entries e = warp + 4 j
+#pragma unroll
+    for (int jb = 0; jb < EW; jb += EW / 2) {  // two batches of 16 partials
+      float pk[EW / 2 * KMAX];
+#pragma unroll
+      for (int j = 0; j < EW / 2; j++) {
+        const int e = warp + FW * (jb + j);
+        float4 be = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < L)
+          be = load_bf4(a.rB + ((size_t)bg * L + e) * FN + lane * 4);
+        else if (e < L + K)
+          be = load_bf4(a.B + (((size_t)b * K + (e - L)) * G + g) * FN + lane * 4);
+#pragma unroll
+        for (int i = 0; i < KMAX; i++) pk[j * KMAX + i] = dot4(be, ci[i]);
+      }
+      // lane l holds partial l >> 1: entry warp + 4 (jb + (l >> 3)), output (l >> 1) & 3
+      const float red = reduce_transpose<EW / 2 * KMAX>(pk, lane);
+      if ((lane & 1) == 0) sc[(lane >> 1) & 3][warp + FW * (jb + (lane >> 3))] = red;
+    }
+  }
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
+  if (!valid) {  // reported by the epilogue kernel (uniform over the block)
+    if (threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
+    return;
+  }
+  const int start = cur.x, count = cur.y, total = count + K;
+  const bool fold = total > L;
+  const int first = fold ? count : 0;
+  // record k on lane k: committed (ring slot sl) or new (record jn)
+  int sl = start + lane;
+  sl = sl < L ? sl : sl - L;
+  const int jn = (lane - count) & 31;
+  const float dtr = __shfl_sync(FULL, dts, sl), dtw = __shfl_sync(FULL, dtn, jn);
+  const float dtk = lane < count ? dtr : (lane < total ? dtw : 0.f);
+  float S = dtk * Ah;  // inclusive scan: S_k = A sum_{j<=k} dt_j
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_up_sync(FULL, S, o);
+    if (lane >= o) S += v;
+  }
+  const float Sb = __shfl_sync(FULL, S, (first - 1) & 31);
+  const float S0 = first > 0 ? Sb : 0.f;
+  const float Sf = __shfl_sync(FULL, S, (count - 1) & 31);
+  const float Pf = expf(Sf);                                // fold: e^{S_{count-1}}
+  const float wf = lane < count ? dtk * expf(Sf - S) : 0.f;  // fold weights
+  const int ek = lane < count ? sl : (lane < total ? L + jn : 0);
+  const uint4 xar = shfl_u4(xsA, sl), xbr = shfl_u4(xsB, sl), xan = shfl_u4(xnA, jn), xbn = shfl_u4(xnB, jn);
+  const uint4 xq[2] = {lane < count ? xar : xan, lane < count ? xbr : xbn};
+  float Pi[KMAX], Sl[KMAX];
+#pragma unroll
+  for (int i = 0; i < KMAX; i++) {
+    Sl[i] = __shfl_sync(FULL, S, (count + i) & 31);
+    Pi[i] = expf(Sl[i] - S0);
+  }
+  __syncthreads();
+  float coef[KMAX];
+#pragma unroll
+  for (int i = 0; i < KMAX; i++) {
+    const int last = count + i;
+    const bool in = i < K && lane >= first && lane <= last;
+    coef[i] = in ? fmaf(dtk * expf(Sl[i] - S), sc[i][ek], lane == last ? Dh : 0.f) : 0.f;
+  }
+  const float gA = silu_fast(bf_to_f(zbA)), gB = silu_fast(bf_to_f(zbB));
+  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
+    if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
+    mbar_wait(&bar, 0);
+    return;
+  }
+  // A block that reads the bf16 copy folds from the fp32 rows in global memory.
+  const bool from_tile = !(copy && fold);
+#pragma unroll
+  for (int half = 0; half < 2; half++) {
+    const int rl = half ? rl1 : rl0;
+    float4 hv[8];
+    if (!from_tile) {
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++)
+        hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + tbase + (size_t)(rl + rr) * FN) + lane);
+    } else if (copy) {
+      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
+    }
+    float xl[8];
+    unpack8(xq[half], xl);
+    if (fold) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, four records per round
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, hv[rr]);
+      const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
+      for (int k0 = 0; k0 < count; k0 += 4) {
+        float4 bk[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          int s = start + k0 + u;
+          s = s < L ? s : s - L;
+          bk[u] = k0 + u < count ? load_bf4(rBp + s * FN) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          const int k = (k0 + u) & 31;
+          const float w = __shfl_sync(FULL, wf, k);  // 0 for k >= count
+#pragma unroll
+          for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[rr], k), bk[u], hv[rr]);
+        }
+      }
+      const size_t off = tbase + (size_t)rl * FN + lane * 4;
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) {
+        __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
+        if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
+      }
+    }
+    const float gate = half ? gB : gA;
+#pragma unroll
+    for (int i = 0; i < KMAX; i++) {
+      if (i < K) {  // uniform
+        float tx[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; rr++) tx[rr] = coef[i] * xl[rr];
+        const float tot = rows8(hv, scale4(Pi[i], ci[i]), tx, lane);
+        const float t = __shfl_sync(FULL, tot, row_src(gr));
+        if (gi == i) store_y<OUT_BF16>(a.y, (((size_t)b * K + i) * H + h) * P + p0 + rl + gr, t * gate);
+      }
+    }
+  }
+  // append the new records' x and z rows of this block
+  auto slot_of = [&](int j) {
+    int s = start + count + j;
+    s = s < L ? s : s - L;
+    return s < L ? s : s - L;
+  };
+  if (lane < K) {
+    const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P;
+    *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xnA;
+    *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xnB;
+  }
+  if (gi < K) {
+    const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P;
+    a.rz[rrow + rA + gr] = zbA;
+    a.rz[rrow + rB2 + gr] = zbB;
+  }
+}
+
+}  // namespace
+
+bool m2_verify_fast_applies(const M2Args& a) {
+  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.K <= KMAX && a.L + a.K <= FW * EW;
+}
+
+cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
+  const dim3 grid(a.H * a.nPB, a.Bt);
+  auto k = out_bf16 ? m2_verify_fast_kernel<true> : m2_verify_fast_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  k<<<grid, FT, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rssm
