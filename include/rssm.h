@@ -225,10 +225,13 @@ typedef struct {
   rssm_bf16* v;  /* [batch, nheads, buf_len, dv] */
   float* g;      /* [batch, nheads, Lp], Lp as in rssm_mamba2_ring.dt */
   float* beta;   /* [batch, nheads, Lp] */
+  float* e;      /* [batch, nheads, buf_len, dv]: each window record's
+                  * correction e_t = beta_t (v_t - alpha_t S_{t-1} k_t), kept
+                  * next to the record (see rssm_gdn_step) */
 } rssm_gdn_ring;
 
-/* Bytes of each ring field, in the order q, k, v, g, beta. */
-RSSM_API int rssm_gdn_ring_bytes(const rssm_gdn_desc* desc, size_t bytes[5]);
+/* Bytes of each ring field, in the order q, k, v, g, beta, e. */
+RSSM_API int rssm_gdn_ring_bytes(const rssm_gdn_desc* desc, size_t bytes[6]);
 
 /* Conventional step: S [batch, nheads, dv, dk] fp32 updated in place;
  * q, k [batch, nheads, dk], v [batch, nheads, dv] bf16; g, beta
@@ -240,7 +243,12 @@ RSSM_API int rssm_gdn_conventional_step(const rssm_gdn_desc* desc, float* S,
                                rssm_stream_t stream);
 
 /* ReplaySSM AR step for Gated DeltaNet: same protocol as rssm_mamba2_step
- * (non-flush steps write no state; the L-th step folds and writes S once). */
+ * (non-flush steps write no state; the L-th step folds and writes S once).
+ * A record's correction e_t depends only on the checkpoint and the records
+ * before it, so it is fixed from the step that appends the record until the
+ * flush that folds it: the step computes e for the current record only,
+ * reads the window's e from ring->e and appends the new one there. The
+ * checkpoint is still never written outside a flush. */
 RSSM_API int rssm_gdn_step(const rssm_gdn_desc* desc, float* S, const rssm_gdn_ring* ring,
                   int32_t* cursors, const rssm_bf16* q, const rssm_bf16* k,
                   const rssm_bf16* v, const float* g, const float* beta,
@@ -249,6 +257,14 @@ RSSM_API int rssm_gdn_step(const rssm_gdn_desc* desc, float* S, const rssm_gdn_r
 /* Standalone flush for Gated DeltaNet (as rssm_mamba2_flush). */
 RSSM_API int rssm_gdn_flush(const rssm_gdn_desc* desc, float* S, const rssm_gdn_ring* ring,
                    int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
+
+/* Fills ring->e for the records already in each sequence's window (count of
+ * them, from its checkpoint S), for windows whose records were written into
+ * the ring directly rather than appended by rssm_gdn_step. The pages have no
+ * counterpart (their windows are only filled by decode steps). Writes ring->e
+ * only; sequences with count == 0 or pending != 0 are skipped. */
+RSSM_API int rssm_gdn_prime(const rssm_gdn_desc* desc, const float* S, const rssm_gdn_ring* ring,
+                   const int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
 
 /* ----------------------------------------------------------------------------
  * Misc

@@ -44,7 +44,7 @@ class rssm_gdn_desc(ctypes.Structure):
 
 
 class rssm_gdn_ring(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in ("q", "k", "v", "g", "beta")]
+    _fields_ = [(n, c_void_p) for n in ("q", "k", "v", "g", "beta", "e")]
 
 
 P = c_void_p
@@ -63,6 +63,7 @@ _SIGNATURES = {
     "rssm_gdn_conventional_step": (c_int, [P] * 8 + [P]),
     "rssm_gdn_step": (c_int, [P] * 11 + [P]),
     "rssm_gdn_flush": (c_int, [P] * 5 + [P]),
+    "rssm_gdn_prime": (c_int, [P] * 5 + [P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -132,8 +133,8 @@ def gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype=RSSM_F32):
     return rssm_gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype)
 
 
-def gdn_ring(q, k, v, g, beta):
-    return rssm_gdn_ring(ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta))
+def gdn_ring(q, k, v, g, beta, e):
+    return rssm_gdn_ring(ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), ptr(e))
 
 
 def _ref(s):
@@ -153,7 +154,7 @@ def rssm_mamba2_ring_bytes(desc):
 
 
 def rssm_gdn_ring_bytes(desc):
-    out = (c_size_t * 5)()
+    out = (c_size_t * 6)()
     check(load().rssm_gdn_ring_bytes(_ref(desc), out), "rssm_gdn_ring_bytes")
     return list(out)
 
@@ -210,4 +211,9 @@ def rssm_gdn_step(desc, S, ring, cursors, q, k, v, g, beta, o, dev_status=None, 
 
 def rssm_gdn_flush(desc, S, ring, cursors, dev_status=None, stream=None):
     return load().rssm_gdn_flush(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status),
+                                 _stream(stream, S))
+
+
+def rssm_gdn_prime(desc, S, ring, cursors, dev_status=None, stream=None):
+    return load().rssm_gdn_prime(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status),
                                  _stream(stream, S))

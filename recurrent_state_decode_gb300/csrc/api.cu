@@ -116,7 +116,7 @@ int rssm_mamba2_ring_bytes(const rssm_mamba2_desc* d, size_t bytes[5]) {
   return RSSM_OK;
 }
 
-int rssm_gdn_ring_bytes(const rssm_gdn_desc* d, size_t bytes[5]) {
+int rssm_gdn_ring_bytes(const rssm_gdn_desc* d, size_t bytes[6]) {
   int rc = check_gdn(d);
   if (rc) return rc;
   if (!bytes) return RSSM_ERR_INVALID_ARG;
@@ -124,6 +124,7 @@ int rssm_gdn_ring_bytes(const rssm_gdn_desc* d, size_t bytes[5]) {
   bytes[0] = bytes[1] = Bt * H * L * d->dk * 2;
   bytes[2] = Bt * H * L * d->dv * 2;
   bytes[3] = bytes[4] = Bt * H * pad4(d->buf_len) * 4;
+  bytes[5] = Bt * H * L * d->dv * 4;
   return RSSM_OK;
 }
 
@@ -277,7 +278,8 @@ int rssm_gdn_step(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, i
   if (rc) return rc;
   if (d->batch == 0) return RSSM_OK;
   if (!ring) return RSSM_ERR_INVALID_ARG;
-  if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, cursors, q, k, v, g, beta, o}))) return rc;
+  if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors, q, k, v, g, beta, o})))
+    return rc;
   if ((rc = check_opt(dev_status))) return rc;
   GdnArgs a = gdn_args(d);
   a.S = S;
@@ -286,6 +288,7 @@ int rssm_gdn_step(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, i
   a.rv = ring->v;
   a.rg = ring->g;
   a.rbeta = ring->beta;
+  a.re = ring->e;
   a.cursors = cursors;
   a.q = q;
   a.k = k;
@@ -314,11 +317,33 @@ int rssm_gdn_flush(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, 
   a.rv = ring->v;
   a.rg = ring->g;
   a.rbeta = ring->beta;
+  a.re = ring->e;
   a.cursors = cursors;
   a.status = dev_status;
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = cuda_rc(gdn_launch(GDN_FLUSH, a, 0, st)))) return rc;
   return cuda_rc(cursor_launch(CUR_FLUSH, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+int rssm_gdn_prime(const rssm_gdn_desc* d, const float* S, const rssm_gdn_ring* ring, const int32_t* cursors,
+                   int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors}))) return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.S = const_cast<float*>(S);  // read only in this mode
+  a.rq = ring->q;
+  a.rk = ring->k;
+  a.rv = ring->v;
+  a.rg = ring->g;
+  a.rbeta = ring->beta;
+  a.re = ring->e;
+  a.cursors = const_cast<int32_t*>(cursors);  // read only in this mode
+  a.status = dev_status;
+  return cuda_rc(gdn_launch(GDN_PRIME, a, 0, (cudaStream_t)stream));
 }
 
 }  // extern "C"

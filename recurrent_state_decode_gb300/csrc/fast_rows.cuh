@@ -27,6 +27,12 @@ __device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
                     __shfl_sync(FULL, v.w, src));
 }
 
+// Every lane must call this (a full-warp shuffle).
+__device__ __forceinline__ float4 shfl_f4(float4 v, int src) {
+  return make_float4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
+                     __shfl_sync(FULL, v.w, src));
+}
+
 // y[r] before the gate for 8 rows: sum over lanes of (h . PC) + t[r], where
 // t[r] is the lane's window term. The total of row rr ends in lane row_src(rr).
 __device__ __forceinline__ float rows8(const float4 (&hv)[8], float4 pc, const float (&t)[8], int lane) {

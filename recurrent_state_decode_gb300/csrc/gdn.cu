@@ -146,10 +146,14 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_conventional_kernel(GdnArgs a
 
 // ------------------------------------------------------------------ replay step / flush
 
-// FLUSH_ONLY: the standalone flush (window = the count committed records, no
-// output, no append). Otherwise the AR step (window = committed + current).
-template <int NJ, bool OUT_BF16, bool FLUSH_ONLY>
+// MODE GDN_STEP: the AR step (window = committed + current; the current
+// record's e_t goes to the ring unless the step flushes). GDN_FLUSH: the
+// standalone flush (window = the count committed records, no output, no
+// append). GDN_PRIME: e_t of the count committed records into the ring, no
+// output, no state written.
+template <int NJ, bool OUT_BF16, int MODE>
 __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
+  constexpr bool FLUSH_ONLY = MODE != GDN_STEP;  // window without a current record
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nRB = (a.DV + GDN_RB - 1) / GDN_RB;
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
   if (FLUSH_ONLY) {
     if (start < 0 || start >= L || count <= 0 || count > L || cur.z != 0) return;
     m = count;
-    flush = true;
+    flush = MODE == GDN_FLUSH;
   } else {
     if (start < 0 || start >= L || count < 0 || count >= L || cur.z != 0) return;
     m = count + 1;
@@ -288,7 +292,13 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
     float e = s.sb[t] * s.vs[(size_t)t * GDN_RB + rloc] - s.bg[t] * u;
     for (int sidx = 0; sidx < t; sidx++) e = fmaf(-s.Mts[t * L + sidx], es_row[(size_t)sidx * GDN_RB], e);
     __syncwarp();
-    if (q4 == 0) es_row[(size_t)t * GDN_RB] = e;
+    if (q4 == 0) {
+      es_row[(size_t)t * GDN_RB] = e;
+      // the ring keeps e of every record it holds: all of them when priming,
+      // the current one on a non-flush step
+      if (MODE == GDN_PRIME || (MODE == GDN_STEP && !flush && t == m - 1))
+        a.re[(bh * L + (start + t) % L) * DV + i0 + rloc] = e;
+    }
     __syncwarp();
   }
   const float gm = s.misc[0];
@@ -360,13 +370,17 @@ cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st
       })
       return e;
     case GDN_STEP:
+      if (gdn_step_fast_applies(a)) return gdn_step_fast_launch(a, out_bf16, st);
       RSSM_DISPATCH_NJ(NJ, {
-        e = out_bf16 ? launch_gdn(gdn_replay_kernel<NJ, true, false>, grid, smem, st, a)
-                     : launch_gdn(gdn_replay_kernel<NJ, false, false>, grid, smem, st, a);
+        e = out_bf16 ? launch_gdn(gdn_replay_kernel<NJ, true, GDN_STEP>, grid, smem, st, a)
+                     : launch_gdn(gdn_replay_kernel<NJ, false, GDN_STEP>, grid, smem, st, a);
       })
       return e;
     case GDN_FLUSH:
-      RSSM_DISPATCH_NJ(NJ, { e = launch_gdn(gdn_replay_kernel<NJ, false, true>, grid, smem, st, a); })
+      RSSM_DISPATCH_NJ(NJ, { e = launch_gdn(gdn_replay_kernel<NJ, false, GDN_FLUSH>, grid, smem, st, a); })
+      return e;
+    case GDN_PRIME:
+      RSSM_DISPATCH_NJ(NJ, { e = launch_gdn(gdn_replay_kernel<NJ, false, GDN_PRIME>, grid, smem, st, a); })
       return e;
   }
   return cudaErrorInvalidValue;

@@ -1,0 +1,223 @@
+// ReplaySSM AR decode step for Gated DeltaNet, shape-specialised fast path:
+// dk = dv = 128, L <= 31 ("How ReplaySSM works": non-flush steps read the
+// checkpoint and the window and write no state; the L-th step folds the window
+// and writes the state once).
+//
+// Algebra (the gated delta rule S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T)
+// + beta_t v_t k_t^T rewritten as S_t = alpha_t S_{t-1} + e_t k_t^T with
+// e_t = beta_t (v_t - alpha_t S_{t-1} k_t)). Window records t = 0..m-1 (the
+// last is the current one), D(t, s) = exp(sum_{s<j<=t} g_j), gamma = D(m-1, -1):
+//   e_cur = beta (v - gamma S0 k - sum_{t<m-1} D(m-1,t) (k_t . k) e_t)
+//   o     = gamma S0 q + sum_{t<m-1} D(m-1,t) (k_t . q) e_t + (k . q) e_cur
+//   S_m   = gamma S0 + sum_{t<=m-1} D(m-1,t) e_t k_t^T             (flush only)
+// e_t of a committed record depends on S0 and earlier records only, so it is
+// read from the ring (written when the record was current) instead of being
+// solved again: a step costs two matvecs of the checkpoint (S0 k, S0 q).
+//
+// One CTA of four warps per (sequence, head, 64 state rows); warp w owns rows
+// 8w..8w+7 and 32+8w..32+8w+7, lane l the float4 column chunk 4l..4l+3. Every
+// load is issued at launch, none waiting on the cursor: the 64 rows by one bulk
+// copy (TMA, non-tensor; never multicast) into shared memory; lane s ring slot
+// s (g, and e of the warp's 16 rows); the current record. Warp w forms the dots
+// k_s . k and k_s . q of ring slots w, w+4, ... (slot L: the current k), one
+// transposed reduction, shared through shared memory. After the cursor, lane t
+// takes record t by a shuffle and one suffix scan gives every D(m-1, t). Per
+// 8-row group one transposed 16-value reduction yields, for each row,
+// gamma S0 k + the window's k-term and gamma S0 q + the window's q-term (the
+// window terms are each lane's partials, added before the reduction).
+#include "fast_rows.cuh"
+#include "kernels.h"
+
+namespace rssm {
+
+namespace {
+
+using namespace fastrows;
+
+constexpr int GD = 128;  // dk = dv
+constexpr int KW = 8;    // dot entries per warp: 4 x 8 >= L + 1
+
+__device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// 16 partials for 8 rows: [rr] = h[rr] . ka + tk[rr], [8 + rr] = h[rr] . qa + tq[rr].
+// Lane l ends with partial l >> 1.
+__device__ __forceinline__ float rows8x2(const float4 (&hv)[8], float4 ka, float4 qa, const float (&tk)[8],
+                                         const float (&tq)[8], int lane) {
+  float v[16];
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) {
+    v[rr] = fmaf(hv[rr].x, ka.x, fmaf(hv[rr].y, ka.y, fmaf(hv[rr].z, ka.z, fmaf(hv[rr].w, ka.w, tk[rr]))));
+    v[8 + rr] = fmaf(hv[rr].x, qa.x, fmaf(hv[rr].y, qa.y, fmaf(hv[rr].z, qa.z, fmaf(hv[rr].w, qa.w, tq[rr]))));
+  }
+  return reduce_transpose<16>(v, lane);
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
+  __shared__ __align__(128) float tile[FPB * GD];
+  __shared__ float skk[FW * KW], skq[FW * KW];  // k_s . k, k_s . q by ring slot; [L] = current
+  __shared__ uint64_t bar;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int L = a.L, H = a.H;
+  const int pb = blockIdx.x & 1, bhi = blockIdx.x >> 1;
+  const int b = bhi / H;
+  const size_t bh = bhi;
+  const int p0 = pb * FPB;
+  const size_t tbase = (bh * GD + p0) * GD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, FPB * GD * 4);
+    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar);
+  }
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
+  const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's row groups (within the block)
+  // ring slot `lane`: g and the cached e of the warp's rows
+  const float gs = lane < L ? a.rg[bh * pad4(L) + lane] : 0.f;
+  float4 e0 = make_float4(0.f, 0.f, 0.f, 0.f), e1 = e0, e2 = e0, e3 = e0;
+  if (lane < L) {
+    const float* ep = a.re + (bh * L + lane) * GD + p0;
+    e0 = ld_f4(ep + rl0);
+    e1 = ld_f4(ep + rl0 + 4);
+    e2 = ld_f4(ep + rl1);
+    e3 = ld_f4(ep + rl1 + 4);
+  }
+  // the current record
+  const uint2 kraw = *reinterpret_cast<const uint2*>(a.k + bh * GD + lane * 4);
+  const uint2 qraw = *reinterpret_cast<const uint2*>(a.q + bh * GD + lane * 4);
+  const float gm = a.g[bh], bm = a.beta[bh];
+  const int vr = (lane >> 1) & 7;  // the row this lane finishes (lanes 0..15)
+  const uint16_t vbA = a.v[bh * GD + p0 + rl0 + vr], vbB = a.v[bh * GD + p0 + rl1 + vr];
+  {  // k_s . k and k_s . q for ring slots s = warp + 4 j (s == L: the current k)
+    const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
+    float pk[2 * KW];
+#pragma unroll
+    for (int j = 0; j < KW; j++) {
+      const int s = warp + FW * j;
+      const float4 ks = s < L ? load_bf4(rkp + s * GD) : (s == L ? bf4_to_f4(kraw) : make_float4(0.f, 0.f, 0.f, 0.f));
+      pk[2 * j] = dot4(ks, bf4_to_f4(kraw));
+      pk[2 * j + 1] = dot4(ks, bf4_to_f4(qraw));
+    }
+    const float red = reduce_transpose<2 * KW>(pk, lane);  // lane l: partial l >> 1 = (slot j = l >> 2, k or q)
+    if ((lane & 1) == 0) ((lane & 2) ? skq : skk)[warp + FW * (lane >> 2)] = red;
+  }
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
+  if (!valid) {  // reported by the cursor kernel (uniform over the block)
+    if (threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
+    return;
+  }
+  const int start = cur.x, count = cur.y, m = count + 1;
+  const bool flush = (m == L);
+  const int scur = start + count < L ? start + count : start + count - L;  // the current record's slot
+  // window, lane t = record t
+  int sl = start + lane;
+  sl = sl < L ? sl : sl - L;
+  const float gr = __shfl_sync(FULL, gs, sl);
+  const float gt = lane < count ? gr : (lane == count ? gm : 0.f);
+  float sfx = gt;  // sum_{t<=j<=m-1} g_j
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_down_sync(FULL, sfx, o);
+    if (lane + o < 32) sfx += v;
+  }
+  float ex = __shfl_down_sync(FULL, sfx, 1);  // sum_{t<j<=m-1} g_j
+  if (lane == 31) ex = 0.f;
+  const float gamma = expf(__shfl_sync(FULL, sfx, 0));
+  const float Dt = expf(ex);  // D(m-1, t)
+  float4 f0 = shfl_f4(e0, sl), f1 = shfl_f4(e1, sl), f2 = shfl_f4(e2, sl), f3 = shfl_f4(e3, sl);
+  if (lane >= count) f0 = f1 = f2 = f3 = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  const int ent = lane < count ? sl : L;
+  const float cK = lane < count ? Dt * skk[ent] : 0.f;
+  const float cQ = lane < count ? Dt * skq[ent] : 0.f;
+  const float kq_cur = skq[L];
+  const float4 ka = scale4(gamma, bf4_to_f4(kraw)), qa = scale4(gamma, bf4_to_f4(qraw));
+  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
+    if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
+    mbar_wait(&bar, 0);
+    return;
+  }
+#pragma unroll
+  for (int half = 0; half < 2; half++) {
+    const int rl = half ? rl1 : rl0;
+    const float4 ea = half ? f2 : f0, eb = half ? f3 : f1;
+    const float el[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};  // e_t of the 8 rows (lane t)
+    float4 hv[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * GD)[lane];
+    float tk[8], tq[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) {
+      tk[rr] = cK * el[rr];
+      tq[rr] = cQ * el[rr];
+    }
+    // lanes 0..15: gamma S0 k + k-term of row vr; lanes 16..31: the q counterpart
+    const float tot = rows8x2(hv, ka, qa, tk, tq, lane);
+    const float yq = __shfl_down_sync(FULL, tot, 16);
+    const float ec = bm * (bf_to_f(half ? vbB : vbA) - tot);  // e of the current record, row vr (lanes < 16)
+    const size_t row = bh * GD + p0 + rl + vr;
+    if (lane < 16 && (lane & 1) == 0) {
+      store_y<OUT_BF16>(a.o, row, fmaf(kq_cur, ec, yq));
+      if (!flush) a.re[(bh * L + scur) * GD + p0 + rl + vr] = ec;
+    }
+    if (flush) {  // S_m = gamma S0 + sum_t D(m-1,t) e_t k_t^T, written once
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(gamma, hv[rr]);
+      const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
+      for (int t0 = 0; t0 < count; t0 += 4) {
+        float4 kt[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          int s = start + t0 + u;
+          s = s < L ? s : s - L;
+          kt[u] = t0 + u < count ? load_bf4(rkp + s * GD) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          const int t = (t0 + u) & 31;
+          const float c = __shfl_sync(FULL, Dt, t);
+#pragma unroll
+          for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(c * __shfl_sync(FULL, el[rr], t), kt[u], hv[rr]);
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(__shfl_sync(FULL, ec, 2 * rr), bf4_to_f4(kraw), hv[rr]);  // current, D = 1
+#pragma unroll
+      for (int rr = 0; rr < 8; rr++) __stcs(reinterpret_cast<float4*>(a.S + tbase + (size_t)(rl + rr) * GD) + lane, hv[rr]);
+    }
+  }
+  if (!flush) {  // append the current record (its e went to the ring above)
+    const size_t vrow = (bh * L + scur) * GD + p0 + vr;
+    if (lane < 16 && (lane & 1) == 0) {
+      a.rv[vrow + rl0] = vbA;
+      a.rv[vrow + rl1] = vbB;
+    }
+    if (pb == 0 && warp == 0) {
+      const size_t krow = (bh * L + scur) * GD + lane * 4;
+      *reinterpret_cast<uint2*>(a.rk + krow) = kraw;
+      *reinterpret_cast<uint2*>(a.rq + krow) = qraw;
+      if (lane == 0) {
+        a.rg[bh * pad4(L) + scur] = gm;
+        a.rbeta[bh * pad4(L) + scur] = bm;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+bool gdn_step_fast_applies(const GdnArgs& a) { return a.DK == GD && a.DV == GD && a.L <= FW * KW - 1; }
+
+cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
+  const long long nblk = (long long)a.Bt * a.H * 2;
+  if (nblk == 0) return cudaSuccess;
+  auto k = out_bf16 ? gdn_step_fast_kernel<true> : gdn_step_fast_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  k<<<(unsigned)nblk, FT, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rssm

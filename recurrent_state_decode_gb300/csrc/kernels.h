@@ -44,6 +44,7 @@ struct GdnArgs {
   float* S;
   uint16_t *rq, *rk, *rv;
   float *rg, *rbeta;
+  float* re;  // cached corrections e_t [Bt, H, L, DV]
   int32_t* cursors;
   const uint16_t *q, *k, *v;
   const float *g, *beta;
@@ -51,9 +52,12 @@ struct GdnArgs {
   int32_t* status;
 };
 
-enum { GDN_CONVENTIONAL = 0, GDN_STEP = 1, GDN_FLUSH = 2 };
+enum { GDN_CONVENTIONAL = 0, GDN_STEP = 1, GDN_FLUSH = 2, GDN_PRIME = 3 };
 
 cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st);
+// Shape-specialised AR step (dk = dv = 128, L <= 31; gdn_step_fast.cu).
+bool gdn_step_fast_applies(const GdnArgs& a);
+cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
 
 // Cursor kernels (one thread per sequence).
 enum { CUR_AR = 0, CUR_FLUSH = 1, CUR_COMMIT = 2 };

@@ -81,7 +81,8 @@ class GDNState:
         self.rv = torch.zeros((batch, nheads, buf_len, dv), dtype=torch.bfloat16, device=dev)
         self.rg = torch.zeros((batch, nheads, (buf_len + 3) // 4 * 4), dtype=torch.float32, device=dev)
         self.rbeta = torch.zeros_like(self.rg)
-        self.ring = bd.gdn_ring(self.rq, self.rk, self.rv, self.rg, self.rbeta)
+        self.re = torch.zeros((batch, nheads, buf_len, dv), dtype=torch.float32, device=dev)
+        self.ring = bd.gdn_ring(self.rq, self.rk, self.rv, self.rg, self.rbeta, self.re)
         self.cursors = torch.zeros((batch, 4), dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -99,6 +100,11 @@ class GDNState:
     def flush(self, stream=None):
         bd.check(bd.rssm_gdn_flush(self.desc, self.S, self.ring, self.cursors, self.status, stream),
                  "rssm_gdn_flush")
+
+    def prime(self, stream=None):
+        """Fill the ring's corrections e for records placed into the window directly."""
+        bd.check(bd.rssm_gdn_prime(self.desc, self.S, self.ring, self.cursors, self.status, stream),
+                 "rssm_gdn_prime")
 
 
 def mamba2_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32, read_copy=None):
@@ -133,4 +139,5 @@ def gdn_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32):
         I.place_window(ring, pre[field], starts, counts, w.buf_len)
     st.cursors[:, 0] = starts
     st.cursors[:, 1] = counts
+    st.prime()
     return st, pre, starts, counts

@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 14
+    assert len(declared) == 15
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -55,7 +55,8 @@ def test_ring_bytes(lib):
     d = bd.mamba2_desc(256, 128, 64, 128, 8, 16)
     assert bd.rssm_mamba2_ring_bytes(d) == [256 * 128 * 16 * 64 * 2] * 2 + [256 * 8 * 16 * 128 * 2] * 2 + [256 * 128 * 16 * 4]
     g = bd.gdn_desc(256, 32, 128, 128, 16)
-    assert bd.rssm_gdn_ring_bytes(g) == [256 * 32 * 16 * 128 * 2] * 3 + [256 * 32 * 16 * 4] * 2
+    assert bd.rssm_gdn_ring_bytes(g) == [256 * 32 * 16 * 128 * 2] * 3 + [256 * 32 * 16 * 4] * 2 + \
+        [256 * 32 * 16 * 128 * 4]
 
 
 ALIGNED = 1 << 20  # a fake, 16-byte aligned address: never dereferenced because validation fails first
@@ -127,7 +128,7 @@ def test_cursor_call_validation(lib):
 
 
 def test_gdn_validation(lib):
-    ring = bd.rssm_gdn_ring(*([ALIGNED] * 5))
+    ring = bd.rssm_gdn_ring(*([ALIGNED] * 6))
     for desc in ((4, 2, 60, 128, 16), (4, 2, 128, 512, 16), (4, 0, 128, 128, 16), (4, 2, 128, 128, 40)):
         d = bd.gdn_desc(*desc)
         assert lib.rssm_gdn_step(ctypes.byref(d), ALIGNED, ctypes.byref(ring), *([ALIGNED] * 7), None, None) == \
@@ -138,6 +139,14 @@ def test_gdn_validation(lib):
     assert lib.rssm_gdn_flush(ctypes.byref(d), ALIGNED, None, ALIGNED, None, None) == bd.RSSM_ERR_INVALID_ARG
     d0 = bd.gdn_desc(0, 2, 128, 128, 16)
     assert lib.rssm_gdn_flush(ctypes.byref(d0), None, None, None, None, None) == bd.RSSM_OK
+    # the step and the prime need the ring's e field
+    no_e = bd.rssm_gdn_ring(*([ALIGNED] * 5), None)
+    assert lib.rssm_gdn_step(ctypes.byref(d), ALIGNED, ctypes.byref(no_e), *([ALIGNED] * 7), None, None) == \
+        bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_gdn_prime(ctypes.byref(d), ALIGNED, ctypes.byref(no_e), ALIGNED, None, None) == \
+        bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_gdn_prime(ctypes.byref(d), ALIGNED, None, ALIGNED, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_gdn_prime(ctypes.byref(d0), None, None, None, None, None) == bd.RSSM_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

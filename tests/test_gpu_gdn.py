@@ -60,7 +60,10 @@ GSHAPES = [
     GW("gdn_L1", 2, 2, 32, 32, 1, 5, seed=73),
     GW("gdn_L32", 2, 2, 32, 48, 32, 70, seed=74),
     GW("gdn_big_tile", 2, 1, 256, 256, 4, 9, seed=75),       # 4 row blocks, 16 chunks per thread
-    GW("gdn_128", 2, 4, 128, 128, 16, 34, seed=76),          # the serving tile
+    GW("gdn_128", 2, 4, 128, 128, 16, 34, seed=76),          # the serving tile (shape-specialised kernel)
+    GW("gdn_128_L1", 2, 3, 128, 128, 1, 6, seed=79),         # every step flushes
+    GW("gdn_128_L5", 3, 2, 128, 128, 5, 23, seed=80),        # ragged window, wraps often
+    GW("gdn_128_L31", 2, 2, 128, 128, 31, 70, seed=81),      # longest window of that kernel
 ]
 
 
@@ -106,4 +109,28 @@ def test_gdn_standalone_flush():
     np.testing.assert_array_equal(cur[:, 1:], 0)
     for b in range(w.batch):
         assert H.rel_l2(H.F64(st.S[b]), exp["state"][b]) <= TOL_CKPT
+    assert H.status(st) == 0
+
+
+@pytest.mark.parametrize("w", [GW("gprime", 3, 2, 128, 128, 16, 1, seed=82),
+                               GW("gprime_small", 3, 2, 40, 24, 7, 1, seed=83)], ids=lambda w: w.name)
+def test_gdn_prime_matches_window_corrections(w):
+    """rssm_gdn_prime fills ring.e with each window record's correction e_t,
+    checked against the oracle's forward substitution."""
+    st, pre, starts, counts = H.gdn_setup(w, "cuda")  # places the windows, then primes
+    S0 = H.F64(st.S)
+    re = H.F64(st.re)
+    checked = 0
+    for b in range(w.batch):
+        c, s0 = int(counts[b]), int(starts[b])
+        if c == 0:
+            continue
+        r = {k: H.F64(v[b, :c]) for k, v in pre.items()}  # [c, H, ...]
+        ks, vs = np.moveaxis(r["k"], 0, 1), np.moveaxis(r["v"], 0, 1)
+        gs, bs = r["g"].T, r["beta"].T
+        _, e = og._window_terms(S0[b], ks, vs, gs, bs)  # e [H, c, dv]
+        slots = [(s0 + t) % w.buf_len for t in range(c)]
+        assert H.rel_l2(re[b][:, slots], e) <= 1e-5
+        checked += 1
+    assert checked > 0
     assert H.status(st) == 0
