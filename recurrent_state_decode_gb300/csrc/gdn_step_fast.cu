@@ -18,7 +18,9 @@
 // 8w..8w+7 and 32+8w..32+8w+7, lane l the float4 column chunk 4l..4l+3. Every
 // load is issued at launch, none waiting on the cursor: the 64 rows by one bulk
 // copy (TMA, non-tensor; never multicast) into shared memory; lane s ring slot
-// s (g, and e of the warp's 16 rows); the current record. Warp w forms the dots
+// s (g); the current record. Once the cursor is known thread 0 also copies the
+// window records' e rows of this block (one 256-byte bulk copy each, on a
+// second mbarrier), so that only the window's corrections are read. Warp w forms the dots
 // k_s . k and k_s . q of ring slots w, w+4, ... (slot L: the current k), one
 // transposed reduction, shared through shared memory. After the cursor, lane t
 // takes record t by a shuffle and one suffix scan gives every D(m-1, t). Per
@@ -36,6 +38,7 @@ using namespace fastrows;
 
 constexpr int GD = 128;  // dk = dv
 constexpr int KW = 8;    // dot entries per warp: 4 x 8 >= L + 1
+constexpr int ES = FPB + 4;  // floats per staged e row (padded against bank conflicts; 16-byte multiple)
 
 __device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
@@ -54,9 +57,11 @@ __device__ __forceinline__ float rows8x2(const float4 (&hv)[8], float4 ka, float
 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
-  __shared__ __align__(128) float tile[FPB * GD];
+  extern __shared__ __align__(128) float dsm[];
+  float* tile = dsm;               // the block's 64 rows
+  float* es = dsm + FPB * GD;      // e of window record t at es + t * ES (the block's rows)
   __shared__ float skk[FW * KW], skq[FW * KW];  // k_s . k, k_s . q by ring slot; [L] = current
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar[2];      // [0] the rows, [1] the window's e
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = a.L, H = a.H;
   const int pb = blockIdx.x & 1, bhi = blockIdx.x >> 1;
@@ -66,23 +71,16 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const size_t tbase = (bh * GD + p0) * GD;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, FPB * GD * 4);
-    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar);
+    mbar_arrive_expect_tx(&bar[0], FPB * GD * 4);
+    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's row groups (within the block)
-  // ring slot `lane`: g and the cached e of the warp's rows
+  // ring slot `lane`: g
   const float gs = lane < L ? a.rg[bh * pad4(L) + lane] : 0.f;
-  float4 e0 = make_float4(0.f, 0.f, 0.f, 0.f), e1 = e0, e2 = e0, e3 = e0;
-  if (lane < L) {
-    const float* ep = a.re + (bh * L + lane) * GD + p0;
-    e0 = ld_f4(ep + rl0);
-    e1 = ld_f4(ep + rl0 + 4);
-    e2 = ld_f4(ep + rl1);
-    e3 = ld_f4(ep + rl1 + 4);
-  }
   // the current record
   const uint2 kraw = *reinterpret_cast<const uint2*>(a.k + bh * GD + lane * 4);
   const uint2 qraw = *reinterpret_cast<const uint2*>(a.q + bh * GD + lane * 4);
@@ -103,12 +101,17 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     if ((lane & 1) == 0) ((lane & 2) ? skq : skk)[warp + FW * (lane >> 2)] = red;
   }
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
-  if (!valid) {  // reported by the cursor kernel (uniform over the block)
-    if (threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
-    return;
+  // An invalid cursor (reported by the cursor kernel) runs as an empty window
+  // with every store masked, so that no lane leaves before the shuffles below.
+  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, m = count + 1;
+  if (threadIdx.x == 0) {  // the window's e rows of this block, in record order
+    mbar_arrive_expect_tx(&bar[1], (uint32_t)count * FPB * 4);
+    for (int t = 0; t < count; t++) {
+      const int s = start + t < L ? start + t : start + t - L;
+      bulk_load(es + t * ES, a.re + (bh * L + s) * GD + p0, FPB * 4, &bar[1]);
+    }
   }
-  const int start = cur.x, count = cur.y, m = count + 1;
-  const bool flush = (m == L);
+  const bool flush = valid && m == L;
   const int scur = start + count < L ? start + count : start + count - L;  // the current record's slot
   // window, lane t = record t
   int sl = start + lane;
@@ -125,24 +128,28 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   if (lane == 31) ex = 0.f;
   const float gamma = expf(__shfl_sync(FULL, sfx, 0));
   const float Dt = expf(ex);  // D(m-1, t)
-  float4 f0 = shfl_f4(e0, sl), f1 = shfl_f4(e1, sl), f2 = shfl_f4(e2, sl), f3 = shfl_f4(e3, sl);
-  if (lane >= count) f0 = f1 = f2 = f3 = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   const int ent = lane < count ? sl : L;
   const float cK = lane < count ? Dt * skk[ent] : 0.f;
   const float cQ = lane < count ? Dt * skq[ent] : 0.f;
   const float kq_cur = skq[L];
   const float4 ka = scale4(gamma, bf4_to_f4(kraw)), qa = scale4(gamma, bf4_to_f4(qraw));
-  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
+  const bool ok0 = mbar_wait(&bar[0], 0), ok1 = mbar_wait(&bar[1], 0);
+  if (!__all_sync(FULL, ok0 && ok1)) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
-    mbar_wait(&bar, 0);
+    mbar_wait(&bar[0], 0);
+    mbar_wait(&bar[1], 0);
     return;
   }
 #pragma unroll
   for (int half = 0; half < 2; half++) {
     const int rl = half ? rl1 : rl0;
-    const float4 ea = half ? f2 : f0, eb = half ? f3 : f1;
-    const float el[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};  // e_t of the 8 rows (lane t)
+    float4 ea = make_float4(0.f, 0.f, 0.f, 0.f), eb = ea;  // e_t of the 8 rows (lane t)
+    if (lane < count) {
+      ea = ld_f4(es + lane * ES + rl);
+      eb = ld_f4(es + lane * ES + rl + 4);
+    }
+    const float el[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
     float4 hv[8];
 #pragma unroll
     for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * GD)[lane];
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     const float yq = __shfl_down_sync(FULL, tot, 16);
     const float ec = bm * (bf_to_f(half ? vbB : vbA) - tot);  // e of the current record, row vr (lanes < 16)
     const size_t row = bh * GD + p0 + rl + vr;
-    if (lane < 16 && (lane & 1) == 0) {
+    if (valid && lane < 16 && (lane & 1) == 0) {
       store_y<OUT_BF16>(a.o, row, fmaf(kq_cur, ec, yq));
       if (!flush) a.re[(bh * L + scur) * GD + p0 + rl + vr] = ec;
     }
@@ -165,20 +172,24 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(gamma, hv[rr]);
       const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
-      for (int t0 = 0; t0 < count; t0 += 4) {
-        float4 kt[4];
+      for (int t0 = 0; t0 < count; t0 += 2) {  // e_t rows from shared memory (a broadcast read)
+        float4 kt[2];
 #pragma unroll
-        for (int u = 0; u < 4; u++) {
+        for (int u = 0; u < 2; u++) {
           int s = start + t0 + u;
           s = s < L ? s : s - L;
           kt[u] = t0 + u < count ? load_bf4(rkp + s * GD) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < 4; u++) {
-          const int t = (t0 + u) & 31;
-          const float c = __shfl_sync(FULL, Dt, t);
+        for (int u = 0; u < 2; u++) {
+          const int t = t0 + u;
+          const float c = __shfl_sync(FULL, Dt, t & 31);
+          if (t < count) {  // uniform
+            const float4 ea2 = ld_f4(es + t * ES + rl), eb2 = ld_f4(es + t * ES + rl + 4);
+            const float et[8] = {ea2.x, ea2.y, ea2.z, ea2.w, eb2.x, eb2.y, eb2.z, eb2.w};
 #pragma unroll
-          for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(c * __shfl_sync(FULL, el[rr], t), kt[u], hv[rr]);
+            for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(c * et[rr], kt[u], hv[rr]);
+          }
         }
       }
 #pragma unroll
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
       for (int rr = 0; rr < 8; rr++) __stcs(reinterpret_cast<float4*>(a.S + tbase + (size_t)(rl + rr) * GD) + lane, hv[rr]);
     }
   }
-  if (!flush) {  // append the current record (its e went to the ring above)
+  if (valid && !flush) {  // append the current record (its e went to the ring above)
     const size_t vrow = (bh * L + scur) * GD + p0 + vr;
     if (lane < 16 && (lane & 1) == 0) {
       a.rv[vrow + rl0] = vbA;
@@ -213,10 +224,12 @@ cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st
   const long long nblk = (long long)a.Bt * a.H * 2;
   if (nblk == 0) return cudaSuccess;
   auto k = out_bf16 ? gdn_step_fast_kernel<true> : gdn_step_fast_kernel<false>;
+  const int smem = (FPB * GD + a.L * ES) * 4;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)nblk, FT, 0, st>>>(a);
+  k<<<(unsigned)nblk, FT, smem, st>>>(a);
   return cudaGetLastError();
 }
 
