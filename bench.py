@@ -175,7 +175,9 @@ def profiled_traffic(profile_file, kernel_sources):
         return None
 
 
-KERNEL_SOURCES = ["recurrent_state_decode_gb300/csrc/mamba2_step.cu", "recurrent_state_decode_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["recurrent_state_decode_gb300/csrc/mamba2_step_fast.cu",
+                  "recurrent_state_decode_gb300/csrc/fast_rows.cuh",
+                  "recurrent_state_decode_gb300/csrc/common.cuh"]
 
 
 # ----------------------------------------------------------------------------- oracle (CPU baseline / reference arm)
@@ -352,7 +354,7 @@ def bench_mamba2_ar(args, dist):
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": peak_kind,
                      "traffic": profiled_traffic("mamba2_step_serving.txt", KERNEL_SOURCES),
-                     "kernel": "m2_step_kernel (+ cursor advance, timed per call)"},
+                     "kernel": "m2_step_fast_kernel (+ the cursor advance kernel, timed per call)"},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "e2e": e2e,
