@@ -141,7 +141,9 @@ RSSM_API int rssm_mamba2_conventional_step(const rssm_mamba2_desc* desc, float* 
  *            and write both.
  *  ring      window records (see rssm_mamba2_ring), cursors [batch, 4]
  *  x .. D, y as in rssm_mamba2_conventional_step.
- * Cursors advance by a second kernel in stream order after the step. */
+ * The cursors advance within the call, in stream order (count + 1, or 0 on
+ * the flushing step); while a call runs, the high 16 bits of a cursor's flags
+ * word are in use. */
 RSSM_API int rssm_mamba2_step(const rssm_mamba2_desc* desc, float* ckpt,
                      rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
                      int32_t* cursors, const rssm_bf16* x, const rssm_bf16* z,

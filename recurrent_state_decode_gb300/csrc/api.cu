@@ -175,6 +175,7 @@ int rssm_mamba2_step(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_rea
   a.status = dev_status;
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = cuda_rc(m2_launch(M2_STEP, a, d->out_dtype == RSSM_BF16, st)))) return rc;
+  if (m2_step_fast_applies(a)) return RSSM_OK;  // that kernel advanced the cursors itself
   return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
 }
 
@@ -299,6 +300,7 @@ int rssm_gdn_step(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, i
   a.status = dev_status;
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = cuda_rc(gdn_launch(GDN_STEP, a, d->out_dtype == RSSM_BF16, st)))) return rc;
+  if (gdn_step_fast_applies(a)) return RSSM_OK;  // that kernel advanced the cursors itself
   return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
 }
 

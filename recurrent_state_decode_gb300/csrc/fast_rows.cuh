@@ -58,5 +58,31 @@ __device__ __forceinline__ void store_y(void* y, size_t i, float v) {
 // silu(z) = z sigmoid(z)
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
+// Arrival of one block on its sequence's cursor, once every thread of the
+// block has read the cursor. The high 16 bits of the cursor's flags word count
+// the blocks of this launch that have arrived (the low 16 bits are the flags
+// themselves); the last of the sequence's `nblocks` blocks applies the AR rule
+// -- count + 1 == L ? 0 : count + 1, on a cursor with 0 <= start < L,
+// 0 <= count < L and pending == 0, else the same error report as the cursor
+// kernel and no move -- and clears the arrival count. Called by one thread.
+__device__ __forceinline__ void arrive_ar_cursor(int32_t* cursors, int b, int4 cur, int nblocks, int L,
+                                                 int32_t* status) {
+  __threadfence();
+  int32_t* wp = cursors + 4 * (size_t)b + 3;
+  const int old = atomicAdd(wp, 1 << 16);
+  if ((old >> 16) != nblocks - 1) return;
+  int4 c = cur;
+  c.w = old & 0xffff;
+  if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L && c.z >= 0))
+    report(status, RSSM_DEV_BAD_CURSOR);
+  else if (c.z != 0)
+    report(status, RSSM_DEV_PENDING);
+  else if (c.y == L)
+    report(status, RSSM_DEV_WINDOW_FULL);
+  else
+    c.y = (c.y + 1 == L) ? 0 : c.y + 1;
+  *reinterpret_cast<int4*>(cursors + 4 * (size_t)b) = c;
+}
+
 }  // namespace fastrows
 }  // namespace rssm

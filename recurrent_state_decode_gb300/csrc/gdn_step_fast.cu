@@ -26,7 +26,9 @@
 // takes record t by a shuffle and one suffix scan gives every D(m-1, t). Per
 // 8-row group one transposed 16-value reduction yields, for each row,
 // gamma S0 k + the window's k-term and gamma S0 q + the window's q-term (the
-// window terms are each lane's partials, added before the reduction).
+// window terms are each lane's partials, added before the reduction). The last
+// of a sequence's blocks to have read its cursor advances it (an arrival count
+// in the high half of the cursor's flags word), so the step is one kernel.
 #include "fast_rows.cuh"
 #include "kernels.h"
 
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const float gamma = expf(__shfl_sync(FULL, sfx, 0));
   const float Dt = expf(ex);  // D(m-1, t)
   __syncthreads();
+  if (threadIdx.x == 0) arrive_ar_cursor(a.cursors, b, cur, a.H * 2, L, a.status);  // every thread has read it
   const int ent = lane < count ? sl : L;
   const float cK = lane < count ? Dt * skk[ent] : 0.f;
   const float cQ = lane < count ? Dt * skq[ent] : 0.f;
@@ -218,7 +221,9 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
 
 }  // namespace
 
-bool gdn_step_fast_applies(const GdnArgs& a) { return a.DK == GD && a.DV == GD && a.L <= FW * KW - 1; }
+bool gdn_step_fast_applies(const GdnArgs& a) {
+  return a.DK == GD && a.DV == GD && a.L <= FW * KW - 1 && a.H * 2 < (1 << 15);
+}
 
 cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   const long long nblk = (long long)a.Bt * a.H * 2;

@@ -418,8 +418,8 @@ cudaError_t m2_launch(int kind, const M2Args& a, int out_bf16, cudaStream_t st) 
       RSSM_DISPATCH_NCH(NCH, { e = launch(m2_flush_kernel<NCH>, grid, smem, st, a); })
       return e;
     case M2_VERIFY:
-      e = m2_verify_fast_applies(a) ? m2_verify_fast_launch(a, out_bf16, st) : m2_verify_launch(a, out_bf16, st);
-      if (e != cudaSuccess) return e;
+      if (m2_verify_fast_applies(a)) return m2_verify_fast_launch(a, out_bf16, st);  // includes the epilogue
+      if ((e = m2_verify_launch(a, out_bf16, st)) != cudaSuccess) return e;
       m2_verify_epilogue_kernel<<<a.Bt, 128, 0, st>>>(a);
       return cudaGetLastError();
   }

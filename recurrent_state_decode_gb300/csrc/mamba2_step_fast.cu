@@ -22,7 +22,9 @@
 // row. On the L-th step the window is folded into the rows and written once,
 // with the bf16 read copy (a block reading the bf16 copy takes its fp32 rows
 // from global memory on that step); otherwise the record is appended to its
-// ring slot. The cursor is only read; a trailing kernel advances it.
+// ring slot. The last of a sequence's blocks to have read its cursor advances
+// it (an arrival count in the high half of the cursor's flags word), so the
+// step needs no second kernel.
 #include "fast_rows.cuh"
 #include "kernels.h"
 
@@ -117,8 +119,12 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
     if ((lane & 3) == 0) sc[warp + FW * reduce8_row(lane)] = red;
   }
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
-  if (!valid) {  // reported by the cursor kernel (uniform over the block)
-    if (threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
+  const int nblocks = a.H * a.nPB;  // blocks of this sequence
+  if (!valid) {  // uniform over the block; the last block of the sequence reports it
+    if (threadIdx.x == 0) {
+      mbar_wait(&bar, 0);  // the copy lands before the block leaves
+      arrive_ar_cursor(a.cursors, b, cur, nblocks, L, a.status);
+    }
     return;
   }
   const int start = cur.x, count = cur.y, m = count + 1;
@@ -141,6 +147,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const float4 pc = scale4(Pm, cm);
   const uint4 xrA = shfl_u4(xsA, sl), xrB = shfl_u4(xsB, sl);
   __syncthreads();
+  if (threadIdx.x == 0) arrive_ar_cursor(a.cursors, b, cur, nblocks, L, a.status);  // every thread has read it
   const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? Dh : 0.f) : 0.f;
   // the gates do not need the checkpoint rows: computed before waiting for them
   const uint4 xq[2] = {lane < count ? xrA : xcA, lane < count ? xrB : xcB};  // lane k: x_k, both groups
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
 }  // namespace
 
 bool m2_step_fast_applies(const M2Args& a) {
-  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.L <= FW * KW - 1;
+  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.L <= FW * KW - 1 && a.H * a.nPB < (1 << 15);
 }
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {

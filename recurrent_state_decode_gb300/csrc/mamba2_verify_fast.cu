@@ -26,8 +26,10 @@
 // + sum_k dt_k e^{S_last - S_k} (B_k . C_i) x_k[r] + D x_last[r]) silu(z_i[r]),
 // last = count + i, one transposed 8-row reduction per output and row group.
 // The new records' x and z rows go to the ring here (these rows are read by
-// this block alone); their B, C and dt rows, which other blocks read, go in the
-// epilogue kernel that follows in stream order.
+// this block alone); their B, C and dt rows, which other blocks read, are
+// appended by the last of the sequence's blocks to finish (an arrival count in
+// the high half of the cursor's flags word), which also marks the cursor
+// pending: a verify is one kernel.
 #include "fast_rows.cuh"
 #include "kernels.h"
 
@@ -39,6 +41,52 @@ using namespace fastrows;
 
 constexpr int KMAX = 4;  // new records per verify on this path
 constexpr int EW = 8;    // B.C entries per warp: 4 warps x 8 = 32 >= L + K
+
+// Epilogue of a verify, run by all threads of the sequence's last block: on a
+// cursor with 0 <= start < L, 0 <= count <= L and pending == 0, append the K
+// new records' B, C (group rows) and dt to the ring and set pending = K, flags
+// = folded; otherwise report as the cursor checks do and leave it (clearing
+// the arrival count in the high half of the flags word).
+__device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur, int flags) {
+  const int L = a.L, H = a.H, G = a.G, K = a.K, tid = threadIdx.x;
+  int4 c = cur;
+  c.w = flags;
+  int err = 0;
+  if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L))
+    err = RSSM_DEV_BAD_CURSOR;
+  else if (c.z != 0)
+    err = RSSM_DEV_PENDING;
+  if (err) {
+    if (tid == 0) {
+      report(a.status, err);
+      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+    }
+    return;
+  }
+  constexpr int NV = FN / 8;  // 16-byte pieces per group row
+  for (int q = tid; q < K * G * NV; q += FT) {
+    const int i = q / (G * NV), r = q - i * G * NV, g = r / NV, v = r - g * NV;
+    int slot = c.x + c.y + i;
+    slot = slot < L ? slot : slot - L;
+    slot = slot < L ? slot : slot - L;
+    const size_t src = (((size_t)b * K + i) * G + g) * FN + v * 8;
+    const size_t dst = (((size_t)b * G + g) * L + slot) * FN + v * 8;
+    *reinterpret_cast<uint4*>(a.rB + dst) = ldg16(a.B + src);
+    *reinterpret_cast<uint4*>(a.rC + dst) = ldg16(a.C + src);
+  }
+  for (int q = tid; q < K * H; q += FT) {
+    const int i = q / H, h = q - i * H;
+    int slot = c.x + c.y + i;
+    slot = slot < L ? slot : slot - L;
+    slot = slot < L ? slot : slot - L;
+    a.rdt[((size_t)b * H + h) * pad4(L) + slot] = a.dt[((size_t)b * K + i) * H + h];
+  }
+  if (tid == 0) {
+    c.z = K;
+    c.w = (c.y + K > L) ? 1 : 0;
+    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+  }
+}
 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
@@ -115,11 +163,9 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
     }
   }
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
-  if (!valid) {  // reported by the epilogue kernel (uniform over the block)
-    if (threadIdx.x == 0) mbar_wait(&bar, 0);  // the copy lands before the block leaves
-    return;
-  }
-  const int start = cur.x, count = cur.y, total = count + K;
+  // An invalid cursor (reported by the epilogue below) runs as an empty window
+  // with every store masked.
+  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, total = count + K;
   const bool fold = total > L;
   const int first = fold ? count : 0;
   // record k on lane k: committed (ring slot sl) or new (record jn)
@@ -157,68 +203,70 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
     coef[i] = in ? fmaf(dtk * expf(Sl[i] - S), sc[i][ek], lane == last ? Dh : 0.f) : 0.f;
   }
   const float gA = silu_fast(bf_to_f(zbA)), gB = silu_fast(bf_to_f(zbB));
-  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
+  const bool landed = __all_sync(FULL, mbar_wait(&bar, 0));  // uniform over the warp
+  if (!landed) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar, 0);
-    return;
   }
   // A block that reads the bf16 copy folds from the fp32 rows in global memory.
   const bool from_tile = !(copy && fold);
+  if (landed) {
 #pragma unroll
-  for (int half = 0; half < 2; half++) {
-    const int rl = half ? rl1 : rl0;
-    float4 hv[8];
-    if (!from_tile) {
+    for (int half = 0; half < 2; half++) {
+      const int rl = half ? rl1 : rl0;
+      float4 hv[8];
+      if (!from_tile) {
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++)
-        hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + tbase + (size_t)(rl + rr) * FN) + lane);
-    } else if (copy) {
-      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
+        for (int rr = 0; rr < 8; rr++)
+          hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + tbase + (size_t)(rl + rr) * FN) + lane);
+      } else if (copy) {
+        const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
-    } else {
+        for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
+      } else {
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
-    }
-    float xl[8];
-    unpack8(xq[half], xl);
-    if (fold) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, four records per round
+        for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
+      }
+      float xl[8];
+      unpack8(xq[half], xl);
+      if (fold) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, four records per round
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, hv[rr]);
-      const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
-      for (int k0 = 0; k0 < count; k0 += 4) {
-        float4 bk[4];
+        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, hv[rr]);
+        const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
+        for (int k0 = 0; k0 < count; k0 += 4) {
+          float4 bk[4];
 #pragma unroll
-        for (int u = 0; u < 4; u++) {
-          int s = start + k0 + u;
-          s = s < L ? s : s - L;
-          bk[u] = k0 + u < count ? load_bf4(rBp + s * FN) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int u = 0; u < 4; u++) {
+            int s = start + k0 + u;
+            s = s < L ? s : s - L;
+            bk[u] = k0 + u < count ? load_bf4(rBp + s * FN) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            const int k = (k0 + u) & 31;
+            const float w = __shfl_sync(FULL, wf, k);  // 0 for k >= count
+#pragma unroll
+            for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[rr], k), bk[u], hv[rr]);
+          }
         }
+        const size_t off = tbase + (size_t)rl * FN + lane * 4;
 #pragma unroll
-        for (int u = 0; u < 4; u++) {
-          const int k = (k0 + u) & 31;
-          const float w = __shfl_sync(FULL, wf, k);  // 0 for k >= count
-#pragma unroll
-          for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[rr], k), bk[u], hv[rr]);
+        for (int rr = 0; rr < 8; rr++) {
+          __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
+          if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
         }
       }
-      const size_t off = tbase + (size_t)rl * FN + lane * 4;
+      const float gate = half ? gB : gA;
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) {
-        __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
-        if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
-      }
-    }
-    const float gate = half ? gB : gA;
+      for (int i = 0; i < KMAX; i++) {
+        if (i < K) {  // uniform
+          float tx[8];
 #pragma unroll
-    for (int i = 0; i < KMAX; i++) {
-      if (i < K) {  // uniform
-        float tx[8];
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++) tx[rr] = coef[i] * xl[rr];
-        const float tot = rows8(hv, scale4(Pi[i], ci[i]), tx, lane);
-        const float t = __shfl_sync(FULL, tot, row_src(gr));
-        if (gi == i) store_y<OUT_BF16>(a.y, (((size_t)b * K + i) * H + h) * P + p0 + rl + gr, t * gate);
+          for (int rr = 0; rr < 8; rr++) tx[rr] = coef[i] * xl[rr];
+          const float tot = rows8(hv, scale4(Pi[i], ci[i]), tx, lane);
+          const float t = __shfl_sync(FULL, tot, row_src(gr));
+          if (valid && gi == i) store_y<OUT_BF16>(a.y, (((size_t)b * K + i) * H + h) * P + p0 + rl + gr, t * gate);
+        }
       }
     }
   }
@@ -228,22 +276,35 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
     s = s < L ? s : s - L;
     return s < L ? s : s - L;
   };
-  if (lane < K) {
+  if (valid && lane < K) {
     const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P;
     *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xnA;
     *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xnB;
   }
-  if (gi < K) {
+  if (valid && gi < K) {
     const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P;
     a.rz[rrow + rA + gr] = zbA;
     a.rz[rrow + rB2 + gr] = zbB;
   }
+  // The last of the sequence's blocks to finish (all of them have read the
+  // committed records by then) appends the new records' B, C and dt and marks
+  // the cursor pending.
+  __shared__ int last_flags;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(a.cursors + 4 * (size_t)b + 3, 1 << 16);
+    last_flags = ((old >> 16) == a.H * a.nPB - 1) ? (old & 0xffff) : -1;
+  }
+  __syncthreads();
+  if (last_flags >= 0) verify_epilogue(a, b, cur, last_flags);
 }
 
 }  // namespace
 
 bool m2_verify_fast_applies(const M2Args& a) {
-  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.K <= KMAX && a.L + a.K <= FW * EW;
+  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.K <= KMAX && a.L + a.K <= FW * EW &&
+         a.H * a.nPB < (1 << 15);
 }
 
 cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {

@@ -134,3 +134,25 @@ def test_gdn_prime_matches_window_corrections(w):
         checked += 1
     assert checked > 0
     assert H.status(st) == 0
+
+
+@pytest.mark.parametrize("w", [GW("gerr", 3, 2, 40, 24, 4, 1, seed=84, prefill=False),
+                               GW("gerr_fast", 3, 2, 128, 128, 4, 1, seed=84, prefill=False)],
+                         ids=lambda w: w.name)
+def test_gdn_device_errors_skip_sequence(w):
+    """Bad cursors are reported, left as they were and skipped; the other sequences step."""
+    dev = "cuda"
+    st, _, _, _ = H.gdn_setup(w, dev)
+    st.cursors[1] = torch.tensor([0, 7, 0, 0], dtype=torch.int32)  # count > L
+    st.cursors[2] = torch.tensor([0, 1, 2, 0], dtype=torch.int32)  # uncommitted drafts
+    before = st.cursors.clone()
+    S0 = st.S.clone()
+    o = st.new_output().fill_(float("nan"))
+    st.step(I.gdn_step_inputs(w, 0, dev), o)
+    torch.cuda.synchronize()
+    assert H.status(st) in (bd.RSSM_DEV_BAD_CURSOR, bd.RSSM_DEV_PENDING)
+    assert torch.isfinite(o[0]).all()
+    assert torch.isnan(o[1:]).all()
+    assert torch.equal(st.cursors[1:], before[1:])
+    assert st.cursors[0].tolist() == [0, 1, 0, 0]
+    assert torch.equal(st.S[1:], S0[1:])

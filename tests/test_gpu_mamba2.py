@@ -231,8 +231,10 @@ def test_spec_all_accepted_equals_ar():
 
 # ----------------------------------------------------------------------------- device-side errors
 
-def test_device_errors_skip_sequence():
-    w = W("err", 4, 2, 16, 32, 1, 4, 1, seed=61, prefill=False)
+@pytest.mark.parametrize("w", [W("err", 4, 2, 16, 32, 1, 4, 1, seed=61, prefill=False),
+                               W("err_fast", 4, 2, 64, 128, 1, 4, 1, seed=61, prefill=False)],
+                         ids=lambda w: w.name)  # generic kernel + cursor kernel; fused cursor advance
+def test_device_errors_skip_sequence(w):
     dev = "cuda"
     st, A, D, _, _, _ = H.mamba2_setup(w, dev)
     st.cursors[1] = torch.tensor([0, 7, 0, 0], dtype=torch.int32)     # count > L
@@ -268,8 +270,10 @@ def test_commit_and_reset_errors():
     assert cur.cpu().tolist() == [[0, 2, 3, 0], [0, 0, 0, 0], [0, 0, 0, 0]]
 
 
-def test_verify_twice_is_rejected():
-    w = W("twice", 2, 2, 16, 32, 1, 8, 1, seed=62, drafts=1, prefill=False)
+@pytest.mark.parametrize("w", [W("twice", 2, 2, 16, 32, 1, 8, 1, seed=62, drafts=1, prefill=False),
+                               W("twice_fast", 2, 2, 64, 128, 1, 8, 1, seed=62, drafts=1, prefill=False)],
+                         ids=lambda w: w.name)
+def test_verify_twice_is_rejected(w):
     dev = "cuda"
     st, A, D, _, _, _ = H.mamba2_setup(w, dev)
     y = st.new_output(w.n_new)
@@ -279,6 +283,7 @@ def test_verify_twice_is_rejected():
     torch.cuda.synchronize()
     assert H.status(st) == bd.RSSM_DEV_PENDING
     assert st.cursors[:, 2].tolist() == [2, 2]
+    assert st.cursors[:, 3].tolist() == [0, 0]  # flags (and the arrival count) untouched by the rejected call
 
 
 def test_downcast_rne():
