@@ -58,21 +58,29 @@ __device__ __forceinline__ void store_y(void* y, size_t i, float v) {
 // silu(z) = z sigmoid(z)
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
-// Arrival of one block on its sequence's cursor, once every thread of the
-// block has read the cursor. The high 16 bits of the cursor's flags word count
-// the blocks of this launch that have arrived (the low 16 bits are the flags
-// themselves); the last of the sequence's `nblocks` blocks applies the AR rule
-// -- count + 1 == L ? 0 : count + 1, on a cursor with 0 <= start < L,
-// 0 <= count < L and pending == 0, else the same error report as the cursor
-// kernel and no move -- and clears the arrival count. Called by one thread.
-__device__ __forceinline__ void arrive_ar_cursor(int32_t* cursors, int b, int4 cur, int nblocks, int L,
+// Arrival of one block on its sequence's cursor: the high 16 bits of the
+// cursor's flags word count the blocks of this launch that have arrived (the
+// low 16 bits are the flags themselves). Taken by one thread once every thread
+// of the block is done with what the sequence's last block will overwrite (for
+// the AR step: the cursor itself); the ticket is only looked at later, so the
+// atomic's round trip overlaps the block's work. Its cursor loads are already
+// consumed, so no fence is needed before it: the last block's update is
+// ordered after every other block's arrival by the atomic itself.
+__device__ __forceinline__ int cursor_ticket(int32_t* cursors, int b) {
+  return atomicAdd(cursors + 4 * (size_t)b + 3, 1 << 16);
+}
+
+__device__ __forceinline__ bool last_ticket(int ticket, int nblocks) { return (ticket >> 16) == nblocks - 1; }
+
+// AR rule, applied by the sequence's last block (one thread): count + 1 == L ?
+// 0 : count + 1 on a cursor with 0 <= start < L, 0 <= count < L and pending ==
+// 0, else the same error report as the cursor kernel and no move; the arrival
+// count is cleared.
+__device__ __forceinline__ void finish_ar_cursor(int32_t* cursors, int b, int4 cur, int ticket, int nblocks, int L,
                                                  int32_t* status) {
-  __threadfence();
-  int32_t* wp = cursors + 4 * (size_t)b + 3;
-  const int old = atomicAdd(wp, 1 << 16);
-  if ((old >> 16) != nblocks - 1) return;
+  if (!last_ticket(ticket, nblocks)) return;
   int4 c = cur;
-  c.w = old & 0xffff;
+  c.w = ticket & 0xffff;
   if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L && c.z >= 0))
     report(status, RSSM_DEV_BAD_CURSOR);
   else if (c.z != 0)

@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   float* es = dsm + FPB * GD;      // e of window record t at es + t * ES (the block's rows)
   __shared__ float skk[FW * KW], skq[FW * KW];  // k_s . k, k_s . q by ring slot; [L] = current
   __shared__ uint64_t bar[2];      // [0] the rows, [1] the window's e
+  __shared__ int4 cur_s;           // the cursor as read, for the sequence's last block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = a.L, H = a.H;
   const int pb = blockIdx.x & 1, bhi = blockIdx.x >> 1;
@@ -131,17 +132,40 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const float gamma = expf(__shfl_sync(FULL, sfx, 0));
   const float Dt = expf(ex);  // D(m-1, t)
   __syncthreads();
-  if (threadIdx.x == 0) arrive_ar_cursor(a.cursors, b, cur, a.H * 2, L, a.status);  // every thread has read it
+  int ticket = 0;
+  if (threadIdx.x == 0) {  // every thread has read the cursor
+    ticket = cursor_ticket(a.cursors, b);
+    cur_s = cur;
+  }
   const int ent = lane < count ? sl : L;
   const float cK = lane < count ? Dt * skk[ent] : 0.f;
   const float cQ = lane < count ? Dt * skq[ent] : 0.f;
   const float kq_cur = skq[L];
   const float4 ka = scale4(gamma, bf4_to_f4(kraw)), qa = scale4(gamma, bf4_to_f4(qraw));
+  // Append the current record now (its e follows below): its slot is outside
+  // the window, so no block reads it for a result.
+  if (valid && !flush) {
+    const size_t vrow = (bh * L + scur) * GD + p0 + vr;
+    if (lane < 16 && (lane & 1) == 0) {
+      a.rv[vrow + rl0] = vbA;
+      a.rv[vrow + rl1] = vbB;
+    }
+    if (pb == 0 && warp == 0) {
+      const size_t krow = (bh * L + scur) * GD + lane * 4;
+      *reinterpret_cast<uint2*>(a.rk + krow) = kraw;
+      *reinterpret_cast<uint2*>(a.rq + krow) = qraw;
+      if (lane == 0) {
+        a.rg[bh * pad4(L) + scur] = gm;
+        a.rbeta[bh * pad4(L) + scur] = bm;
+      }
+    }
+  }
   const bool ok0 = mbar_wait(&bar[0], 0), ok1 = mbar_wait(&bar[1], 0);
   if (!__all_sync(FULL, ok0 && ok1)) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar[0], 0);
     mbar_wait(&bar[1], 0);
+    if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, cur_s, ticket, a.H * 2, L, a.status);
     return;
   }
 #pragma unroll
@@ -201,22 +225,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
       for (int rr = 0; rr < 8; rr++) __stcs(reinterpret_cast<float4*>(a.S + tbase + (size_t)(rl + rr) * GD) + lane, hv[rr]);
     }
   }
-  if (valid && !flush) {  // append the current record (its e went to the ring above)
-    const size_t vrow = (bh * L + scur) * GD + p0 + vr;
-    if (lane < 16 && (lane & 1) == 0) {
-      a.rv[vrow + rl0] = vbA;
-      a.rv[vrow + rl1] = vbB;
-    }
-    if (pb == 0 && warp == 0) {
-      const size_t krow = (bh * L + scur) * GD + lane * 4;
-      *reinterpret_cast<uint2*>(a.rk + krow) = kraw;
-      *reinterpret_cast<uint2*>(a.rq + krow) = qraw;
-      if (lane == 0) {
-        a.rg[bh * pad4(L) + scur] = gm;
-        a.rbeta[bh * pad4(L) + scur] = bm;
-      }
-    }
-  }
+  if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, cur_s, ticket, a.H * 2, L, a.status);
 }
 
 }  // namespace

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   __shared__ __align__(128) float tile[FPB * FN];  // the block's rows (fp32, or bf16 in the first half)
   __shared__ float sc[FW * KW];                    // c_s = B_s . C by ring slot; [L] = current
   __shared__ uint64_t bar;
+  __shared__ int4 scur;  // the cursor as read, for the sequence's last block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
   const int h = blockIdx.x / a.nPB, pb = blockIdx.x - h * a.nPB;
@@ -122,8 +123,9 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const int nblocks = a.H * a.nPB;  // blocks of this sequence
   if (!valid) {  // uniform over the block; the last block of the sequence reports it
     if (threadIdx.x == 0) {
+      const int ticket = cursor_ticket(a.cursors, b);
       mbar_wait(&bar, 0);  // the copy lands before the block leaves
-      arrive_ar_cursor(a.cursors, b, cur, nblocks, L, a.status);
+      finish_ar_cursor(a.cursors, b, cur, ticket, nblocks, L, a.status);
     }
     return;
   }
@@ -147,14 +149,36 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const float4 pc = scale4(Pm, cm);
   const uint4 xrA = shfl_u4(xsA, sl), xrB = shfl_u4(xsB, sl);
   __syncthreads();
-  if (threadIdx.x == 0) arrive_ar_cursor(a.cursors, b, cur, nblocks, L, a.status);  // every thread has read it
+  int ticket = 0;
+  if (threadIdx.x == 0) {  // every thread has read the cursor
+    ticket = cursor_ticket(a.cursors, b);
+    scur = cur;
+  }
   const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? Dh : 0.f) : 0.f;
   // the gates do not need the checkpoint rows: computed before waiting for them
   const uint4 xq[2] = {lane < count ? xrA : xcA, lane < count ? xrB : xcB};  // lane k: x_k, both groups
   const float gA = silu_fast(zA), gB = silu_fast(zB);
+  // Append the current record now: its slot is outside the window (no block
+  // reads it for a result; this block's own loads of it are consumed above).
+  if (!flush) {  // x, z rows of this warp's groups; dt, B, C once
+    const int slot = start + count < L ? start + count : start + count - L;
+    const size_t rrow = ((size_t)bh * L + slot) * P;
+    if (lane == 0) *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xcA;
+    if (lane == 1) *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xcB;
+    if (lane == 2 || lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + (lane == 3 ? rB2 : rA)) = zap;
+    if (warp == 0 && pb == 0) {
+      if (lane == 4) a.rdt[(size_t)bh * pad4(L) + slot] = dtc;
+      if (h == g * (H / a.G)) {  // the group's first head
+        const size_t brow = ((size_t)bg * L + slot) * FN + lane * 4;
+        *reinterpret_cast<uint2*>(a.rB + brow) = braw;
+        *reinterpret_cast<uint2*>(a.rC + brow) = craw;
+      }
+    }
+  }
   if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar, 0);
+    if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, scur, ticket, nblocks, L, a.status);
     return;
   }
   // A block that reads the bf16 copy folds from the fp32 rows in global memory.
@@ -185,21 +209,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
     }
   }
 
-  if (!flush) {  // append the current record: x, z rows of this warp's groups; dt, B, C once
-    const int slot = start + count < L ? start + count : start + count - L;
-    const size_t rrow = ((size_t)bh * L + slot) * P;
-    if (lane == 0) *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xcA;
-    if (lane == 1) *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xcB;
-    if (lane == 2 || lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + (lane == 3 ? rB2 : rA)) = zap;
-    if (warp == 0 && pb == 0) {
-      if (lane == 4) a.rdt[(size_t)bh * pad4(L) + slot] = dtc;
-      if (h == g * (H / a.G)) {  // the group's first head
-        const size_t brow = ((size_t)bg * L + slot) * FN + lane * 4;
-        *reinterpret_cast<uint2*>(a.rB + brow) = braw;
-        *reinterpret_cast<uint2*>(a.rC + brow) = craw;
-      }
-    }
-  }
+  if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, scur, ticket, nblocks, L, a.status);
 }
 
 }  // namespace

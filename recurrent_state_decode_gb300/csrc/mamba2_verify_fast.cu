@@ -195,6 +195,10 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
     Pi[i] = expf(Sl[i] - S0);
   }
   __syncthreads();
+  // Without a fold the epilogue writes free ring slots only: this block is done
+  // with what it overwrites (dots, dt) and arrives now; a folding block arrives
+  // after its fold.
+  int ticket = (threadIdx.x == 0 && !fold) ? cursor_ticket(a.cursors, b) : 0;
   float coef[KMAX];
 #pragma unroll
   for (int i = 0; i < KMAX; i++) {
@@ -203,6 +207,23 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
     coef[i] = in ? fmaf(dtk * expf(Sl[i] - S), sc[i][ek], lane == last ? Dh : 0.f) : 0.f;
   }
   const float gA = silu_fast(bf_to_f(zbA)), gB = silu_fast(bf_to_f(zbB));
+  // Append the new records' x and z rows of this block now: its committed x
+  // rows are in registers already (the fold and the outputs use those).
+  auto slot_of = [&](int j) {
+    int s = start + count + j;
+    s = s < L ? s : s - L;
+    return s < L ? s : s - L;
+  };
+  if (valid && lane < K) {
+    const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P;
+    *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xnA;
+    *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xnB;
+  }
+  if (valid && gi < K) {
+    const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P;
+    a.rz[rrow + rA + gr] = zbA;
+    a.rz[rrow + rB2 + gr] = zbB;
+  }
   const bool landed = __all_sync(FULL, mbar_wait(&bar, 0));  // uniform over the warp
   if (!landed) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
@@ -270,32 +291,16 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
       }
     }
   }
-  // append the new records' x and z rows of this block
-  auto slot_of = [&](int j) {
-    int s = start + count + j;
-    s = s < L ? s : s - L;
-    return s < L ? s : s - L;
-  };
-  if (valid && lane < K) {
-    const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P;
-    *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xnA;
-    *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xnB;
-  }
-  if (valid && gi < K) {
-    const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P;
-    a.rz[rrow + rA + gr] = zbA;
-    a.rz[rrow + rB2 + gr] = zbB;
-  }
-  // The last of the sequence's blocks to finish (all of them have read the
-  // committed records by then) appends the new records' B, C and dt and marks
-  // the cursor pending.
+  // The last of the sequence's blocks to arrive (all of them are done with the
+  // ring rows the append overwrites) appends the new records' B, C and dt and
+  // marks the cursor pending.
   __shared__ int last_flags;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int old = atomicAdd(a.cursors + 4 * (size_t)b + 3, 1 << 16);
-    last_flags = ((old >> 16) == a.H * a.nPB - 1) ? (old & 0xffff) : -1;
+  if (fold) {  // uniform: the committed B rows were read by the fold until here
+    __syncthreads();
+    if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);
   }
+  __syncthreads();
+  if (threadIdx.x == 0) last_flags = last_ticket(ticket, a.H * a.nPB) ? (ticket & 0xffff) : -1;
   __syncthreads();
   if (last_flags >= 0) verify_epilogue(a, b, cur, last_flags);
 }
