@@ -59,6 +59,8 @@ M2Args m2_args(const rssm_mamba2_desc* d) {
   a.PB = rows_per_block(a.P, a.N);
   a.nPB = (a.P + a.PB - 1) / a.PB;
   a.K = 1;
+  const int hpg = a.H / a.G;
+  a.hpg_log2 = (hpg & (hpg - 1)) == 0 ? __builtin_ctz(hpg) : -1;
   return a;
 }
 

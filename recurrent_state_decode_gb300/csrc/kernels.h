@@ -12,6 +12,7 @@ struct M2Args {
   int Bt, H, P, N, G, L;
   int PB, nPB;  // rows per block, row blocks per (sequence, head) tile
   int K;        // records per verify (1 for the AR step)
+  int hpg_log2;  // log2(H / G) when H / G is a power of two, else -1
   float* ckpt;
   uint16_t* ckpt_read;
   uint16_t *rx, *rz, *rB, *rC;

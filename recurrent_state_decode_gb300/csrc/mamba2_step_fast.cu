@@ -72,10 +72,9 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   __shared__ uint64_t bar;
   __shared__ int4 scur;  // the cursor as read, for the sequence's last block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.y;
-  const int h = blockIdx.x / a.nPB, pb = blockIdx.x - h * a.nPB;
+  const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int L = a.L, P = a.P, H = a.H;
-  const int g = h / (H / a.G);
+  const int g = h >> a.hpg_log2;  // H / G heads per group, a power of two on this path
   const int bh = b * H + h, bg = b * a.G + g;
   const int p0 = pb * FPB;
   const bool copy = a.ckpt_read != nullptr;
@@ -168,7 +167,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
     if (lane == 2 || lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + (lane == 3 ? rB2 : rA)) = zap;
     if (warp == 0 && pb == 0) {
       if (lane == 4) a.rdt[(size_t)bh * pad4(L) + slot] = dtc;
-      if (h == g * (H / a.G)) {  // the group's first head
+      if (h == (g << a.hpg_log2)) {  // the group's first head
         const size_t brow = ((size_t)bg * L + slot) * FN + lane * 4;
         *reinterpret_cast<uint2*>(a.rB + brow) = braw;
         *reinterpret_cast<uint2*>(a.rC + brow) = craw;
@@ -202,7 +201,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
     float xl[8], tx[8];
     unpack8(xq[half], xl);
 #pragma unroll
-    for (int rr = 0; rr < 8; rr++) tx[rr] = lane < m ? coef * xl[rr] : 0.f;
+    for (int rr = 0; rr < 8; rr++) tx[rr] = coef * xl[rr];  // coef = 0 off the window; x finite there
     gate_store<OUT_BF16>(a, xrow + p0 + rl, half ? gB : gA, rows8(hv, pc, tx, lane), lane);
     if (flush) {
       fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)rl * FN + lane * 4, lane);
@@ -215,11 +214,12 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
 }  // namespace
 
 bool m2_step_fast_applies(const M2Args& a) {
-  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.L <= FW * KW - 1 && a.H * a.nPB < (1 << 15);
+  return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.L <= FW * KW - 1 && a.H * a.nPB < (1 << 15) &&
+         a.hpg_log2 >= 0;
 }
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
-  const dim3 grid(a.H * a.nPB, a.Bt);
+  const dim3 grid(a.nPB, a.H, a.Bt);
   auto k = out_bf16 ? m2_step_fast_kernel<true> : m2_step_fast_kernel<false>;
   // six 32 KiB tiles per SM need the largest shared-memory split of the unified L1
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,

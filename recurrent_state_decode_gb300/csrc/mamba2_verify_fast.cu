@@ -94,10 +94,9 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
   __shared__ float sc[KMAX][FW * EW];              // B_e . C_i
   __shared__ uint64_t bar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.y;
-  const int h = blockIdx.x / a.nPB, pb = blockIdx.x - h * a.nPB;
+  const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int L = a.L, P = a.P, H = a.H, G = a.G, K = a.K;
-  const int g = h / (H / G);
+  const int g = h >> a.hpg_log2;  // H / G heads per group, a power of two on this path
   const int bh = b * H + h, bg = b * G + g;
   const int p0 = pb * FPB;
   const bool copy = a.ckpt_read != nullptr;
@@ -309,11 +308,12 @@ __global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
 
 bool m2_verify_fast_applies(const M2Args& a) {
   return a.N == FN && a.P % FPB == 0 && a.PB == FPB && a.K <= KMAX && a.L + a.K <= FW * EW &&
-         a.H * a.nPB < (1 << 15);
+         a.H * a.nPB < (1 << 15) &&
+         a.hpg_log2 >= 0;
 }
 
 cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
-  const dim3 grid(a.H * a.nPB, a.Bt);
+  const dim3 grid(a.nPB, a.H, a.Bt);
   auto k = out_bf16 ? m2_verify_fast_kernel<true> : m2_verify_fast_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
