@@ -67,9 +67,8 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   __shared__ int4 cur_s;           // the cursor as read, for the sequence's last block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = a.L, H = a.H;
-  const int pb = blockIdx.x & 1, bhi = blockIdx.x >> 1;
-  const int b = bhi / H;
-  const size_t bh = bhi;
+  const int pb = blockIdx.x, b = blockIdx.z;
+  const size_t bh = (size_t)b * H + blockIdx.y;
   const int p0 = pb * FPB;
   const size_t tbase = (bh * GD + p0) * GD;
 
@@ -231,19 +230,19 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
 }  // namespace
 
 bool gdn_step_fast_applies(const GdnArgs& a) {
-  return a.DK == GD && a.DV == GD && a.L <= FW * KW - 1 && a.H * 2 < (1 << 15);
+  return a.DK == GD && a.DV == GD && a.L <= FW * KW - 1 && a.H * 2 < (1 << 15) && a.H <= 65535 &&
+         a.Bt <= 65535;
 }
 
 cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
-  const long long nblk = (long long)a.Bt * a.H * 2;
-  if (nblk == 0) return cudaSuccess;
+  if (a.Bt == 0) return cudaSuccess;
   auto k = out_bf16 ? gdn_step_fast_kernel<true> : gdn_step_fast_kernel<false>;
   const int smem = (FPB * GD + a.L * ES) * 4;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)nblk, FT, smem, st>>>(a);
+  k<<<dim3(2, a.H, a.Bt), FT, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -89,7 +89,7 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
 }
 
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(FT, 5) m2_verify_fast_kernel(M2Args a) {
+__global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   __shared__ __align__(128) float tile[FPB * FN];  // the block's rows (fp32, or bf16 in the first half)
   __shared__ float sc[KMAX][FW * EW];              // B_e . C_i
   __shared__ uint64_t bar;
