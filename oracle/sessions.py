@@ -166,3 +166,46 @@ def gdn_ar_session(S0, prefill, starts, counts, steps, L):
             cs[b] = nc
             flushed[b] = fl
         yield {"o": o, "flushed": flushed, "state": S, "cursors": np.array(cs, np.int64)}
+
+
+def gdn_spec_session(S0, prefill, starts, counts, verifies, kepts, L):
+    """Speculative decode for Gated DeltaNet ("ReplaySSM", introduction:
+    drafts verified output-only, rejected ones dropped by moving a pointer).
+    ``verifies`` yields record dicts with a draft axis (q,k [Bt,K,H,dk],
+    v [Bt,K,H,dv], g,beta [Bt,K,H]); ``kepts`` yields kept [Bt].
+
+    Output i of a verify continues conventional decoding from the committed
+    state through drafts 0..i. Yields per verify a dict: o [Bt,K,H,dv];
+    folded [Bt]; committed_state (the state before the verify: a folded
+    sequence's checkpoint must equal it); cursors_verify, cursors_commit
+    [Bt,4]; state (the committed state after the commit).
+    """
+    S = gdn_prefill(S0, prefill, counts)
+    cs = [(int(s), int(c), 0, 0) for s, c in zip(starts, counts)]
+    for rec, kept in zip(verifies, kepts):
+        K = rec["q"].shape[1]
+        committed = S
+        folded = np.zeros(len(cs), bool)
+        for b, c in enumerate(cs):
+            nc, _, fold, ok = cur.verify(c, K, L)
+            assert ok
+            cs[b] = nc
+            folded[b] = fold
+        cv = np.array(cs, np.int64)
+        Ss, os_ = [], []
+        Si = committed
+        for i in range(K):
+            Si, oi = _gdn_step(Si, _take(rec, i))
+            Ss.append(Si)
+            os_.append(oi)
+        o = np.stack(os_, axis=1)
+        kept = np.asarray(kept)
+        S = committed.copy()
+        for b in range(len(cs)):
+            if kept[b] > 0:
+                S[b] = Ss[kept[b] - 1][b]
+            nc, ok = cur.commit(cs[b], int(kept[b]), L)
+            assert ok
+            cs[b] = nc
+        yield {"o": o, "folded": folded, "committed_state": committed,
+               "cursors_verify": cv, "cursors_commit": np.array(cs, np.int64), "state": S}

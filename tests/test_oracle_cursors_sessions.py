@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from oracle import cursors as cur
-from oracle import mamba2, sessions
+from oracle import gdn, mamba2, sessions
 
 
 def test_ar_trace_by_hand():
@@ -134,3 +134,58 @@ def test_flush_expected_equals_replay(rng):
     ref = mamba2.replay_state(h0[0], np.moveaxis(xs, 0, 1), np.moveaxis(Bh, 0, 1), np.moveaxis(dts, 0, 1), A)
     np.testing.assert_allclose(out[0], ref, rtol=1e-12)
     np.testing.assert_array_equal(out[1], h0[1])
+
+
+def _gdn_records(rng, Bt, H, dk, dv, n):
+    q = rng.standard_normal((Bt, n, H, dk))
+    k = rng.standard_normal((Bt, n, H, dk))
+    return {"q": q / np.linalg.norm(q, axis=-1, keepdims=True), "k": k / np.linalg.norm(k, axis=-1, keepdims=True),
+            "v": rng.standard_normal((Bt, n, H, dv)), "g": -np.log1p(np.exp(rng.standard_normal((Bt, n, H)))),
+            "beta": 1 / (1 + np.exp(-rng.standard_normal((Bt, n, H))))}
+
+
+@pytest.mark.parametrize("reject", [False, True])
+def test_gdn_spec_session_matches_ar(rng, reject):
+    """GDN spec decode with kept drafts equals AR decode over exactly the kept
+    tokens (outputs, committed state); cursors follow the verify/commit rules."""
+    Bt, H, dk, dv, L, K, V = 3, 2, 4, 3, 6, 3, 7
+    S0 = 0.1 * rng.standard_normal((Bt, H, dv, dk))
+    drafts = [_gdn_records(rng, Bt, H, dk, dv, K) for _ in range(V)]
+    kepts = [rng.integers(1, K + 1, Bt) if reject else np.full(Bt, K) for _ in range(V)]
+    starts, counts = np.array([0, 2, 5]), np.zeros(Bt, int)
+    spec = list(sessions.gdn_spec_session(S0, None, starts, counts, drafts, kepts, L))
+    for b in range(Bt):
+        S = S0[b:b + 1]
+        for v in range(V):
+            for i in range(kepts[v][b]):
+                r = {k: a[b:b + 1, i] for k, a in drafts[v].items()}
+                S, o = gdn.conventional_step(S, r["q"], r["k"], r["v"], r["g"], r["beta"])
+                np.testing.assert_allclose(spec[v]["o"][b, i], o[0], rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(spec[v]["state"][b], S[0], rtol=1e-12, atol=1e-14)
+        c = spec[-1]["cursors_commit"][b]
+        assert 0 <= c[1] <= L and c[2] == 0
+    # a rejected draft's output is still the continuation through it
+    v, b = 0, 0
+    S = S0[b:b + 1]
+    for i in range(K):
+        r = {k: a[b:b + 1, i] for k, a in drafts[v].items()}
+        S, o = gdn.conventional_step(S, r["q"], r["k"], r["v"], r["g"], r["beta"])
+        np.testing.assert_allclose(spec[v]["o"][b, i], o[0], rtol=1e-12, atol=1e-14)
+
+
+def test_gdn_spec_session_folds_like_mamba2(rng):
+    """The fold flags and cursor trace depend only on the cursor rules: the
+    GDN and Mamba-2 sessions agree on them for the same kept counts."""
+    Bt, L, K, V = 4, 5, 3, 9
+    starts, counts = np.array([0, 1, 4, 2]), np.array([0, 3, 4, 1])
+    kepts = [rng.integers(1, K + 1, Bt) for _ in range(V)]
+    g = list(sessions.gdn_spec_session(np.zeros((Bt, 1, 2, 2)), _gdn_records(rng, Bt, 1, 2, 2, L - 1), starts, counts,
+                                       [_gdn_records(rng, Bt, 1, 2, 2, K) for _ in range(V)], kepts, L))
+    m = list(sessions.mamba2_spec_session(np.zeros((Bt, 1, 2, 2)), _records(rng, Bt, 1, 2, 2, 1, L - 1), starts, counts,
+                                          [_records(rng, Bt, 1, 2, 2, 1, K) for _ in range(V)], kepts,
+                                          -np.ones(1), np.zeros(1), L))
+    for a, c in zip(g, m):
+        np.testing.assert_array_equal(a["folded"], c["folded"])
+        np.testing.assert_array_equal(a["cursors_verify"], c["cursors_verify"])
+        np.testing.assert_array_equal(a["cursors_commit"], c["cursors_commit"])
+    assert any(x["folded"].any() for x in g)
