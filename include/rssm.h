@@ -260,6 +260,24 @@ RSSM_API int rssm_gdn_step(const rssm_gdn_desc* desc, float* S, const rssm_gdn_r
 RSSM_API int rssm_gdn_flush(const rssm_gdn_desc* desc, float* S, const rssm_gdn_ring* ring,
                    int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
 
+/* Speculative verify for Gated DeltaNet (as rssm_mamba2_spec_verify: "How
+ * ReplaySSM works", drafts appended to the buffer; "ReplaySSM" repository,
+ * introduction, output-only verification and rollback by moving a pointer).
+ * Appends n_new = K records per sequence at ring slots (start + count + i)
+ * mod L, with their corrections e, and computes, output-only, o_i for i < K:
+ * the output after the committed records plus new records 0..i. If count + K
+ * > L the committed window is first folded into S (written once). Needs
+ * pending == 0; sets pending = K and flags = folded. Must be followed by one
+ * rssm_commit_cursors.
+ *  q, k [batch, K, nheads, dk]; v [batch, K, nheads, dv] (bf16);
+ *  g, beta [batch, K, nheads] fp32; o [batch, K, nheads, dv] of out_dtype.
+ *  1 <= n_new <= buf_len (else RSSM_ERR_INVALID_ARG). */
+RSSM_API int rssm_gdn_spec_verify(const rssm_gdn_desc* desc, int n_new, float* S,
+                         const rssm_gdn_ring* ring, int32_t* cursors,
+                         const rssm_bf16* q, const rssm_bf16* k, const rssm_bf16* v,
+                         const float* g, const float* beta, void* o,
+                         int32_t* dev_status, rssm_stream_t stream);
+
 /* Fills ring->e for the records already in each sequence's window (count of
  * them, from its checkpoint S), for windows whose records were written into
  * the ring directly rather than appended by rssm_gdn_step. The pages have no

@@ -64,6 +64,7 @@ _SIGNATURES = {
     "rssm_gdn_step": (c_int, [P] * 11 + [P]),
     "rssm_gdn_flush": (c_int, [P] * 5 + [P]),
     "rssm_gdn_prime": (c_int, [P] * 5 + [P]),
+    "rssm_gdn_spec_verify": (c_int, [P, c_int] + [P] * 11),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -217,3 +218,9 @@ def rssm_gdn_flush(desc, S, ring, cursors, dev_status=None, stream=None):
 def rssm_gdn_prime(desc, S, ring, cursors, dev_status=None, stream=None):
     return load().rssm_gdn_prime(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status),
                                  _stream(stream, S))
+
+
+def rssm_gdn_spec_verify(desc, n_new, S, ring, cursors, q, k, v, g, beta, o, dev_status=None, stream=None):
+    return load().rssm_gdn_spec_verify(
+        _ref(desc), int(n_new), ptr(S), _ref(ring), ptr(cursors), ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), ptr(o),
+        ptr(dev_status), _stream(stream, S))

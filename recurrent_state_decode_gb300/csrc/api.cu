@@ -81,6 +81,7 @@ GdnArgs gdn_args(const rssm_gdn_desc* d) {
   a.DK = d->dk;
   a.DV = d->dv;
   a.L = d->buf_len;
+  a.K = 1;
   return a;
 }
 
@@ -327,6 +328,37 @@ int rssm_gdn_flush(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, 
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = cuda_rc(gdn_launch(GDN_FLUSH, a, 0, st)))) return rc;
   return cuda_rc(cursor_launch(CUR_FLUSH, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+int rssm_gdn_spec_verify(const rssm_gdn_desc* d, int n_new, float* S, const rssm_gdn_ring* ring, int32_t* cursors,
+                         const rssm_bf16* q, const rssm_bf16* k, const rssm_bf16* v, const float* g,
+                         const float* beta, void* o, int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (n_new < 1 || n_new > d->buf_len) return RSSM_ERR_INVALID_ARG;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors, q, k, v, g, beta, o})))
+    return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.K = n_new;
+  a.S = S;
+  a.rq = ring->q;
+  a.rk = ring->k;
+  a.rv = ring->v;
+  a.rg = ring->g;
+  a.rbeta = ring->beta;
+  a.re = ring->e;
+  a.cursors = cursors;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.o = o;
+  a.status = dev_status;
+  return cuda_rc(gdn_verify_launch(a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
 }
 
 int rssm_gdn_prime(const rssm_gdn_desc* d, const float* S, const rssm_gdn_ring* ring, const int32_t* cursors,

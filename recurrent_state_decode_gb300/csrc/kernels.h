@@ -46,6 +46,7 @@ struct GdnArgs {
   uint16_t *rq, *rk, *rv;
   float *rg, *rbeta;
   float* re;  // cached corrections e_t [Bt, H, L, DV]
+  int K;      // records per verify (1 for the AR step)
   int32_t* cursors;
   const uint16_t *q, *k, *v;
   const float *g, *beta;
@@ -54,6 +55,9 @@ struct GdnArgs {
 };
 
 enum { GDN_CONVENTIONAL = 0, GDN_STEP = 1, GDN_FLUSH = 2, GDN_PRIME = 3 };
+
+// Speculative verify for Gated DeltaNet (gdn_verify.cu): K new records per sequence.
+cudaError_t gdn_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
 
 cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st);
 // Shape-specialised AR step (dk = dv = 128, L <= 31; gdn_step_fast.cu).

@@ -68,6 +68,11 @@ class GDNWorkload:
     seed: int
     zero_ckpt: bool = False
     prefill: bool = True
+    drafts: int = 0          # T; 0 = autoregressive decode
+
+    @property
+    def n_new(self):
+        return self.drafts + 1
 
 
 WORKLOADS = {
@@ -76,6 +81,7 @@ WORKLOADS = {
     "mamba2_spec": Mamba2Workload("mamba2_spec", 512, 128, 64, 128, 8, 16, 128, seed=1002, drafts=3),
     "gdn_serving": GDNWorkload("gdn_serving", 256, 32, 128, 128, 16, 256, seed=1003),
     "mamba2_bf16_read": Mamba2Workload("mamba2_bf16_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy=True),
+    "gdn_spec": GDNWorkload("gdn_spec", 512, 32, 128, 128, 16, 128, seed=1005, drafts=3),
 }
 
 
@@ -169,6 +175,11 @@ def gdn_records(w, stream, index, n, device):
 def gdn_step_inputs(w, t, device):
     r = gdn_records(w, "step", t, 1, device)
     return {k: v[:, 0].contiguous() for k, v in r.items()}
+
+
+def gdn_verify_inputs(w, t, device):
+    """Records of verify step t: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g,beta [Bt,K,H] fp32."""
+    return {k: v.contiguous() for k, v in gdn_records(w, "step", t, w.n_new, device).items()}
 
 
 def gdn_prefill(w, device):

@@ -101,6 +101,19 @@ class GDNState:
         bd.check(bd.rssm_gdn_flush(self.desc, self.S, self.ring, self.cursors, self.status, stream),
                  "rssm_gdn_flush")
 
+    def new_verify_output(self, n_new):
+        return torch.empty((self.batch, n_new, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
+
+    def verify(self, rec, o, stream=None):
+        """rec: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g,beta [Bt,K,H] fp32; o [Bt,K,H,dv]."""
+        bd.check(bd.rssm_gdn_spec_verify(self.desc, rec["q"].shape[1], self.S, self.ring, self.cursors, rec["q"],
+                                         rec["k"], rec["v"], rec["g"], rec["beta"], o, self.status, stream),
+                 "rssm_gdn_spec_verify")
+
+    def commit(self, kept, stream=None):
+        bd.check(bd.rssm_commit_cursors(self.cursors, kept, self.batch, self.buf_len, self.status, stream),
+                 "rssm_commit_cursors")
+
     def prime(self, stream=None):
         """Fill the ring's corrections e for records placed into the window directly."""
         bd.check(bd.rssm_gdn_prime(self.desc, self.S, self.ring, self.cursors, self.status, stream),

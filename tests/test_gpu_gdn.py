@@ -156,3 +156,79 @@ def test_gdn_device_errors_skip_sequence(w):
     assert torch.equal(st.cursors[1:], before[1:])
     assert st.cursors[0].tolist() == [0, 1, 0, 0]
     assert torch.equal(st.S[1:], S0[1:])
+
+
+# ----------------------------------------------------------------------------- speculative verify
+
+def run_gdn_spec(w, out_dtype=bd.RSSM_F32, seqs=None, steps=None):
+    dev = "cuda"
+    st, pre, starts, counts = H.gdn_setup(w, dev, out_dtype)
+    seqs = list(range(w.batch)) if seqs is None else list(seqs)
+    fv, fk = H.Feed(), H.Feed()
+    sess = sessions.gdn_spec_session(H.F64(st.S[seqs]), H.sub(pre, seqs), starts[seqs].cpu().numpy(),
+                                     counts[seqs].cpu().numpy(), fv, fk, w.buf_len)
+    o = st.new_verify_output(w.n_new)
+    folds = 0
+    for t in range(w.steps if steps is None else steps):
+        rec = I.gdn_verify_inputs(w, t, dev)
+        kept = I.accepted_kept(w, t, dev)
+        fv.rec = H.sub(rec, seqs)
+        fk.rec = kept[seqs].cpu().numpy()
+        st.verify(rec, o)
+        cv = st.cursors[seqs].cpu().numpy()
+        st.commit(kept)
+        exp = next(sess)
+        og_ = H.F64(o[seqs])
+        if out_dtype == bd.RSSM_F32:
+            assert H.rel_l2(og_, exp["o"]) <= TOL_Y32, t
+        else:
+            assert H.bf16_excess(og_, exp["o"]) <= TOL_BF16_EXCESS, t
+        np.testing.assert_array_equal(cv, exp["cursors_verify"])
+        np.testing.assert_array_equal(st.cursors[seqs].cpu().numpy(), exp["cursors_commit"])
+        for i, b in enumerate(seqs):
+            if exp["folded"][i]:
+                folds += 1
+                assert H.rel_l2(H.F64(st.S[b]), exp["committed_state"][i]) <= TOL_CKPT, (t, b)
+    assert H.status(st) == 0
+    return folds
+
+
+GSPEC = [
+    GW("gspec_small", 3, 2, 64, 64, 16, 20, seed=91, drafts=3),
+    GW("gspec_ragged", 3, 3, 40, 24, 5, 12, seed=92, drafts=2),
+    GW("gspec_K_eq_L", 3, 2, 32, 32, 4, 8, seed=93, drafts=3),      # K = L: every verify with count > 0 folds
+    GW("gspec_K1", 3, 2, 32, 48, 4, 10, seed=94, drafts=0),         # one record per verify
+    GW("gspec_128", 3, 4, 128, 128, 16, 24, seed=95, drafts=3),     # the serving tile
+    GW("gspec_128_L5", 2, 2, 128, 128, 5, 14, seed=96, drafts=3),   # folds often
+]
+
+
+@pytest.mark.parametrize("w", GSPEC, ids=lambda w: w.name)
+def test_gdn_spec(w):
+    assert run_gdn_spec(w) > 0 or w.name == "gspec_K1"
+
+
+def test_gdn_spec_bf16_out():
+    run_gdn_spec(GSPEC[4], out_dtype=bd.RSSM_BF16)
+
+
+def test_gdn_spec_all_accepted_equals_ar():
+    """Every draft kept: speculative decode produces AR decode's outputs and
+    state for the same tokens (GPU against GPU, then a flush of both)."""
+    w = GW("gacc", 2, 2, 128, 128, 16, 6, seed=97, drafts=3, prefill=False)
+    dev = "cuda"
+    sa, _, _, _ = H.gdn_setup(w, dev)
+    ss, _, _, _ = H.gdn_setup(w, dev)
+    oa = sa.new_output()
+    os_ = ss.new_verify_output(w.n_new)
+    for t in range(w.steps):
+        rec = I.gdn_verify_inputs(w, t, dev)
+        ss.verify(rec, os_)
+        ss.commit(torch.full((w.batch,), w.n_new, dtype=torch.int32, device=dev))
+        for i in range(w.n_new):
+            sa.step({k: v[:, i].contiguous() for k, v in rec.items()}, oa)
+            assert H.rel_l2(H.F64(os_[:, i]), H.F64(oa)) <= TOL_Y32, (t, i)
+    sa.flush()
+    ss.flush()
+    assert H.rel_l2(H.F64(ss.S), H.F64(sa.S)) <= TOL_CKPT
+    assert H.status(sa) == 0 and H.status(ss) == 0
