@@ -13,7 +13,7 @@
 // the committed window is folded first, S0' = e^{G_{c-1}} S0 + sum_{t<c}
 // D(c-1, t) e_t k_t^T (c = count), written once; the outputs are the same
 // whether computed from S0 with every record or from S0' with the new ones.
-#include "common.cuh"
+#include "gdn_common.cuh"
 #include "kernels.h"
 
 namespace rssm {
@@ -22,8 +22,6 @@ namespace {
 
 constexpr int GV_THREADS = 128;
 constexpr int GV_MAXR = 64;  // records in view: L + K <= 2 * RSSM_MAX_BUF_LEN
-
-__device__ __forceinline__ int wrap(int s, int L) { return s < L ? s : s - L; }
 
 // Row `r` of record t's key (t < count: ring slot; else new record t - count).
 __device__ __forceinline__ const uint16_t* key_of(const GdnArgs& a, size_t bh, int b, int h, int t, int start,
@@ -124,44 +122,15 @@ __global__ void __launch_bounds__(GV_THREADS) gdn_verify_kernel(GdnArgs a) {
   }
 }
 
-// One block per sequence, after the verify in stream order: checks the cursor as
-// the verify did, appends the new records' k, q (rows), g and beta, then sets
-// pending = K and the fold flag.
+// One block per sequence, after the verify in stream order.
 __global__ void __launch_bounds__(GV_THREADS) gdn_verify_epilogue_kernel(GdnArgs a) {
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const int L = a.L, K = a.K, H = a.H, DK = a.DK;
-  int4 c = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
-  if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L)) {
-    if (tid == 0) report(a.status, RSSM_DEV_BAD_CURSOR);
-    return;
-  }
-  if (c.z != 0) {
-    if (tid == 0) report(a.status, RSSM_DEV_PENDING);
-    return;
-  }
-  const int nv = DK >> 3;
-  for (int q = tid; q < K * H * nv; q += GV_THREADS) {
-    const int j = q / (H * nv), r = q - j * H * nv, h = r / nv, v = r - h * nv;
-    const size_t slot = ((size_t)b * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
-    const size_t src = (((size_t)b * K + j) * H + h) * DK + v * 8;
-    *reinterpret_cast<uint4*>(a.rk + slot * DK + v * 8) = *reinterpret_cast<const uint4*>(a.k + src);
-    *reinterpret_cast<uint4*>(a.rq + slot * DK + v * 8) = *reinterpret_cast<const uint4*>(a.q + src);
-  }
-  for (int q = tid; q < K * H; q += GV_THREADS) {
-    const int j = q / H, h = q - j * H;
-    const size_t s = ((size_t)b * H + h) * pad4(L) + wrap(wrap(c.x + c.y + j, L), L);
-    a.rg[s] = a.g[((size_t)b * K + j) * H + h];
-    a.rbeta[s] = a.beta[((size_t)b * K + j) * H + h];
-  }
-  if (tid == 0) {
-    c.z = K;
-    c.w = (c.y + K > L) ? 1 : 0;
-    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
-  }
+  const int4 c = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)blockIdx.x);
+  gdn_verify_epilogue(a, blockIdx.x, c, c.w);
 }
 
 cudaError_t gdn_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
+  if (gdn_verify_fast_applies(a)) return gdn_verify_fast_launch(a, out_bf16, st);
   if (out_bf16)
     gdn_verify_kernel<true><<<a.Bt * a.H, GV_THREADS, 0, st>>>(a);
   else

@@ -58,6 +58,9 @@ enum { GDN_CONVENTIONAL = 0, GDN_STEP = 1, GDN_FLUSH = 2, GDN_PRIME = 3 };
 
 // Speculative verify for Gated DeltaNet (gdn_verify.cu): K new records per sequence.
 cudaError_t gdn_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
+// Shape-specialised verify (dk = dv = 128, K <= 4, L + K <= 32; gdn_verify_fast.cu), epilogue included.
+bool gdn_verify_fast_applies(const GdnArgs& a);
+cudaError_t gdn_verify_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
 
 cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st);
 // Shape-specialised AR step (dk = dv = 128, L <= 31; gdn_step_fast.cu).

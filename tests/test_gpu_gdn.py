@@ -200,12 +200,15 @@ GSPEC = [
     GW("gspec_K1", 3, 2, 32, 48, 4, 10, seed=94, drafts=0),         # one record per verify
     GW("gspec_128", 3, 4, 128, 128, 16, 24, seed=95, drafts=3),     # the serving tile
     GW("gspec_128_L5", 2, 2, 128, 128, 5, 14, seed=96, drafts=3),   # folds often
+    GW("gspec_128_K1", 2, 2, 128, 128, 8, 12, seed=98, drafts=0),
+    GW("gspec_128_K2", 3, 2, 128, 128, 8, 12, seed=99, drafts=1),
+    GW("gspec_128_L28", 2, 2, 128, 128, 28, 24, seed=100, drafts=3),  # L + K = 32, the longest view
 ]
 
 
 @pytest.mark.parametrize("w", GSPEC, ids=lambda w: w.name)
 def test_gdn_spec(w):
-    assert run_gdn_spec(w) > 0 or w.name == "gspec_K1"
+    assert run_gdn_spec(w) > 0 or w.name in ("gspec_K1", "gspec_128_K1")
 
 
 def test_gdn_spec_bf16_out():
@@ -232,3 +235,18 @@ def test_gdn_spec_all_accepted_equals_ar():
     ss.flush()
     assert H.rel_l2(H.F64(ss.S), H.F64(sa.S)) <= TOL_CKPT
     assert H.status(sa) == 0 and H.status(ss) == 0
+
+
+@pytest.mark.parametrize("w", [GW("gtwice", 2, 2, 40, 24, 8, 1, seed=101, drafts=1, prefill=False),
+                               GW("gtwice_fast", 2, 2, 128, 128, 8, 1, seed=101, drafts=1, prefill=False)],
+                         ids=lambda w: w.name)
+def test_gdn_verify_twice_is_rejected(w):
+    dev = "cuda"
+    st, _, _, _ = H.gdn_setup(w, dev)
+    o = st.new_verify_output(w.n_new)
+    rec = I.gdn_verify_inputs(w, 0, dev)
+    st.verify(rec, o)
+    st.verify(rec, o)
+    torch.cuda.synchronize()
+    assert H.status(st) == bd.RSSM_DEV_PENDING
+    assert st.cursors.cpu().tolist() == [[0, 0, 2, 0], [0, 0, 2, 0]]
