@@ -5,8 +5,9 @@ writes once), the denominator of the roofline fraction: the checkpoint is
 read every step (bf16 read copy on non-flush steps when present) and written
 only on a flush; the current record is read once and appended to the ring;
 past records contribute the fields later steps read (Mamba-2 x, B, dt;
-Gated DeltaNet k, v, g, beta); outputs are written once; each cursor is read
-and written (16 + 16 bytes).
+Gated DeltaNet k, g and the record's cached correction e, dv fp32 -- the
+method keeps e beside each record, so v and beta are not read back); outputs
+are written once; each cursor is read and written (16 + 16 bytes).
 """
 
 CURSOR = 32
@@ -55,23 +56,34 @@ def mamba2_verify_bytes(H, P, N, G, L, K, counts, read_copy=False, out_bytes=2):
 def gdn_parts(H, DK, DV, out_bytes):
     tile = H * DV * DK * 4
     rec = H * (2 * DK * 2 + DV * 2 + 8)                # q, k, v, g, beta
-    past = H * (DK * 2 + DV * 2 + 8)                   # k, v, g, beta
+    e = H * DV * 4                                     # a record's cached correction
+    past = H * (DK * 2 + 4) + e                        # k, g, e
     o = H * DV * out_bytes
-    return tile, rec, past, o
+    return tile, rec, e, past, o
 
 
 def gdn_step_bytes(H, DK, DV, L, counts, out_bytes=2):
-    tile, rec, past, o = gdn_parts(H, DK, DV, out_bytes)
+    tile, rec, e, past, o = gdn_parts(H, DK, DV, out_bytes)
     total = 0
     for c in counts:
         if c + 1 == L:
             total += 2 * tile + rec
         else:
-            total += tile + 2 * rec
+            total += tile + 2 * rec + e
         total += c * past + o + CURSOR
     return total
 
 
+def gdn_verify_bytes(H, DK, DV, L, K, counts, out_bytes=2):
+    """One verify + commit; counts = committed window counts before the verify."""
+    tile, rec, e, past, o = gdn_parts(H, DK, DV, out_bytes)
+    total = 0
+    for c in counts:
+        total += 2 * tile if c + K > L else tile
+        total += K * (2 * rec + e) + c * past + K * o + 2 * CURSOR + 4
+    return total
+
+
 def gdn_conventional_bytes(H, DK, DV, batch, out_bytes=2):
-    tile, rec, past, o = gdn_parts(H, DK, DV, out_bytes)
+    tile, rec, e, past, o = gdn_parts(H, DK, DV, out_bytes)
     return batch * (2 * tile + rec + o)

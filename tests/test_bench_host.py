@@ -61,8 +61,14 @@ def test_bytes_model_serving_cycle():
     assert per_seq == pytest.approx(expect)
     conv = bm.mamba2_conventional_bytes(H, P, N, G, 1)
     assert conv == 2 * 4194304 + 37376 + 16384
-    # GDN serving shape: 2 MiB state per sequence
+    # GDN serving shape: 2 MiB state per sequence; a past record is read back as
+    # k, g and its cached correction e (dv fp32), and an append stores e too
     g = sum(bm.gdn_step_bytes(32, 128, 128, 16, [c]) for c in range(16)) / 16
     rec = 32 * (2 * 256 + 256 + 8)
-    past = 32 * (256 + 256 + 8)
-    assert g == pytest.approx(2097152 * 17 / 16 + (15 * 2 * rec + rec) / 16 + 7.5 * past + 32 * 128 * 2 + 32)
+    e = 32 * 512
+    past = 32 * (256 + 4) + e
+    assert g == pytest.approx(2097152 * 17 / 16 + (15 * (2 * rec + e) + rec) / 16 + 7.5 * past + 32 * 128 * 2 + 32)
+    # GDN verify, K = 4: a fold on count 13 (13 + 4 > 16), none on count 12
+    v = bm.gdn_verify_bytes(32, 128, 128, 16, 4, [12, 13])
+    assert v == (2097152 + 4 * (2 * rec + e) + 12 * past + 4 * 32 * 128 * 2 + 68) + \
+        (2 * 2097152 + 4 * (2 * rec + e) + 13 * past + 4 * 32 * 128 * 2 + 68)

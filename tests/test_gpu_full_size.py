@@ -144,6 +144,41 @@ def test_gdn_serving_full_size():
     assert H.status(st) == 0
 
 
+def test_gdn_spec_full_size():
+    """Gated DeltaNet speculative decode: batch 512, 32 heads, 128x128 state,
+    K = 4 records per verify, accepted ~U{0..3}, 128 verify steps, fold on overflow."""
+    w = I.WORKLOADS["gdn_spec"]
+    dev = "cuda"
+    st, pre, starts, counts = H.gdn_setup(w, dev, bd.RSSM_BF16)
+    seqs = spread(counts, 3)
+    fv, fk = H.Feed(), H.Feed()
+    sess = sessions.gdn_spec_session(H.F64(st.S[seqs]), H.sub(pre, seqs), starts[seqs].cpu().numpy(),
+                                     counts[seqs].cpu().numpy(), fv, fk, w.buf_len)
+    model = [(int(s), int(c), 0, 0) for s, c in zip(starts.cpu(), counts.cpu())]
+    o = st.new_verify_output(w.n_new)
+    folds = 0
+    for t in range(w.steps):
+        rec = I.gdn_verify_inputs(w, t, dev)
+        kept = I.accepted_kept(w, t, dev)
+        fv.rec = H.sub(rec, seqs)
+        fk.rec = kept[seqs].cpu().numpy()
+        st.verify(rec, o)
+        model = [oc.verify(c, w.n_new, w.buf_len)[0] for c in model]
+        np.testing.assert_array_equal(st.cursors.cpu().numpy(), np.array(model))
+        st.commit(kept)
+        model = [oc.commit(c, k, w.buf_len)[0] for c, k in zip(model, kept.cpu().tolist())]
+        np.testing.assert_array_equal(st.cursors.cpu().numpy(), np.array(model))
+        exp = next(sess)
+        assert H.bf16_excess(H.F64(o[seqs]), exp["o"]) <= TOL_BF16_EXCESS, t
+        assert torch.isfinite(o).all()
+        for i, b in enumerate(seqs):
+            if exp["folded"][i]:
+                folds += 1
+                assert H.rel_l2(H.F64(st.S[b]), exp["committed_state"][i]) <= TOL_CKPT, (t, b)
+    assert folds > 0
+    assert H.status(st) == 0
+
+
 def test_bf16_read_copy_4096_steps():
     """fp32 recurrence checkpoint + bf16 read copy, 4096 steps: the output error
     stays within 1e-2 relative L2 and does not grow (rounding of the read copy
