@@ -143,6 +143,28 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// d += A (16x8 tf32, row-major fragment: a0 (g, t), a1 (g+8, t), a2 (g, t+4),
+// a3 (g+8, t+4)) * B (8x8 tf32, column fragment: b0 (t, g), b1 (t+4, g)), fp32
+// accumulate; d0, d1 = (g, 2t), (g, 2t+1), d2, d3 = (g+8, 2t), (g+8, 2t+1);
+// g = lane / 4, t = lane % 4.
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp32 x = hi + lo with hi exactly representable in tf32 (the top 11 mantissa
+// bits) and lo rounded to tf32, so that two tf32 products with an operand that
+// is exact in tf32 (a bf16 value) recover x * y to about 2^-21 relative.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
 // ---------------------------------------------------------------- status
 
 __device__ __forceinline__ void report(int32_t* status, int code) {

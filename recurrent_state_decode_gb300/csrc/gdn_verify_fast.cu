@@ -38,28 +38,14 @@ constexpr int ES = FPB + 4;  // floats per staged e row (padded; 16-byte multipl
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// 32 partials for 8 rows x 4 vectors: [j * 8 + rr] = h[rr] . vec_j + cf[j] * el[rr].
-// Lane l ends with partial l (vector l >> 3, row l & 7).
-__device__ __forceinline__ float rows8x4(const float4 (&hv)[8], const float* vecs, const float (&gam)[KMAX],
-                                         const float (&cf)[KMAX], const float (&el)[8], int lane) {
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < KMAX; j++) {
-    const float4 c = scale4(gam[j], lds4(vecs + j * GD + lane * 4));
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++)
-      v[j * 8 + rr] = fmaf(hv[rr].x, c.x, fmaf(hv[rr].y, c.y, fmaf(hv[rr].z, c.z, fmaf(hv[rr].w, c.w, cf[j] * el[rr]))));
-  }
-  return reduce_transpose<32>(v, lane);
-}
-
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;                 // the block's 64 rows
   float* vecs = dsm + FPB * GD;      // [0..3] new k_j, [4..7] new q_i (fp32)
   float* es = vecs + 2 * KMAX * GD;  // e of committed record t at es + t * ES
-  __shared__ float skk[KMAX][FW * EW], skq[KMAX][FW * EW];  // k_e . k_j, k_e . q_i
+  __shared__ float tbl[2 * KMAX][FW * EW];  // [n][e]: k_e . vec_n; vec 0..3 = new k_j, 4..7 = new q_i
+  __shared__ float cf[2 * KMAX][33];        // [n][t]: D(a_n, t) (k_t . vec_n) of committed record t (padded rows)
   __shared__ uint64_t bar[2];
   __shared__ int4 cur_s;
   __shared__ int last_flags;
@@ -79,18 +65,19 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;
-  const int gj = lane >> 3, gr = lane & 7;  // (new record, row) this lane finishes
+  const int qg = lane >> 2, qt = lane & 3;   // tensor-core fragment coordinates
+  const int rA = rl0 + qg, rB = rl1 + qg;    // the rows of this lane's accumulator fragments
   const float gs = lane < L ? a.rg[bh * pad4(L) + lane] : 0.f;
   float gn = 0.f, bn = 0.f;
   if (lane < K) {
     gn = a.g[((size_t)b * K + lane) * H + h];
     bn = a.beta[((size_t)b * K + lane) * H + h];
   }
-  uint16_t vbA = 0, vbB = 0;
-  if (gj < K) {
-    const size_t vrow = (((size_t)b * K + gj) * H + h) * GD + p0 + gr;
-    vbA = a.v[vrow + rl0];
-    vbB = a.v[vrow + rl1];
+  uint32_t vtA = 0, vtB = 0;  // v of new record qt at rows rA, rB (bf16 bits)
+  if (qt < K) {
+    const size_t vrow = (((size_t)b * K + qt) * H + h) * GD + p0;
+    vtA = a.v[vrow + rA];
+    vtB = a.v[vrow + rB];
   }
   // the new records' k and q, fp32, in shared memory (each warp its own rows of the table)
   for (int v = warp; v < 2 * KMAX; v += FW) {
@@ -120,7 +107,7 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
       for (int j = 0; j < KMAX; j++) pk[m * KMAX + j] = dot4(ke, vv[j]);
     }
     const float red = reduce_transpose<EW * KMAX>(pk, lane);  // lane l: entry warp + 4 (l >> 2), vector l & 3
-    (pass ? skq : skk)[lane & 3][warp + FW * (lane >> 2)] = red;
+    tbl[pass * KMAX + (lane & 3)][warp + FW * (lane >> 2)] = red;
   }
   // An invalid cursor (reported by the epilogue) runs as an empty window with
   // every store masked.
@@ -160,18 +147,16 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   __syncthreads();  // the dot tables
   int ticket = 0;
   if (threadIdx.x == 0 && !fold) ticket = cursor_ticket(a.cursors, b);  // done with the ring's k and g
-  float cK[KMAX], cQ[KMAX];
+  if (warp == 0) {  // window coefficients of committed record `lane`, one row per vector
 #pragma unroll
-  for (int j = 0; j < KMAX; j++) {
-    const float d = lane < count ? expf(Ga[j] - G) : 0.f;
-    cK[j] = d * skk[j][sl];
-    cQ[j] = d * skq[j][sl];
+    for (int n = 0; n < 2 * KMAX; n++) cf[n][lane] = lane < count ? expf(Ga[n & (KMAX - 1)] - G) * tbl[n][sl] : 0.f;
   }
+  __syncthreads();  // the coefficient table
   float cpl = 0.f;
   if (lane < 16) {
-    if (cj2 < cj && cj < K) cpl = expf(Gx - Gy) * skk[cj][L + cj2];
+    if (cj2 < cj && cj < K) cpl = expf(Gx - Gy) * tbl[cj][L + cj2];
   } else {
-    if (cj2 <= cj && cj < K) cpl = expf(Gx - Gy) * skq[cj][L + cj2];
+    if (cj2 <= cj && cj < K) cpl = expf(Gx - Gy) * tbl[KMAX + cj][L + cj2];
   }
   const bool ok0 = mbar_wait(&bar[0], 0), ok1 = mbar_wait(&bar[1], 0);
   const bool landed = __all_sync(FULL, ok0 && ok1);  // uniform over the warp
@@ -181,48 +166,112 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     mbar_wait(&bar[1], 0);
   }
   if (landed) {
+    // S0 . [k_0..k_3, q_0..q_3] for rows (rA, rB) on the tensor cores: per 16
+    // columns two k-steps of m16n8k8 (lane t takes the float4 at column 4t, so
+    // the k order is permuted alike in A and B), S0 split into two tf32 parts.
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int rl = half ? rl1 : rl0;
-      float4 hv[8];
+    for (int jb = 0; jb < GD / 16; jb++) {
+      const int col = 16 * jb + 4 * qt;
+      const float4 r0 = lds4(tile + rA * GD + col), r1 = lds4(tile + rB * GD + col);
+      const float4 bv = lds4(vecs + qg * GD + col);
+      uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+      split_tf32(r0.x, h0, l0);
+      split_tf32(r1.x, h1, l1);
+      split_tf32(r0.y, h2, l2);
+      split_tf32(r1.y, h3, l3);
+      mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+      mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+      split_tf32(r0.z, h0, l0);
+      split_tf32(r1.z, h1, l1);
+      split_tf32(r0.w, h2, l2);
+      split_tf32(r1.w, h3, l3);
+      mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+      mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+    }
+    // + the committed window: sum_t D(a_n, t) (k_t . vec_n) e_t[row]
+    const int n0 = 2 * qt, n1 = n0 + 1;
+    float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
+    for (int t = 0; t < count; t++) {
+      const float c0 = cf[n0][t], c1 = cf[n1][t];
+      const float eA = es[t * ES + rA], eB = es[t * ES + rB];
+      w00 = fmaf(c0, eA, w00);
+      w01 = fmaf(c1, eA, w01);
+      w10 = fmaf(c0, eB, w10);
+      w11 = fmaf(c1, eB, w11);
+    }
+    const float ga0 = expf(__shfl_sync(FULL, G, (count + (n0 & 3)) & 31));
+    const float ga1 = expf(__shfl_sync(FULL, G, (count + (n1 & 3)) & 31));
+    // X (vectors 0..3, lanes t = 0, 1) or Y (vectors 4..7, lanes t = 2, 3), rows rA / rB
+    const float x00 = fmaf(ga0, acc[0], w00), x01 = fmaf(ga1, acc[1], w01);
+    const float x10 = fmaf(ga0, acc[2], w10), x11 = fmaf(ga1, acc[3], w11);
+    // the new records' e, solved in order (every lane of the quad, rows rA and rB)
+    const int qb = lane & ~3;
+    float XA[KMAX], XB[KMAX], vA[KMAX], vB[KMAX];
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = lds4(tile + (rl + rr) * GD + lane * 4);
-      float el[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // e of committed record `lane`, the 8 rows
-      if (lane < count) {
-        const float4 ea = lds4(es + lane * ES + rl), eb = lds4(es + lane * ES + rl + 4);
-        el[0] = ea.x; el[1] = ea.y; el[2] = ea.z; el[3] = ea.w;
-        el[4] = eb.x; el[5] = eb.y; el[6] = eb.z; el[7] = eb.w;
+    for (int j = 0; j < KMAX; j++) {
+      XA[j] = __shfl_sync(FULL, (j & 1) ? x01 : x00, qb + (j >> 1));
+      XB[j] = __shfl_sync(FULL, (j & 1) ? x11 : x10, qb + (j >> 1));
+      vA[j] = bf_to_f((uint16_t)__shfl_sync(FULL, vtA, qb + j));
+      vB[j] = bf_to_f((uint16_t)__shfl_sync(FULL, vtB, qb + j));
+    }
+    float eA[KMAX], eB[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; j++) {
+      const float bj = __shfl_sync(FULL, bn, j);  // 0 for j >= K
+      float ra = vA[j] - XA[j], rb = vB[j] - XB[j];
+#pragma unroll
+      for (int j2 = 0; j2 < j; j2++) {
+        const float m = __shfl_sync(FULL, cpl, 4 * j + j2);
+        ra = fmaf(-m, eA[j2], ra);
+        rb = fmaf(-m, eB[j2], rb);
       }
-      // lane (j, r): e^{G_a} S0 k_j + sum over the committed window of D (k_t . k_j) e_t
-      const float X = rows8x4(hv, vecs, gam, cK, el, lane);
-      const float vm = bf_to_f(half ? vbB : vbA);
-      float en[KMAX];  // e of new record j at this lane's row
+      eA[j] = bj * ra;
+      eB[j] = bj * rb;
+    }
+    // outputs i0, i0 + 1 on lanes t = 2, 3: Y + sum_{j<=i} D(a_i, a_j) (k_j . q_i) e_j
+    const int i0 = (2 * qt) & 3;
+    float oA0 = x00, oA1 = x01, oB0 = x10, oB1 = x11;
 #pragma unroll
-      for (int j = 0; j < KMAX; j++) {
-        float rhs = vm - X;
-#pragma unroll
-        for (int j2 = 0; j2 < j; j2++) rhs = fmaf(-__shfl_sync(FULL, cpl, 4 * j + j2), en[j2], rhs);
-        en[j] = __shfl_sync(FULL, __shfl_sync(FULL, bn, j) * rhs, 8 * j + gr);
+    for (int j = 0; j < KMAX; j++) {
+      const float c0 = __shfl_sync(FULL, cpl, (16 + 4 * i0 + j) & 31);
+      const float c1 = __shfl_sync(FULL, cpl, (16 + 4 * (i0 + 1) + j) & 31);
+      oA0 = fmaf(c0, eA[j], oA0);
+      oA1 = fmaf(c1, eA[j], oA1);
+      oB0 = fmaf(c0, eB[j], oB0);
+      oB1 = fmaf(c1, eB[j], oB1);
+    }
+    if (valid && qt >= 2) {
+      const size_t o0 = (((size_t)b * K + i0) * H + h) * GD + p0;
+      if (i0 < K) {
+        store_y<OUT_BF16>(a.o, o0 + rA, oA0);
+        store_y<OUT_BF16>(a.o, o0 + rB, oB0);
       }
-      const float Y = rows8x4(hv, vecs + KMAX * GD, gam, cQ, el, lane);
-      float o = Y;
-#pragma unroll
-      for (int j = 0; j < KMAX; j++) {
-        const float c = __shfl_sync(FULL, cpl, (16 + 4 * gj + j) & 31);
-        o = fmaf(c, en[j], o);  // c = 0 unless j <= gj < K
+      if (i0 + 1 < K) {
+        store_y<OUT_BF16>(a.o, o0 + (size_t)H * GD + rA, oA1);
+        store_y<OUT_BF16>(a.o, o0 + (size_t)H * GD + rB, oB1);
       }
-      if (valid && gj < K) {
-        float my = en[0];
+    }
+    if (valid && qt < K) {  // the new record qt's e and v rows, at rows rA, rB
+      float ma = eA[0], mb = eB[0];
 #pragma unroll
-        for (int j = 1; j < KMAX; j++) my = gj == j ? en[j] : my;
-        store_y<OUT_BF16>(a.o, (((size_t)b * K + gj) * H + h) * GD + p0 + rl + gr, o);
-        const size_t slot = bh * L + wrap(wrap(start + count + gj, L), L);
-        a.re[slot * GD + p0 + rl + gr] = my;
-        a.rv[slot * GD + p0 + rl + gr] = half ? vbB : vbA;
+      for (int j = 1; j < KMAX; j++) {
+        ma = qt == j ? eA[j] : ma;
+        mb = qt == j ? eB[j] : mb;
       }
-      if (fold) {  // S0' = e^{G_{c-1}} S0 + sum_{t<c} D(c-1, t) e_t k_t^T, written once
+      const size_t slot = bh * L + wrap(wrap(start + count + qt, L), L);
+      a.re[slot * GD + p0 + rA] = ma;
+      a.re[slot * GD + p0 + rB] = mb;
+      a.rv[slot * GD + p0 + rA] = (uint16_t)vtA;
+      a.rv[slot * GD + p0 + rB] = (uint16_t)vtB;
+    }
+    if (fold) {  // S0' = e^{G_{c-1}} S0 + sum_{t<c} D(c-1, t) e_t k_t^T, written once
 #pragma unroll
-        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, hv[rr]);
+      for (int half = 0; half < 2; half++) {
+        const int rl = half ? rl1 : rl0;
+        float4 hv[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, lds4(tile + (rl + rr) * GD + lane * 4));
         for (int t0 = 0; t0 < count; t0 += 2) {
           float4 kt[2];
 #pragma unroll
