@@ -11,13 +11,14 @@
 // lane s ring slot s (g); lane j new record j (g, beta); lane 8j + r the v of
 // new record j at row r of each group; the new records' k and q into shared
 // memory (fp32). Entry e of the dot tables is ring slot e (e < L) or new
-// record e - L; warp w forms (k_e . k_j) and (k_e . q_i) for entries w, w+4, ...
-// (two transposed 32-value reductions). After the cursor: the window records'
-// e rows by one 256-byte bulk copy each (second mbarrier) and one inclusive
-// warp scan of g. Per 8-row group two transposed 32-value reductions give, for
-// each (new record j, row r), e^{G_a} S0 k_j + the committed window's k-term
-// and e^{G_a} S0 q_i + its q-term; the new records' e are then solved in
-// order (one shuffle each) and the outputs completed. If count + K > L the
+// record e - L; (k_e . k_j) and (k_e . q_i) for all 32 entries come from two
+// warps' tensor-core products [32 x 128] . [128 x 8]. After the cursor: the
+// window records' e rows by one 256-byte bulk copy each (second mbarrier), one
+// inclusive warp scan of g, and a per-block table of the committed records'
+// coefficients D (k_t . vec). Each warp then forms S0 . [k_0..k_3, q_0..q_3] for
+// its 16 rows as m16n8k8 tf32 mma (the fp32 state split into two tf32 parts),
+// adds the committed window's terms, solves the new records' e in order within
+// each quad and completes the outputs. If count + K > L the
 // committed window is folded into the rows, written once. The new records'
 // v and e rows go to the ring here; their k, q, g, beta (read by the other
 // block of the head) are appended by the sequence's last block to arrive,
@@ -87,27 +88,33 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     reinterpret_cast<float4*>(vecs + v * GD)[lane] = f;
   }
   __syncthreads();
-  // dot tables for entries e = warp + 4 m: ring slot e (e < L) or new record e - L
+  // dot tables tbl[n][e] = k_e . vec_n for entries e < 32 (ring slot e if e < L,
+  // new record e - L if e < L + K, else 0): [32 x 128] . [128 x 8] on the
+  // tensor cores, warp w < 2 taking entries 16 w .. 16 w + 15 (bf16 inputs are
+  // exact in tf32, so one mma per k-step).
   const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
+  if (warp < 2) {
+    const int e0 = 16 * warp + qg, e1 = e0 + 8;
+    const uint16_t* g0 = e0 < L ? a.rk + (bh * L + e0) * GD : nullptr;
+    const uint16_t* g1 = e1 < L ? a.rk + (bh * L + e1) * GD : nullptr;
+    const float* s0 = (e0 >= L && e0 < L + K) ? vecs + (e0 - L) * GD : nullptr;
+    const float* s1 = (e1 >= L && e1 < L + K) ? vecs + (e1 - L) * GD : nullptr;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int pass = 0; pass < 2; pass++) {
-    float4 vv[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; j++) vv[j] = lds4(vecs + (pass * KMAX + j) * GD + lane * 4);
-    float pk[EW * KMAX];
-#pragma unroll
-    for (int m = 0; m < EW; m++) {
-      const int e = warp + FW * m;
-      float4 ke = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < L)
-        ke = load_bf4(rkp + e * GD);
-      else if (e < L + K)
-        ke = lds4(vecs + (e - L) * GD + lane * 4);
-#pragma unroll
-      for (int j = 0; j < KMAX; j++) pk[m * KMAX + j] = dot4(ke, vv[j]);
+    for (int jb = 0; jb < GD / 16; jb++) {
+      const int col = 16 * jb + 4 * qt;
+      const float4 r0 = g0 ? load_bf4(g0 + col) : (s0 ? lds4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
+      const float4 r1 = g1 ? load_bf4(g1 + col) : (s1 ? lds4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
+      const float4 bv = lds4(vecs + qg * GD + col);
+      mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y), __float_as_uint(r1.y),
+                    __float_as_uint(bv.x), __float_as_uint(bv.y));
+      mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w), __float_as_uint(r1.w),
+                    __float_as_uint(bv.z), __float_as_uint(bv.w));
     }
-    const float red = reduce_transpose<EW * KMAX>(pk, lane);  // lane l: entry warp + 4 (l >> 2), vector l & 3
-    tbl[pass * KMAX + (lane & 3)][warp + FW * (lane >> 2)] = red;
+    tbl[2 * qt][e0] = acc[0];
+    tbl[2 * qt + 1][e0] = acc[1];
+    tbl[2 * qt][e1] = acc[2];
+    tbl[2 * qt + 1][e1] = acc[3];
   }
   // An invalid cursor (reported by the epilogue) runs as an empty window with
   // every store masked.
