@@ -88,11 +88,33 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
   }
 }
 
+// Rows rA, rB of the state at columns col..col+3 as the kernel reads them: the
+// fp32 tile, the bf16 read copy in the tile, or (a folding block of the read
+// copy) the fp32 rows in global memory.
+__device__ __forceinline__ void state_rows(const float* tile, const float* gstate, bool bf16, int rA, int rB, int col,
+                                           float4& r0, float4& r1) {
+  if (gstate) {
+    r0 = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)rA * FN + col));
+    r1 = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)rB * FN + col));
+  } else if (bf16) {
+    const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
+    r0 = load_bf4(t16 + rA * FN + col);
+    r1 = load_bf4(t16 + rB * FN + col);
+  } else {
+    r0 = *reinterpret_cast<const float4*>(tile + rA * FN + col);
+    r1 = *reinterpret_cast<const float4*>(tile + rB * FN + col);
+  }
+}
+
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
-  __shared__ __align__(128) float tile[FPB * FN];  // the block's rows (fp32, or bf16 in the first half)
-  __shared__ float sc[KMAX][FW * EW];              // B_e . C_i
+  extern __shared__ __align__(128) float dsm[];
+  float* tile = dsm;                                                  // the block's rows (fp32, or bf16)
+  uint16_t* xs = reinterpret_cast<uint16_t*>(dsm + FPB * FN);         // x of record k, row r: xs[k * FPB + r]
+  __shared__ float tbl[KMAX][FW * EW];                                // B_e . C_i
+  __shared__ float cf[KMAX][33];                                      // window coefficient of record k, output i
   __shared__ uint64_t bar;
+  __shared__ int last_flags;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int L = a.L, P = a.P, H = a.H, G = a.G, K = a.K;
@@ -111,62 +133,81 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;
-  const int rA = p0 + rl0, rB2 = p0 + rl1;
+  const int qg = lane >> 2, qt = lane & 3;  // tensor-core fragment coordinates
+  const int rA = rl0 + qg, rB = rl1 + qg;   // rows of this lane's accumulator fragments (within the block)
   // ring slot `lane`
   const float dts = lane < L ? a.rdt[(size_t)bh * pad4(L) + lane] : 0.f;
   uint4 xsA = make_uint4(0, 0, 0, 0), xsB = xsA, xnA = xsA, xnB = xsA;
   if (lane < L) {
-    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P;
-    xsA = ldg16(xp + rA);
-    xsB = ldg16(xp + rB2);
+    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P + p0;
+    xsA = ldg16(xp + rl0);
+    xsB = ldg16(xp + rl1);
   }
   // new record `lane`
   const size_t nrow = ((size_t)b * K + lane) * H + h;
   float dtn = 0.f;
   if (lane < K) {
     dtn = a.dt[nrow];
-    xnA = ldg16(a.x + nrow * P + rA);
-    xnB = ldg16(a.x + nrow * P + rB2);
+    xnA = ldg16(a.x + nrow * P + p0 + rl0);
+    xnB = ldg16(a.x + nrow * P + p0 + rl1);
   }
-  // gate z of new record gi at row gr of each row group
+  // gate z of outputs n = 2 qt, 2 qt + 1 at rows rA, rB (lanes qt < 2); the z append rows
+  float zg[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int u = 0; u < 2; u++) {
+    const int n = 2 * qt + u;
+    if (n < K) {
+      const size_t zrow = (((size_t)b * K + n) * H + h) * P + p0;
+      zg[u][0] = bf_to_f(a.z[zrow + rA]);
+      zg[u][1] = bf_to_f(a.z[zrow + rB]);
+    }
+  }
   const int gi = lane >> 3, gr = lane & 7;
   uint16_t zbA = 0, zbB = 0;
   if (gi < K) {
-    const size_t zrow = (((size_t)b * K + gi) * H + h) * P;
-    zbA = a.z[zrow + rA + gr];
-    zbB = a.z[zrow + rB2 + gr];
+    const size_t zrow = (((size_t)b * K + gi) * H + h) * P + p0;
+    zbA = a.z[zrow + rl0 + gr];
+    zbB = a.z[zrow + rl1 + gr];
   }
   const float Ah = a.A[h], Dh = a.D[h];
-  float4 ci[KMAX];  // the lane's column chunk of C_i
+  // the lane's B-fragment source: C_n, n = qg (zero for n >= K)
+  const uint16_t* cvec = qg < K ? a.C + (((size_t)b * K + qg) * G + g) * FN : nullptr;
+  // dot table tbl[i][e] = B_e . C_i for entries e < 32 (ring slot e if e < L, new
+  // record e - L if e < L + K, else 0): [32 x 128] . [128 x 8] on the tensor
+  // cores, warp w < 2 taking entries 16 w .. 16 w + 15 (bf16 inputs are exact in tf32)
+  if (warp < 2) {
+    const int e0 = 16 * warp + qg, e1 = e0 + 8;
+    auto row_of = [&](int e) -> const uint16_t* {
+      if (e < L) return a.rB + ((size_t)bg * L + e) * FN;
+      if (e < L + K) return a.B + (((size_t)b * K + (e - L)) * G + g) * FN;
+      return nullptr;
+    };
+    const uint16_t* s0 = row_of(e0);
+    const uint16_t* s1 = row_of(e1);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < KMAX; i++)
-    ci[i] = i < K ? load_bf4(a.C + (((size_t)b * K + i) * G + g) * FN + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-  {  // sc[i][e] = B_e . C_i for entries e = warp + 4 j
-#pragma unroll
-    for (int jb = 0; jb < EW; jb += EW / 2) {  // two batches of 16 partials
-      float pk[EW / 2 * KMAX];
-#pragma unroll
-      for (int j = 0; j < EW / 2; j++) {
-        const int e = warp + FW * (jb + j);
-        float4 be = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (e < L)
-          be = load_bf4(a.rB + ((size_t)bg * L + e) * FN + lane * 4);
-        else if (e < L + K)
-          be = load_bf4(a.B + (((size_t)b * K + (e - L)) * G + g) * FN + lane * 4);
-#pragma unroll
-        for (int i = 0; i < KMAX; i++) pk[j * KMAX + i] = dot4(be, ci[i]);
-      }
-      // lane l holds partial l >> 1: entry warp + 4 (jb + (l >> 3)), output (l >> 1) & 3
-      const float red = reduce_transpose<EW / 2 * KMAX>(pk, lane);
-      if ((lane & 1) == 0) sc[(lane >> 1) & 3][warp + FW * (jb + (lane >> 3))] = red;
+    for (int jb = 0; jb < FN / 16; jb++) {
+      const int col = 16 * jb + 4 * qt;
+      const float4 r0 = s0 ? load_bf4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 r1 = s1 ? load_bf4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 bv = cvec ? load_bf4(cvec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y), __float_as_uint(r1.y),
+                    __float_as_uint(bv.x), __float_as_uint(bv.y));
+      mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w), __float_as_uint(r1.w),
+                    __float_as_uint(bv.z), __float_as_uint(bv.w));
+    }
+    if (qt < 2) {  // columns 2 qt, 2 qt + 1 are outputs 0..3
+      tbl[2 * qt][e0] = acc[0];
+      tbl[2 * qt + 1][e0] = acc[1];
+      tbl[2 * qt][e1] = acc[2];
+      tbl[2 * qt + 1][e1] = acc[3];
     }
   }
-  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
   // An invalid cursor (reported by the epilogue below) runs as an empty window
   // with every store masked.
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
   const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, total = count + K;
   const bool fold = total > L;
-  const int first = fold ? count : 0;
   // record k on lane k: committed (ring slot sl) or new (record jn)
   int sl = start + lane;
   sl = sl < L ? sl : sl - L;
@@ -179,77 +220,130 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     const float v = __shfl_up_sync(FULL, S, o);
     if (lane >= o) S += v;
   }
-  const float Sb = __shfl_sync(FULL, S, (first - 1) & 31);
-  const float S0 = first > 0 ? Sb : 0.f;
   const float Sf = __shfl_sync(FULL, S, (count - 1) & 31);
   const float Pf = expf(Sf);                                // fold: e^{S_{count-1}}
   const float wf = lane < count ? dtk * expf(Sf - S) : 0.f;  // fold weights
   const int ek = lane < count ? sl : (lane < total ? L + jn : 0);
   const uint4 xar = shfl_u4(xsA, sl), xbr = shfl_u4(xsB, sl), xan = shfl_u4(xnA, jn), xbn = shfl_u4(xnB, jn);
   const uint4 xq[2] = {lane < count ? xar : xan, lane < count ? xbr : xbn};
-  float Pi[KMAX], Sl[KMAX];
-#pragma unroll
-  for (int i = 0; i < KMAX; i++) {
-    Sl[i] = __shfl_sync(FULL, S, (count + i) & 31);
-    Pi[i] = expf(Sl[i] - S0);
+  if (lane < total) {  // this warp's rows of every record's x, in record order
+    *reinterpret_cast<uint4*>(xs + lane * FPB + rl0) = xq[0];
+    *reinterpret_cast<uint4*>(xs + lane * FPB + rl1) = xq[1];
   }
-  __syncthreads();
+  __syncthreads();  // the dot table (and each warp's x rows)
   // Without a fold the epilogue writes free ring slots only: this block is done
   // with what it overwrites (dots, dt) and arrives now; a folding block arrives
   // after its fold.
   int ticket = (threadIdx.x == 0 && !fold) ? cursor_ticket(a.cursors, b) : 0;
-  float coef[KMAX];
+  // Outputs come from the checkpoint and every record since it (the fold only
+  // writes the checkpoint): output i = e^{S_a} (h0 . C_i) + sum_{k<=a} cf[i][k] x_k,
+  // a = count + i, cf = dt_k e^{S_a - S_k} (B_k . C_i) (+ D on record a).
+  if (warp == 0) {
 #pragma unroll
-  for (int i = 0; i < KMAX; i++) {
-    const int last = count + i;
-    const bool in = i < K && lane >= first && lane <= last;
-    coef[i] = in ? fmaf(dtk * expf(Sl[i] - S), sc[i][ek], lane == last ? Dh : 0.f) : 0.f;
+    for (int i = 0; i < KMAX; i++) {
+      const float Sa = __shfl_sync(FULL, S, (count + i) & 31);
+      cf[i][lane] = (i < K && lane <= count + i) ? fmaf(dtk * expf(Sa - S), tbl[i][ek], lane == count + i ? Dh : 0.f)
+                                                 : 0.f;
+    }
   }
-  const float gA = silu_fast(bf_to_f(zbA)), gB = silu_fast(bf_to_f(zbB));
   // Append the new records' x and z rows of this block now: its committed x
-  // rows are in registers already (the fold and the outputs use those).
+  // rows are in registers and shared memory already.
   auto slot_of = [&](int j) {
     int s = start + count + j;
     s = s < L ? s : s - L;
     return s < L ? s : s - L;
   };
   if (valid && lane < K) {
-    const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P;
-    *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xnA;
-    *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xnB;
+    const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P + p0;
+    *reinterpret_cast<uint4*>(a.rx + rrow + rl0) = xnA;
+    *reinterpret_cast<uint4*>(a.rx + rrow + rl1) = xnB;
   }
   if (valid && gi < K) {
-    const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P;
-    a.rz[rrow + rA + gr] = zbA;
-    a.rz[rrow + rB2 + gr] = zbB;
+    const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P + p0;
+    a.rz[rrow + rl0 + gr] = zbA;
+    a.rz[rrow + rl1 + gr] = zbB;
   }
+  const float Pn0 = expf(__shfl_sync(FULL, S, (count + 2 * qt) & 31));
+  const float Pn1 = expf(__shfl_sync(FULL, S, (count + 2 * qt + 1) & 31));
+  __syncthreads();  // the coefficient table
   const bool landed = __all_sync(FULL, mbar_wait(&bar, 0));  // uniform over the warp
   if (!landed) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar, 0);
   }
-  // A block that reads the bf16 copy folds from the fp32 rows in global memory.
-  const bool from_tile = !(copy && fold);
+  // A block that reads the bf16 copy folds (and, on that step, outputs) from the
+  // fp32 rows in global memory.
+  const float* gstate = (copy && fold) ? a.ckpt + tbase : nullptr;
+  const bool t16 = copy && !fold;
   if (landed) {
+    // h0 . [C_0..C_3] for rows (rA, rB) as m16n8k8 tf32 mma; an fp32 state is
+    // split into two tf32 parts, the bf16 read copy is exact in tf32
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int rl = half ? rl1 : rl0;
-      float4 hv[8];
-      if (!from_tile) {
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++)
-          hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + tbase + (size_t)(rl + rr) * FN) + lane);
-      } else if (copy) {
-        const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
+    for (int jb = 0; jb < FN / 16; jb++) {
+      const int col = 16 * jb + 4 * qt;
+      float4 r0, r1;
+      state_rows(tile, gstate, t16, rA, rB, col, r0, r1);
+      const float4 bv = cvec ? load_bf4(cvec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t16) {  // uniform
+        mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y),
+                      __float_as_uint(r1.y), __float_as_uint(bv.x), __float_as_uint(bv.y));
+        mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w),
+                      __float_as_uint(r1.w), __float_as_uint(bv.z), __float_as_uint(bv.w));
       } else {
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
+        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+        split_tf32(r0.x, h0, l0);
+        split_tf32(r1.x, h1, l1);
+        split_tf32(r0.y, h2, l2);
+        split_tf32(r1.y, h3, l3);
+        mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+        mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+        split_tf32(r0.z, h0, l0);
+        split_tf32(r1.z, h1, l1);
+        split_tf32(r0.w, h2, l2);
+        split_tf32(r1.w, h3, l3);
+        mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+        mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
       }
-      float xl[8];
-      unpack8(xq[half], xl);
-      if (fold) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, four records per round
+    }
+    if (qt < 2) {  // outputs n0 = 2 qt, n1 = n0 + 1 at rows rA, rB
+      const int n0 = 2 * qt, n1 = n0 + 1;
+      float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
+      for (int k = 0; k < total; k++) {
+        const float c0 = cf[n0][k], c1 = cf[n1][k];
+        const float xa = bf_to_f(xs[k * FPB + rA]), xb = bf_to_f(xs[k * FPB + rB]);
+        w00 = fmaf(c0, xa, w00);
+        w01 = fmaf(c1, xa, w01);
+        w10 = fmaf(c0, xb, w10);
+        w11 = fmaf(c1, xb, w11);
+      }
+      if (valid) {
+        const size_t y0 = (((size_t)b * K + n0) * H + h) * P + p0;
+        if (n0 < K) {
+          store_y<OUT_BF16>(a.y, y0 + rA, fmaf(Pn0, acc[0], w00) * silu_fast(zg[0][0]));
+          store_y<OUT_BF16>(a.y, y0 + rB, fmaf(Pn0, acc[2], w10) * silu_fast(zg[0][1]));
+        }
+        if (n1 < K) {
+          store_y<OUT_BF16>(a.y, y0 + (size_t)H * P + rA, fmaf(Pn1, acc[1], w01) * silu_fast(zg[1][0]));
+          store_y<OUT_BF16>(a.y, y0 + (size_t)H * P + rB, fmaf(Pn1, acc[3], w11) * silu_fast(zg[1][1]));
+        }
+      }
+    }
+    if (fold) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, written once (with the bf16 copy)
+#pragma unroll
+      for (int half = 0; half < 2; half++) {
+        const int rl = half ? rl1 : rl0;
+        float4 hv[8];
+        if (gstate) {
+#pragma unroll
+          for (int rr = 0; rr < 8; rr++)
+            hv[rr] = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)(rl + rr) * FN) + lane);
+        } else {
+#pragma unroll
+          for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
+        }
+        float xl[8];
+        unpack8(xq[half], xl);
 #pragma unroll
         for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, hv[rr]);
         const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
@@ -276,24 +370,11 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
           if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
         }
       }
-      const float gate = half ? gB : gA;
-#pragma unroll
-      for (int i = 0; i < KMAX; i++) {
-        if (i < K) {  // uniform
-          float tx[8];
-#pragma unroll
-          for (int rr = 0; rr < 8; rr++) tx[rr] = coef[i] * xl[rr];
-          const float tot = rows8(hv, scale4(Pi[i], ci[i]), tx, lane);
-          const float t = __shfl_sync(FULL, tot, row_src(gr));
-          if (valid && gi == i) store_y<OUT_BF16>(a.y, (((size_t)b * K + i) * H + h) * P + p0 + rl + gr, t * gate);
-        }
-      }
     }
   }
   // The last of the sequence's blocks to arrive (all of them are done with the
   // ring rows the append overwrites) appends the new records' B, C and dt and
   // marks the cursor pending.
-  __shared__ int last_flags;
   if (fold) {  // uniform: the committed B rows were read by the fold until here
     __syncthreads();
     if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);
@@ -315,10 +396,12 @@ bool m2_verify_fast_applies(const M2Args& a) {
 cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
   const dim3 grid(a.nPB, a.H, a.Bt);
   auto k = out_bf16 ? m2_verify_fast_kernel<true> : m2_verify_fast_kernel<false>;
+  const int smem = FPB * FN * 4 + (a.L + a.K) * FPB * 2;  // tile + the records' x rows
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, FT, 0, st>>>(a);
+  k<<<grid, FT, smem, st>>>(a);
   return cudaGetLastError();
 }
 
