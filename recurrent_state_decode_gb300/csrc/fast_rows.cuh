@@ -4,6 +4,7 @@
 // float4 column chunk 4l..4l+3 of each.
 #pragma once
 #include "common.cuh"
+#include "kernels.h"
 
 namespace rssm {
 namespace fastrows {
@@ -90,6 +91,35 @@ __device__ __forceinline__ void finish_ar_cursor(int32_t* cursors, int b, int4 c
   else
     c.y = (c.y + 1 == L) ? 0 : c.y + 1;
   *reinterpret_cast<int4*>(cursors + 4 * (size_t)b) = c;
+}
+
+// gate: silu(z) of row (lane & 7), computed before the rows land
+template <bool OUT_BF16>
+__device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float gate, float tot, int lane) {
+  const float t = __shfl_sync(FULL, tot, row_src(lane & 7));
+  if (lane < 8) store_y<OUT_BF16>(a.y, obase + lane, t * gate);
+}
+
+// h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the bf16 copy).
+__device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm, float wk, const float (&xl)[8],
+                                      int m, int count, int start, int bg, size_t off, int lane) {
+  const int L = a.L;
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pm, hv[rr]);
+  const uint16_t* rB = a.rB + (size_t)bg * L * FN + lane * 4;
+  for (int k = 0; k < m; k++) {
+    const float w = __shfl_sync(FULL, wk, k);
+    int s = start + k;
+    s = s < L ? s : s - L;
+    const float4 bk = load_bf4(k < count ? rB + s * FN : a.B + (size_t)bg * FN + lane * 4);
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[rr], k), bk, hv[rr]);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) {
+    __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
+    if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
+  }
 }
 
 }  // namespace fastrows

@@ -94,8 +94,18 @@ def test_shapes(w, out):
     run_ar(w, out_dtype=out)
 
 
-@pytest.mark.parametrize("w", [SHAPES[0], SHAPES[3], W("rc", 3, 4, 64, 128, 2, 16, 40, seed=19)],
-                         ids=lambda w: w.name)
+READ_COPY = [
+    SHAPES[0], SHAPES[3],
+    W("rc", 3, 4, 64, 128, 2, 16, 40, seed=19),            # two heads of a group per block
+    W("rc_g1", 2, 3, 64, 128, 3, 8, 20, seed=20),          # one head per group: one head per block
+    W("rc_p128", 2, 4, 128, 128, 2, 8, 20, seed=21),       # two row blocks per head
+    W("rc_L31", 2, 4, 64, 128, 1, 31, 70, seed=22),        # longest window of the shape-specialised kernels
+    W("rc_L1", 2, 4, 64, 128, 2, 1, 5, seed=23),           # every step flushes
+    W("rc_hpg4", 2, 8, 64, 128, 2, 5, 12, seed=24),        # two head pairs per group
+]
+
+
+@pytest.mark.parametrize("w", READ_COPY, ids=lambda w: w.name)
 def test_read_copy_small(w):
     run_ar(w, read_copy=True)
 
