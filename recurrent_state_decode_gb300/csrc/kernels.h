@@ -32,9 +32,6 @@ cudaError_t m2_step_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // Shape-specialised AR step (dstate 128, headdim a multiple of 64; mamba2_step_fast.cu).
 bool m2_step_fast_applies(const M2Args& a);
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st);
-// The same for the bf16 read copy, two heads of a group per block (mamba2_step_read16.cu).
-bool m2_step_read16_applies(const M2Args& a);
-cudaError_t m2_step_read16_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // The persistent speculative verify (mamba2_verify.cu); its epilogue kernel is in mamba2.cu.
 cudaError_t m2_verify_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // Shape-specialised verify (dstate 128, headdim a multiple of 64, K <= 4; mamba2_verify_fast.cu).

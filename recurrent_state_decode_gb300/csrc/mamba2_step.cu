@@ -256,7 +256,6 @@ cudaError_t launch_step(const M2Args& a, cudaStream_t st) {
 
 cudaError_t m2_step_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
   if (a.Bt * a.H * a.nPB == 0) return cudaSuccess;
-  if (m2_step_read16_applies(a)) return m2_step_read16_launch(a, out_bf16, st);
   if (m2_step_fast_applies(a)) return m2_step_fast_launch(a, out_bf16, st);
   const bool small_window = a.L <= 16, narrow = a.N <= 128;
   if (small_window) {
