@@ -36,9 +36,10 @@ using namespace fastrows;
 
 constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
-  __shared__ __align__(128) float tile[FPB * FN];  // the block's rows (fp32, or bf16 in the first half)
+// RD16: the block reads the bf16 read copy (16 KiB tiles, eight blocks per SM).
+template <bool OUT_BF16, bool RD16>
+__global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a) {
+  extern __shared__ __align__(128) float tile[];  // the block's rows (fp32, or bf16)
   __shared__ float sc[FW * KW];                    // c_s = B_s . C by ring slot; [L] = current
   __shared__ uint64_t bar;
   __shared__ int4 scur;  // the cursor as read, for the sequence's last block
@@ -48,7 +49,7 @@ __global__ void __launch_bounds__(FT, 6) m2_step_fast_kernel(M2Args a) {
   const int g = h >> a.hpg_log2;  // H / G heads per group, a power of two on this path
   const int bh = b * H + h, bg = b * a.G + g;
   const int p0 = pb * FPB;
-  const bool copy = a.ckpt_read != nullptr;
+  constexpr bool copy = RD16;  // a.ckpt_read != nullptr
   const size_t tbase = ((size_t)bh * P + p0) * FN;  // element offset of the block's row 0
 
   if (threadIdx.x == 0) {
@@ -191,12 +192,15 @@ bool m2_step_fast_applies(const M2Args& a) {
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
   const dim3 grid(a.nPB, a.H, a.Bt);
-  auto k = out_bf16 ? m2_step_fast_kernel<true> : m2_step_fast_kernel<false>;
-  // six 32 KiB tiles per SM need the largest shared-memory split of the unified L1
+  const bool rd16 = a.ckpt_read != nullptr;
+  auto k = rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true> : m2_step_fast_kernel<false, true>)
+                : (out_bf16 ? m2_step_fast_kernel<true, false> : m2_step_fast_kernel<false, false>);
+  const int smem = FPB * FN * (rd16 ? 2 : 4);
+  // six 32 KiB (eight 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  k<<<grid, FT, 0, st>>>(a);
+  k<<<grid, FT, smem, st>>>(a);
   return cudaGetLastError();
 }
 
