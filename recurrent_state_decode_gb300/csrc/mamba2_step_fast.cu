@@ -39,7 +39,10 @@ constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 // RD16: the block reads the bf16 read copy (16 KiB tiles, eight blocks per SM).
 template <bool OUT_BF16, bool RD16>
 __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a) {
-  extern __shared__ __align__(128) float tile[];  // the block's rows (fp32, or bf16)
+  // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
+  __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
+  extern __shared__ __align__(128) float tile_d[];
+  float* const tile = RD16 ? tile_d : tile_s;
   __shared__ float sc[FW * KW];                    // c_s = B_s . C by ring slot; [L] = current
   __shared__ uint64_t bar;
   __shared__ int4 scur;  // the cursor as read, for the sequence's last block
@@ -195,7 +198,7 @@ cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) 
   const bool rd16 = a.ckpt_read != nullptr;
   auto k = rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true> : m2_step_fast_kernel<false, true>)
                 : (out_bf16 ? m2_step_fast_kernel<true, false> : m2_step_fast_kernel<false, false>);
-  const int smem = FPB * FN * (rd16 ? 2 : 4);
+  const int smem = rd16 ? FPB * FN * 2 : 0;
   // six 32 KiB (eight 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
