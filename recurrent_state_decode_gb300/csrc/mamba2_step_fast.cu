@@ -52,7 +52,9 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   const int g = h >> a.hpg_log2;  // H / G heads per group, a power of two on this path
   const int bh = b * H + h, bg = b * a.G + g;
   const int p0 = pb * FPB;
-  constexpr bool copy = RD16;  // a.ckpt_read != nullptr
+  // a bf16 read copy is present (known at compile time only in the read-copy instantiation; the
+  // fp32 one keeps the run-time test, which measured faster there)
+  const bool copy = RD16 || a.ckpt_read != nullptr;
   const size_t tbase = ((size_t)bh * P + p0) * FN;  // element offset of the block's row 0
 
   if (threadIdx.x == 0) {
