@@ -75,8 +75,9 @@ enum {
   RSSM_DEV_TIMEOUT = 6      /* a bounded wait for an asynchronous copy expired */
 };
 
-/* Output element types. */
-enum { RSSM_F32 = 0, RSSM_BF16 = 1 };
+/* Element types: of outputs (RSSM_F32, RSSM_BF16) and of the checkpoint's
+ * read copy (RSSM_BF16, RSSM_F16). */
+enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2 };
 
 /* Limits of this build. */
 #define RSSM_MAX_BUF_LEN 32 /* L in [1, 32] */
@@ -96,6 +97,8 @@ typedef struct {
   int batch, nheads, headdim, dstate, ngroups;
   int buf_len;   /* L, the window length */
   int out_dtype; /* RSSM_F32 or RSSM_BF16: element type of y */
+  int read_dtype; /* element type of the read copy ckpt_read, when one is
+                   * passed: RSSM_BF16 (0 reads as RSSM_BF16) or RSSM_F16 */
 } rssm_mamba2_desc;
 
 /* Ring buffer of window records, head- (or group-) major so that one
@@ -135,7 +138,7 @@ RSSM_API int rssm_mamba2_conventional_step(const rssm_mamba2_desc* desc, float* 
  *  - c + 1 == L (flush): folds the L records into the checkpoint, writes it
  *    (and ckpt_read, if given) once, computes y; count becomes 0.
  *  ckpt      [batch, nheads, headdim, dstate] fp32 recurrence checkpoint
- *  ckpt_read same shape in bf16, or NULL. When given, non-flush steps read
+ *  ckpt_read same shape in desc->read_dtype (bf16 or fp16), or NULL. When given, non-flush steps read
  *            it instead of ckpt (the low-precision read copy of "ReplaySSM",
  *            introduction, "Separate state precisions"); flushes read ckpt
  *            and write both.
@@ -201,9 +204,11 @@ RSSM_API int rssm_commit_cursors(int32_t* cursors, const int32_t* kept, int batc
 RSSM_API int rssm_reset_cursors(int32_t* cursors, const int32_t* slots, int n_slots,
                        int batch, int32_t* dev_status, rssm_stream_t stream);
 
-/* fp32 -> bf16 read copy, round to nearest even ("ReplaySSM", introduction,
- * "Separate state precisions"). src [n] fp32, dst [n] bf16. */
-RSSM_API int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n,
+/* fp32 -> low-precision read copy, round to nearest even ("ReplaySSM",
+ * introduction, "Separate state precisions"). src [n] fp32, dst [n] of dtype
+ * RSSM_BF16 or RSSM_F16 (16-bit elements; fp16 saturates to +-inf above its
+ * range). Any other dtype: RSSM_ERR_INVALID_ARG. */
+RSSM_API int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, int dtype,
                              rssm_stream_t stream);
 
 /* ----------------------------------------------------------------------------

@@ -27,12 +27,14 @@ RSSM_DEV_BAD_SLOT = 5
 RSSM_DEV_TIMEOUT = 6
 RSSM_F32 = 0
 RSSM_BF16 = 1
+RSSM_F16 = 2
 
 c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
 
 
 class rssm_mamba2_desc(ctypes.Structure):
-    _fields_ = [(n, c_int) for n in ("batch", "nheads", "headdim", "dstate", "ngroups", "buf_len", "out_dtype")]
+    _fields_ = [(n, c_int) for n in ("batch", "nheads", "headdim", "dstate", "ngroups", "buf_len", "out_dtype",
+                                     "read_dtype")]
 
 
 class rssm_mamba2_ring(ctypes.Structure):
@@ -59,7 +61,7 @@ _SIGNATURES = {
     "rssm_mamba2_spec_verify": (c_int, [P, c_int] + [P] * 14),
     "rssm_commit_cursors": (c_int, [P, P, c_int, c_int, P, P]),
     "rssm_reset_cursors": (c_int, [P, P, c_int, c_int, P, P]),
-    "rssm_checkpoint_downcast": (c_int, [P, P, c_size_t, P]),
+    "rssm_checkpoint_downcast": (c_int, [P, P, c_size_t, c_int, P]),
     "rssm_gdn_conventional_step": (c_int, [P] * 8 + [P]),
     "rssm_gdn_step": (c_int, [P] * 11 + [P]),
     "rssm_gdn_flush": (c_int, [P] * 5 + [P]),
@@ -122,8 +124,8 @@ def _stream(stream, *tensors):
     return None
 
 
-def mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype=RSSM_F32):
-    return rssm_mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype)
+def mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype=RSSM_F32, read_dtype=0):
+    return rssm_mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype, read_dtype)
 
 
 def mamba2_ring(x, z, B, C, dt):
@@ -195,8 +197,11 @@ def rssm_reset_cursors(cursors, slots, n_slots, batch, dev_status=None, stream=N
                                      _stream(stream, cursors))
 
 
-def rssm_checkpoint_downcast(src, dst, n, stream=None):
-    return load().rssm_checkpoint_downcast(ptr(src), ptr(dst), int(n), _stream(stream, src))
+def rssm_checkpoint_downcast(src, dst, n, dtype=None, stream=None):
+    if dtype is None:
+        import torch
+        dtype = RSSM_F16 if dst.dtype == torch.float16 else RSSM_BF16
+    return load().rssm_checkpoint_downcast(ptr(src), ptr(dst), int(n), int(dtype), _stream(stream, src))
 
 
 def rssm_gdn_conventional_step(desc, S, q, k, v, g, beta, o, stream=None):

@@ -31,6 +31,7 @@ int check_m2(const rssm_mamba2_desc* d) {
   if (!dim_ok(d->headdim) || !dim_ok(d->dstate)) return RSSM_ERR_INVALID_ARG;
   if (d->buf_len < 1 || d->buf_len > RSSM_MAX_BUF_LEN) return RSSM_ERR_INVALID_ARG;
   if (d->out_dtype != RSSM_F32 && d->out_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
+  if (d->read_dtype != 0 && d->read_dtype != RSSM_BF16 && d->read_dtype != RSSM_F16) return RSSM_ERR_INVALID_ARG;
   const int pb = rows_per_block(d->headdim, d->dstate);
   const long long grid = (long long)d->batch * d->nheads * ((d->headdim + pb - 1) / pb);
   if (grid > INT_MAX || d->batch > 65535) return RSSM_ERR_UNSUPPORTED;
@@ -59,6 +60,7 @@ M2Args m2_args(const rssm_mamba2_desc* d) {
   a.PB = rows_per_block(a.P, a.N);
   a.nPB = (a.P + a.PB - 1) / a.PB;
   a.K = 1;
+  a.read_f16 = d->read_dtype == RSSM_F16;
   const int hpg = a.H / a.G;
   a.hpg_log2 = (hpg & (hpg - 1)) == 0 ? __builtin_ctz(hpg) : -1;
   return a;
@@ -250,11 +252,12 @@ int rssm_reset_cursors(int32_t* cursors, const int32_t* slots, int n_slots, int 
   return cuda_rc(reset_launch(cursors, slots, n_slots, batch, dev_status, (cudaStream_t)stream));
 }
 
-int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, rssm_stream_t stream) {
+int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, int dtype, rssm_stream_t stream) {
+  if (dtype != RSSM_BF16 && dtype != RSSM_F16) return RSSM_ERR_INVALID_ARG;
   if (n == 0) return RSSM_OK;
   int rc;
   if ((rc = check_ptrs({src, dst}))) return rc;
-  return cuda_rc(downcast_launch(src, dst, n, (cudaStream_t)stream));
+  return cuda_rc(downcast_launch(src, dst, n, dtype == RSSM_F16, (cudaStream_t)stream));
 }
 
 int rssm_gdn_conventional_step(const rssm_gdn_desc* d, float* S, const rssm_bf16* q, const rssm_bf16* k,

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -43,6 +44,24 @@ __device__ __forceinline__ float bf_to_f(uint16_t v) { return __uint_as_float(((
 __device__ __forceinline__ float4 load_bf4(const uint16_t* p) {
   return bf4_to_f4(*reinterpret_cast<const uint2*>(p));
 }
+
+// fp16 <-> fp32 (the read copy's other element type), through the CUDA half intrinsics.
+__device__ __forceinline__ float4 load_h4(const uint16_t* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+__device__ __forceinline__ uint2 f4_to_h4(float4 v) {
+  const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// The read copy's four elements at p as fp32, and four fp32 rounded (RNE) to
+// it; f16 selects fp16 over bf16 (uniform over a launch).
+__device__ __forceinline__ float4 load_rc4(const uint16_t* p, bool f16) { return f16 ? load_h4(p) : load_bf4(p); }
+__device__ __forceinline__ uint2 to_rc4(float4 v, bool f16) { return f16 ? f4_to_h4(v) : f4_to_bf4(v); }
 
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));

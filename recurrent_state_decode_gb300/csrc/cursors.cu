@@ -55,16 +55,16 @@ __global__ void reset_kernel(int32_t* cursors, const int32_t* slots, int n, int 
   *reinterpret_cast<int4*>(cursors + 4 * (size_t)s) = make_int4(0, 0, 0, 0);
 }
 
-__global__ void downcast_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n) {
+__global__ void downcast_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n, bool f16) {
   const size_t n4 = n >> 2;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
     const float4 v = __ldcs(reinterpret_cast<const float4*>(src) + i);
-    __stcs(reinterpret_cast<uint2*>(dst) + i, f4_to_bf4(v));
+    __stcs(reinterpret_cast<uint2*>(dst) + i, to_rc4(v, f16));
   }
   if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
     const size_t i = (n4 << 2) + threadIdx.x;
-    dst[i] = f_to_bf(src[i]);
+    dst[i] = f16 ? __half_as_ushort(__float2half_rn(src[i])) : f_to_bf(src[i]);
   }
 }
 
@@ -82,12 +82,12 @@ cudaError_t reset_launch(int32_t* cursors, const int32_t* slots, int n_slots, in
   return cudaGetLastError();
 }
 
-cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, cudaStream_t st) {
+cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, bool f16, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
   size_t blocks = ((n >> 2) + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks == 0) blocks = 1;
-  downcast_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, dst, n);
+  downcast_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, dst, n, f16);
   return cudaGetLastError();
 }
 

@@ -118,7 +118,7 @@ __device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm
 #pragma unroll
   for (int rr = 0; rr < 8; rr++) {
     __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
-    if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
+    if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), to_rc4(hv[rr], a.read_f16));
   }
 }
 

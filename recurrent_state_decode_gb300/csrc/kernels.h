@@ -13,6 +13,7 @@ struct M2Args {
   int PB, nPB;  // rows per block, row blocks per (sequence, head) tile
   int K;        // records per verify (1 for the AR step)
   int hpg_log2;  // log2(H / G) when H / G is a power of two, else -1
+  int read_f16;  // the read copy ckpt_read holds fp16 (else bf16)
   float* ckpt;
   uint16_t* ckpt_read;
   uint16_t *rx, *rz, *rB, *rC;
@@ -74,7 +75,7 @@ cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int b
                           cudaStream_t st);
 cudaError_t reset_launch(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* status,
                          cudaStream_t st);
-cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, cudaStream_t st);
+cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, bool f16, cudaStream_t st);
 
 // Row stride of the per-record scalar rings (dt; g, beta): L rounded up to a
 // multiple of 4 slots, so that a row is a whole number of 16-byte units.

@@ -169,7 +169,7 @@ __device__ __forceinline__ void store_out(void* y, size_t i, float v) {
 // if back != nullptr, the fp32 rows back to shared memory.
 template <int NCH>
 __device__ __forceinline__ void fold_group(float4 (&hv)[8][NCH], const M2Smem& s, int r0, int PB, int N, int m,
-                                           float P, int lane, float* g32, uint16_t* g16, float* back) {
+                                           float P, int lane, float* g32, uint16_t* g16, bool f16, float* back) {
 #pragma unroll
   for (int rr = 0; rr < 8; rr++)
 #pragma unroll
@@ -196,7 +196,7 @@ __device__ __forceinline__ void fold_group(float4 (&hv)[8][NCH], const M2Smem& s
       if (c * 4 < N) {
         const size_t o = (size_t)(r0 + rr) * N + c * 4;
         __stcs(reinterpret_cast<float4*>(g32 + o), hv[rr][j]);
-        if (g16) __stcs(reinterpret_cast<uint2*>(g16 + o), f4_to_bf4(hv[rr][j]));
+        if (g16) __stcs(reinterpret_cast<uint2*>(g16 + o), to_rc4(hv[rr][j], f16));
         if (back) *reinterpret_cast<float4*>(back + o) = hv[rr][j];
       }
     }
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(128) m2_flush_kernel(M2Args a) {
         hv[rr][j] = (c * 4 < N) ? tile_chunk<NCH>(s, false, r0 + rr, N, c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     fold_group<NCH>(hv, s, r0, PB, N, m, Pm, lane, a.ckpt + tile_off,
-                    a.ckpt_read ? a.ckpt_read + tile_off : nullptr, nullptr);
+                    a.ckpt_read ? a.ckpt_read + tile_off : nullptr, a.read_f16, nullptr);
   }
 }
 

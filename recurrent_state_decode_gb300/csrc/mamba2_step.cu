@@ -70,7 +70,7 @@ __device__ __forceinline__ void load_head(HeadData<NCH>& d, const M2Args& a, siz
       if (rows && c * 4 < N) {
         const size_t row = toff + (size_t)rr * N;
         d.hv[rr][jj] = fp32_rows ? __ldcs(reinterpret_cast<const float4*>(a.ckpt + row) + c)
-                                 : load_bf4(a.ckpt_read + row + c * 4);
+                                 : load_rc4(a.ckpt_read + row + c * 4, a.read_f16);
       }
     }
   d.dts = lane < L ? a.rdt[bh * pad4(L) + lane] : 0.f;
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, NCH == 1 ? 2 : 1) m2_step_kernel(M2Ar
             if (c * 4 < N) {
               const size_t o = toff + (size_t)r * N + c * 4;
               __stcs(reinterpret_cast<float4*>(a.ckpt + o), d.hv[r][jj]);
-              if (has_copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), f4_to_bf4(d.hv[r][jj]));
+              if (has_copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), to_rc4(d.hv[r][jj], a.read_f16));
             }
           }
       } else {  // 3b. append the current record: x, z rows of this warp, dt once per head

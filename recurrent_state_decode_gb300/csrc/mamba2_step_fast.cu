@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
     } else if (copy) {
       const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = load_bf4(t16 + (rl + rr) * FN);
+      for (int rr = 0; rr < 8; rr++) hv[rr] = load_rc4(t16 + (rl + rr) * FN, a.read_f16);
     } else {
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];

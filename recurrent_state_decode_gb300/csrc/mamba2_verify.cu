@@ -276,7 +276,7 @@ __device__ __forceinline__ void vconsume_tile(const M2Args& a, const VLayout& la
 #pragma unroll
       for (int jj = 0; jj < NCH; jj++) {
         const int c = lane + 32 * jj;
-        hv[rr][jj] = (c * 4 < N) ? (rd16 ? load_bf4(t16 + (size_t)(r0 + rr) * N + c * 4)
+        hv[rr][jj] = (c * 4 < N) ? (rd16 ? load_rc4(t16 + (size_t)(r0 + rr) * N + c * 4, a.read_f16)
                                          : reinterpret_cast<const float4*>(t32 + (size_t)(r0 + rr) * N)[c])
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -309,7 +309,7 @@ __device__ __forceinline__ void vconsume_tile(const M2Args& a, const VLayout& la
           if (c * 4 < N) {
             const size_t o = toff + (size_t)rr * N + c * 4;
             __stcs(reinterpret_cast<float4*>(a.ckpt + o), hv[rr][jj]);
-            if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), f4_to_bf4(hv[rr][jj]));
+            if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + o), to_rc4(hv[rr][jj], a.read_f16));
           }
         }
     }

@@ -91,15 +91,15 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
 // Rows rA, rB of the state at columns col..col+3 as the kernel reads them: the
 // fp32 tile, the bf16 read copy in the tile, or (a folding block of the read
 // copy) the fp32 rows in global memory.
-__device__ __forceinline__ void state_rows(const float* tile, const float* gstate, bool bf16, int rA, int rB, int col,
-                                           float4& r0, float4& r1) {
+__device__ __forceinline__ void state_rows(const float* tile, const float* gstate, bool bf16, bool f16, int rA, int rB,
+                                           int col, float4& r0, float4& r1) {
   if (gstate) {
     r0 = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)rA * FN + col));
     r1 = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)rB * FN + col));
   } else if (bf16) {
     const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
-    r0 = load_bf4(t16 + rA * FN + col);
-    r1 = load_bf4(t16 + rB * FN + col);
+    r0 = load_rc4(t16 + rA * FN + col, f16);
+    r1 = load_rc4(t16 + rB * FN + col, f16);
   } else {
     r0 = *reinterpret_cast<const float4*>(tile + rA * FN + col);
     r1 = *reinterpret_cast<const float4*>(tile + rB * FN + col);
@@ -277,13 +277,13 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   const bool t16 = copy && !fold;
   if (landed) {
     // h0 . [C_0..C_3] for rows (rA, rB) as m16n8k8 tf32 mma; an fp32 state is
-    // split into two tf32 parts, the bf16 read copy is exact in tf32
+    // split into two tf32 parts, the bf16 or fp16 read copy is exact in tf32
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int jb = 0; jb < FN / 16; jb++) {
       const int col = 16 * jb + 4 * qt;
       float4 r0, r1;
-      state_rows(tile, gstate, t16, rA, rB, col, r0, r1);
+      state_rows(tile, gstate, t16, a.read_f16, rA, rB, col, r0, r1);
       const float4 bv = cvec ? load_bf4(cvec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (t16) {  // uniform
         mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y),
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
 #pragma unroll
         for (int rr = 0; rr < 8; rr++) {
           __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
-          if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), f4_to_bf4(hv[rr]));
+          if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), to_rc4(hv[rr], a.read_f16));
         }
       }
     }

@@ -10,18 +10,21 @@ from . import binding as bd
 
 
 class Mamba2State:
-    """Checkpoint (+ optional bf16 read copy), ring buffer, cursors and a
-    device status word for one Mamba-2 layer of `batch` sequences."""
+    """Checkpoint (+ optional read copy: read_copy True or "bf16" for bf16,
+    "f16" for fp16), ring buffer, cursors and a device status word for one
+    Mamba-2 layer of `batch` sequences."""
 
     def __init__(self, batch, nheads, headdim, dstate, ngroups, buf_len, device="cuda",
                  read_copy=False, out_dtype=bd.RSSM_F32):
         self.batch, self.nheads, self.headdim, self.dstate = batch, nheads, headdim, dstate
         self.ngroups, self.buf_len, self.out_dtype = ngroups, buf_len, out_dtype
-        self.desc = bd.mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype)
+        f16 = read_copy == "f16"
+        self.desc = bd.mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype,
+                                   bd.RSSM_F16 if f16 else bd.RSSM_BF16)
         dev = torch.device(device)
         self.ckpt = torch.zeros((batch, nheads, headdim, dstate), dtype=torch.float32, device=dev)
-        self.ckpt_read = (torch.zeros((batch, nheads, headdim, dstate), dtype=torch.bfloat16, device=dev)
-                          if read_copy else None)
+        self.ckpt_read = (torch.zeros((batch, nheads, headdim, dstate), dtype=torch.float16 if f16 else torch.bfloat16,
+                                      device=dev) if read_copy else None)
         self.rx = torch.zeros((batch, nheads, buf_len, headdim), dtype=torch.bfloat16, device=dev)
         self.rz = torch.zeros_like(self.rx)
         self.rB = torch.zeros((batch, ngroups, buf_len, dstate), dtype=torch.bfloat16, device=dev)
@@ -40,7 +43,7 @@ class Mamba2State:
         return torch.empty(shape, dtype=self.y_dtype, device=self.ckpt.device)
 
     def downcast(self, stream=None):
-        bd.check(bd.rssm_checkpoint_downcast(self.ckpt, self.ckpt_read, self.ckpt.numel(), stream),
+        bd.check(bd.rssm_checkpoint_downcast(self.ckpt, self.ckpt_read, self.ckpt.numel(), None, stream),
                  "rssm_checkpoint_downcast")
 
     def step(self, rec, A, D, y, stream=None):

@@ -71,6 +71,8 @@ ARGS9 = [ALIGNED] * 9  # cursors, x, z, B, C, dt, A, D, y
     (4, 8, 64, 128, 1, 33),    # L > 32
     (-1, 8, 64, 128, 1, 16),   # negative batch
     (4, 8, 64, 128, 1, 16, 7),  # bad out_dtype
+    (4, 8, 64, 128, 1, 16, 0, 9),  # bad read_dtype
+    (4, 8, 64, 128, 1, 16, 0, bd.RSSM_F32 + 3),
 ])
 def test_mamba2_desc_validation(lib, desc):
     d = bd.mamba2_desc(*desc)
@@ -123,8 +125,9 @@ def test_cursor_call_validation(lib):
     assert lib.rssm_reset_cursors(None, None, 0, 4, None, None) == bd.RSSM_OK
     assert lib.rssm_reset_cursors(ALIGNED, None, 2, 4, None, None) == bd.RSSM_ERR_INVALID_ARG
     assert lib.rssm_reset_cursors(ALIGNED, ALIGNED, -1, 4, None, None) == bd.RSSM_ERR_INVALID_ARG
-    assert lib.rssm_checkpoint_downcast(None, None, 0, None) == bd.RSSM_OK
-    assert lib.rssm_checkpoint_downcast(ALIGNED, ALIGNED + 2, 8, None) == bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_checkpoint_downcast(None, None, 0, bd.RSSM_BF16, None) == bd.RSSM_OK
+    assert lib.rssm_checkpoint_downcast(ALIGNED, ALIGNED + 2, 8, bd.RSSM_F16, None) == bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_checkpoint_downcast(ALIGNED, ALIGNED, 8, bd.RSSM_F32, None) == bd.RSSM_ERR_INVALID_ARG
 
 
 def test_gdn_validation(lib):

@@ -179,11 +179,12 @@ def test_gdn_spec_full_size():
     assert H.status(st) == 0
 
 
-def test_bf16_read_copy_4096_steps():
-    """fp32 recurrence checkpoint + bf16 read copy, 4096 steps: the output error
-    stays within 1e-2 relative L2 and does not grow (rounding of the read copy
-    never enters the recurrence)."""
-    w = I.WORKLOADS["mamba2_bf16_read"]
+@pytest.mark.parametrize("name", ["mamba2_bf16_read", "mamba2_f16_read"])
+def test_read_copy_4096_steps(name):
+    """fp32 recurrence checkpoint + bf16 (or fp16) read copy, 4096 steps: the
+    output error stays within 1e-2 relative L2 and does not grow (rounding of
+    the read copy never enters the recurrence)."""
+    w = I.WORKLOADS[name]
     dev = "cuda"
     st, A, D, pre, starts, counts = H.mamba2_setup(w, dev, bd.RSSM_F32)
     assert st.ckpt_read is not None

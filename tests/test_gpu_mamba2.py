@@ -62,7 +62,7 @@ def run_ar(w, out_dtype=bd.RSSM_F32, seqs=None, read_copy=None, steps=None, trac
                 e = H.rel_l2(H.F64(st.ckpt[b]), exp["state"][i])
                 assert e <= TOL_CKPT, (t, b, e)
                 if read_copy:  # the read copy is the RNE downcast of the new checkpoint
-                    assert torch.equal(st.ckpt_read[b], st.ckpt[b].to(torch.bfloat16))
+                    assert torch.equal(st.ckpt_read[b], st.ckpt[b].to(st.ckpt_read.dtype))
     assert H.status(st) == 0
     return flushes
 
@@ -106,8 +106,9 @@ READ_COPY = [
 
 
 @pytest.mark.parametrize("w", READ_COPY, ids=lambda w: w.name)
-def test_read_copy_small(w):
-    run_ar(w, read_copy=True)
+@pytest.mark.parametrize("rc", [True, "f16"], ids=["bf16", "f16"])
+def test_read_copy_small(w, rc):
+    run_ar(w, read_copy=rc)
 
 
 def test_conventional_kernel():
@@ -213,6 +214,8 @@ def test_spec(w):
 def test_spec_bf16_out_and_read_copy():
     run_spec(SPEC[0], out_dtype=bd.RSSM_BF16)
     run_spec(SPEC[0], read_copy=True)
+    run_spec(SPEC[0], read_copy="f16")
+    run_spec(W("spec_fast", 3, 4, 64, 128, 2, 16, 12, seed=45, drafts=3), read_copy="f16")
 
 
 def test_spec_all_accepted_equals_ar():
@@ -301,8 +304,13 @@ def test_downcast_rne():
     x = torch.randn(1001, device=dev) * 3
     x[:5] = torch.tensor([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -0.0, float("inf"), 1e-40])  # ties to even, signed zero, inf, subnormal
     out = torch.empty(1001, dtype=torch.bfloat16, device=dev)
-    bd.check(bd.rssm_checkpoint_downcast(x, out, 1001))
+    bd.check(bd.rssm_checkpoint_downcast(x, out, 1001, bd.RSSM_BF16))
     assert torch.equal(out.view(torch.int16), x.to(torch.bfloat16).view(torch.int16))
+    # fp16: ties to even at 1 + 2^-11 and 1 + 3 * 2^-11, overflow to inf, fp16 subnormals
+    x[:5] = torch.tensor([1.0 + 2 ** -11, 1.0 + 3 * 2 ** -11, 70000.0, -3e-6, 2 ** -25])
+    h = torch.empty(1001, dtype=torch.float16, device=dev)
+    bd.check(bd.rssm_checkpoint_downcast(x, h, 1001, bd.RSSM_F16))
+    assert torch.equal(h.view(torch.int16), x.to(torch.float16).view(torch.int16))
 
 
 def test_reset_then_decode():
