@@ -175,13 +175,14 @@ __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// fp32 x = hi + lo with hi exactly representable in tf32 (the top 11 mantissa
-// bits) and lo rounded to tf32, so that two tf32 products with an operand that
-// is exact in tf32 (a bf16 value) recover x * y to about 2^-21 relative.
+// fp32 x = hi + lo with hi exactly representable in tf32 (the top 11
+// significand bits) and lo = x - hi exact in fp32; a tf32 mma reads only the
+// top 19 bits of each operand, so lo enters truncated to 11 significant bits.
+// Two tf32 products with an operand that is exact in tf32 (a bf16 or fp16
+// value) then recover x * y to within 2^-20 relative.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
   hi = __float_as_uint(x) & 0xffffe000u;
-  const float r = x - __uint_as_float(hi);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
 // ---------------------------------------------------------------- status
