@@ -64,6 +64,7 @@ GSHAPES = [
     GW("gdn_128_L1", 2, 3, 128, 128, 1, 6, seed=79),         # every step flushes
     GW("gdn_128_L5", 3, 2, 128, 128, 5, 23, seed=80),        # ragged window, wraps often
     GW("gdn_128_L31", 2, 2, 128, 128, 31, 70, seed=81),      # longest window of that kernel
+    GW("gdn_128_H3", 3, 3, 128, 128, 7, 20, seed=85),         # odd head count
 ]
 
 
