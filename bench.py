@@ -2,7 +2,7 @@
 """Benchmark of the ReplaySSM decode path on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mamba2_serving|mamba2_spec|gdn_serving|gdn_spec|mamba2_bf16_read|mamba2_f16_read|mamba2_tiny]
+                    [--workload mamba2_serving|mamba2_spec|gdn_serving|gdn_spec|mamba2_bf16_read|mamba2_f16_read|mamba2_f8_read|mamba2_tiny]
     python bench.py --mode profile --steps 3 --warmup 1      # a few calls, no timing (for ncu)
 
 A step is one decode step of one layer over the whole batch: one
@@ -262,7 +262,8 @@ def workload_config(w, args):
         if hasattr(w, k):
             cfg[k] = getattr(w, k)
     rc = getattr(w, "read_copy", False)
-    cfg["state"] = "fp32 checkpoint" + ((" + fp16 read copy" if rc == "f16" else " + bf16 read copy") if rc else "")
+    rc_name = {"f16": " + fp16 read copy", "f8": " + fp8 e4m3 read copy (row scales)"}.get(rc, " + bf16 read copy")
+    cfg["state"] = "fp32 checkpoint" + (rc_name if rc else "")
     cfg["io_dtype"] = "bf16 records, " + args.out_dtype + " outputs"
     cfg["l2"] = "working set larger than L2: the full checkpoint is streamed every step"
     return cfg
@@ -404,7 +405,7 @@ def other_workloads(args, dev, out, out_bytes, K, W_, dist, stream):
     res = {}
 
     # bf16 and fp16 read copies of the checkpoint (non-flush steps read 2 bytes per state element)
-    for name in ("mamba2_bf16_read", "mamba2_f16_read"):
+    for name in ("mamba2_bf16_read", "mamba2_f16_read", "mamba2_f8_read"):
         w = I.WORKLOADS[name]
         st, A, D, _, _, counts0 = mamba2_from_workload(w, dev, out)
         recs = [I.mamba2_step_inputs(w, t, dev) for t in range(W_ + K)]
@@ -416,7 +417,7 @@ def other_workloads(args, dev, out, out_bytes, K, W_, dist, stream):
         bd.check(int(st.status.item()), "device status")
         c0 = counts0.cpu().tolist()
         nbytes = sum(bm.mamba2_step_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len,
-                                          [(c + W_ + i) % w.buf_len for c in c0], True, out_bytes)
+                                          [(c + W_ + i) % w.buf_len for c in c0], w.read_copy, out_bytes)
                      for i in range(K)) / K
         us = ms * 1e3 / K
         res[w.name] = {"us_per_step": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,

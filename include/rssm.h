@@ -76,8 +76,8 @@ enum {
 };
 
 /* Element types: of outputs (RSSM_F32, RSSM_BF16) and of the checkpoint's
- * read copy (RSSM_BF16, RSSM_F16). */
-enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2 };
+ * read copy (RSSM_BF16, RSSM_F16, RSSM_FP8_E4M3). */
+enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2, RSSM_FP8_E4M3 = 3 };
 
 /* Limits of this build. */
 #define RSSM_MAX_BUF_LEN 32 /* L in [1, 32] */
@@ -98,7 +98,14 @@ typedef struct {
   int buf_len;   /* L, the window length */
   int out_dtype; /* RSSM_F32 or RSSM_BF16: element type of y */
   int read_dtype; /* element type of the read copy ckpt_read, when one is
-                   * passed: RSSM_BF16 (0 reads as RSSM_BF16) or RSSM_F16 */
+                   * passed: RSSM_BF16 (0 reads as RSSM_BF16), RSSM_F16, or
+                   * RSSM_FP8_E4M3 -- then ckpt_read holds batch * nheads *
+                   * headdim * dstate e4m3 bytes followed by one fp32 scale
+                   * per state row ([batch, nheads, headdim]); a value reads
+                   * as e4m3 * scale, scale = max|row| / 448. FP8 needs
+                   * dstate 128, headdim a multiple of 64, buf_len <= 31 and
+                   * a power-of-two nheads / ngroups (else
+                   * RSSM_ERR_UNSUPPORTED). */
 } rssm_mamba2_desc;
 
 /* Ring buffer of window records, head- (or group-) major so that one
@@ -210,6 +217,14 @@ RSSM_API int rssm_reset_cursors(int32_t* cursors, const int32_t* slots, int n_sl
  * range). Any other dtype: RSSM_ERR_INVALID_ARG. */
 RSSM_API int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, int dtype,
                              rssm_stream_t stream);
+
+/* The read copy of a whole Mamba-2 checkpoint in desc->read_dtype ("ReplaySSM",
+ * introduction, "Separate state precisions"), for a checkpoint written by the
+ * caller (a new request, a reset slot): ckpt [batch, nheads, headdim, dstate]
+ * fp32; ckpt_read laid out as rssm_mamba2_desc.read_dtype says. Round to
+ * nearest even; fp8 rows are scaled by their own max|row| / 448. */
+RSSM_API int rssm_mamba2_downcast(const rssm_mamba2_desc* desc, const float* ckpt, void* ckpt_read,
+                         rssm_stream_t stream);
 
 /* ----------------------------------------------------------------------------
  * Gated DeltaNet

@@ -28,6 +28,7 @@ RSSM_DEV_TIMEOUT = 6
 RSSM_F32 = 0
 RSSM_BF16 = 1
 RSSM_F16 = 2
+RSSM_FP8_E4M3 = 3
 
 c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
 
@@ -62,6 +63,7 @@ _SIGNATURES = {
     "rssm_commit_cursors": (c_int, [P, P, c_int, c_int, P, P]),
     "rssm_reset_cursors": (c_int, [P, P, c_int, c_int, P, P]),
     "rssm_checkpoint_downcast": (c_int, [P, P, c_size_t, c_int, P]),
+    "rssm_mamba2_downcast": (c_int, [P, P, P, P]),
     "rssm_gdn_conventional_step": (c_int, [P] * 8 + [P]),
     "rssm_gdn_step": (c_int, [P] * 11 + [P]),
     "rssm_gdn_flush": (c_int, [P] * 5 + [P]),
@@ -229,3 +231,7 @@ def rssm_gdn_spec_verify(desc, n_new, S, ring, cursors, q, k, v, g, beta, o, dev
     return load().rssm_gdn_spec_verify(
         _ref(desc), int(n_new), ptr(S), _ref(ring), ptr(cursors), ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), ptr(o),
         ptr(dev_status), _stream(stream, S))
+
+
+def rssm_mamba2_downcast(desc, ckpt, ckpt_read, stream=None):
+    return load().rssm_mamba2_downcast(_ref(desc), ptr(ckpt), ptr(ckpt_read), _stream(stream, ckpt))

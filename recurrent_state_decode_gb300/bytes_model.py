@@ -21,15 +21,26 @@ def mamba2_parts(H, P, N, G, out_bytes):
     return tile32, rec, past, y
 
 
+def read_copy_bytes(H, P, N, read_copy):
+    """Bytes of one sequence's read copy: 2 per element (bf16, fp16), or 1 per
+    element plus a 4-byte scale per row (fp8); 0 without a copy."""
+    if not read_copy:
+        return 0
+    if read_copy == "f8":
+        return H * P * N + 4 * H * P
+    return 2 * H * P * N
+
+
 def mamba2_step_bytes(H, P, N, G, L, counts, read_copy=False, out_bytes=2):
     """One AR step; counts = each sequence's window count before the step."""
     tile32, rec, past, y = mamba2_parts(H, P, N, G, out_bytes)
+    rc = read_copy_bytes(H, P, N, read_copy)
     total = 0
     for c in counts:
-        if c + 1 == L:  # flush: read fp32, write fp32 (+ bf16 copy); the record is folded, not stored
-            total += 2 * tile32 + (tile32 // 2 if read_copy else 0) + rec
+        if c + 1 == L:  # flush: read fp32, write fp32 (+ the read copy); the record is folded, not stored
+            total += 2 * tile32 + rc + rec
         else:
-            total += (tile32 // 2 if read_copy else tile32) + 2 * rec
+            total += (rc if read_copy else tile32) + 2 * rec
         total += c * past + y + CURSOR
     return total
 
@@ -42,13 +53,14 @@ def mamba2_conventional_bytes(H, P, N, G, batch, out_bytes=2):
 def mamba2_verify_bytes(H, P, N, G, L, K, counts, read_copy=False, out_bytes=2):
     """One verify + commit; counts = committed window counts before the verify."""
     tile32, rec, past, y = mamba2_parts(H, P, N, G, out_bytes)
+    rc = read_copy_bytes(H, P, N, read_copy)
     total = 0
     for c in counts:
         fold = c + K > L
         if fold:
-            total += 2 * tile32 + (tile32 // 2 if read_copy else 0)
+            total += 2 * tile32 + rc
         else:
-            total += tile32 // 2 if read_copy else tile32
+            total += rc if read_copy else tile32
         total += 2 * K * rec + c * past + K * y + 2 * CURSOR + 4
     return total
 

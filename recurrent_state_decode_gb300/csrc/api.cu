@@ -31,10 +31,17 @@ int check_m2(const rssm_mamba2_desc* d) {
   if (!dim_ok(d->headdim) || !dim_ok(d->dstate)) return RSSM_ERR_INVALID_ARG;
   if (d->buf_len < 1 || d->buf_len > RSSM_MAX_BUF_LEN) return RSSM_ERR_INVALID_ARG;
   if (d->out_dtype != RSSM_F32 && d->out_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
-  if (d->read_dtype != 0 && d->read_dtype != RSSM_BF16 && d->read_dtype != RSSM_F16) return RSSM_ERR_INVALID_ARG;
+  if (d->read_dtype != 0 && d->read_dtype != RSSM_BF16 && d->read_dtype != RSSM_F16 && d->read_dtype != RSSM_FP8_E4M3)
+    return RSSM_ERR_INVALID_ARG;
   const int pb = rows_per_block(d->headdim, d->dstate);
   const long long grid = (long long)d->batch * d->nheads * ((d->headdim + pb - 1) / pb);
   if (grid > INT_MAX || d->batch > 65535) return RSSM_ERR_UNSUPPORTED;
+  if (d->read_dtype == RSSM_FP8_E4M3) {  // the fp8 read copy lives on the shape-specialised kernels only
+    const int hpg = d->nheads / d->ngroups;
+    if (d->dstate != 128 || d->headdim % 64 != 0 || d->buf_len > 31 || (hpg & (hpg - 1)) != 0 ||
+        (long long)d->nheads * (d->headdim / 64) >= (1 << 15))
+      return RSSM_ERR_UNSUPPORTED;
+  }
   return RSSM_OK;
 }
 
@@ -61,6 +68,7 @@ M2Args m2_args(const rssm_mamba2_desc* d) {
   a.nPB = (a.P + a.PB - 1) / a.PB;
   a.K = 1;
   a.read_f16 = d->read_dtype == RSSM_F16;
+  a.read_f8 = d->read_dtype == RSSM_FP8_E4M3;
   const int hpg = a.H / a.G;
   a.hpg_log2 = (hpg & (hpg - 1)) == 0 ? __builtin_ctz(hpg) : -1;
   return a;
@@ -231,6 +239,7 @@ int rssm_mamba2_spec_verify(const rssm_mamba2_desc* d, int n_new, float* ckpt, r
   a.D = D;
   a.y = y;
   a.status = dev_status;
+  if (a.read_f8 && a.ckpt_read && !m2_verify_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;  // fp8: K <= 4, L + K <= 32
   return cuda_rc(m2_launch(M2_VERIFY, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
 }
 
@@ -258,6 +267,18 @@ int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, int dty
   int rc;
   if ((rc = check_ptrs({src, dst}))) return rc;
   return cuda_rc(downcast_launch(src, dst, n, dtype == RSSM_F16, (cudaStream_t)stream));
+}
+
+int rssm_mamba2_downcast(const rssm_mamba2_desc* d, const float* ckpt, void* ckpt_read, rssm_stream_t stream) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if ((rc = check_ptrs({ckpt, ckpt_read}))) return rc;
+  const size_t rows = (size_t)d->batch * d->nheads * d->headdim;
+  if (d->read_dtype == RSSM_FP8_E4M3)
+    return cuda_rc(downcast_f8_launch(ckpt, static_cast<uint8_t*>(ckpt_read), rows, (cudaStream_t)stream));
+  return cuda_rc(downcast_launch(ckpt, static_cast<uint16_t*>(ckpt_read), rows * d->dstate, d->read_dtype == RSSM_F16,
+                                 (cudaStream_t)stream));
 }
 
 int rssm_gdn_conventional_step(const rssm_gdn_desc* d, float* S, const rssm_bf16* q, const rssm_bf16* k,

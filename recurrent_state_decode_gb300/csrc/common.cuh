@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,6 +63,28 @@ __device__ __forceinline__ uint2 f4_to_h4(float4 v) {
 // it; f16 selects fp16 over bf16 (uniform over a launch).
 __device__ __forceinline__ float4 load_rc4(const uint16_t* p, bool f16) { return f16 ? load_h4(p) : load_bf4(p); }
 __device__ __forceinline__ uint2 to_rc4(float4 v, bool f16) { return f16 ? f4_to_h4(v) : f4_to_bf4(v); }
+
+// fp8 e4m3 read copy: four values at p (unscaled), and four fp32 rounded to
+// e4m3 (nearest even, saturating at +-448) packed in one word, through the
+// CUDA fp8 conversion intrinsics.
+__device__ __forceinline__ float4 load_f8x4(const uint8_t* p) {
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u >> 16), __NV_E4M3);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ uint32_t f4_to_f8x4(float4 v) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v.x, v.y), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v.z, v.w), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// Largest magnitude e4m3 represents; an fp8 read-copy row is stored as
+// value / scale with scale = max|row| / E4M3_MAX.
+constexpr float E4M3_MAX = 448.f;
 
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
@@ -141,6 +164,19 @@ __device__ __forceinline__ float reduce_transpose(float (&p)[V], int lane) {
     }
   }
   return p[0];
+}
+
+// One row of 128 fp32 values (lane: the float4 at column 4 lane) into the fp8
+// read copy: stored as value * (448 / max|row|), nearest even, with the row's
+// scale max|row| / 448 in scales[row] (0 for a row of zeros). Every lane must
+// call this.
+__device__ __forceinline__ void store_f8_row(uint8_t* q, float* scales, size_t row, float4 v, int lane) {
+  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+  const float inv = m > 0.f ? E4M3_MAX / m : 0.f;
+  *reinterpret_cast<uint32_t*>(q + row * 128 + lane * 4) = f4_to_f8x4(scale4(inv, v));
+  if (lane == 0) scales[row] = m / E4M3_MAX;
 }
 
 // ---------------------------------------------------------------- warp-level tensor-core pieces

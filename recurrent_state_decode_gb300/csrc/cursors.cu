@@ -68,6 +68,16 @@ __global__ void downcast_kernel(const float* __restrict__ src, uint16_t* __restr
   }
 }
 
+// fp8 read copy, one warp per row of 128 values; the row scales follow the
+// rows * 128 bytes of e4m3 values.
+__global__ void downcast_f8_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, size_t rows) {
+  const int lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;  // uniform over the warp
+  const float4 v = __ldcs(reinterpret_cast<const float4*>(src + row * 128) + lane);
+  store_f8_row(dst, reinterpret_cast<float*>(dst + rows * 128), row, v, lane);
+}
+
 cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status,
                           cudaStream_t st) {
   if (batch <= 0) return cudaSuccess;
@@ -88,6 +98,12 @@ cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, bool f16,
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks == 0) blocks = 1;
   downcast_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, dst, n, f16);
+  return cudaGetLastError();
+}
+
+cudaError_t downcast_f8_launch(const float* src, uint8_t* dst, size_t rows, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  downcast_f8_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(src, dst, rows);
   return cudaGetLastError();
 }
 

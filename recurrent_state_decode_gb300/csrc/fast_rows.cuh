@@ -100,7 +100,23 @@ __device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float 
   if (lane < 8) store_y<OUT_BF16>(a.y, obase + lane, t * gate);
 }
 
-// h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the bf16 copy).
+// The read copy (if any) of 8 rows of the state: element offset `off` of row
+// 0's float4 at column 4 lane; every lane must call this.
+__device__ __forceinline__ void store_read_copy8(const M2Args& a, const float4 (&hv)[8], size_t off, int lane) {
+  if (!a.ckpt_read) return;
+  if (a.read_f8) {
+    uint8_t* q = reinterpret_cast<uint8_t*>(a.ckpt_read);
+    float* scales = reinterpret_cast<float*>(q + (size_t)a.Bt * a.H * a.P * FN);
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) store_f8_row(q, scales, off / FN + rr, hv[rr], lane);
+  } else {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++)
+      __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), to_rc4(hv[rr], a.read_f16));
+  }
+}
+
+// h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the read copy).
 __device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm, float wk, const float (&xl)[8],
                                       int m, int count, int start, int bg, size_t off, int lane) {
   const int L = a.L;
@@ -116,10 +132,8 @@ __device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm
     for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(w * __shfl_sync(FULL, xl[rr], k), bk, hv[rr]);
   }
 #pragma unroll
-  for (int rr = 0; rr < 8; rr++) {
-    __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
-    if (a.ckpt_read) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), to_rc4(hv[rr], a.read_f16));
-  }
+  for (int rr = 0; rr < 8; rr++) __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
+  store_read_copy8(a, hv, off, lane);
 }
 
 }  // namespace fastrows

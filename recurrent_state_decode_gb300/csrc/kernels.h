@@ -14,6 +14,7 @@ struct M2Args {
   int K;        // records per verify (1 for the AR step)
   int hpg_log2;  // log2(H / G) when H / G is a power of two, else -1
   int read_f16;  // the read copy ckpt_read holds fp16 (else bf16)
+  int read_f8;   // the read copy holds e4m3 values, then one fp32 scale per state row
   float* ckpt;
   uint16_t* ckpt_read;
   uint16_t *rx, *rz, *rB, *rC;
@@ -76,6 +77,8 @@ cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int b
 cudaError_t reset_launch(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* status,
                          cudaStream_t st);
 cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, bool f16, cudaStream_t st);
+// fp8 read copy of `rows` rows of 128 fp32 values, with one scale per row after the bytes.
+cudaError_t downcast_f8_launch(const float* src, uint8_t* dst, size_t rows, cudaStream_t st);
 
 // Row stride of the per-record scalar rings (dt; g, beta): L rounded up to a
 // multiple of 4 slots, so that a row is a whole number of 16-byte units.

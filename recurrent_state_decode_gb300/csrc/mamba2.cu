@@ -169,7 +169,8 @@ __device__ __forceinline__ void store_out(void* y, size_t i, float v) {
 // if back != nullptr, the fp32 rows back to shared memory.
 template <int NCH>
 __device__ __forceinline__ void fold_group(float4 (&hv)[8][NCH], const M2Smem& s, int r0, int PB, int N, int m,
-                                           float P, int lane, float* g32, uint16_t* g16, bool f16, float* back) {
+                                           float P, int lane, float* g32, uint16_t* g16, bool f16, float* back,
+                                           uint8_t* q8 = nullptr, float* sc8 = nullptr, size_t row0 = 0) {
 #pragma unroll
   for (int rr = 0; rr < 8; rr++)
 #pragma unroll
@@ -200,6 +201,10 @@ __device__ __forceinline__ void fold_group(float4 (&hv)[8][NCH], const M2Smem& s
         if (back) *reinterpret_cast<float4*>(back + o) = hv[rr][j];
       }
     }
+  if (NCH == 1 && q8) {  // fp8 read copy: rows of 128 values, one float4 per lane
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) store_f8_row(q8, sc8, row0 + r0 + rr, hv[rr][0], lane);
+  }
 }
 
 // ------------------------------------------------------------------ conventional step
@@ -326,8 +331,11 @@ __global__ void __launch_bounds__(128) m2_flush_kernel(M2Args a) {
         const int c = lane + 32 * j;
         hv[rr][j] = (c * 4 < N) ? tile_chunk<NCH>(s, false, r0 + rr, N, c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    uint8_t* q8 = (a.ckpt_read && a.read_f8) ? reinterpret_cast<uint8_t*>(a.ckpt_read) : nullptr;
+    float* sc8 = q8 ? reinterpret_cast<float*>(q8 + (size_t)a.Bt * a.H * a.P * a.N) : nullptr;
     fold_group<NCH>(hv, s, r0, PB, N, m, Pm, lane, a.ckpt + tile_off,
-                    a.ckpt_read ? a.ckpt_read + tile_off : nullptr, a.read_f16, nullptr);
+                    (a.ckpt_read && !a.read_f8) ? a.ckpt_read + tile_off : nullptr, a.read_f16, nullptr, q8, sc8,
+                    tile_off / N);
   }
 }
 

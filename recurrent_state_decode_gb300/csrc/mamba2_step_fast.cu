@@ -60,9 +60,17 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    const uint32_t bytes = FPB * FN * (copy ? 2 : 4);
-    mbar_arrive_expect_tx(&bar, bytes);
-    bulk_load(tile, copy ? (const void*)(a.ckpt_read + tbase) : (const void*)(a.ckpt + tbase), bytes, &bar);
+    if (copy && a.read_f8) {  // e4m3 rows, then their 64 scales after them
+      const uint8_t* q = reinterpret_cast<const uint8_t*>(a.ckpt_read);
+      const float* scales = reinterpret_cast<const float*>(q + (size_t)a.Bt * H * P * FN);
+      mbar_arrive_expect_tx(&bar, FPB * FN + FPB * 4);
+      bulk_load(tile, q + tbase, FPB * FN, &bar);
+      bulk_load(reinterpret_cast<uint8_t*>(tile) + FPB * FN, scales + tbase / FN, FPB * 4, &bar);
+    } else {
+      const uint32_t bytes = FPB * FN * (copy ? 2 : 4);
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_load(tile, copy ? (const void*)(a.ckpt_read + tbase) : (const void*)(a.ckpt + tbase), bytes, &bar);
+    }
   }
   // everything else, at launch: cursor, window records, current record, gate
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
@@ -168,9 +176,16 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
       for (int rr = 0; rr < 8; rr++)
         hv[rr] = __ldcs(reinterpret_cast<const float4*>(a.ckpt + tbase + (size_t)(rl + rr) * FN) + lane);
     } else if (copy) {
-      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
+      if (a.read_f8) {  // e4m3 values times their row's scale
+        const uint8_t* t8 = reinterpret_cast<const uint8_t*>(tile) + lane * 4;
+        const float* ts = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(tile) + FPB * FN);
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = load_rc4(t16 + (rl + rr) * FN, a.read_f16);
+        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(ts[rl + rr], load_f8x4(t8 + (rl + rr) * FN));
+      } else {
+        const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile) + lane * 4;
+#pragma unroll
+        for (int rr = 0; rr < 8; rr++) hv[rr] = load_rc4(t16 + (rl + rr) * FN, a.read_f16);
+      }
     } else {
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];

@@ -91,11 +91,15 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
 // Rows rA, rB of the state at columns col..col+3 as the kernel reads them: the
 // fp32 tile, the bf16 read copy in the tile, or (a folding block of the read
 // copy) the fp32 rows in global memory.
-__device__ __forceinline__ void state_rows(const float* tile, const float* gstate, bool bf16, bool f16, int rA, int rB,
-                                           int col, float4& r0, float4& r1) {
+__device__ __forceinline__ void state_rows(const float* tile, const float* gstate, bool bf16, bool f16, bool f8, int rA,
+                                           int rB, int col, float4& r0, float4& r1) {
   if (gstate) {
     r0 = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)rA * FN + col));
     r1 = __ldcs(reinterpret_cast<const float4*>(gstate + (size_t)rB * FN + col));
+  } else if (bf16 && f8) {  // e4m3 values, unscaled (exact in tf32): the caller scales the rows
+    const uint8_t* t8 = reinterpret_cast<const uint8_t*>(tile);
+    r0 = load_f8x4(t8 + rA * FN + col);
+    r1 = load_f8x4(t8 + rB * FN + col);
   } else if (bf16) {
     const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
     r0 = load_rc4(t16 + rA * FN + col, f16);
@@ -127,9 +131,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    const uint32_t bytes = FPB * FN * (copy ? 2 : 4);
+    const uint32_t bytes = FPB * FN * (copy ? (a.read_f8 ? 1 : 2) : 4);
     mbar_arrive_expect_tx(&bar, bytes);
-    bulk_load(tile, copy ? (const void*)(a.ckpt_read + tbase) : (const void*)(a.ckpt + tbase), bytes, &bar);
+    const void* src = !copy ? (const void*)(a.ckpt + tbase)
+                            : (a.read_f8 ? (const void*)(reinterpret_cast<const uint8_t*>(a.ckpt_read) + tbase)
+                                         : (const void*)(a.ckpt_read + tbase));
+    bulk_load(tile, src, bytes, &bar);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     for (int jb = 0; jb < FN / 16; jb++) {
       const int col = 16 * jb + 4 * qt;
       float4 r0, r1;
-      state_rows(tile, gstate, t16, a.read_f16, rA, rB, col, r0, r1);
+      state_rows(tile, gstate, t16, a.read_f16, a.read_f8, rA, rB, col, r0, r1);
       const float4 bv = cvec ? load_bf4(cvec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (t16) {  // uniform
         mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y),
@@ -305,6 +312,15 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
         mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
         mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
       }
+    }
+    if (t16 && a.read_f8) {  // e4m3 rows times their scales (the scale of a row factors out of its dots)
+      const float* scales = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(a.ckpt_read) +
+                                                           (size_t)a.Bt * H * P * FN);
+      const float sA = scales[tbase / FN + rA], sB = scales[tbase / FN + rB];
+      acc[0] *= sA;
+      acc[1] *= sA;
+      acc[2] *= sB;
+      acc[3] *= sB;
     }
     if (qt < 2) {  // outputs n0 = 2 qt, n1 = n0 + 1 at rows rA, rB
       const int n0 = 2 * qt, n1 = n0 + 1;
@@ -365,10 +381,8 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
         }
         const size_t off = tbase + (size_t)rl * FN + lane * 4;
 #pragma unroll
-        for (int rr = 0; rr < 8; rr++) {
-          __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
-          if (copy) __stcs(reinterpret_cast<uint2*>(a.ckpt_read + off + (size_t)rr * FN), to_rc4(hv[rr], a.read_f16));
-        }
+        for (int rr = 0; rr < 8; rr++) __stcs(reinterpret_cast<float4*>(a.ckpt + off + (size_t)rr * FN), hv[rr]);
+        store_read_copy8(a, hv, off, lane);
       }
     }
   }

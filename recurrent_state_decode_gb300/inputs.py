@@ -49,7 +49,7 @@ class Mamba2Workload:
     zero_ckpt: bool = False
     prefill: bool = True
     drafts: int = 0          # T; 0 = autoregressive decode
-    read_copy: object = False  # read copy of the checkpoint: False, True (bf16) or "f16"
+    read_copy: object = False  # read copy of the checkpoint: False, True (bf16), "f16" or "f8"
 
     @property
     def n_new(self):
@@ -82,6 +82,7 @@ WORKLOADS = {
     "gdn_serving": GDNWorkload("gdn_serving", 256, 32, 128, 128, 16, 256, seed=1003),
     "mamba2_bf16_read": Mamba2Workload("mamba2_bf16_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy=True),
     "mamba2_f16_read": Mamba2Workload("mamba2_f16_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy="f16"),
+    "mamba2_f8_read": Mamba2Workload("mamba2_f8_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy="f8"),
     "gdn_spec": GDNWorkload("gdn_spec", 512, 32, 128, 128, 16, 128, seed=1005, drafts=3),
 }
 

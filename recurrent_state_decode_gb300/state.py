@@ -11,20 +11,28 @@ from . import binding as bd
 
 class Mamba2State:
     """Checkpoint (+ optional read copy: read_copy True or "bf16" for bf16,
-    "f16" for fp16), ring buffer, cursors and a device status word for one
-    Mamba-2 layer of `batch` sequences."""
+    "f16" for fp16, "f8" for e4m3 with one fp32 scale per state row), ring
+    buffer, cursors and a device status word for one Mamba-2 layer of
+    `batch` sequences."""
 
     def __init__(self, batch, nheads, headdim, dstate, ngroups, buf_len, device="cuda",
                  read_copy=False, out_dtype=bd.RSSM_F32):
         self.batch, self.nheads, self.headdim, self.dstate = batch, nheads, headdim, dstate
         self.ngroups, self.buf_len, self.out_dtype = ngroups, buf_len, out_dtype
-        f16 = read_copy == "f16"
+        f16, f8 = read_copy == "f16", read_copy == "f8"
         self.desc = bd.mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype,
-                                   bd.RSSM_F16 if f16 else bd.RSSM_BF16)
+                                   bd.RSSM_FP8_E4M3 if f8 else (bd.RSSM_F16 if f16 else bd.RSSM_BF16))
         dev = torch.device(device)
         self.ckpt = torch.zeros((batch, nheads, headdim, dstate), dtype=torch.float32, device=dev)
-        self.ckpt_read = (torch.zeros((batch, nheads, headdim, dstate), dtype=torch.float16 if f16 else torch.bfloat16,
-                                      device=dev) if read_copy else None)
+        if f8:  # e4m3 bytes, then one fp32 scale per state row
+            n, rows = batch * nheads * headdim * dstate, batch * nheads * headdim
+            self.ckpt_read = torch.zeros(n + 4 * rows, dtype=torch.uint8, device=dev)
+            self.read_q = self.ckpt_read[:n].view(batch, nheads, headdim, dstate)
+            self.read_scale = self.ckpt_read[n:].view(torch.float32).view(batch, nheads, headdim)
+        else:
+            self.ckpt_read = (torch.zeros((batch, nheads, headdim, dstate),
+                                          dtype=torch.float16 if f16 else torch.bfloat16, device=dev)
+                              if read_copy else None)
         self.rx = torch.zeros((batch, nheads, buf_len, headdim), dtype=torch.bfloat16, device=dev)
         self.rz = torch.zeros_like(self.rx)
         self.rB = torch.zeros((batch, ngroups, buf_len, dstate), dtype=torch.bfloat16, device=dev)
@@ -43,8 +51,7 @@ class Mamba2State:
         return torch.empty(shape, dtype=self.y_dtype, device=self.ckpt.device)
 
     def downcast(self, stream=None):
-        bd.check(bd.rssm_checkpoint_downcast(self.ckpt, self.ckpt_read, self.ckpt.numel(), None, stream),
-                 "rssm_checkpoint_downcast")
+        bd.check(bd.rssm_mamba2_downcast(self.desc, self.ckpt, self.ckpt_read, stream), "rssm_mamba2_downcast")
 
     def step(self, rec, A, D, y, stream=None):
         bd.check(bd.rssm_mamba2_step(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors,

@@ -60,3 +60,14 @@ def gdn_setup(w, device="cuda", out_dtype=bd.RSSM_F32):
 
 def status(st):
     return int(st.status.item())
+
+
+def ref_f8(x):
+    """Reference fp8 read copy of fp32 rows x [..., 128]: (e4m3 bytes, fp32 row
+    scales) with scale = max|row| / 448 and values x * (448 / max|row|) rounded
+    to nearest even, as the arithmetic of the format fixes them."""
+    import torch
+    m = x.abs().amax(dim=-1, keepdim=True)
+    inv = torch.where(m > 0, torch.tensor(448.0, device=x.device) / m, torch.zeros_like(m))
+    q = (x * inv).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q, (m / 448.0).squeeze(-1)

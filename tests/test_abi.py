@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 16
+    assert len(declared) == 17
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -72,13 +72,26 @@ ARGS9 = [ALIGNED] * 9  # cursors, x, z, B, C, dt, A, D, y
     (-1, 8, 64, 128, 1, 16),   # negative batch
     (4, 8, 64, 128, 1, 16, 7),  # bad out_dtype
     (4, 8, 64, 128, 1, 16, 0, 9),  # bad read_dtype
-    (4, 8, 64, 128, 1, 16, 0, bd.RSSM_F32 + 3),
+    (4, 8, 64, 128, 1, 16, 0, bd.RSSM_FP8_E4M3 + 1),
 ])
 def test_mamba2_desc_validation(lib, desc):
     d = bd.mamba2_desc(*desc)
     ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
     assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, None, ctypes.byref(ring), *ARGS9, None, None) == \
         bd.RSSM_ERR_INVALID_ARG
+
+
+def test_fp8_read_copy_needs_the_specialised_shapes(lib):
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    for desc in ((4, 8, 64, 64, 1, 16), (4, 8, 48, 128, 1, 16), (4, 8, 64, 128, 1, 32), (4, 6, 64, 128, 2, 16)):
+        d = bd.mamba2_desc(*desc, 0, bd.RSSM_FP8_E4M3)  # dstate != 128, headdim % 64, L > 31, 3 heads per group
+        assert lib.rssm_mamba2_step(ctypes.byref(d), ALIGNED, ALIGNED, ctypes.byref(ring), *ARGS9, None, None) == \
+            bd.RSSM_ERR_UNSUPPORTED
+        assert lib.rssm_mamba2_downcast(ctypes.byref(d), ALIGNED, ALIGNED, None) == bd.RSSM_ERR_UNSUPPORTED
+    d = bd.mamba2_desc(4, 8, 64, 128, 1, 16, 0, bd.RSSM_FP8_E4M3)
+    assert lib.rssm_mamba2_spec_verify(ctypes.byref(d), 8, ALIGNED, ALIGNED, ctypes.byref(ring), *ARGS9,
+                                       None, None) == bd.RSSM_ERR_UNSUPPORTED  # K > 4
+    assert lib.rssm_mamba2_downcast(ctypes.byref(d), ALIGNED, ALIGNED + 4, None) == bd.RSSM_ERR_MISALIGNED
 
 
 def test_empty_batch_is_noop(lib):

@@ -179,7 +179,7 @@ def test_gdn_spec_full_size():
     assert H.status(st) == 0
 
 
-@pytest.mark.parametrize("name", ["mamba2_bf16_read", "mamba2_f16_read"])
+@pytest.mark.parametrize("name", ["mamba2_bf16_read", "mamba2_f16_read", "mamba2_f8_read"])
 def test_read_copy_4096_steps(name):
     """fp32 recurrence checkpoint + bf16 (or fp16) read copy, 4096 steps: the
     output error stays within 1e-2 relative L2 and does not grow (rounding of
@@ -205,7 +205,7 @@ def test_read_copy_4096_steps(name):
             if exp["flushed"][i]:
                 worst_ckpt = max(worst_ckpt, H.rel_l2(H.F64(st.ckpt[b]), exp["state"][i]))
     trace = np.array(trace)
-    assert trace.max() <= TOL_READ_COPY
+    assert trace.max() <= (2.0 ** -4 if w.read_copy == "f8" else TOL_READ_COPY)  # e4m3 half-ulp for fp8
     assert trace[-512:].max() <= 1.25 * trace[:512].max()
     slope = np.polyfit(np.arange(len(trace)), trace, 1)[0]
     assert slope < 1e-7, slope

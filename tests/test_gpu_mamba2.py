@@ -13,10 +13,12 @@ import harness as H
 from oracle import sessions
 from recurrent_state_decode_gb300 import binding as bd
 from recurrent_state_decode_gb300 import inputs as I
+from recurrent_state_decode_gb300.state import Mamba2State
 from recurrent_state_decode_gb300.inputs import Mamba2Workload as W
 
 pytestmark = pytest.mark.gpu
 
+TOL_READ_F8 = 2.0 ** -4  # e4m3 half-ulp: the largest relative error of a checkpoint element read
 TOL_Y32, TOL_CKPT, TOL_BF16_EXCESS, TOL_READ_COPY = 1e-4, 1e-5, 2e-3, 1e-2
 
 
@@ -31,6 +33,7 @@ def gpu_lib():
 def run_ar(w, out_dtype=bd.RSSM_F32, seqs=None, read_copy=None, steps=None, trace=None):
     dev = "cuda"
     st, A, D, pre, starts, counts = H.mamba2_setup(w, dev, out_dtype, read_copy)
+    rc_f8 = read_copy == "f8"
     read_copy = st.ckpt_read is not None
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
     feed = H.Feed()
@@ -48,7 +51,7 @@ def run_ar(w, out_dtype=bd.RSSM_F32, seqs=None, read_copy=None, steps=None, trac
             err = H.rel_l2(yg, exp["y"])
             if trace is not None:
                 trace.append(err)
-            assert err <= TOL_READ_COPY, (t, err)
+            assert err <= (TOL_READ_F8 if rc_f8 else TOL_READ_COPY), (t, err)
         elif out_dtype == bd.RSSM_F32:
             err = H.rel_l2(yg, exp["y"])
             assert err <= TOL_Y32, (t, err)
@@ -61,7 +64,10 @@ def run_ar(w, out_dtype=bd.RSSM_F32, seqs=None, read_copy=None, steps=None, trac
                 flushes += 1
                 e = H.rel_l2(H.F64(st.ckpt[b]), exp["state"][i])
                 assert e <= TOL_CKPT, (t, b, e)
-                if read_copy:  # the read copy is the RNE downcast of the new checkpoint
+                if read_copy and rc_f8:  # the fp8 read copy is the scaled RNE downcast of the new checkpoint
+                    q, sc = H.ref_f8(st.ckpt[b])
+                    assert torch.equal(st.read_q[b], q) and torch.equal(st.read_scale[b], sc)
+                elif read_copy:  # the read copy is the RNE downcast of the new checkpoint
                     assert torch.equal(st.ckpt_read[b], st.ckpt[b].to(st.ckpt_read.dtype))
     assert H.status(st) == 0
     return flushes
@@ -112,6 +118,11 @@ READ_COPY = [
 @pytest.mark.parametrize("rc", [True, "f16"], ids=["bf16", "f16"])
 def test_read_copy_small(w, rc):
     run_ar(w, read_copy=rc)
+
+
+@pytest.mark.parametrize("w", READ_COPY[2:], ids=lambda w: w.name)  # the shape-specialised shapes
+def test_read_copy_f8(w):
+    run_ar(w, read_copy="f8")
 
 
 def test_conventional_kernel():
@@ -168,6 +179,7 @@ def test_standalone_flush():
 def run_spec(w, seqs=None, steps=None, out_dtype=bd.RSSM_F32, read_copy=None):
     dev = "cuda"
     st, A, D, pre, starts, counts = H.mamba2_setup(w, dev, out_dtype, read_copy)
+    rc_f8 = read_copy == "f8"
     read_copy = st.ckpt_read is not None
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
     fv, fk = H.Feed(), H.Feed()
@@ -186,7 +198,7 @@ def run_spec(w, seqs=None, steps=None, out_dtype=bd.RSSM_F32, read_copy=None):
         exp = next(sess)
         yg = H.F64(y[seqs])
         if read_copy:
-            assert H.rel_l2(yg, exp["y"]) <= TOL_READ_COPY
+            assert H.rel_l2(yg, exp["y"]) <= (TOL_READ_F8 if rc_f8 else TOL_READ_COPY), t
         elif out_dtype == bd.RSSM_F32:
             assert H.rel_l2(yg, exp["y"]) <= TOL_Y32, t
         else:
@@ -222,6 +234,7 @@ def test_spec_bf16_out_and_read_copy():
     run_spec(SPEC[0], read_copy=True)
     run_spec(SPEC[0], read_copy="f16")
     run_spec(W("spec_fast", 3, 4, 64, 128, 2, 16, 12, seed=45, drafts=3), read_copy="f16")
+    run_spec(W("spec_fast", 3, 4, 64, 128, 2, 16, 12, seed=45, drafts=3), read_copy="f8")
 
 
 def test_spec_all_accepted_equals_ar():
@@ -317,6 +330,22 @@ def test_downcast_rne():
     h = torch.empty(1001, dtype=torch.float16, device=dev)
     bd.check(bd.rssm_checkpoint_downcast(x, h, 1001, bd.RSSM_F16))
     assert torch.equal(h.view(torch.int16), x.to(torch.float16).view(torch.int16))
+
+
+def test_downcast_f8_rows():
+    """The fp8 read copy of a whole checkpoint: e4m3 bytes and row scales equal
+    the scaled round-to-nearest-even conversion, row by row (zero rows, rows
+    whose max is negative, a row of one value)."""
+    w = W("f8dc", 3, 2, 64, 128, 1, 8, 1, seed=64)
+    st = Mamba2State(w.batch, w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len, "cuda", read_copy="f8")
+    st.ckpt.copy_(torch.randn_like(st.ckpt) * torch.logspace(-6, 3, 128, device="cuda"))
+    st.ckpt[0, 0, 0] = 0.0
+    st.ckpt[0, 0, 1] = -torch.rand(128, device="cuda") - 1.0
+    st.ckpt[0, 1, 2] = 3.25
+    st.downcast()
+    q, sc = H.ref_f8(st.ckpt)
+    assert torch.equal(st.read_q, q) and torch.equal(st.read_scale, sc)
+    assert st.read_scale[0, 0, 0].item() == 0.0
 
 
 def test_reset_then_decode():
