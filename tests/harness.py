@@ -68,6 +68,7 @@ def ref_f8(x):
     to nearest even, as the arithmetic of the format fixes them."""
     import torch
     m = x.abs().amax(dim=-1, keepdim=True)
-    inv = torch.where(m > 0, torch.tensor(448.0, device=x.device) / m, torch.zeros_like(m))
+    c448 = torch.full_like(m, 448.0)  # tensor / tensor: IEEE fp32 division, as the format's definition reads
+    inv = torch.where(m > 0, c448 / m, torch.zeros_like(m))
     q = (x * inv).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
-    return q, (m / 448.0).squeeze(-1)
+    return q, (m / c448).squeeze(-1)
