@@ -28,6 +28,22 @@
  *    affected sequence is skipped: its checkpoint, ring and cursor are left
  *    as they were and its outputs are not written. Pass NULL to ignore them.
  *  - batch == 0 is a valid empty call: nothing is launched.
+ *  - State slots (the descriptors' state_slots): by default batch row b of a
+ *    call's records and outputs uses state row b (checkpoint, read copy, ring
+ *    and cursor). Given state_slots [batch] int32, row b uses state row
+ *    state_slots[b] of state arrays holding n_slots rows, so a serving engine
+ *    keeps its states in fixed slots and gathers no state. A slot of -1 marks
+ *    a padding row: it is skipped (its outputs are not written, no state is
+ *    touched). Any other slot outside [0, n_slots) is reported as
+ *    RSSM_DEV_BAD_SLOT and its row skipped. Two rows of one call must not
+ *    name the same slot (their state updates would race). State slots are
+ *    honoured by the decode calls (step, spec_verify) on the shape-specialised
+ *    kernels -- Mamba-2 dstate 128, headdim a multiple of 64, a power-of-two
+ *    nheads / ngroups; Gated DeltaNet dk = dv = 128 -- and by
+ *    rssm_commit_cursors_slots; elsewhere a non-NULL state_slots returns
+ *    RSSM_ERR_UNSUPPORTED. Calls on whole state arrays (flush, prime,
+ *    downcast, conventional steps) take state_slots = NULL with batch = the
+ *    number of state rows.
  *
  * Cursor: int32 [batch, 4] = {start, count, pending, flags} per sequence.
  *  start   ring slot of the oldest record since the checkpoint, [0, L)
@@ -71,7 +87,8 @@ enum {
   RSSM_DEV_WINDOW_FULL = 2, /* AR step on a window holding L records */
   RSSM_DEV_PENDING = 3,     /* step, verify or flush before the last verify was committed */
   RSSM_DEV_BAD_KEPT = 4,    /* commit with kept < 0 or kept > pending */
-  RSSM_DEV_BAD_SLOT = 5,    /* reset of a slot outside [0, batch) */
+  RSSM_DEV_BAD_SLOT = 5,    /* a state slot outside its range (reset: [0, batch);
+                             * state_slots: -1 or [0, n_slots)) */
   RSSM_DEV_TIMEOUT = 6      /* a bounded wait for an asynchronous copy expired */
 };
 
@@ -99,13 +116,19 @@ typedef struct {
   int out_dtype; /* RSSM_F32 or RSSM_BF16: element type of y */
   int read_dtype; /* element type of the read copy ckpt_read, when one is
                    * passed: RSSM_BF16 (0 reads as RSSM_BF16), RSSM_F16, or
-                   * RSSM_FP8_E4M3 -- then ckpt_read holds batch * nheads *
-                   * headdim * dstate e4m3 bytes followed by one fp32 scale
-                   * per state row ([batch, nheads, headdim]); a value reads
+                   * RSSM_FP8_E4M3 -- then ckpt_read holds S * nheads *
+                   * headdim * dstate e4m3 bytes (S state rows: batch, or
+                   * n_slots) followed by one fp32 scale per state row
+                   * ([S, nheads, headdim]); a value reads
                    * as e4m3 * scale, scale = max|row| / 448. FP8 needs
                    * dstate 128, headdim a multiple of 64, buf_len <= 31 and
                    * a power-of-two nheads / ngroups (else
                    * RSSM_ERR_UNSUPPORTED). */
+  const int32_t* state_slots; /* [batch] state row of each batch row (-1:
+                               * padding), or NULL: row b uses state row b */
+  int n_slots;                /* state rows when state_slots is given: the
+                               * leading dimension of ckpt, ckpt_read, the
+                               * ring and the cursors (else batch) */
 } rssm_mamba2_desc;
 
 /* Ring buffer of window records, head- (or group-) major so that one
@@ -204,6 +227,14 @@ RSSM_API int rssm_commit_cursors(int32_t* cursors, const int32_t* kept, int batc
                         int buf_len, int32_t* dev_status,
                         rssm_stream_t stream);
 
+/* rssm_commit_cursors for a call made with state slots: kept [batch] is per
+ * batch row and applies to cursor state_slots[b] of n_slots; rows whose slot is
+ * -1 are skipped, other slots outside [0, n_slots) reported as
+ * RSSM_DEV_BAD_SLOT. */
+RSSM_API int rssm_commit_cursors_slots(int32_t* cursors, const int32_t* kept, const int32_t* state_slots,
+                              int batch, int n_slots, int buf_len, int32_t* dev_status,
+                              rssm_stream_t stream);
+
 /* Reset the cursors of the listed sequences to {0, 0, 0, 0} (a new request in
  * that slot; "Core implementation files": the reset call). slots [n_slots]
  * int32 in [0, batch). The checkpoint is not touched: the caller writes it,
@@ -239,6 +270,8 @@ typedef struct {
   int batch, nheads, dk, dv;
   int buf_len;
   int out_dtype; /* element type of o */
+  const int32_t* state_slots; /* as in rssm_mamba2_desc */
+  int n_slots;
 } rssm_gdn_desc;
 
 typedef struct {

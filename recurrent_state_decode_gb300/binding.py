@@ -35,7 +35,7 @@ c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_vo
 
 class rssm_mamba2_desc(ctypes.Structure):
     _fields_ = [(n, c_int) for n in ("batch", "nheads", "headdim", "dstate", "ngroups", "buf_len", "out_dtype",
-                                     "read_dtype")]
+                                     "read_dtype")] + [("state_slots", c_void_p), ("n_slots", c_int)]
 
 
 class rssm_mamba2_ring(ctypes.Structure):
@@ -43,7 +43,8 @@ class rssm_mamba2_ring(ctypes.Structure):
 
 
 class rssm_gdn_desc(ctypes.Structure):
-    _fields_ = [(n, c_int) for n in ("batch", "nheads", "dk", "dv", "buf_len", "out_dtype")]
+    _fields_ = [(n, c_int) for n in ("batch", "nheads", "dk", "dv", "buf_len", "out_dtype")] + [
+        ("state_slots", c_void_p), ("n_slots", c_int)]
 
 
 class rssm_gdn_ring(ctypes.Structure):
@@ -61,6 +62,7 @@ _SIGNATURES = {
     "rssm_mamba2_flush": (c_int, [P] * 7 + [P]),
     "rssm_mamba2_spec_verify": (c_int, [P, c_int] + [P] * 14),
     "rssm_commit_cursors": (c_int, [P, P, c_int, c_int, P, P]),
+    "rssm_commit_cursors_slots": (c_int, [P, P, P, c_int, c_int, c_int, P, P]),
     "rssm_reset_cursors": (c_int, [P, P, c_int, c_int, P, P]),
     "rssm_checkpoint_downcast": (c_int, [P, P, c_size_t, c_int, P]),
     "rssm_mamba2_downcast": (c_int, [P, P, P, P]),
@@ -126,16 +128,19 @@ def _stream(stream, *tensors):
     return None
 
 
-def mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype=RSSM_F32, read_dtype=0):
-    return rssm_mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype, read_dtype)
+def mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype=RSSM_F32, read_dtype=0,
+                state_slots=None, n_slots=0):
+    """state_slots: int32 [batch] state row per batch row (-1 padding), with n_slots state rows."""
+    return rssm_mamba2_desc(batch, nheads, headdim, dstate, ngroups, buf_len, out_dtype, read_dtype,
+                            ptr(state_slots), n_slots)
 
 
 def mamba2_ring(x, z, B, C, dt):
     return rssm_mamba2_ring(ptr(x), ptr(z), ptr(B), ptr(C), ptr(dt))
 
 
-def gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype=RSSM_F32):
-    return rssm_gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype)
+def gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype=RSSM_F32, state_slots=None, n_slots=0):
+    return rssm_gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype, ptr(state_slots), n_slots)
 
 
 def gdn_ring(q, k, v, g, beta, e):
@@ -192,6 +197,11 @@ def rssm_mamba2_spec_verify(desc, n_new, ckpt, ckpt_read, ring, cursors, x, z, B
 def rssm_commit_cursors(cursors, kept, batch, buf_len, dev_status=None, stream=None):
     return load().rssm_commit_cursors(ptr(cursors), ptr(kept), int(batch), int(buf_len), ptr(dev_status),
                                       _stream(stream, cursors))
+
+
+def rssm_commit_cursors_slots(cursors, kept, state_slots, batch, n_slots, buf_len, dev_status=None, stream=None):
+    return load().rssm_commit_cursors_slots(ptr(cursors), ptr(kept), ptr(state_slots), int(batch), int(n_slots),
+                                            int(buf_len), ptr(dev_status), _stream(stream, cursors))
 
 
 def rssm_reset_cursors(cursors, slots, n_slots, batch, dev_status=None, stream=None):

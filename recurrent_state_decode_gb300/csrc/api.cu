@@ -25,6 +25,19 @@ int check_ptrs(std::initializer_list<const void*> ps) {
 
 int check_opt(const void* p) { return (p && !aligned16(p)) ? RSSM_ERR_MISALIGNED : RSSM_OK; }
 
+// A state-slot table needs 0 <= n_slots <= RSSM_MAX_BATCH.
+int check_slots(const int32_t* slots, int n_slots) {
+  if (!slots) return RSSM_OK;
+  if (n_slots < 0) return RSSM_ERR_INVALID_ARG;
+  return n_slots > RSSM_MAX_BATCH ? RSSM_ERR_UNSUPPORTED : RSSM_OK;
+}
+
+// State rows of the arrays a call addresses.
+template <typename Desc>
+size_t state_rows(const Desc* d) {
+  return d->state_slots ? (size_t)d->n_slots : (size_t)d->batch;
+}
+
 int check_m2(const rssm_mamba2_desc* d) {
   if (!d) return RSSM_ERR_INVALID_ARG;
   if (d->batch < 0 || d->nheads < 1 || d->ngroups < 1 || d->nheads % d->ngroups != 0) return RSSM_ERR_INVALID_ARG;
@@ -35,7 +48,8 @@ int check_m2(const rssm_mamba2_desc* d) {
     return RSSM_ERR_INVALID_ARG;
   const int pb = rows_per_block(d->headdim, d->dstate);
   const long long grid = (long long)d->batch * d->nheads * ((d->headdim + pb - 1) / pb);
-  if (grid > INT_MAX || d->batch > 65535) return RSSM_ERR_UNSUPPORTED;
+  if (grid > INT_MAX || d->batch > RSSM_MAX_BATCH) return RSSM_ERR_UNSUPPORTED;
+  if (int rc = check_slots(d->state_slots, d->n_slots)) return rc;
   if (d->read_dtype == RSSM_FP8_E4M3) {  // the fp8 read copy lives on the shape-specialised kernels only
     const int hpg = d->nheads / d->ngroups;
     if (d->dstate != 128 || d->headdim % 64 != 0 || d->buf_len > 31 || (hpg & (hpg - 1)) != 0 ||
@@ -53,7 +67,7 @@ int check_gdn(const rssm_gdn_desc* d) {
   if (d->out_dtype != RSSM_F32 && d->out_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
   const long long grid = (long long)d->batch * d->nheads * ((d->dv + 63) / 64);
   if (grid > INT_MAX) return RSSM_ERR_UNSUPPORTED;
-  return RSSM_OK;
+  return check_slots(d->state_slots, d->n_slots);
 }
 
 M2Args m2_args(const rssm_mamba2_desc* d) {
@@ -71,6 +85,8 @@ M2Args m2_args(const rssm_mamba2_desc* d) {
   a.read_f8 = d->read_dtype == RSSM_FP8_E4M3;
   const int hpg = a.H / a.G;
   a.hpg_log2 = (hpg & (hpg - 1)) == 0 ? __builtin_ctz(hpg) : -1;
+  a.slots = d->state_slots;
+  a.Sn = (int)state_rows(d);
   return a;
 }
 
@@ -92,6 +108,8 @@ GdnArgs gdn_args(const rssm_gdn_desc* d) {
   a.DV = d->dv;
   a.L = d->buf_len;
   a.K = 1;
+  a.slots = d->state_slots;
+  a.Sn = (int)state_rows(d);
   return a;
 }
 
@@ -99,7 +117,7 @@ GdnArgs gdn_args(const rssm_gdn_desc* d) {
 
 extern "C" {
 
-int rssm_version(void) { return 100; }
+int rssm_version(void) { return 200; }
 
 const char* rssm_status_string(int code) {
   switch (code) {
@@ -112,7 +130,7 @@ const char* rssm_status_string(int code) {
     case RSSM_DEV_WINDOW_FULL: return "device: AR step on a full window (flush or commit first)";
     case RSSM_DEV_PENDING: return "device: previous verify not committed";
     case RSSM_DEV_BAD_KEPT: return "device: kept outside [0, pending]";
-    case RSSM_DEV_BAD_SLOT: return "device: reset slot outside [0, batch)";
+    case RSSM_DEV_BAD_SLOT: return "device: state slot out of range";
     case RSSM_DEV_TIMEOUT: return "device: bounded wait for a bulk copy expired";
     default: return "unknown status code";
   }
@@ -122,7 +140,7 @@ int rssm_mamba2_ring_bytes(const rssm_mamba2_desc* d, size_t bytes[5]) {
   int rc = check_m2(d);
   if (rc) return rc;
   if (!bytes) return RSSM_ERR_INVALID_ARG;
-  const size_t Bt = d->batch, H = d->nheads, L = d->buf_len, G = d->ngroups;
+  const size_t Bt = state_rows(d), H = d->nheads, L = d->buf_len, G = d->ngroups;
   bytes[0] = bytes[1] = Bt * H * L * d->headdim * 2;
   bytes[2] = bytes[3] = Bt * G * L * d->dstate * 2;
   bytes[4] = Bt * H * pad4(d->buf_len) * 4;
@@ -133,7 +151,7 @@ int rssm_gdn_ring_bytes(const rssm_gdn_desc* d, size_t bytes[6]) {
   int rc = check_gdn(d);
   if (rc) return rc;
   if (!bytes) return RSSM_ERR_INVALID_ARG;
-  const size_t Bt = d->batch, H = d->nheads, L = d->buf_len;
+  const size_t Bt = state_rows(d), H = d->nheads, L = d->buf_len;
   bytes[0] = bytes[1] = Bt * H * L * d->dk * 2;
   bytes[2] = Bt * H * L * d->dv * 2;
   bytes[3] = bytes[4] = Bt * H * pad4(d->buf_len) * 4;
@@ -146,6 +164,7 @@ int rssm_mamba2_conventional_step(const rssm_mamba2_desc* d, float* state, const
                                   const float* D, void* y, rssm_stream_t stream) {
   int rc = check_m2(d);
   if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if ((rc = check_ptrs({state, x, z, B, C, dt, A, D, y}))) return rc;
   M2Args a = m2_args(d);
@@ -187,6 +206,7 @@ int rssm_mamba2_step(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_rea
   a.y = y;
   a.status = dev_status;
   cudaStream_t st = (cudaStream_t)stream;
+  if (a.slots && !m2_step_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;  // state slots: shape-specialised path
   if ((rc = cuda_rc(m2_launch(M2_STEP, a, d->out_dtype == RSSM_BF16, st)))) return rc;
   if (m2_step_fast_applies(a)) return RSSM_OK;  // that kernel advanced the cursors itself
   return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
@@ -196,6 +216,7 @@ int rssm_mamba2_flush(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_re
                       int32_t* cursors, const float* A, int32_t* dev_status, rssm_stream_t stream) {
   int rc = check_m2(d);
   if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if (!ring) return RSSM_ERR_INVALID_ARG;
   if ((rc = check_ptrs({ckpt, ring->x, ring->B, ring->dt, cursors, A}))) return rc;
@@ -239,7 +260,8 @@ int rssm_mamba2_spec_verify(const rssm_mamba2_desc* d, int n_new, float* ckpt, r
   a.D = D;
   a.y = y;
   a.status = dev_status;
-  if (a.read_f8 && a.ckpt_read && !m2_verify_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;  // fp8: K <= 4, L + K <= 32
+  // fp8 read copies and state slots: the shape-specialised path only (K <= 4, L + K <= 32)
+  if (((a.read_f8 && a.ckpt_read) || a.slots) && !m2_verify_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;
   return cuda_rc(m2_launch(M2_VERIFY, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
 }
 
@@ -250,6 +272,17 @@ int rssm_commit_cursors(int32_t* cursors, const int32_t* kept, int batch, int bu
   int rc;
   if ((rc = check_ptrs({cursors, kept})) || (rc = check_opt(dev_status))) return rc;
   return cuda_rc(cursor_launch(CUR_COMMIT, cursors, kept, batch, buf_len, dev_status, (cudaStream_t)stream));
+}
+
+int rssm_commit_cursors_slots(int32_t* cursors, const int32_t* kept, const int32_t* state_slots, int batch,
+                              int n_slots, int buf_len, int32_t* dev_status, rssm_stream_t stream) {
+  if (batch < 0 || n_slots < 0 || buf_len < 1 || buf_len > RSSM_MAX_BUF_LEN) return RSSM_ERR_INVALID_ARG;
+  if (batch == 0) return RSSM_OK;
+  int rc;
+  if ((rc = check_ptrs({cursors, kept})) || (rc = check_opt(dev_status))) return rc;
+  if (!state_slots) return RSSM_ERR_INVALID_ARG;
+  return cuda_rc(cursor_launch(CUR_COMMIT, cursors, kept, batch, buf_len, dev_status, (cudaStream_t)stream,
+                               state_slots, n_slots));
 }
 
 int rssm_reset_cursors(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* dev_status,
@@ -272,6 +305,7 @@ int rssm_checkpoint_downcast(const float* src, rssm_bf16* dst, size_t n, int dty
 int rssm_mamba2_downcast(const rssm_mamba2_desc* d, const float* ckpt, void* ckpt_read, rssm_stream_t stream) {
   int rc = check_m2(d);
   if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if ((rc = check_ptrs({ckpt, ckpt_read}))) return rc;
   const size_t rows = (size_t)d->batch * d->nheads * d->headdim;
@@ -286,6 +320,7 @@ int rssm_gdn_conventional_step(const rssm_gdn_desc* d, float* S, const rssm_bf16
                                rssm_stream_t stream) {
   int rc = check_gdn(d);
   if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if ((rc = check_ptrs({S, q, k, v, g, beta, o}))) return rc;
   GdnArgs a = gdn_args(d);
@@ -326,6 +361,7 @@ int rssm_gdn_step(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, i
   a.o = o;
   a.status = dev_status;
   cudaStream_t st = (cudaStream_t)stream;
+  if (a.slots && !gdn_step_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;  // state slots: shape-specialised path
   if ((rc = cuda_rc(gdn_launch(GDN_STEP, a, d->out_dtype == RSSM_BF16, st)))) return rc;
   if (gdn_step_fast_applies(a)) return RSSM_OK;  // that kernel advanced the cursors itself
   return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
@@ -335,6 +371,7 @@ int rssm_gdn_flush(const rssm_gdn_desc* d, float* S, const rssm_gdn_ring* ring, 
                    rssm_stream_t stream) {
   int rc = check_gdn(d);
   if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if (!ring) return RSSM_ERR_INVALID_ARG;
   if ((rc = check_ptrs({S, ring->k, ring->v, ring->g, ring->beta, cursors}))) return rc;
@@ -382,6 +419,7 @@ int rssm_gdn_spec_verify(const rssm_gdn_desc* d, int n_new, float* S, const rssm
   a.beta = beta;
   a.o = o;
   a.status = dev_status;
+  if (a.slots && !gdn_verify_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;  // state slots: shape-specialised path
   return cuda_rc(gdn_verify_launch(a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
 }
 
@@ -389,6 +427,7 @@ int rssm_gdn_prime(const rssm_gdn_desc* d, const float* S, const rssm_gdn_ring* 
                    int32_t* dev_status, rssm_stream_t stream) {
   int rc = check_gdn(d);
   if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if (!ring) return RSSM_ERR_INVALID_ARG;
   if ((rc = check_ptrs({S, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors}))) return rc;

@@ -227,6 +227,18 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// State row of batch row b: b itself, or slots[b] of n state rows when a slot
+// table is given. A padding row (slot -1) and a slot outside [0, n) both give
+// -1; the latter is reported (RSSM_DEV_BAD_SLOT) by the threads for which
+// `reporter` holds (one per row is enough).
+__device__ __forceinline__ int state_slot(const int32_t* slots, int n, int b, int32_t* status, bool reporter) {
+  if (!slots) return b;
+  const int s = __ldg(slots + b);
+  if (s >= 0 && s < n) return s;
+  if (s != -1 && reporter) report(status, RSSM_DEV_BAD_SLOT);
+  return -1;
+}
+
 // ---------------------------------------------------------------- mbarrier + bulk copy
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

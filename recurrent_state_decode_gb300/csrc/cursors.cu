@@ -6,6 +6,7 @@
 //   commit    needs 0 <= kept <= pending: if folded {start += count mod L; count = 0};
 //             count += kept; pending = 0; flags = 0
 //   reset     cursor = {0, 0, 0, 0}
+// With a slot table, batch row b's cursor is the one of its state slot.
 // The compute kernels only read cursors; these run after them in stream
 // order, so no block ever sees a cursor another block of the same launch moved.
 #include "common.cuh"
@@ -13,10 +14,13 @@
 
 namespace rssm {
 
-__global__ void cursor_kernel(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status) {
+__global__ void cursor_kernel(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status,
+                              const int32_t* slots, int n_state) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
-  int4 c = *reinterpret_cast<int4*>(cursors + 4 * (size_t)b);
+  const int s = state_slot(slots, n_state, b, status, true);
+  if (s < 0) return;
+  int4 c = *reinterpret_cast<int4*>(cursors + 4 * (size_t)s);
   const bool range_ok = c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L && c.z >= 0;
   if (!range_ok) {
     report(status, RSSM_DEV_BAD_CURSOR);
@@ -41,7 +45,7 @@ __global__ void cursor_kernel(int mode, int32_t* cursors, const int32_t* kept, i
     c.z = 0;
     c.w = 0;
   }
-  *reinterpret_cast<int4*>(cursors + 4 * (size_t)b) = c;
+  *reinterpret_cast<int4*>(cursors + 4 * (size_t)s) = c;
 }
 
 __global__ void reset_kernel(int32_t* cursors, const int32_t* slots, int n, int batch, int32_t* status) {
@@ -79,9 +83,9 @@ __global__ void downcast_f8_kernel(const float* __restrict__ src, uint8_t* __res
 }
 
 cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status,
-                          cudaStream_t st) {
+                          cudaStream_t st, const int32_t* slots, int n_state) {
   if (batch <= 0) return cudaSuccess;
-  cursor_kernel<<<(batch + 127) / 128, 128, 0, st>>>(mode, cursors, kept, batch, L, status);
+  cursor_kernel<<<(batch + 127) / 128, 128, 0, st>>>(mode, cursors, kept, batch, L, status, slots, n_state);
   return cudaGetLastError();
 }
 

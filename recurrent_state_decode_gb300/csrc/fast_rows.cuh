@@ -106,7 +106,7 @@ __device__ __forceinline__ void store_read_copy8(const M2Args& a, const float4 (
   if (!a.ckpt_read) return;
   if (a.read_f8) {
     uint8_t* q = reinterpret_cast<uint8_t*>(a.ckpt_read);
-    float* scales = reinterpret_cast<float*>(q + (size_t)a.Bt * a.H * a.P * FN);
+    float* scales = reinterpret_cast<float*>(q + (size_t)a.Sn * a.H * a.P * FN);
 #pragma unroll
     for (int rr = 0; rr < 8; rr++) store_f8_row(q, scales, off / FN + rr, hv[rr], lane);
   } else {
@@ -116,13 +116,14 @@ __device__ __forceinline__ void store_read_copy8(const M2Args& a, const float4 (
   }
 }
 
-// h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the read copy).
+// h1 = P h0 + sum_k (w_k x_k[r]) B_k for 8 rows, written once (and the read copy);
+// the window's B rows are ring group row sg, the current record's is record group row bg.
 __device__ __forceinline__ void fold8(const M2Args& a, float4 (&hv)[8], float Pm, float wk, const float (&xl)[8],
-                                      int m, int count, int start, int bg, size_t off, int lane) {
+                                      int m, int count, int start, int sg, int bg, size_t off, int lane) {
   const int L = a.L;
 #pragma unroll
   for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pm, hv[rr]);
-  const uint16_t* rB = a.rB + (size_t)bg * L * FN + lane * 4;
+  const uint16_t* rB = a.rB + (size_t)sg * L * FN + lane * 4;
   for (int k = 0; k < m; k++) {
     const float w = __shfl_sync(FULL, wk, k);
     int s = start + k;

@@ -12,8 +12,9 @@ __device__ __forceinline__ int wrap(int s, int L) { return s < L ? s : s - L; }
 // 0 <= start < L, 0 <= count <= L and pending == 0, append the K new records'
 // k, q (rows), g and beta at slots (start + count + j) mod L and set pending =
 // K, flags = folded; otherwise report as the cursor checks do and leave the
-// cursor with its flags word set to `flags`.
-__device__ __forceinline__ void gdn_verify_epilogue(const GdnArgs& a, int b, int4 c, int flags) {
+// cursor with its flags word set to `flags`. The records of batch row b go to
+// the ring rows (and cursor) of its state slot sb.
+__device__ __forceinline__ void gdn_verify_epilogue(const GdnArgs& a, int b, int sb, int4 c, int flags) {
   const int L = a.L, K = a.K, H = a.H, DK = a.DK, tid = threadIdx.x, nt = blockDim.x;
   c.w = flags;
   int err = 0;
@@ -24,28 +25,28 @@ __device__ __forceinline__ void gdn_verify_epilogue(const GdnArgs& a, int b, int
   if (err) {
     if (tid == 0) {
       report(a.status, err);
-      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)sb) = c;
     }
     return;
   }
   const int nv = DK >> 3;
   for (int q = tid; q < K * H * nv; q += nt) {
     const int j = q / (H * nv), r = q - j * H * nv, h = r / nv, v = r - h * nv;
-    const size_t slot = ((size_t)b * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
+    const size_t slot = ((size_t)sb * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
     const size_t src = (((size_t)b * K + j) * H + h) * DK + v * 8;
     *reinterpret_cast<uint4*>(a.rk + slot * DK + v * 8) = *reinterpret_cast<const uint4*>(a.k + src);
     *reinterpret_cast<uint4*>(a.rq + slot * DK + v * 8) = *reinterpret_cast<const uint4*>(a.q + src);
   }
   for (int q = tid; q < K * H; q += nt) {
     const int j = q / H, h = q - j * H;
-    const size_t s = ((size_t)b * H + h) * pad4(L) + wrap(wrap(c.x + c.y + j, L), L);
+    const size_t s = ((size_t)sb * H + h) * pad4(L) + wrap(wrap(c.x + c.y + j, L), L);
     a.rg[s] = a.g[((size_t)b * K + j) * H + h];
     a.rbeta[s] = a.beta[((size_t)b * K + j) * H + h];
   }
   if (tid == 0) {
     c.z = K;
     c.w = (c.y + K > L) ? 1 : 0;
-    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)sb) = c;
   }
 }
 

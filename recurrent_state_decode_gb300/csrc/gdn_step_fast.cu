@@ -57,7 +57,8 @@ __device__ __forceinline__ float rows8x2(const float4 (&hv)[8], float4 ka, float
   return reduce_transpose<16>(v, lane);
 }
 
-template <bool OUT_BF16>
+// SLOTS: batch rows name their state rows through a slot table.
+template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;               // the block's 64 rows
@@ -68,9 +69,13 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = a.L, H = a.H;
   const int pb = blockIdx.x, b = blockIdx.z;
-  const size_t bh = (size_t)b * H + blockIdx.y;
+  // the batch row's state slot; a padding row (or a reported bad slot) leaves at once
+  const int sb = SLOTS ? state_slot(a.slots, a.Sn, b, a.status, pb == 0 && blockIdx.y == 0 && threadIdx.x == 0) : b;
+  if (SLOTS && sb < 0) return;
+  const size_t bh = (size_t)b * H + blockIdx.y;   // the record's rows (q, k, v, g, beta, o)
+  const size_t sh = (size_t)sb * H + blockIdx.y;  // the state's rows (S, ring, cursor)
   const int p0 = pb * FPB;
-  const size_t tbase = (bh * GD + p0) * GD;
+  const size_t tbase = (sh * GD + p0) * GD;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[0], 1);
@@ -79,10 +84,10 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     mbar_arrive_expect_tx(&bar[0], FPB * GD * 4);
     bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
   }
-  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's row groups (within the block)
   // ring slot `lane`: g
-  const float gs = lane < L ? a.rg[bh * pad4(L) + lane] : 0.f;
+  const float gs = lane < L ? a.rg[sh * pad4(L) + lane] : 0.f;
   // the current record
   const uint2 kraw = *reinterpret_cast<const uint2*>(a.k + bh * GD + lane * 4);
   const uint2 qraw = *reinterpret_cast<const uint2*>(a.q + bh * GD + lane * 4);
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const int vr = (lane >> 1) & 7;  // the row this lane finishes (lanes 0..15)
   const uint16_t vbA = a.v[bh * GD + p0 + rl0 + vr], vbB = a.v[bh * GD + p0 + rl1 + vr];
   {  // k_s . k and k_s . q for ring slots s = warp + 4 j (s == L: the current k)
-    const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
+    const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
     float pk[2 * KW];
 #pragma unroll
     for (int j = 0; j < KW; j++) {
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     mbar_arrive_expect_tx(&bar[1], (uint32_t)count * FPB * 4);
     for (int t = 0; t < count; t++) {
       const int s = start + t < L ? start + t : start + t - L;
-      bulk_load(es + t * ES, a.re + (bh * L + s) * GD + p0, FPB * 4, &bar[1]);
+      bulk_load(es + t * ES, a.re + (sh * L + s) * GD + p0, FPB * 4, &bar[1]);
     }
   }
   const bool flush = valid && m == L;
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   __syncthreads();
   int ticket = 0;
   if (threadIdx.x == 0) {  // every thread has read the cursor
-    ticket = cursor_ticket(a.cursors, b);
+    ticket = cursor_ticket(a.cursors, sb);
     cur_s = cur;
   }
   const int ent = lane < count ? sl : L;
@@ -144,18 +149,18 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   // Append the current record now (its e follows below): its slot is outside
   // the window, so no block reads it for a result.
   if (valid && !flush) {
-    const size_t vrow = (bh * L + scur) * GD + p0 + vr;
+    const size_t vrow = (sh * L + scur) * GD + p0 + vr;
     if (lane < 16 && (lane & 1) == 0) {
       a.rv[vrow + rl0] = vbA;
       a.rv[vrow + rl1] = vbB;
     }
     if (pb == 0 && warp == 0) {
-      const size_t krow = (bh * L + scur) * GD + lane * 4;
+      const size_t krow = (sh * L + scur) * GD + lane * 4;
       *reinterpret_cast<uint2*>(a.rk + krow) = kraw;
       *reinterpret_cast<uint2*>(a.rq + krow) = qraw;
       if (lane == 0) {
-        a.rg[bh * pad4(L) + scur] = gm;
-        a.rbeta[bh * pad4(L) + scur] = bm;
+        a.rg[sh * pad4(L) + scur] = gm;
+        a.rbeta[sh * pad4(L) + scur] = bm;
       }
     }
   }
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar[0], 0);
     mbar_wait(&bar[1], 0);
-    if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, cur_s, ticket, a.H * 2, L, a.status);
+    if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, cur_s, ticket, a.H * 2, L, a.status);
     return;
   }
 #pragma unroll
@@ -192,12 +197,12 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     const size_t row = bh * GD + p0 + rl + vr;
     if (valid && lane < 16 && (lane & 1) == 0) {
       store_y<OUT_BF16>(a.o, row, fmaf(kq_cur, ec, yq));
-      if (!flush) a.re[(bh * L + scur) * GD + p0 + rl + vr] = ec;
+      if (!flush) a.re[(sh * L + scur) * GD + p0 + rl + vr] = ec;
     }
     if (flush) {  // S_m = gamma S0 + sum_t D(m-1,t) e_t k_t^T, written once
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(gamma, hv[rr]);
-      const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
+      const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
       for (int t0 = 0; t0 < count; t0 += 2) {  // e_t rows from shared memory (a broadcast read)
         float4 kt[2];
 #pragma unroll
@@ -224,19 +229,20 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
       for (int rr = 0; rr < 8; rr++) __stcs(reinterpret_cast<float4*>(a.S + tbase + (size_t)(rl + rr) * GD) + lane, hv[rr]);
     }
   }
-  if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, cur_s, ticket, a.H * 2, L, a.status);
+  if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, cur_s, ticket, a.H * 2, L, a.status);
 }
 
 }  // namespace
 
 bool gdn_step_fast_applies(const GdnArgs& a) {
   return a.DK == GD && a.DV == GD && a.L <= FW * KW - 1 && a.H * 2 < (1 << 15) && a.H <= 65535 &&
-         a.Bt <= 65535;
+         a.Bt <= 65535 && a.Sn <= 65535;
 }
 
 cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
-  auto k = out_bf16 ? gdn_step_fast_kernel<true> : gdn_step_fast_kernel<false>;
+  auto k = a.slots ? (out_bf16 ? gdn_step_fast_kernel<true, true> : gdn_step_fast_kernel<false, true>)
+                   : (out_bf16 ? gdn_step_fast_kernel<true, false> : gdn_step_fast_kernel<false, false>);
   const int smem = (FPB * GD + a.L * ES) * 4;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);

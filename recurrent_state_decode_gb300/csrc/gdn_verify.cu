@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(GV_THREADS) gdn_verify_kernel(GdnArgs a) {
 // One block per sequence, after the verify in stream order.
 __global__ void __launch_bounds__(GV_THREADS) gdn_verify_epilogue_kernel(GdnArgs a) {
   const int4 c = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)blockIdx.x);
-  gdn_verify_epilogue(a, blockIdx.x, c, c.w);
+  gdn_verify_epilogue(a, blockIdx.x, blockIdx.x, c, c.w);
 }
 
 cudaError_t gdn_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {

@@ -39,7 +39,8 @@ constexpr int ES = FPB + 4;  // floats per staged e row (padded; 16-byte multipl
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-template <bool OUT_BF16>
+// SLOTS: batch rows name their state rows through a slot table.
+template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;                 // the block's 64 rows
@@ -53,9 +54,12 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int L = a.L, H = a.H, K = a.K;
-  const size_t bh = (size_t)b * H + h;
+  // the batch row's state slot; a padding row (or a reported bad slot) leaves at once
+  const int sb = SLOTS ? state_slot(a.slots, a.Sn, b, a.status, pb == 0 && h == 0 && threadIdx.x == 0) : b;
+  if (SLOTS && sb < 0) return;
+  const size_t sh = (size_t)sb * H + h;  // the state's rows (S, ring, cursor)
   const int p0 = pb * FPB;
-  const size_t tbase = (bh * GD + p0) * GD;
+  const size_t tbase = (sh * GD + p0) * GD;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[0], 1);
@@ -64,11 +68,11 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     mbar_arrive_expect_tx(&bar[0], FPB * GD * 4);
     bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
   }
-  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)sb);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;
   const int qg = lane >> 2, qt = lane & 3;   // tensor-core fragment coordinates
   const int rA = rl0 + qg, rB = rl1 + qg;    // the rows of this lane's accumulator fragments
-  const float gs = lane < L ? a.rg[bh * pad4(L) + lane] : 0.f;
+  const float gs = lane < L ? a.rg[sh * pad4(L) + lane] : 0.f;
   float gn = 0.f, bn = 0.f;
   if (lane < K) {
     gn = a.g[((size_t)b * K + lane) * H + h];
@@ -92,11 +96,11 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   // new record e - L if e < L + K, else 0): [32 x 128] . [128 x 8] on the
   // tensor cores, warp w < 2 taking entries 16 w .. 16 w + 15 (bf16 inputs are
   // exact in tf32, so one mma per k-step).
-  const uint16_t* rkp = a.rk + bh * L * GD + lane * 4;
+  const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
   if (warp < 2) {
     const int e0 = 16 * warp + qg, e1 = e0 + 8;
-    const uint16_t* g0 = e0 < L ? a.rk + (bh * L + e0) * GD : nullptr;
-    const uint16_t* g1 = e1 < L ? a.rk + (bh * L + e1) * GD : nullptr;
+    const uint16_t* g0 = e0 < L ? a.rk + (sh * L + e0) * GD : nullptr;
+    const uint16_t* g1 = e1 < L ? a.rk + (sh * L + e1) * GD : nullptr;
     const float* s0 = (e0 >= L && e0 < L + K) ? vecs + (e0 - L) * GD : nullptr;
     const float* s1 = (e1 >= L && e1 < L + K) ? vecs + (e1 - L) * GD : nullptr;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     cur_s = cur;
     mbar_arrive_expect_tx(&bar[1], (uint32_t)count * FPB * 4);
     for (int t = 0; t < count; t++)
-      bulk_load(es + t * ES, a.re + (bh * L + wrap(start + t, L)) * GD + p0, FPB * 4, &bar[1]);
+      bulk_load(es + t * ES, a.re + (sh * L + wrap(start + t, L)) * GD + p0, FPB * 4, &bar[1]);
   }
   // record t on lane t: committed (ring slot sl) or new (record jn)
   int sl = start + lane;
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   const float Gx = __shfl_sync(FULL, G, (count + cj) & 31), Gy = __shfl_sync(FULL, G, (count + cj2) & 31);
   __syncthreads();  // the dot tables
   int ticket = 0;
-  if (threadIdx.x == 0 && !fold) ticket = cursor_ticket(a.cursors, b);  // done with the ring's k and g
+  if (threadIdx.x == 0 && !fold) ticket = cursor_ticket(a.cursors, sb);  // done with the ring's k and g
   if (warp == 0) {  // window coefficients of committed record `lane`, one row per vector
 #pragma unroll
     for (int n = 0; n < 2 * KMAX; n++) cf[n][lane] = lane < count ? expf(Ga[n & (KMAX - 1)] - G) * tbl[n][sl] : 0.f;
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
         ma = qt == j ? eA[j] : ma;
         mb = qt == j ? eB[j] : mb;
       }
-      const size_t slot = bh * L + wrap(wrap(start + count + qt, L), L);
+      const size_t slot = sh * L + wrap(wrap(start + count + qt, L), L);
       a.re[slot * GD + p0 + rA] = ma;
       a.re[slot * GD + p0 + rB] = mb;
       a.rv[slot * GD + p0 + rA] = (uint16_t)vtA;
@@ -304,24 +308,25 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   }
   if (fold) {  // uniform: the fold read the ring's k rows until here
     __syncthreads();
-    if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);
+    if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, sb);
   }
   __syncthreads();
   if (threadIdx.x == 0) last_flags = last_ticket(ticket, 2 * H) ? (ticket & 0xffff) : -1;
   __syncthreads();
-  if (last_flags >= 0) gdn_verify_epilogue(a, b, cur_s, last_flags);
+  if (last_flags >= 0) gdn_verify_epilogue(a, b, sb, cur_s, last_flags);
 }
 
 }  // namespace
 
 bool gdn_verify_fast_applies(const GdnArgs& a) {
   return a.DK == GD && a.DV == GD && a.K <= KMAX && a.L + a.K <= FW * EW && 2 * a.H < (1 << 15) && a.H <= 65535 &&
-         a.Bt <= 65535;
+         a.Bt <= 65535 && a.Sn <= 65535;
 }
 
 cudaError_t gdn_verify_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
-  auto k = out_bf16 ? gdn_verify_fast_kernel<true> : gdn_verify_fast_kernel<false>;
+  auto k = a.slots ? (out_bf16 ? gdn_verify_fast_kernel<true, true> : gdn_verify_fast_kernel<false, true>)
+                   : (out_bf16 ? gdn_verify_fast_kernel<true, false> : gdn_verify_fast_kernel<false, false>);
   const int smem = (FPB * GD + 2 * KMAX * GD + a.L * ES) * 4;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);

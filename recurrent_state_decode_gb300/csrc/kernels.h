@@ -24,6 +24,8 @@ struct M2Args {
   const float *dt, *A, *D;
   void* y;
   int32_t* status;
+  const int32_t* slots;  // [Bt] state row of each batch row (-1: padding), or null: row b uses state row b
+  int Sn;                // state rows (the leading dimension of ckpt, ckpt_read, the ring and the cursors)
 };
 
 enum { M2_CONVENTIONAL = 0, M2_STEP = 1, M2_FLUSH = 2, M2_VERIFY = 3 };
@@ -54,6 +56,8 @@ struct GdnArgs {
   const float *g, *beta;
   void* o;
   int32_t* status;
+  const int32_t* slots;  // as in M2Args
+  int Sn;
 };
 
 enum { GDN_CONVENTIONAL = 0, GDN_STEP = 1, GDN_FLUSH = 2, GDN_PRIME = 3 };
@@ -72,8 +76,9 @@ cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st
 // Cursor kernels (one thread per sequence).
 enum { CUR_AR = 0, CUR_FLUSH = 1, CUR_COMMIT = 2 };
 
+// `slots` (or null): cursor of batch row b is slots[b] of n_state (-1 skipped).
 cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status,
-                          cudaStream_t st);
+                          cudaStream_t st, const int32_t* slots = nullptr, int n_state = 0);
 cudaError_t reset_launch(int32_t* cursors, const int32_t* slots, int n_slots, int batch, int32_t* status,
                          cudaStream_t st);
 cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, bool f16, cudaStream_t st);

@@ -25,6 +25,8 @@
 // ring slot. The last of a sequence's blocks to have read its cursor advances
 // it (an arrival count in the high half of the cursor's flags word), so the
 // step needs no second kernel.
+#include <type_traits>
+
 #include "fast_rows.cuh"
 #include "kernels.h"
 
@@ -37,7 +39,8 @@ using namespace fastrows;
 constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 
 // RD16: the block reads the bf16 read copy (16 KiB tiles, eight blocks per SM).
-template <bool OUT_BF16, bool RD16>
+// SLOTS: batch rows name their state rows through a slot table.
+template <bool OUT_BF16, bool RD16, bool SLOTS>
 __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
   __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
@@ -50,19 +53,23 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int L = a.L, P = a.P, H = a.H;
   const int g = h >> a.hpg_log2;  // H / G heads per group, a power of two on this path
-  const int bh = b * H + h, bg = b * a.G + g;
+  // the batch row's state slot; a padding row (or a reported bad slot) leaves at once
+  const int sb = SLOTS ? state_slot(a.slots, a.Sn, b, a.status, pb == 0 && h == 0 && threadIdx.x == 0) : b;
+  if (SLOTS && sb < 0) return;
+  const int bh = b * H + h, bg = b * a.G + g;    // the record's rows (x, z, B, C, dt, y)
+  const int sh = sb * H + h, sg = sb * a.G + g;  // the state's rows (checkpoint, ring, cursor)
   const int p0 = pb * FPB;
   // a bf16 read copy is present (known at compile time only in the read-copy instantiation; the
   // fp32 one keeps the run-time test, which measured faster there)
   const bool copy = RD16 || a.ckpt_read != nullptr;
-  const size_t tbase = ((size_t)bh * P + p0) * FN;  // element offset of the block's row 0
+  const size_t tbase = ((size_t)sh * P + p0) * FN;  // element offset of the block's row 0
 
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
     if (copy && a.read_f8) {  // e4m3 rows, then their 64 scales after them
       const uint8_t* q = reinterpret_cast<const uint8_t*>(a.ckpt_read);
-      const float* scales = reinterpret_cast<const float*>(q + (size_t)a.Bt * H * P * FN);
+      const float* scales = reinterpret_cast<const float*>(q + (size_t)a.Sn * H * P * FN);
       mbar_arrive_expect_tx(&bar, FPB * FN + FPB * 4);
       bulk_load(tile, q + tbase, FPB * FN, &bar);
       bulk_load(reinterpret_cast<uint8_t*>(tile) + FPB * FN, scales + tbase / FN, FPB * 4, &bar);
@@ -73,15 +80,15 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
     }
   }
   // everything else, at launch: cursor, window records, current record, gate
-  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's two row groups (within the block)
   const int rA = p0 + rl0, rB2 = p0 + rl1;          // ... within the head
   const size_t xrow = (size_t)bh * P;
-  const float dts = lane < L ? a.rdt[(size_t)bh * pad4(L) + lane] : 0.f;
+  const float dts = lane < L ? a.rdt[(size_t)sh * pad4(L) + lane] : 0.f;
   const float dtc = a.dt[bh], Ah = a.A[h], Dh = a.D[h];
   uint4 xsA = make_uint4(0, 0, 0, 0), xsB = xsA;
   if (lane < L) {
-    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P;
+    const uint16_t* xp = a.rx + ((size_t)sh * L + lane) * P;
     xsA = ldg16(xp + rA);
     xsB = ldg16(xp + rB2);
   }
@@ -92,7 +99,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   const uint2 braw = *reinterpret_cast<const uint2*>(a.B + (size_t)bg * FN + lane * 4);
   const float4 cm = bf4_to_f4(craw);
   {  // c_s = B_s . C for slots s = warp + 4 i (s == L: the current record)
-    const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
+    const uint16_t* rBp = a.rB + (size_t)sg * L * FN + lane * 4;
     const float4 bc = bf4_to_f4(braw);
     float pk[KW];
 #pragma unroll
@@ -107,9 +114,9 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   const int nblocks = a.H * a.nPB;  // blocks of this sequence
   if (!valid) {  // uniform over the block; the last block of the sequence reports it
     if (threadIdx.x == 0) {
-      const int ticket = cursor_ticket(a.cursors, b);
+      const int ticket = cursor_ticket(a.cursors, sb);
       mbar_wait(&bar, 0);  // the copy lands before the block leaves
-      finish_ar_cursor(a.cursors, b, cur, ticket, nblocks, L, a.status);
+      finish_ar_cursor(a.cursors, sb, cur, ticket, nblocks, L, a.status);
     }
     return;
   }
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   __syncthreads();
   int ticket = 0;
   if (threadIdx.x == 0) {  // every thread has read the cursor
-    ticket = cursor_ticket(a.cursors, b);
+    ticket = cursor_ticket(a.cursors, sb);
     scur = cur;
   }
   const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? Dh : 0.f) : 0.f;
@@ -146,14 +153,14 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   // reads it for a result; this block's own loads of it are consumed above).
   if (!flush) {  // x, z rows of this warp's groups; dt, B, C once
     const int slot = start + count < L ? start + count : start + count - L;
-    const size_t rrow = ((size_t)bh * L + slot) * P;
+    const size_t rrow = ((size_t)sh * L + slot) * P;
     if (lane == 0) *reinterpret_cast<uint4*>(a.rx + rrow + rA) = xcA;
     if (lane == 1) *reinterpret_cast<uint4*>(a.rx + rrow + rB2) = xcB;
     if (lane == 2 || lane == 3) *reinterpret_cast<uint4*>(a.rz + rrow + (lane == 3 ? rB2 : rA)) = zap;
     if (warp == 0 && pb == 0) {
-      if (lane == 4) a.rdt[(size_t)bh * pad4(L) + slot] = dtc;
+      if (lane == 4) a.rdt[(size_t)sh * pad4(L) + slot] = dtc;
       if (h == (g << a.hpg_log2)) {  // the group's first head
-        const size_t brow = ((size_t)bg * L + slot) * FN + lane * 4;
+        const size_t brow = ((size_t)sg * L + slot) * FN + lane * 4;
         *reinterpret_cast<uint2*>(a.rB + brow) = braw;
         *reinterpret_cast<uint2*>(a.rC + brow) = craw;
       }
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
   if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     mbar_wait(&bar, 0);
-    if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, scur, ticket, nblocks, L, a.status);
+    if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
     return;
   }
   // A block that reads the bf16 copy folds from the fp32 rows in global memory.
@@ -196,11 +203,11 @@ __global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a
     for (int rr = 0; rr < 8; rr++) tx[rr] = coef * xl[rr];  // coef = 0 off the window; x finite there
     gate_store<OUT_BF16>(a, xrow + p0 + rl, half ? gB : gA, rows8(hv, pc, tx, lane), lane);
     if (flush) {
-      fold8(a, hv, Pm, wk, xl, m, count, start, bg, tbase + (size_t)rl * FN + lane * 4, lane);
+      fold8(a, hv, Pm, wk, xl, m, count, start, sg, bg, tbase + (size_t)rl * FN + lane * 4, lane);
     }
   }
 
-  if (threadIdx.x == 0) finish_ar_cursor(a.cursors, b, scur, ticket, nblocks, L, a.status);
+  if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
 }
 
 }  // namespace
@@ -213,8 +220,12 @@ bool m2_step_fast_applies(const M2Args& a) {
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
   const dim3 grid(a.nPB, a.H, a.Bt);
   const bool rd16 = a.ckpt_read != nullptr;
-  auto k = rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true> : m2_step_fast_kernel<false, true>)
-                : (out_bf16 ? m2_step_fast_kernel<true, false> : m2_step_fast_kernel<false, false>);
+  auto pick = [&](auto slots) {
+    constexpr bool S = decltype(slots)::value;
+    return rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true, S> : m2_step_fast_kernel<false, true, S>)
+                : (out_bf16 ? m2_step_fast_kernel<true, false, S> : m2_step_fast_kernel<false, false, S>);
+  };
+  auto k = a.slots ? pick(std::true_type{}) : pick(std::false_type{});
   const int smem = rd16 ? FPB * FN * 2 : 0;
   // six 32 KiB (eight 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -47,7 +47,8 @@ constexpr int EW = 8;    // B.C entries per warp: 4 warps x 8 = 32 >= L + K
 // new records' B, C (group rows) and dt to the ring and set pending = K, flags
 // = folded; otherwise report as the cursor checks do and leave it (clearing
 // the arrival count in the high half of the flags word).
-__device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur, int flags) {
+// Batch row b's records go to the ring rows of its state slot sb.
+__device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int sb, int4 cur, int flags) {
   const int L = a.L, H = a.H, G = a.G, K = a.K, tid = threadIdx.x;
   int4 c = cur;
   c.w = flags;
@@ -59,7 +60,7 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
   if (err) {
     if (tid == 0) {
       report(a.status, err);
-      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)sb) = c;
     }
     return;
   }
@@ -70,7 +71,7 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
     slot = slot < L ? slot : slot - L;
     slot = slot < L ? slot : slot - L;
     const size_t src = (((size_t)b * K + i) * G + g) * FN + v * 8;
-    const size_t dst = (((size_t)b * G + g) * L + slot) * FN + v * 8;
+    const size_t dst = (((size_t)sb * G + g) * L + slot) * FN + v * 8;
     *reinterpret_cast<uint4*>(a.rB + dst) = ldg16(a.B + src);
     *reinterpret_cast<uint4*>(a.rC + dst) = ldg16(a.C + src);
   }
@@ -79,12 +80,12 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int4 cur
     int slot = c.x + c.y + i;
     slot = slot < L ? slot : slot - L;
     slot = slot < L ? slot : slot - L;
-    a.rdt[((size_t)b * H + h) * pad4(L) + slot] = a.dt[((size_t)b * K + i) * H + h];
+    a.rdt[((size_t)sb * H + h) * pad4(L) + slot] = a.dt[((size_t)b * K + i) * H + h];
   }
   if (tid == 0) {
     c.z = K;
     c.w = (c.y + K > L) ? 1 : 0;
-    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)sb) = c;
   }
 }
 
@@ -110,7 +111,8 @@ __device__ __forceinline__ void state_rows(const float* tile, const float* gstat
   }
 }
 
-template <bool OUT_BF16>
+// SLOTS: batch rows name their state rows through a slot table.
+template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;                                                  // the block's rows (fp32, or bf16)
@@ -123,10 +125,13 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int L = a.L, P = a.P, H = a.H, G = a.G, K = a.K;
   const int g = h >> a.hpg_log2;  // H / G heads per group, a power of two on this path
-  const int bh = b * H + h, bg = b * G + g;
+  // the batch row's state slot; a padding row (or a reported bad slot) leaves at once
+  const int sb = SLOTS ? state_slot(a.slots, a.Sn, b, a.status, pb == 0 && h == 0 && threadIdx.x == 0) : b;
+  if (SLOTS && sb < 0) return;
+  const int sh = sb * H + h, sg = sb * G + g;  // the state's rows (checkpoint, ring, cursor)
   const int p0 = pb * FPB;
   const bool copy = a.ckpt_read != nullptr;
-  const size_t tbase = ((size_t)bh * P + p0) * FN;
+  const size_t tbase = ((size_t)sh * P + p0) * FN;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -138,15 +143,15 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
                                          : (const void*)(a.ckpt_read + tbase));
     bulk_load(tile, src, bytes, &bar);
   }
-  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * b);
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;
   const int qg = lane >> 2, qt = lane & 3;  // tensor-core fragment coordinates
   const int rA = rl0 + qg, rB = rl1 + qg;   // rows of this lane's accumulator fragments (within the block)
   // ring slot `lane`
-  const float dts = lane < L ? a.rdt[(size_t)bh * pad4(L) + lane] : 0.f;
+  const float dts = lane < L ? a.rdt[(size_t)sh * pad4(L) + lane] : 0.f;
   uint4 xsA = make_uint4(0, 0, 0, 0), xsB = xsA, xnA = xsA, xnB = xsA;
   if (lane < L) {
-    const uint16_t* xp = a.rx + ((size_t)bh * L + lane) * P + p0;
+    const uint16_t* xp = a.rx + ((size_t)sh * L + lane) * P + p0;
     xsA = ldg16(xp + rl0);
     xsB = ldg16(xp + rl1);
   }
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   if (warp < 2) {
     const int e0 = 16 * warp + qg, e1 = e0 + 8;
     auto row_of = [&](int e) -> const uint16_t* {
-      if (e < L) return a.rB + ((size_t)bg * L + e) * FN;
+      if (e < L) return a.rB + ((size_t)sg * L + e) * FN;
       if (e < L + K) return a.B + (((size_t)b * K + (e - L)) * G + g) * FN;
       return nullptr;
     };
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   // Without a fold the epilogue writes free ring slots only: this block is done
   // with what it overwrites (dots, dt) and arrives now; a folding block arrives
   // after its fold.
-  int ticket = (threadIdx.x == 0 && !fold) ? cursor_ticket(a.cursors, b) : 0;
+  int ticket = (threadIdx.x == 0 && !fold) ? cursor_ticket(a.cursors, sb) : 0;
   // Outputs come from the checkpoint and every record since it (the fold only
   // writes the checkpoint): output i = e^{S_a} (h0 . C_i) + sum_{k<=a} cf[i][k] x_k,
   // a = count + i, cf = dt_k e^{S_a - S_k} (B_k . C_i) (+ D on record a).
@@ -261,12 +266,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     return s < L ? s : s - L;
   };
   if (valid && lane < K) {
-    const size_t rrow = ((size_t)bh * L + slot_of(lane)) * P + p0;
+    const size_t rrow = ((size_t)sh * L + slot_of(lane)) * P + p0;
     *reinterpret_cast<uint4*>(a.rx + rrow + rl0) = xnA;
     *reinterpret_cast<uint4*>(a.rx + rrow + rl1) = xnB;
   }
   if (valid && gi < K) {
-    const size_t rrow = ((size_t)bh * L + slot_of(gi)) * P + p0;
+    const size_t rrow = ((size_t)sh * L + slot_of(gi)) * P + p0;
     a.rz[rrow + rl0 + gr] = zbA;
     a.rz[rrow + rl1 + gr] = zbB;
   }
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     }
     if (t16 && a.read_f8) {  // e4m3 rows times their scales (the scale of a row factors out of its dots)
       const float* scales = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(a.ckpt_read) +
-                                                           (size_t)a.Bt * H * P * FN);
+                                                           (size_t)a.Sn * H * P * FN);
       const float sA = scales[tbase / FN + rA], sB = scales[tbase / FN + rB];
       acc[0] *= sA;
       acc[1] *= sA;
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
         unpack8(xq[half], xl);
 #pragma unroll
         for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, hv[rr]);
-        const uint16_t* rBp = a.rB + (size_t)bg * L * FN + lane * 4;
+        const uint16_t* rBp = a.rB + (size_t)sg * L * FN + lane * 4;
         for (int k0 = 0; k0 < count; k0 += 4) {
           float4 bk[4];
 #pragma unroll
@@ -391,12 +396,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   // marks the cursor pending.
   if (fold) {  // uniform: the committed B rows were read by the fold until here
     __syncthreads();
-    if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);
+    if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, sb);
   }
   __syncthreads();
   if (threadIdx.x == 0) last_flags = last_ticket(ticket, a.H * a.nPB) ? (ticket & 0xffff) : -1;
   __syncthreads();
-  if (last_flags >= 0) verify_epilogue(a, b, cur, last_flags);
+  if (last_flags >= 0) verify_epilogue(a, b, sb, cur, last_flags);
 }
 
 }  // namespace
@@ -409,7 +414,8 @@ bool m2_verify_fast_applies(const M2Args& a) {
 
 cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
   const dim3 grid(a.nPB, a.H, a.Bt);
-  auto k = out_bf16 ? m2_verify_fast_kernel<true> : m2_verify_fast_kernel<false>;
+  auto k = a.slots ? (out_bf16 ? m2_verify_fast_kernel<true, true> : m2_verify_fast_kernel<false, true>)
+                   : (out_bf16 ? m2_verify_fast_kernel<true, false> : m2_verify_fast_kernel<false, false>);
   const int smem = FPB * FN * 4 + (a.L + a.K) * FPB * 2;  // tile + the records' x rows
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);

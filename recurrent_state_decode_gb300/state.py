@@ -13,7 +13,11 @@ class Mamba2State:
     """Checkpoint (+ optional read copy: read_copy True or "bf16" for bf16,
     "f16" for fp16, "f8" for e4m3 with one fp32 scale per state row), ring
     buffer, cursors and a device status word for one Mamba-2 layer of
-    `batch` sequences."""
+    `batch` sequences.
+
+    The decode calls take an optional ``slots`` (int32 [rows] on the device):
+    batch row r then uses state row slots[r] of this object's ``batch`` rows
+    (-1: a padding row, skipped), and records / outputs have ``rows`` rows."""
 
     def __init__(self, batch, nheads, headdim, dstate, ngroups, buf_len, device="cuda",
                  read_copy=False, out_dtype=bd.RSSM_F32):
@@ -46,15 +50,23 @@ class Mamba2State:
     def y_dtype(self):
         return torch.bfloat16 if self.out_dtype == bd.RSSM_BF16 else torch.float32
 
-    def new_output(self, n_new=0):
-        shape = (self.batch, self.nheads, self.headdim) if n_new == 0 else (self.batch, n_new, self.nheads, self.headdim)
+    def new_output(self, n_new=0, rows=None):
+        rows = self.batch if rows is None else rows
+        shape = (rows, self.nheads, self.headdim) if n_new == 0 else (rows, n_new, self.nheads, self.headdim)
         return torch.empty(shape, dtype=self.y_dtype, device=self.ckpt.device)
+
+    def slot_desc(self, slots):
+        """The descriptor of a call whose batch rows use state rows ``slots``."""
+        d = self.desc
+        return bd.mamba2_desc(slots.numel(), d.nheads, d.headdim, d.dstate, d.ngroups, d.buf_len, d.out_dtype,
+                              d.read_dtype, state_slots=slots, n_slots=self.batch)
 
     def downcast(self, stream=None):
         bd.check(bd.rssm_mamba2_downcast(self.desc, self.ckpt, self.ckpt_read, stream), "rssm_mamba2_downcast")
 
-    def step(self, rec, A, D, y, stream=None):
-        bd.check(bd.rssm_mamba2_step(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors,
+    def step(self, rec, A, D, y, stream=None, slots=None):
+        desc = self.desc if slots is None else self.slot_desc(slots)
+        bd.check(bd.rssm_mamba2_step(desc, self.ckpt, self.ckpt_read, self.ring, self.cursors,
                                      rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
                                      self.status, stream), "rssm_mamba2_step")
 
@@ -62,23 +74,33 @@ class Mamba2State:
         bd.check(bd.rssm_mamba2_flush(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors, A,
                                       self.status, stream), "rssm_mamba2_flush")
 
-    def verify(self, rec, A, D, y, stream=None):
+    def verify(self, rec, A, D, y, stream=None, slots=None):
         n_new = rec["x"].shape[1]
-        bd.check(bd.rssm_mamba2_spec_verify(self.desc, n_new, self.ckpt, self.ckpt_read, self.ring, self.cursors,
+        desc = self.desc if slots is None else self.slot_desc(slots)
+        bd.check(bd.rssm_mamba2_spec_verify(desc, n_new, self.ckpt, self.ckpt_read, self.ring, self.cursors,
                                             rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
                                             self.status, stream), "rssm_mamba2_spec_verify")
 
-    def commit(self, kept, stream=None):
-        bd.check(bd.rssm_commit_cursors(self.cursors, kept, self.batch, self.buf_len, self.status, stream),
-                 "rssm_commit_cursors")
+    def commit(self, kept, stream=None, slots=None):
+        _commit(self, kept, stream, slots)
 
     def reset(self, slots, stream=None):
         bd.check(bd.rssm_reset_cursors(self.cursors, slots, slots.numel(), self.batch, self.status, stream),
                  "rssm_reset_cursors")
 
 
+def _commit(st, kept, stream, slots):
+    if slots is None:
+        bd.check(bd.rssm_commit_cursors(st.cursors, kept, st.batch, st.buf_len, st.status, stream),
+                 "rssm_commit_cursors")
+    else:
+        bd.check(bd.rssm_commit_cursors_slots(st.cursors, kept, slots, slots.numel(), st.batch, st.buf_len,
+                                              st.status, stream), "rssm_commit_cursors_slots")
+
+
 class GDNState:
-    """Checkpoint S, ring buffer, cursors and status word for one Gated DeltaNet layer."""
+    """Checkpoint S, ring buffer, cursors and status word for one Gated DeltaNet
+    layer; ``slots`` on the decode calls as in Mamba2State."""
 
     def __init__(self, batch, nheads, dk, dv, buf_len, device="cuda", out_dtype=bd.RSSM_F32):
         self.batch, self.nheads, self.dk, self.dv, self.buf_len = batch, nheads, dk, dv, buf_len
@@ -100,29 +122,37 @@ class GDNState:
     def o_dtype(self):
         return torch.bfloat16 if self.out_dtype == bd.RSSM_BF16 else torch.float32
 
-    def new_output(self):
-        return torch.empty((self.batch, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
+    def new_output(self, rows=None):
+        rows = self.batch if rows is None else rows
+        return torch.empty((rows, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
 
-    def step(self, rec, o, stream=None):
-        bd.check(bd.rssm_gdn_step(self.desc, self.S, self.ring, self.cursors, rec["q"], rec["k"], rec["v"],
+    def slot_desc(self, slots):
+        d = self.desc
+        return bd.gdn_desc(slots.numel(), d.nheads, d.dk, d.dv, d.buf_len, d.out_dtype, state_slots=slots,
+                           n_slots=self.batch)
+
+    def step(self, rec, o, stream=None, slots=None):
+        desc = self.desc if slots is None else self.slot_desc(slots)
+        bd.check(bd.rssm_gdn_step(desc, self.S, self.ring, self.cursors, rec["q"], rec["k"], rec["v"],
                                   rec["g"], rec["beta"], o, self.status, stream), "rssm_gdn_step")
 
     def flush(self, stream=None):
         bd.check(bd.rssm_gdn_flush(self.desc, self.S, self.ring, self.cursors, self.status, stream),
                  "rssm_gdn_flush")
 
-    def new_verify_output(self, n_new):
-        return torch.empty((self.batch, n_new, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
+    def new_verify_output(self, n_new, rows=None):
+        rows = self.batch if rows is None else rows
+        return torch.empty((rows, n_new, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
 
-    def verify(self, rec, o, stream=None):
+    def verify(self, rec, o, stream=None, slots=None):
         """rec: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g,beta [Bt,K,H] fp32; o [Bt,K,H,dv]."""
-        bd.check(bd.rssm_gdn_spec_verify(self.desc, rec["q"].shape[1], self.S, self.ring, self.cursors, rec["q"],
+        desc = self.desc if slots is None else self.slot_desc(slots)
+        bd.check(bd.rssm_gdn_spec_verify(desc, rec["q"].shape[1], self.S, self.ring, self.cursors, rec["q"],
                                          rec["k"], rec["v"], rec["g"], rec["beta"], o, self.status, stream),
                  "rssm_gdn_spec_verify")
 
-    def commit(self, kept, stream=None):
-        bd.check(bd.rssm_commit_cursors(self.cursors, kept, self.batch, self.buf_len, self.status, stream),
-                 "rssm_commit_cursors")
+    def commit(self, kept, stream=None, slots=None):
+        _commit(self, kept, stream, slots)
 
     def prime(self, stream=None):
         """Fill the ring's corrections e for records placed into the window directly."""

@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 17
+    assert len(declared) == 18
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -45,7 +45,7 @@ def test_header_compiles_as_c(tmp_path):
 
 
 def test_status_strings(lib):
-    assert bd.rssm_version() == 100
+    assert bd.rssm_version() == 200
     for code in (0, -1, -2, -3, -4, 1, 2, 3, 4, 5, 6):
         assert bd.status_string(code) != "unknown status code"
     assert bd.status_string(999) == "unknown status code"
@@ -163,6 +163,51 @@ def test_gdn_validation(lib):
         bd.RSSM_ERR_INVALID_ARG
     assert lib.rssm_gdn_prime(ctypes.byref(d), ALIGNED, None, ALIGNED, None, None) == bd.RSSM_ERR_INVALID_ARG
     assert lib.rssm_gdn_prime(ctypes.byref(d0), None, None, None, None, None) == bd.RSSM_OK
+
+
+def test_state_slot_host_checks(lib):
+    """State slots: ring sizes follow n_slots; calls outside the shape-specialised
+    decode kernels reject a slot table; n_slots is range-checked. Every case
+    returns before any launch."""
+    d = bd.mamba2_desc(4, 8, 64, 128, 1, 16, state_slots=ALIGNED, n_slots=10)
+    assert bd.rssm_mamba2_ring_bytes(d)[0] == 10 * 8 * 16 * 64 * 2
+    g = bd.gdn_desc(4, 2, 128, 128, 16, state_slots=ALIGNED, n_slots=7)
+    assert bd.rssm_gdn_ring_bytes(g)[5] == 7 * 2 * 16 * 128 * 4
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    rb = ctypes.byref(ring)
+    generic = bd.mamba2_desc(4, 8, 48, 64, 1, 16, state_slots=ALIGNED, n_slots=8)  # not dstate 128
+    assert lib.rssm_mamba2_step(ctypes.byref(generic), ALIGNED, None, rb, *ARGS9, None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_mamba2_spec_verify(ctypes.byref(generic), 2, ALIGNED, None, rb, *ARGS9, None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_mamba2_spec_verify(ctypes.byref(d), 8, ALIGNED, None, rb, *ARGS9, None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED  # K > 4: the persistent verify takes no slot table
+    assert lib.rssm_mamba2_flush(ctypes.byref(d), ALIGNED, None, rb, ALIGNED, ALIGNED, None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_mamba2_conventional_step(ctypes.byref(d), *([ALIGNED] * 9), None) == bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_mamba2_downcast(ctypes.byref(d), ALIGNED, ALIGNED, None) == bd.RSSM_ERR_UNSUPPORTED
+    for n_slots, rc in ((-1, bd.RSSM_ERR_INVALID_ARG), (70000, bd.RSSM_ERR_UNSUPPORTED)):
+        bad = bd.mamba2_desc(4, 8, 64, 128, 1, 16, state_slots=ALIGNED, n_slots=n_slots)
+        assert lib.rssm_mamba2_step(ctypes.byref(bad), ALIGNED, None, rb, *ARGS9, None, None) == rc
+        badg = bd.gdn_desc(4, 2, 128, 128, 16, state_slots=ALIGNED, n_slots=n_slots)
+        assert lib.rssm_gdn_flush(ctypes.byref(badg), ALIGNED, None, ALIGNED, None, None) == rc
+    gring = bd.rssm_gdn_ring(*([ALIGNED] * 6))
+    g64 = bd.gdn_desc(4, 2, 64, 128, 16, state_slots=ALIGNED, n_slots=8)  # not dk = dv = 128
+    assert lib.rssm_gdn_step(ctypes.byref(g64), ALIGNED, ctypes.byref(gring), *([ALIGNED] * 7), None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_gdn_spec_verify(ctypes.byref(g64), 2, ALIGNED, ctypes.byref(gring), *([ALIGNED] * 7), None,
+                                    None) == bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_gdn_flush(ctypes.byref(g), ALIGNED, ctypes.byref(gring), ALIGNED, None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_gdn_prime(ctypes.byref(g), ALIGNED, ctypes.byref(gring), ALIGNED, None, None) == \
+        bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_gdn_conventional_step(ctypes.byref(g), *([ALIGNED] * 8), None) == bd.RSSM_ERR_UNSUPPORTED
+    # commit with slots
+    assert lib.rssm_commit_cursors_slots(ALIGNED, ALIGNED, None, 4, 8, 16, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_commit_cursors_slots(ALIGNED, ALIGNED, ALIGNED, 4, -1, 16, None, None) == \
+        bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_commit_cursors_slots(ALIGNED, ALIGNED, ALIGNED, 4, 8, 0, None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_commit_cursors_slots(None, None, None, 0, 8, 16, None, None) == bd.RSSM_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
