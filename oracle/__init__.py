@@ -29,6 +29,8 @@ the replay (unrolled) forms follow from them by algebra. Modules:
 * ``mamba2``  -- conventional recurrence (the reference result) and the
   unrolled replay formula.
 * ``gdn``     -- the same for Gated DeltaNet.
+* ``kda``     -- the same for Kimi Delta Attention (the gated delta rule with
+  a decay per key channel; the pages name the layer and give no equation).
 * ``cursors`` -- integer model of the ring-buffer cursors.
 * ``sessions`` -- drivers that run whole decode sessions (AR and speculative)
   with the conventional recurrence and the cursor model, producing every

@@ -15,6 +15,7 @@ import numpy as np
 
 from . import cursors as cur
 from . import gdn
+from . import kda
 from . import mamba2
 
 
@@ -209,3 +210,38 @@ def gdn_spec_session(S0, prefill, starts, counts, verifies, kepts, L):
             cs[b] = nc
         yield {"o": o, "folded": folded, "committed_state": committed,
                "cursors_verify": cv, "cursors_commit": np.array(cs, np.int64), "state": S}
+
+
+# ----------------------------------------------------------------------------- Kimi Delta Attention
+
+def _kda_step(S, r):
+    return kda.conventional_step(S, _f64(r["q"]), _f64(r["k"]), _f64(r["v"]), _f64(r["g"]), _f64(r["beta"]))
+
+
+def kda_prefill(S0, prefill, counts):
+    S = _f64(S0).copy()
+    counts = np.asarray(counts)
+    n = prefill["q"].shape[1] if prefill is not None else 0
+    for j in range(n):
+        mask = j < counts
+        if not mask.any():
+            break
+        Sn, _ = _kda_step(S, _take(prefill, j))
+        S = _where(mask, Sn, S)
+    return S
+
+
+def kda_ar_session(S0, prefill, starts, counts, steps, L):
+    """AR decode for Kimi Delta Attention; records q,k,g [Bt,H,dk], v [Bt,H,dv],
+    beta [Bt,H]. Yields dicts like gdn_ar_session."""
+    S = kda_prefill(S0, prefill, counts)
+    cs = [(int(s), int(c), 0, 0) for s, c in zip(starts, counts)]
+    for rec in steps:
+        S, o = _kda_step(S, rec)
+        flushed = np.zeros(len(cs), bool)
+        for b, c in enumerate(cs):
+            nc, slot, fl, ok = cur.ar_step(c, L)
+            assert ok
+            cs[b] = nc
+            flushed[b] = fl
+        yield {"o": o, "flushed": flushed, "state": S, "cursors": np.array(cs, np.int64)}

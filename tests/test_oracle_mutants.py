@@ -10,8 +10,10 @@ import numpy as np
 import pytest
 
 import oracle.gdn as gdn
+import oracle.kda as kda
 import oracle.mamba2 as mamba2
 import test_oracle_gdn as pins_gdn
+import test_oracle_kda as pins_kda
 import test_oracle_mamba2 as pins_m2
 
 
@@ -104,3 +106,62 @@ def test_replay_weight_mutant_caught(monkeypatch):
     monkeypatch.setattr(mamba2, "replay_weights", _wrong_weights)
     with pytest.raises(AssertionError):
         pins_m2.test_replay_equals_conventional(np.random.default_rng(3), 5)
+
+
+def _kda(variant):
+    def step(S, q, k, v, g, beta):
+        S = np.asarray(S, np.float64)
+        k = np.asarray(k, np.float64)
+        g = np.asarray(g, np.float64)
+        if variant == "scalar_decay":  # one mean decay per head instead of one per channel
+            g = np.repeat(g.mean(axis=-1, keepdims=True), g.shape[-1], axis=-1)
+        alpha = np.exp(-g if variant == "alpha_sign" else g)
+        beta = np.asarray(beta, np.float64)[..., None, None]
+        if variant == "decay_value_side":
+            Sd = alpha[..., :, None] * S
+        else:
+            Sd = S * alpha[..., None, :]
+        write = (1.0 if variant == "no_beta_on_v" else beta) * np.asarray(v, np.float64)[..., :, None] * k[..., None, :]
+        if variant == "decay_after_delta":
+            Sk = np.einsum("...ij,...j->...i", S, k)
+            S_new = (S - beta * Sk[..., :, None] * k[..., None, :]) * alpha[..., None, :] + write
+        elif variant == "erase_not_decayed":
+            Sk = np.einsum("...ij,...j->...i", S, k)
+            S_new = Sd - beta * Sk[..., :, None] * k[..., None, :] + write
+        else:
+            Sdk = np.einsum("...ij,...j->...i", Sd, k)
+            S_new = Sd - beta * Sdk[..., :, None] * k[..., None, :] + write
+        o = np.einsum("...ij,...j->...i", S if variant == "output_from_old" else S_new, np.asarray(q, np.float64))
+        return S_new, o
+    return step
+
+
+@pytest.mark.parametrize("variant", ["alpha_sign", "scalar_decay", "decay_value_side", "decay_after_delta",
+                                     "erase_not_decayed", "no_beta_on_v", "output_from_old"])
+def test_kda_pins_catch(monkeypatch, variant):
+    monkeypatch.setattr(kda, "conventional_step", _kda(variant))
+    with np.errstate(over="ignore", invalid="ignore"):  # a growing mutant may overflow on the strong-decay pin
+        failed = _run_pins(pins_kda)
+    assert failed, f"mutant {variant} passed every KDA pin"
+
+
+def _kda_undecayed_keys(S0, ks, vs, gs, betas):
+    # drops the channel-wise decay of earlier keys in the corrections' coupling terms
+    S0 = np.asarray(S0, np.float64)
+    ks = np.asarray(ks, np.float64)
+    gs = np.asarray(gs, np.float64)
+    m = ks.shape[-2]
+    Gp = np.cumsum(gs, axis=-2)
+    e = np.zeros(vs.shape[:-2] + (m, vs.shape[-1]))
+    for t in range(m):
+        rhs = vs[..., t, :] - np.einsum("...ij,...j->...i", S0, np.exp(Gp[..., t, :]) * ks[..., t, :])
+        for i in range(t):
+            rhs = rhs - np.einsum("...j,...j->...", ks[..., i, :], ks[..., t, :])[..., None] * e[..., i, :]
+        e[..., t, :] = np.asarray(betas, np.float64)[..., t, None] * rhs
+    return Gp, e
+
+
+def test_kda_replay_mutant_caught(monkeypatch):
+    monkeypatch.setattr(kda, "_window_terms", _kda_undecayed_keys)
+    with pytest.raises(AssertionError):
+        pins_kda.test_replay_equals_conventional(np.random.default_rng(3), 5)
