@@ -2,7 +2,7 @@
 """Benchmark of the ReplaySSM decode path on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mamba2_serving|mamba2_spec|gdn_serving|gdn_spec|mamba2_bf16_read|mamba2_f16_read|mamba2_f8_read|mamba2_tiny]
+                    [--workload mamba2_serving|mamba2_spec|gdn_serving|gdn_spec|kda_serving|mamba2_bf16_read|mamba2_f16_read|mamba2_f8_read|mamba2_tiny]
     python bench.py --mode profile --steps 3 --warmup 1      # a few calls, no timing (for ncu)
 
 A step is one decode step of one layer over the whole batch: one
@@ -400,7 +400,7 @@ def other_workloads(args, dev, out, out_bytes, K, W_, dist, stream):
     from recurrent_state_decode_gb300 import binding as bd
     from recurrent_state_decode_gb300 import bytes_model as bm
     from recurrent_state_decode_gb300 import inputs as I
-    from recurrent_state_decode_gb300.state import gdn_from_workload, mamba2_from_workload
+    from recurrent_state_decode_gb300.state import gdn_from_workload, kda_from_workload, mamba2_from_workload
     peak, _ = measured_peak()
     res = {}
 
@@ -490,6 +490,39 @@ def other_workloads(args, dev, out, out_bytes, K, W_, dist, stream):
     cms, _ = time_calls(conv, K, stream)
     cus = cms * 1e3 / K
     cbytes = bm.gdn_conventional_bytes(w.nheads, w.dk, w.dv, w.batch, out_bytes)
+    res[w.name] = {"us_per_step": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                   "algorithmic_bytes_per_step": nbytes, "conventional_us_per_step": cus,
+                   "conventional_hbm_gbs": cbytes / (cus * 1e-6) / 1e9, "speedup_vs_conventional": cus / us,
+                   "steps": K}
+    del st, recs, S
+    torch.cuda.empty_cache()
+
+    # Kimi Delta Attention AR step vs its conventional kernel
+    w = I.WORKLOADS["kda_serving"]
+    st, _, _, counts0 = kda_from_workload(w, dev, out)
+    recs = [I.kda_step_inputs(w, t, dev) for t in range(W_ + K)]
+    o = st.new_output()
+    for t in range(W_):
+        st.step(recs[t], o)
+    torch.cuda.synchronize()
+    ms, _ = time_calls(lambda i: st.step(recs[W_ + i], o), K, stream)
+    bd.check(int(st.status.item()), "device status")
+    c0 = counts0.cpu().tolist()
+    nbytes = sum(bm.kda_step_bytes(w.nheads, w.dk, w.dv, w.buf_len, [(c + W_ + i) % w.buf_len for c in c0],
+                                   out_bytes) for i in range(K)) / K
+    us = ms * 1e3 / K
+    S = st.S.clone()
+    oc = st.new_output()
+
+    def kconv(i):
+        r = recs[W_ + i]
+        bd.check(bd.rssm_kda_conventional_step(st.desc, S, r["q"], r["k"], r["v"], r["g"], r["beta"], oc))
+
+    kconv(0)
+    torch.cuda.synchronize()
+    cms, _ = time_calls(kconv, K, stream)
+    cus = cms * 1e3 / K
+    cbytes = bm.kda_conventional_bytes(w.nheads, w.dk, w.dv, w.batch, out_bytes)
     res[w.name] = {"us_per_step": us, "hbm_gbs": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
                    "algorithmic_bytes_per_step": nbytes, "conventional_us_per_step": cus,
                    "conventional_hbm_gbs": cbytes / (cus * 1e-6) / 1e9, "speedup_vs_conventional": cus / us,
@@ -595,7 +628,7 @@ def profile_other(args, dist):
 
     from recurrent_state_decode_gb300 import binding as bd
     from recurrent_state_decode_gb300 import inputs as I
-    from recurrent_state_decode_gb300.state import gdn_from_workload, mamba2_from_workload
+    from recurrent_state_decode_gb300.state import gdn_from_workload, kda_from_workload, mamba2_from_workload
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     out = bd.RSSM_BF16 if args.out_dtype == "bf16" else bd.RSSM_F32
@@ -606,6 +639,11 @@ def profile_other(args, dist):
         o = st.new_output()
         for t in range(n):
             st.step(I.gdn_step_inputs(w, t, dev), o)
+    elif args.workload == "kda_serving":
+        st, _, _, _ = kda_from_workload(w, dev, out)
+        o = st.new_output()
+        for t in range(n):
+            st.step(I.kda_step_inputs(w, t, dev), o)
     elif args.workload == "gdn_spec":
         st, _, _, _ = gdn_from_workload(w, dev, out)
         o = st.new_verify_output(w.n_new)
@@ -632,7 +670,7 @@ def main(argv=None):
         else:
             from recurrent_state_decode_gb300 import binding
             binding.load()
-            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec", "gdn_spec"):
+            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec", "gdn_spec", "kda_serving"):
                 res = profile_other(args, dist)
             elif args.workload.startswith("mamba2") and "spec" not in args.workload:
                 res = bench_mamba2_ar(args, dist)

@@ -39,7 +39,7 @@
  *    name the same slot (their state updates would race). State slots are
  *    honoured by the decode calls (step, spec_verify) on the shape-specialised
  *    kernels -- Mamba-2 dstate 128, headdim a multiple of 64, a power-of-two
- *    nheads / ngroups; Gated DeltaNet dk = dv = 128 -- and by
+ *    nheads / ngroups; Gated DeltaNet and KDA dk = dv = 128 -- and by
  *    rssm_commit_cursors_slots; elsewhere a non-NULL state_slots returns
  *    RSSM_ERR_UNSUPPORTED. Calls on whole state arrays (flush, prime,
  *    downcast, conventional steps) take state_slots = NULL with batch = the
@@ -214,7 +214,7 @@ RSSM_API int rssm_mamba2_spec_verify(const rssm_mamba2_desc* desc, int n_new,
                             rssm_stream_t stream);
 
 /* ----------------------------------------------------------------------------
- * Cursors (shared by Mamba-2 and Gated DeltaNet)
+ * Cursors (shared by Mamba-2, Gated DeltaNet and KDA)
  */
 
 /* Commit after a verify ("ReplaySSM", introduction, "Cheap rollback";
@@ -337,6 +337,68 @@ RSSM_API int rssm_gdn_spec_verify(const rssm_gdn_desc* desc, int n_new, float* S
  * counterpart (their windows are only filled by decode steps). Writes ring->e
  * only; sequences with count == 0 or pending != 0 are skipped. */
 RSSM_API int rssm_gdn_prime(const rssm_gdn_desc* desc, const float* S, const rssm_gdn_ring* ring,
+                   const int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Kimi Delta Attention (KDA)
+ *
+ * The gated delta rule with a decay per key channel (the pages name KDA as an
+ * SSM layer in "Why SSM layers slow down hybrid models" and report ReplaySSM
+ * added to a KDA decode kernel in the "ReplaySSM" repository page, section
+ * "Adoption"; the recurrence is the published KDA one). Per (sequence, head),
+ * state S[dv, dk], alpha = exp(g) with g [dk] (g <= 0):
+ *   S = S Diag(alpha) (I - beta k k^T) + beta v k^T;   o = S q
+ * A record is (q, k [dk] bf16; v [dv] bf16; g [dk] fp32; beta fp32). The
+ * descriptor is the Gated DeltaNet one (state slots included).
+ * The replay calls (step, flush, prime) need dk = dv = 128 (else
+ * RSSM_ERR_UNSUPPORTED); the step also needs buf_len <= 31.
+ */
+typedef rssm_gdn_desc rssm_kda_desc;
+
+typedef struct {
+  rssm_bf16* q;  /* [batch, nheads, buf_len, dk] */
+  rssm_bf16* k;  /* [batch, nheads, buf_len, dk] */
+  rssm_bf16* v;  /* [batch, nheads, buf_len, dv] */
+  float* g;      /* [batch, nheads, buf_len, dk]: each record's log decay per channel */
+  float* beta;   /* [batch, nheads, Lp], Lp as in rssm_mamba2_ring.dt */
+  float* e;      /* [batch, nheads, buf_len, dv]: each window record's correction
+                  * e_t = beta_t (v_t - S_{t-1} (alpha_t * k_t)) (see rssm_kda_step) */
+} rssm_kda_ring;
+
+/* Bytes of each ring field, in the order q, k, v, g, beta, e. */
+RSSM_API int rssm_kda_ring_bytes(const rssm_kda_desc* desc, size_t bytes[6]);
+
+/* Conventional step: S [batch, nheads, dv, dk] fp32 updated in place;
+ * q, k [batch, nheads, dk], v [batch, nheads, dv] bf16; g [batch, nheads, dk]
+ * and beta [batch, nheads] fp32; o [batch, nheads, dv] of desc->out_dtype.
+ * Any dk, dv the descriptor allows. */
+RSSM_API int rssm_kda_conventional_step(const rssm_kda_desc* desc, float* S,
+                               const rssm_bf16* q, const rssm_bf16* k,
+                               const rssm_bf16* v, const float* g,
+                               const float* beta, void* o,
+                               rssm_stream_t stream);
+
+/* ReplaySSM AR step for KDA: the protocol of rssm_gdn_step (non-flush steps
+ * write no state; the L-th step folds the window and writes S once; the
+ * cursors advance within the call). With G the per-channel sum of the log
+ * decays from a window record to the current one, a window record's key
+ * enters as k * exp(G) (channel-wise); its correction e_t is fixed from the
+ * step that appends it until the flush that folds it, so the step reads the
+ * window's e from ring->e and appends the current record's.
+ * Records as in rssm_kda_conventional_step. */
+RSSM_API int rssm_kda_step(const rssm_kda_desc* desc, float* S, const rssm_kda_ring* ring,
+                  int32_t* cursors, const rssm_bf16* q, const rssm_bf16* k,
+                  const rssm_bf16* v, const float* g, const float* beta,
+                  void* o, int32_t* dev_status, rssm_stream_t stream);
+
+/* Standalone flush for KDA (as rssm_gdn_flush); folds each window with the
+ * corrections kept in ring->e. */
+RSSM_API int rssm_kda_flush(const rssm_kda_desc* desc, float* S, const rssm_kda_ring* ring,
+                   int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
+
+/* Fills ring->e for windows written into the ring directly (as
+ * rssm_gdn_prime). Writes ring->e only. */
+RSSM_API int rssm_kda_prime(const rssm_kda_desc* desc, const float* S, const rssm_kda_ring* ring,
                    const int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
 
 /* ----------------------------------------------------------------------------

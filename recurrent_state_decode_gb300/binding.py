@@ -51,6 +51,10 @@ class rssm_gdn_ring(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("q", "k", "v", "g", "beta", "e")]
 
 
+rssm_kda_desc = rssm_gdn_desc   # the same struct in rssm.h
+rssm_kda_ring = rssm_gdn_ring   # same fields; g holds one log decay per key channel
+
+
 P = c_void_p
 _SIGNATURES = {
     "rssm_version": (c_int, []),
@@ -71,6 +75,11 @@ _SIGNATURES = {
     "rssm_gdn_flush": (c_int, [P] * 5 + [P]),
     "rssm_gdn_prime": (c_int, [P] * 5 + [P]),
     "rssm_gdn_spec_verify": (c_int, [P, c_int] + [P] * 11),
+    "rssm_kda_ring_bytes": (c_int, [P, P]),
+    "rssm_kda_conventional_step": (c_int, [P] * 8 + [P]),
+    "rssm_kda_step": (c_int, [P] * 11 + [P]),
+    "rssm_kda_flush": (c_int, [P] * 5 + [P]),
+    "rssm_kda_prime": (c_int, [P] * 5 + [P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -245,3 +254,36 @@ def rssm_gdn_spec_verify(desc, n_new, S, ring, cursors, q, k, v, g, beta, o, dev
 
 def rssm_mamba2_downcast(desc, ckpt, ckpt_read, stream=None):
     return load().rssm_mamba2_downcast(_ref(desc), ptr(ckpt), ptr(ckpt_read), _stream(stream, ckpt))
+
+
+def kda_desc(batch, nheads, dk, dv, buf_len, out_dtype=RSSM_F32, state_slots=None, n_slots=0):
+    return gdn_desc(batch, nheads, dk, dv, buf_len, out_dtype, state_slots, n_slots)
+
+
+def kda_ring(q, k, v, g, beta, e):
+    return gdn_ring(q, k, v, g, beta, e)
+
+
+def rssm_kda_ring_bytes(desc):
+    out = (c_size_t * 6)()
+    check(load().rssm_kda_ring_bytes(_ref(desc), out), "rssm_kda_ring_bytes")
+    return list(out)
+
+
+def rssm_kda_conventional_step(desc, S, q, k, v, g, beta, o, stream=None):
+    return load().rssm_kda_conventional_step(
+        _ref(desc), ptr(S), ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), ptr(o), _stream(stream, S))
+
+
+def rssm_kda_step(desc, S, ring, cursors, q, k, v, g, beta, o, dev_status=None, stream=None):
+    return load().rssm_kda_step(
+        _ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), ptr(o),
+        ptr(dev_status), _stream(stream, S))
+
+
+def rssm_kda_flush(desc, S, ring, cursors, dev_status=None, stream=None):
+    return load().rssm_kda_flush(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status), _stream(stream, S))
+
+
+def rssm_kda_prime(desc, S, ring, cursors, dev_status=None, stream=None):
+    return load().rssm_kda_prime(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status), _stream(stream, S))

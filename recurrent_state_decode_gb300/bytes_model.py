@@ -6,7 +6,8 @@ read every step (bf16 read copy on non-flush steps when present) and written
 only on a flush; the current record is read once and appended to the ring;
 past records contribute the fields later steps read (Mamba-2 x, B, dt;
 Gated DeltaNet k, g and the record's cached correction e, dv fp32 -- the
-method keeps e beside each record, so v and beta are not read back); outputs
+method keeps e beside each record, so v and beta are not read back; Kimi
+Delta Attention the same with g one fp32 per key channel); outputs
 are written once; each cursor is read and written (16 + 16 bytes).
 """
 
@@ -98,4 +99,30 @@ def gdn_verify_bytes(H, DK, DV, L, K, counts, out_bytes=2):
 
 def gdn_conventional_bytes(H, DK, DV, batch, out_bytes=2):
     tile, rec, e, past, o = gdn_parts(H, DK, DV, out_bytes)
+    return batch * (2 * tile + rec + o)
+
+
+def kda_parts(H, DK, DV, out_bytes):
+    tile = H * DV * DK * 4
+    rec = H * (2 * DK * 2 + DV * 2 + DK * 4 + 4)       # q, k, v, g (per key channel), beta
+    e = H * DV * 4                                     # a record's cached correction
+    past = H * (DK * 2 + DK * 4) + e                   # k, g, e
+    o = H * DV * out_bytes
+    return tile, rec, e, past, o
+
+
+def kda_step_bytes(H, DK, DV, L, counts, out_bytes=2):
+    tile, rec, e, past, o = kda_parts(H, DK, DV, out_bytes)
+    total = 0
+    for c in counts:
+        if c + 1 == L:
+            total += 2 * tile + rec
+        else:
+            total += tile + 2 * rec + e
+        total += c * past + o + CURSOR
+    return total
+
+
+def kda_conventional_bytes(H, DK, DV, batch, out_bytes=2):
+    tile, rec, e, past, o = kda_parts(H, DK, DV, out_bytes)
     return batch * (2 * tile + rec + o)

@@ -445,4 +445,112 @@ int rssm_gdn_prime(const rssm_gdn_desc* d, const float* S, const rssm_gdn_ring* 
   return cuda_rc(gdn_launch(GDN_PRIME, a, 0, (cudaStream_t)stream));
 }
 
+// ---------------------------------------------------------------- Kimi Delta Attention
+
+int rssm_kda_ring_bytes(const rssm_kda_desc* d, size_t bytes[6]) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (!bytes) return RSSM_ERR_INVALID_ARG;
+  const size_t Bt = state_rows(d), H = d->nheads, L = d->buf_len;
+  bytes[0] = bytes[1] = Bt * H * L * d->dk * 2;
+  bytes[2] = Bt * H * L * d->dv * 2;
+  bytes[3] = Bt * H * L * d->dk * 4;
+  bytes[4] = Bt * H * pad4(d->buf_len) * 4;
+  bytes[5] = Bt * H * L * d->dv * 4;
+  return RSSM_OK;
+}
+
+int rssm_kda_conventional_step(const rssm_kda_desc* d, float* S, const rssm_bf16* q, const rssm_bf16* k,
+                               const rssm_bf16* v, const float* g, const float* beta, void* o,
+                               rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
+  if (d->batch == 0) return RSSM_OK;
+  if ((rc = check_ptrs({S, q, k, v, g, beta, o}))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.S = S;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.o = o;
+  return cuda_rc(kda_launch(GDN_CONVENTIONAL, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
+}
+
+namespace {
+void set_kda_ring(GdnArgs& a, const rssm_kda_ring* r) {
+  a.rq = r->q;
+  a.rk = r->k;
+  a.rv = r->v;
+  a.rg = r->g;
+  a.rbeta = r->beta;
+  a.re = r->e;
+}
+}  // namespace
+
+int rssm_kda_step(const rssm_kda_desc* d, float* S, const rssm_kda_ring* ring, int32_t* cursors, const rssm_bf16* q,
+                  const rssm_bf16* k, const rssm_bf16* v, const float* g, const float* beta, void* o,
+                  int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors, q, k, v, g, beta, o})))
+    return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  if (!kda_step_fast_applies(a)) return RSSM_ERR_UNSUPPORTED;  // dk = dv = 128, L <= 31
+  a.S = S;
+  set_kda_ring(a, ring);
+  a.cursors = cursors;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.o = o;
+  a.status = dev_status;
+  return cuda_rc(kda_launch(GDN_STEP, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));  // cursors advance inside
+}
+
+int rssm_kda_flush(const rssm_kda_desc* d, float* S, const rssm_kda_ring* ring, int32_t* cursors, int32_t* dev_status,
+                   rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->k, ring->g, ring->e, cursors}))) return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  if (!kda_window_applies(a)) return RSSM_ERR_UNSUPPORTED;
+  a.S = S;
+  set_kda_ring(a, ring);
+  a.cursors = cursors;
+  a.status = dev_status;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = cuda_rc(kda_launch(GDN_FLUSH, a, 0, st)))) return rc;
+  return cuda_rc(cursor_launch(CUR_FLUSH, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
+}
+
+int rssm_kda_prime(const rssm_kda_desc* d, const float* S, const rssm_kda_ring* ring, const int32_t* cursors,
+                   int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors}))) return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  if (!kda_window_applies(a)) return RSSM_ERR_UNSUPPORTED;
+  a.S = const_cast<float*>(S);  // read only in this mode
+  set_kda_ring(a, ring);
+  a.cursors = const_cast<int32_t*>(cursors);  // read only in this mode
+  a.status = dev_status;
+  return cuda_rc(kda_launch(GDN_PRIME, a, 0, (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -44,6 +44,20 @@ __device__ __forceinline__ float rows8(const float4 (&hv)[8], float4 pc, const f
   return reduce_transpose<8>(v, lane);
 }
 
+// Two matvecs of 8 rows at once (the delta-rule kernels' S0 k and S0 q): 16
+// partials, [rr] = h[rr] . ka + tk[rr] and [8 + rr] = h[rr] . qa + tq[rr];
+// lane l ends with the total of partial l >> 1.
+__device__ __forceinline__ float rows8x2(const float4 (&hv)[8], float4 ka, float4 qa, const float (&tk)[8],
+                                         const float (&tq)[8], int lane) {
+  float v[16];
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) {
+    v[rr] = fmaf(hv[rr].x, ka.x, fmaf(hv[rr].y, ka.y, fmaf(hv[rr].z, ka.z, fmaf(hv[rr].w, ka.w, tk[rr]))));
+    v[8 + rr] = fmaf(hv[rr].x, qa.x, fmaf(hv[rr].y, qa.y, fmaf(hv[rr].z, qa.z, fmaf(hv[rr].w, qa.w, tq[rr]))));
+  }
+  return reduce_transpose<16>(v, lane);
+}
+
 __device__ __forceinline__ int row_src(int rr) {
   return ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
 }

@@ -44,19 +44,6 @@ constexpr int ES = FPB + 4;  // floats per staged e row (padded against bank con
 
 __device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// 16 partials for 8 rows: [rr] = h[rr] . ka + tk[rr], [8 + rr] = h[rr] . qa + tq[rr].
-// Lane l ends with partial l >> 1.
-__device__ __forceinline__ float rows8x2(const float4 (&hv)[8], float4 ka, float4 qa, const float (&tk)[8],
-                                         const float (&tq)[8], int lane) {
-  float v[16];
-#pragma unroll
-  for (int rr = 0; rr < 8; rr++) {
-    v[rr] = fmaf(hv[rr].x, ka.x, fmaf(hv[rr].y, ka.y, fmaf(hv[rr].z, ka.z, fmaf(hv[rr].w, ka.w, tk[rr]))));
-    v[8 + rr] = fmaf(hv[rr].x, qa.x, fmaf(hv[rr].y, qa.y, fmaf(hv[rr].z, qa.z, fmaf(hv[rr].w, qa.w, tq[rr]))));
-  }
-  return reduce_transpose<16>(v, lane);
-}
-
 // SLOTS: batch rows name their state rows through a slot table.
 template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {

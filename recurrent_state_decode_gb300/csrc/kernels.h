@@ -73,6 +73,15 @@ cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st
 bool gdn_step_fast_applies(const GdnArgs& a);
 cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
 
+// Kimi Delta Attention (kda.cu, kda_step_fast.cu) takes GdnArgs with g, rg
+// holding one log decay per key channel: g [Bt, H, DK], rg [Bt, H, L, DK].
+// GDN_CONVENTIONAL, GDN_STEP, GDN_FLUSH and GDN_PRIME name its kernels too.
+cudaError_t kda_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st);
+// The replay kernels' shapes: dk = dv = 128 (the step also L <= 31).
+bool kda_window_applies(const GdnArgs& a);
+bool kda_step_fast_applies(const GdnArgs& a);
+cudaError_t kda_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
+
 // Cursor kernels (one thread per sequence).
 enum { CUR_AR = 0, CUR_FLUSH = 1, CUR_COMMIT = 2 };
 

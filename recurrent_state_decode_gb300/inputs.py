@@ -12,6 +12,9 @@ own. Distributions (per workload):
 * Gated DeltaNet records: q, k ~ N(0, 1), L2-normalised per head in fp32,
   then bf16; v ~ N(0, 1) in bf16; g = -softplus(N(0, 1)); beta =
   sigmoid(N(0, 1)), fp32.
+* Kimi Delta Attention records: q, k, v, beta as for Gated DeltaNet; g per
+  key channel = -softplus(N(-1, 1.5)), fp32 (a spread of slow and fast
+  channels: per-token decay from about 0.99 down to about 0.05).
 * Checkpoint: zero (the tiny workload) or 0.1 * N(0, 1) in fp32.
 * Initial window: per sequence a start slot and a fill count ~ U{0..L-1}
   (so flushes are staggered across the batch), the filled records drawn
@@ -75,6 +78,12 @@ class GDNWorkload:
         return self.drafts + 1
 
 
+@dataclass(frozen=True)
+class KDAWorkload(GDNWorkload):
+    """A Kimi Delta Attention workload: the Gated DeltaNet fields, records with
+    one log decay per key channel."""
+
+
 WORKLOADS = {
     "mamba2_tiny": Mamba2Workload("mamba2_tiny", 4, 8, 64, 128, 1, 16, 64, seed=1000, zero_ckpt=True, prefill=False),
     "mamba2_serving": Mamba2Workload("mamba2_serving", 256, 128, 64, 128, 8, 16, 256, seed=1001),
@@ -84,6 +93,7 @@ WORKLOADS = {
     "mamba2_f16_read": Mamba2Workload("mamba2_f16_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy="f16"),
     "mamba2_f8_read": Mamba2Workload("mamba2_f8_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy="f8"),
     "gdn_spec": GDNWorkload("gdn_spec", 512, 32, 128, 128, 16, 128, seed=1005, drafts=3),
+    "kda_serving": KDAWorkload("kda_serving", 256, 32, 128, 128, 16, 256, seed=1006),
 }
 
 
@@ -186,6 +196,32 @@ def gdn_verify_inputs(w, t, device):
 
 def gdn_prefill(w, device):
     return gdn_records(w, "prefill", 0, max(w.buf_len - 1, 1), device)
+
+
+# ----------------------------------------------------------------------------- Kimi Delta Attention
+
+def kda_records(w, stream, index, n, device):
+    """q,k [Bt,n,H,dk] bf16 (unit norm before rounding); v [Bt,n,H,dv] bf16;
+    g [Bt,n,H,dk] fp32 (per key channel); beta [Bt,n,H] fp32."""
+    gen = generator(device, w.seed, stream, index)
+    Bt, H = w.batch, w.nheads
+    q = torch.randn((Bt, n, H, w.dk), generator=gen, device=device)
+    k = torch.randn((Bt, n, H, w.dk), generator=gen, device=device)
+    q = (q / q.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn((Bt, n, H, w.dv), generator=gen, device=device).to(torch.bfloat16)
+    g = (-F.softplus(torch.randn((Bt, n, H, w.dk), generator=gen, device=device) * 1.5 - 1.0)).float()
+    beta = torch.sigmoid(torch.randn((Bt, n, H), generator=gen, device=device)).float()
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta}
+
+
+def kda_step_inputs(w, t, device):
+    r = kda_records(w, "step", t, 1, device)
+    return {k: v[:, 0].contiguous() for k, v in r.items()}
+
+
+def kda_prefill(w, device):
+    return kda_records(w, "prefill", 0, max(w.buf_len - 1, 1), device)
 
 
 # ----------------------------------------------------------------------------- ring placement

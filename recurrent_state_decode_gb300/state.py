@@ -160,6 +160,33 @@ class GDNState:
                  "rssm_gdn_prime")
 
 
+class KDAState(GDNState):
+    """Checkpoint S, ring buffer (g with one log decay per key channel), cursors
+    and status word for one Kimi Delta Attention layer."""
+
+    def __init__(self, batch, nheads, dk, dv, buf_len, device="cuda", out_dtype=bd.RSSM_F32):
+        super().__init__(batch, nheads, dk, dv, buf_len, device, out_dtype)
+        self.rg = torch.zeros((batch, nheads, buf_len, dk), dtype=torch.float32, device=self.S.device)
+        self.ring = bd.kda_ring(self.rq, self.rk, self.rv, self.rg, self.rbeta, self.re)
+
+    def step(self, rec, o, stream=None, slots=None):
+        desc = self.desc if slots is None else self.slot_desc(slots)
+        bd.check(bd.rssm_kda_step(desc, self.S, self.ring, self.cursors, rec["q"], rec["k"], rec["v"],
+                                  rec["g"], rec["beta"], o, self.status, stream), "rssm_kda_step")
+
+    def flush(self, stream=None):
+        bd.check(bd.rssm_kda_flush(self.desc, self.S, self.ring, self.cursors, self.status, stream),
+                 "rssm_kda_flush")
+
+    def prime(self, stream=None):
+        """Fill the ring's corrections e for records placed into the window directly."""
+        bd.check(bd.rssm_kda_prime(self.desc, self.S, self.ring, self.cursors, self.status, stream),
+                 "rssm_kda_prime")
+
+    def verify(self, rec, o, stream=None, slots=None):
+        raise NotImplementedError("the KDA layer has no speculative verify in this library")
+
+
 def mamba2_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32, read_copy=None):
     """A Mamba2State at the start of workload ``w`` (see ``inputs``): checkpoint,
     pre-filled windows and cursors; the read copy is downcast if present.
@@ -188,6 +215,21 @@ def gdn_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32):
     st.S.copy_(I.gdn_checkpoint(w, device))
     starts, counts = I.initial_cursors(w, device)
     pre = I.gdn_prefill(w, device)
+    for field, ring in (("q", st.rq), ("k", st.rk), ("v", st.rv), ("g", st.rg), ("beta", st.rbeta)):
+        I.place_window(ring, pre[field], starts, counts, w.buf_len)
+    st.cursors[:, 0] = starts
+    st.cursors[:, 1] = counts
+    st.prime()
+    return st, pre, starts, counts
+
+
+def kda_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32):
+    """A KDAState at the start of workload ``w``. Returns (state, prefill, starts, counts)."""
+    from . import inputs as I
+    st = KDAState(w.batch, w.nheads, w.dk, w.dv, w.buf_len, device, out_dtype=out_dtype)
+    st.S.copy_(I.gdn_checkpoint(w, device))
+    starts, counts = I.initial_cursors(w, device)
+    pre = I.kda_prefill(w, device)
     for field, ring in (("q", st.rq), ("k", st.rk), ("v", st.rv), ("g", st.rg), ("beta", st.rbeta)):
         I.place_window(ring, pre[field], starts, counts, w.buf_len)
     st.cursors[:, 0] = starts

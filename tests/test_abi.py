@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 18
+    assert len(declared) == 23
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -208,6 +208,36 @@ def test_state_slot_host_checks(lib):
         bd.RSSM_ERR_INVALID_ARG
     assert lib.rssm_commit_cursors_slots(ALIGNED, ALIGNED, ALIGNED, 4, 8, 0, None, None) == bd.RSSM_ERR_INVALID_ARG
     assert lib.rssm_commit_cursors_slots(None, None, None, 0, 8, 16, None, None) == bd.RSSM_OK
+
+
+def test_kda_host_checks(lib):
+    """Kimi Delta Attention: ring sizes (g one fp32 per key channel), the replay
+    calls' shape limits and their argument checks; every case returns before a launch."""
+    d = bd.kda_desc(4, 2, 128, 128, 16)
+    assert bd.rssm_kda_ring_bytes(d) == [4 * 2 * 16 * 128 * 2] * 3 + [4 * 2 * 16 * 128 * 4, 4 * 2 * 16 * 4,
+                                                                       4 * 2 * 16 * 128 * 4]
+    ring = bd.rssm_kda_ring(*([ALIGNED] * 6))
+    rb = ctypes.byref(ring)
+    for desc in ((4, 2, 64, 128, 16), (4, 2, 128, 64, 16), (4, 2, 128, 128, 32)):  # dk, dv != 128; L = 32
+        dd = bd.kda_desc(*desc)
+        assert lib.rssm_kda_step(ctypes.byref(dd), ALIGNED, rb, *([ALIGNED] * 7), None, None) == \
+            bd.RSSM_ERR_UNSUPPORTED
+    dd = bd.kda_desc(4, 2, 64, 128, 16)
+    assert lib.rssm_kda_flush(ctypes.byref(dd), ALIGNED, rb, ALIGNED, None, None) == bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_kda_prime(ctypes.byref(dd), ALIGNED, rb, ALIGNED, None, None) == bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_kda_step(ctypes.byref(d), ALIGNED + 4, rb, *([ALIGNED] * 7), None, None) == \
+        bd.RSSM_ERR_MISALIGNED
+    assert lib.rssm_kda_step(ctypes.byref(d), ALIGNED, None, *([ALIGNED] * 7), None, None) == bd.RSSM_ERR_INVALID_ARG
+    no_g = bd.rssm_kda_ring(ALIGNED, ALIGNED, ALIGNED, None, ALIGNED, ALIGNED)
+    assert lib.rssm_kda_flush(ctypes.byref(d), ALIGNED, ctypes.byref(no_g), ALIGNED, None, None) == \
+        bd.RSSM_ERR_INVALID_ARG
+    ds = bd.kda_desc(4, 2, 128, 128, 16, state_slots=ALIGNED, n_slots=8)
+    assert lib.rssm_kda_flush(ctypes.byref(ds), ALIGNED, rb, ALIGNED, None, None) == bd.RSSM_ERR_UNSUPPORTED
+    assert lib.rssm_kda_conventional_step(ctypes.byref(ds), *([ALIGNED] * 8), None) == bd.RSSM_ERR_UNSUPPORTED
+    d0 = bd.kda_desc(0, 2, 128, 128, 16)
+    assert lib.rssm_kda_step(ctypes.byref(d0), None, None, *([None] * 7), None, None) == bd.RSSM_OK
+    assert lib.rssm_kda_conventional_step(ctypes.byref(bd.kda_desc(4, 2, 60, 128, 16)), *([ALIGNED] * 8), None) == \
+        bd.RSSM_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

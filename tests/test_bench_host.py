@@ -72,3 +72,9 @@ def test_bytes_model_serving_cycle():
     v = bm.gdn_verify_bytes(32, 128, 128, 16, 4, [12, 13])
     assert v == (2097152 + 4 * (2 * rec + e) + 12 * past + 4 * 32 * 128 * 2 + 68) + \
         (2 * 2097152 + 4 * (2 * rec + e) + 13 * past + 4 * 32 * 128 * 2 + 68)
+    # KDA serving shape: as GDN, with g one fp32 per key channel in the record and past records
+    kd = sum(bm.kda_step_bytes(32, 128, 128, 16, [c]) for c in range(16)) / 16
+    krec = 32 * (2 * 256 + 256 + 512 + 4)
+    kpast = 32 * (256 + 512) + e
+    assert kd == pytest.approx(2097152 * 17 / 16 + (15 * (2 * krec + e) + krec) / 16 + 7.5 * kpast + 32 * 128 * 2 + 32)
+    assert bm.kda_conventional_bytes(32, 128, 128, 2) == 2 * (2 * 2097152 + krec + 32 * 128 * 2)

@@ -144,6 +144,39 @@ def test_gdn_serving_full_size():
     assert H.status(st) == 0
 
 
+def test_kda_serving_full_size():
+    """Kimi Delta Attention at the bench's size: batch 256, 32 heads, 128x128
+    state, L=16, staggered windows, 256 steps; the cursor trace of the whole
+    batch against the cursor model."""
+    from recurrent_state_decode_gb300.state import kda_from_workload
+    w = I.WORKLOADS["kda_serving"]
+    dev = "cuda"
+    st, pre, starts, counts = kda_from_workload(w, dev, bd.RSSM_BF16)
+    seqs = spread(counts, 3)
+    feed = H.Feed()
+    sess = sessions.kda_ar_session(H.F64(st.S[seqs]), H.sub(pre, seqs), starts[seqs].cpu().numpy(),
+                                   counts[seqs].cpu().numpy(), feed, w.buf_len)
+    cur = [(int(a), int(c), 0, 0) for a, c in zip(starts.tolist(), counts.tolist())]
+    o = st.new_output()
+    flushes = 0
+    for t in range(w.steps):
+        rec = I.kda_step_inputs(w, t, dev)
+        feed.rec = H.sub(rec, seqs)
+        st.step(rec, o)
+        exp = next(sess)
+        assert H.bf16_excess(H.F64(o[seqs]), exp["o"]) <= TOL_BF16_EXCESS, t
+        for i, b in enumerate(seqs):
+            if exp["flushed"][i]:
+                flushes += 1
+                assert H.rel_l2(H.F64(st.S[b]), exp["state"][i]) <= TOL_CKPT, (t, b)
+        cur = [oc.ar_step(c, w.buf_len)[0] for c in cur]
+        if t % 64 == 63:
+            np.testing.assert_array_equal(st.cursors.cpu().numpy(), np.array(cur))
+    assert torch.isfinite(o).all()
+    assert flushes == len(seqs) * (w.steps // w.buf_len)
+    assert H.status(st) == 0
+
+
 def test_gdn_spec_full_size():
     """Gated DeltaNet speculative decode: batch 512, 32 heads, 128x128 state,
     K = 4 records per verify, accepted ~U{0..3}, 128 verify steps, fold on overflow."""
