@@ -100,7 +100,47 @@ __device__ __forceinline__ float4 scale4(float s, float4 a) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// A 16-byte aligned float4 (shared or global memory).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+
+// Eight bf16 values (one uint4) to fp32.
+__device__ __forceinline__ void unpack8(uint4 u, float* f) {
+  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
+}
+
+// Ring slot of s in [0, 2L).
+__device__ __forceinline__ int wrap(int s, int L) { return s < L ? s : s - L; }
+
+// An output element, fp32 or bf16 (round to nearest even).
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_out(void* y, size_t i, float v) {
+  if (OUT_BF16)
+    reinterpret_cast<uint16_t*>(y)[i] = f_to_bf(v);
+  else
+    reinterpret_cast<float*>(y)[i] = v;
+}
+
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+
 // ---------------------------------------------------------------- reductions
+
+// Every lane must call these (full-warp shuffles).
+__device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
+  return make_uint4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
+                    __shfl_sync(FULL, v.w, src));
+}
+
+// Sum over the four lanes of a quad.
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(FULL, v, 1);
+  v += __shfl_xor_sync(FULL, v, 2);
+  return v;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -17,17 +17,6 @@ constexpr int HALF = 32;    // a warp's second row group starts here
 
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
-__device__ __forceinline__ void unpack8(uint4 u, float* f) {
-  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
-  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
-}
-
-// Every lane must call this (a full-warp shuffle).
-__device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
-  return make_uint4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
-                    __shfl_sync(FULL, v.w, src));
-}
-
 // Every lane must call this (a full-warp shuffle).
 __device__ __forceinline__ float4 shfl_f4(float4 v, int src) {
   return make_float4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
@@ -60,14 +49,6 @@ __device__ __forceinline__ float rows8x2(const float4 (&hv)[8], float4 ka, float
 
 __device__ __forceinline__ int row_src(int rr) {
   return ((rr >> 2) & 1) * 16 + ((rr >> 1) & 1) * 8 + (rr & 1) * 4;
-}
-
-template <bool OUT_BF16>
-__device__ __forceinline__ void store_y(void* y, size_t i, float v) {
-  if (OUT_BF16)
-    reinterpret_cast<uint16_t*>(y)[i] = f_to_bf(v);
-  else
-    reinterpret_cast<float*>(y)[i] = v;
 }
 
 // silu(z) = z sigmoid(z)
@@ -111,7 +92,7 @@ __device__ __forceinline__ void finish_ar_cursor(int32_t* cursors, int b, int4 c
 template <bool OUT_BF16>
 __device__ __forceinline__ void gate_store(const M2Args& a, size_t obase, float gate, float tot, int lane) {
   const float t = __shfl_sync(FULL, tot, row_src(lane & 7));
-  if (lane < 8) store_y<OUT_BF16>(a.y, obase + lane, t * gate);
+  if (lane < 8) store_out<OUT_BF16>(a.y, obase + lane, t * gate);
 }
 
 // The read copy (if any) of 8 rows of the state: element offset `off` of row

@@ -40,13 +40,11 @@ struct GdnSmem {
   uint64_t* bars;  // [8]
 };
 
-__host__ __device__ inline size_t gdn_align16(size_t v) { return (v + 15) & ~size_t(15); }
-
 __host__ __device__ inline size_t gdn_smem_layout(int RB, int DK, int L, unsigned char* base, GdnSmem* s) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
-    off = gdn_align16(off + bytes);
+    off = align16(off + bytes);
     return o;
   };
   size_t o_tile = take((size_t)RB * DK * 4), o_ks = take((size_t)L * DK * 4), o_q = take((size_t)DK * 4);
@@ -80,20 +78,6 @@ __device__ __forceinline__ void bf_row_to_smem(float* dst, const uint16_t* src, 
     reinterpret_cast<float4*>(dst + i * 8)[0] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
     reinterpret_cast<float4*>(dst + i * 8)[1] = make_float4(bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w));
   }
-}
-
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(FULL, v, 1);
-  v += __shfl_xor_sync(FULL, v, 2);
-  return v;
-}
-
-template <bool OUT_BF16>
-__device__ __forceinline__ void gdn_store_out(void* o, size_t i, float v) {
-  if (OUT_BF16)
-    reinterpret_cast<uint16_t*>(o)[i] = f_to_bf(v);
-  else
-    reinterpret_cast<float*>(o)[i] = v;
 }
 
 // ------------------------------------------------------------------ conventional
@@ -141,7 +125,7 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_conventional_kernel(GdnArgs a
     }
   }
   o = quad_sum(o);
-  if (active && q4 == 0) gdn_store_out<OUT_BF16>(a.o, bh * DV + row, o);
+  if (active && q4 == 0) store_out<OUT_BF16>(a.o, bh * DV + row, o);
 }
 
 // ------------------------------------------------------------------ replay step / flush
@@ -312,7 +296,7 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
     w = quad_sum(w);
     float o = gm * w;
     for (int t = 0; t < m; t++) o = fmaf(s.oc[t], es_row[(size_t)t * GDN_RB], o);
-    if (q4 == 0) gdn_store_out<OUT_BF16>(a.o, bh * DV + i0 + rloc, o);
+    if (q4 == 0) store_out<OUT_BF16>(a.o, bh * DV + i0 + rloc, o);
   }
   if (flush) {
 #pragma unroll

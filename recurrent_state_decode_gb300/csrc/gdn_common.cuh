@@ -5,8 +5,6 @@
 
 namespace rssm {
 
-__device__ __forceinline__ int wrap(int s, int L) { return s < L ? s : s - L; }
-
 // Epilogue of a Gated DeltaNet verify for sequence b, run by a whole block once
 // no block of the sequence reads the ring rows it overwrites: on a cursor with
 // 0 <= start < L, 0 <= count <= L and pending == 0, append the K new records'

@@ -42,8 +42,6 @@ constexpr int GD = 128;  // dk = dv
 constexpr int KW = 8;    // dot entries per warp: 4 x 8 >= L + 1
 constexpr int ES = FPB + 4;  // floats per staged e row (padded against bank conflicts; 16-byte multiple)
 
-__device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
 // SLOTS: batch rows name their state rows through a slot table.
 template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
@@ -164,8 +162,8 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     const int rl = half ? rl1 : rl0;
     float4 ea = make_float4(0.f, 0.f, 0.f, 0.f), eb = ea;  // e_t of the 8 rows (lane t)
     if (lane < count) {
-      ea = ld_f4(es + lane * ES + rl);
-      eb = ld_f4(es + lane * ES + rl + 4);
+      ea = ld4(es + lane * ES + rl);
+      eb = ld4(es + lane * ES + rl + 4);
     }
     const float el[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
     float4 hv[8];
@@ -183,7 +181,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     const float ec = bm * (bf_to_f(half ? vbB : vbA) - tot);  // e of the current record, row vr (lanes < 16)
     const size_t row = bh * GD + p0 + rl + vr;
     if (valid && lane < 16 && (lane & 1) == 0) {
-      store_y<OUT_BF16>(a.o, row, fmaf(kq_cur, ec, yq));
+      store_out<OUT_BF16>(a.o, row, fmaf(kq_cur, ec, yq));
       if (!flush) a.re[(sh * L + scur) * GD + p0 + rl + vr] = ec;
     }
     if (flush) {  // S_m = gamma S0 + sum_t D(m-1,t) e_t k_t^T, written once
@@ -203,7 +201,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
           const int t = t0 + u;
           const float c = __shfl_sync(FULL, Dt, t & 31);
           if (t < count) {  // uniform
-            const float4 ea2 = ld_f4(es + t * ES + rl), eb2 = ld_f4(es + t * ES + rl + 4);
+            const float4 ea2 = ld4(es + t * ES + rl), eb2 = ld4(es + t * ES + rl + 4);
             const float et[8] = {ea2.x, ea2.y, ea2.z, ea2.w, eb2.x, eb2.y, eb2.z, eb2.w};
 #pragma unroll
             for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(c * et[rr], kt[u], hv[rr]);

@@ -37,8 +37,6 @@ constexpr int KMAX = 4;      // new records per verify on this path
 constexpr int EW = 8;        // dot entries per warp: 4 x 8 = 32 >= L + K
 constexpr int ES = FPB + 4;  // floats per staged e row (padded; 16-byte multiple)
 
-__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
 // SLOTS: batch rows name their state rows through a slot table.
 template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
@@ -107,9 +105,9 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
 #pragma unroll
     for (int jb = 0; jb < GD / 16; jb++) {
       const int col = 16 * jb + 4 * qt;
-      const float4 r0 = g0 ? load_bf4(g0 + col) : (s0 ? lds4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
-      const float4 r1 = g1 ? load_bf4(g1 + col) : (s1 ? lds4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
-      const float4 bv = lds4(vecs + qg * GD + col);
+      const float4 r0 = g0 ? load_bf4(g0 + col) : (s0 ? ld4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
+      const float4 r1 = g1 ? load_bf4(g1 + col) : (s1 ? ld4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
+      const float4 bv = ld4(vecs + qg * GD + col);
       mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y), __float_as_uint(r1.y),
                     __float_as_uint(bv.x), __float_as_uint(bv.y));
       mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w), __float_as_uint(r1.w),
@@ -184,8 +182,8 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
 #pragma unroll
     for (int jb = 0; jb < GD / 16; jb++) {
       const int col = 16 * jb + 4 * qt;
-      const float4 r0 = lds4(tile + rA * GD + col), r1 = lds4(tile + rB * GD + col);
-      const float4 bv = lds4(vecs + qg * GD + col);
+      const float4 r0 = ld4(tile + rA * GD + col), r1 = ld4(tile + rB * GD + col);
+      const float4 bv = ld4(vecs + qg * GD + col);
       uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
       split_tf32(r0.x, h0, l0);
       split_tf32(r1.x, h1, l1);
@@ -255,12 +253,12 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     if (valid && qt >= 2) {
       const size_t o0 = (((size_t)b * K + i0) * H + h) * GD + p0;
       if (i0 < K) {
-        store_y<OUT_BF16>(a.o, o0 + rA, oA0);
-        store_y<OUT_BF16>(a.o, o0 + rB, oB0);
+        store_out<OUT_BF16>(a.o, o0 + rA, oA0);
+        store_out<OUT_BF16>(a.o, o0 + rB, oB0);
       }
       if (i0 + 1 < K) {
-        store_y<OUT_BF16>(a.o, o0 + (size_t)H * GD + rA, oA1);
-        store_y<OUT_BF16>(a.o, o0 + (size_t)H * GD + rB, oB1);
+        store_out<OUT_BF16>(a.o, o0 + (size_t)H * GD + rA, oA1);
+        store_out<OUT_BF16>(a.o, o0 + (size_t)H * GD + rB, oB1);
       }
     }
     if (valid && qt < K) {  // the new record qt's e and v rows, at rows rA, rB
@@ -282,7 +280,7 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
         const int rl = half ? rl1 : rl0;
         float4 hv[8];
 #pragma unroll
-        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, lds4(tile + (rl + rr) * GD + lane * 4));
+        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, ld4(tile + (rl + rr) * GD + lane * 4));
         for (int t0 = 0; t0 < count; t0 += 2) {
           float4 kt[2];
 #pragma unroll
@@ -293,7 +291,7 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
             const int t = t0 + u;
             const float c = __shfl_sync(FULL, wf, t & 31);
             if (t < count) {  // uniform
-              const float4 ea2 = lds4(es + t * ES + rl), eb2 = lds4(es + t * ES + rl + 4);
+              const float4 ea2 = ld4(es + t * ES + rl), eb2 = ld4(es + t * ES + rl + 4);
               const float et[8] = {ea2.x, ea2.y, ea2.z, ea2.w, eb2.x, eb2.y, eb2.z, eb2.w};
 #pragma unroll
               for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(c * et[rr], kt[u], hv[rr]);

@@ -24,19 +24,9 @@ constexpr int CONV_THREADS = 256;
 constexpr int CONV_RB = 64;       // state rows per conventional block
 constexpr int WMAX = 32;          // records in a window
 
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
-__device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
-
 __device__ __forceinline__ float4 exp4(float4 a) { return make_float4(expf(a.x), expf(a.y), expf(a.z), expf(a.w)); }
 
 __device__ __forceinline__ float4 sub4(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
-
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(FULL, v, 1);
-  v += __shfl_xor_sync(FULL, v, 2);
-  return v;
-}
 
 // ------------------------------------------------------------------ conventional
 
@@ -87,7 +77,7 @@ __global__ void __launch_bounds__(CONV_THREADS) kda_conventional_kernel(GdnArgs 
     }
   }
   o = quad_sum(o);
-  if (active && q4 == 0) store_y<OUT_BF16>(a.o, bh * DV + row, o);
+  if (active && q4 == 0) store_out<OUT_BF16>(a.o, bh * DV + row, o);
 }
 
 // ------------------------------------------------------------------ window: flush / prime

@@ -42,12 +42,6 @@ constexpr int GD = 128;      // dk = dv
 constexpr int KW = 8;        // dot entries per warp: 4 x 8 >= L + 1
 constexpr int ES = FPB + 4;  // floats per staged e row (padded against bank conflicts; 16-byte multiple)
 
-__device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
-__device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
-
-__device__ __forceinline__ int wrap_slot(int s, int L) { return s < L ? s : s - L; }
-
 // SLOTS: batch rows name their state rows through a slot table.
 template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
@@ -100,7 +94,7 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   if (threadIdx.x == 0) {  // the window's e rows (this block's) and g rows, in record order
     mbar_arrive_expect_tx(&bar[1], (uint32_t)count * (FPB + GD) * 4);
     for (int t = 0; t < count; t++) {
-      const size_t row = sh * L + wrap_slot(start + t, L);
+      const size_t row = sh * L + wrap(start + t, L);
       bulk_load(es + t * ES, a.re + row * GD + p0, FPB * 4, &bar[1]);
       bulk_load(fd + t * GD, a.rg + row * GD, GD * 4, &bar[1]);
     }
@@ -121,7 +115,7 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   const bool live = valid && landed;
   const int m = cnt + 1;
   const bool flush = live && m == L;
-  const int scur = wrap_slot(start + count, L);  // the current record's slot
+  const int scur = wrap(start + count, L);  // the current record's slot
   {  // channel suffix sums, backwards over the window: f_t = exp(sum_{t<j<=m-1} g_j)
     const int c = threadIdx.x;
     float acc = gc;
@@ -143,7 +137,7 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
       pos = pos < 0 ? pos + L : pos;  // the slot's record index in the window
       float4 ks = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s < L && pos < cnt)
-        ks = mul4(bf4_to_f4(kr[j]), ld_f4(fd + pos * GD + lane * 4));
+        ks = mul4(bf4_to_f4(kr[j]), ld4(fd + pos * GD + lane * 4));
       else if (s == L)
         ks = kc;
       pk[2 * j] = dot4(ks, kc);
@@ -158,7 +152,7 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   const float cK = lane < cnt ? skk[sl] : 0.f;  // lane t: record t's coefficients
   const float cQ = lane < cnt ? skq[sl] : 0.f;
   const float kq_cur = skq[L];
-  const float4 gm4 = ld_f4(gam + lane * 4);
+  const float4 gm4 = ld4(gam + lane * 4);
   const float4 ka = mul4(gm4, kc), qa = mul4(gm4, qc);
   // Append the current record now (its e follows below): its slot is outside
   // the window, so no block reads it for a result.
@@ -189,13 +183,13 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
     const int rl = half ? rl1 : rl0;
     float4 ea = make_float4(0.f, 0.f, 0.f, 0.f), eb = ea;  // e_t of the 8 rows (lane t)
     if (lane < cnt) {
-      ea = ld_f4(es + lane * ES + rl);
-      eb = ld_f4(es + lane * ES + rl + 4);
+      ea = ld4(es + lane * ES + rl);
+      eb = ld4(es + lane * ES + rl + 4);
     }
     const float el[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
     float4 hv[8];
 #pragma unroll
-    for (int rr = 0; rr < 8; rr++) hv[rr] = ld_f4(tile + (rl + rr) * GD + lane * 4);
+    for (int rr = 0; rr < 8; rr++) hv[rr] = ld4(tile + (rl + rr) * GD + lane * 4);
     float tk[8], tq[8];
 #pragma unroll
     for (int rr = 0; rr < 8; rr++) {
@@ -207,7 +201,7 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
     const float yq = __shfl_down_sync(FULL, tot, 16);
     const float ec = bm * (bf_to_f(half ? vbB : vbA) - tot);  // e of the current record, row vr (lanes < 16)
     if (live && lane < 16 && (lane & 1) == 0) {
-      store_y<OUT_BF16>(a.o, bh * GD + p0 + rl + vr, fmaf(kq_cur, ec, yq));
+      store_out<OUT_BF16>(a.o, bh * GD + p0 + rl + vr, fmaf(kq_cur, ec, yq));
       if (!flush) a.re[(sh * L + scur) * GD + p0 + rl + vr] = ec;
     }
     if (flush) {  // S_m = S0 Diag(Gamma) + sum_t e_t (f_t * k_t)^T, written once
@@ -219,14 +213,14 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
 #pragma unroll
         for (int u = 0; u < 2; u++) {
           const int t = t0 + u;
-          kt[u] = t < cnt ? mul4(load_bf4(rkp + wrap_slot(start + t, L) * GD), ld_f4(fd + t * GD + lane * 4))
+          kt[u] = t < cnt ? mul4(load_bf4(rkp + wrap(start + t, L) * GD), ld4(fd + t * GD + lane * 4))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < 2; u++) {
           const int t = t0 + u;
           if (t < cnt) {  // uniform
-            const float4 ea2 = ld_f4(es + t * ES + rl), eb2 = ld_f4(es + t * ES + rl + 4);
+            const float4 ea2 = ld4(es + t * ES + rl), eb2 = ld4(es + t * ES + rl + 4);
             const float et[8] = {ea2.x, ea2.y, ea2.z, ea2.w, eb2.x, eb2.y, eb2.z, eb2.w};
 #pragma unroll
             for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(et[rr], kt[u], hv[rr]);

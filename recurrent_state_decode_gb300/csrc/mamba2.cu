@@ -42,7 +42,6 @@ struct M2Smem {
   uint64_t* bars;  // [4]
 };
 
-__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 // W = records held in shared memory, Lf = records folded, K = outputs.
 __host__ __device__ inline size_t m2_smem_layout(int PB, int N, int W, int Lf, int K, unsigned char* base,
@@ -154,14 +153,6 @@ template <int NCH>
 __device__ __forceinline__ float4 tile_chunk(const M2Smem& s, bool rd16, int row, int N, int c) {
   if (rd16) return load_bf4(reinterpret_cast<const uint16_t*>(s.tile) + (size_t)row * N + c * 4);
   return reinterpret_cast<const float4*>(s.tile + (size_t)row * N)[c];
-}
-
-template <bool OUT_BF16>
-__device__ __forceinline__ void store_out(void* y, size_t i, float v) {
-  if (OUT_BF16)
-    reinterpret_cast<uint16_t*>(y)[i] = f_to_bf(v);
-  else
-    reinterpret_cast<float*>(y)[i] = v;
 }
 
 // Fold one 8-row group: h1 = P h0 + sum_k wx[k][r] B_k, for the lane's column

@@ -36,16 +36,6 @@ namespace {
 constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
 
-__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
-  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
-  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
-}
-
-__device__ __forceinline__ uint4 shfl_u4(uint4 v, int src) {
-  return make_uint4(__shfl_sync(FULL, v.x, src), __shfl_sync(FULL, v.y, src), __shfl_sync(FULL, v.z, src),
-                    __shfl_sync(FULL, v.w, src));
-}
-
 // What one head needs besides the dots: its checkpoint rows and records.
 template <int NCH>
 struct HeadData {

@@ -341,12 +341,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
       if (valid) {
         const size_t y0 = (((size_t)b * K + n0) * H + h) * P + p0;
         if (n0 < K) {
-          store_y<OUT_BF16>(a.y, y0 + rA, fmaf(Pn0, acc[0], w00) * silu_fast(zg[0][0]));
-          store_y<OUT_BF16>(a.y, y0 + rB, fmaf(Pn0, acc[2], w10) * silu_fast(zg[0][1]));
+          store_out<OUT_BF16>(a.y, y0 + rA, fmaf(Pn0, acc[0], w00) * silu_fast(zg[0][0]));
+          store_out<OUT_BF16>(a.y, y0 + rB, fmaf(Pn0, acc[2], w10) * silu_fast(zg[0][1]));
         }
         if (n1 < K) {
-          store_y<OUT_BF16>(a.y, y0 + (size_t)H * P + rA, fmaf(Pn1, acc[1], w01) * silu_fast(zg[1][0]));
-          store_y<OUT_BF16>(a.y, y0 + (size_t)H * P + rB, fmaf(Pn1, acc[3], w11) * silu_fast(zg[1][1]));
+          store_out<OUT_BF16>(a.y, y0 + (size_t)H * P + rA, fmaf(Pn1, acc[1], w01) * silu_fast(zg[1][0]));
+          store_out<OUT_BF16>(a.y, y0 + (size_t)H * P + rB, fmaf(Pn1, acc[3], w11) * silu_fast(zg[1][1]));
         }
       }
     }
