@@ -105,3 +105,29 @@ def test_gdn_steps_replay_from_a_graph():
         assert torch.equal(oa[t], ob[t]), t
     assert torch.equal(sa.S, sb.S) and torch.equal(sa.re, sb.re) and torch.equal(sa.cursors, sb.cursors)
     assert H.status(sa) == 0 and H.status(sb) == 0
+
+
+def test_kda_steps_replay_from_a_graph():
+    from recurrent_state_decode_gb300.inputs import KDAWorkload as KW
+    from recurrent_state_decode_gb300.state import kda_from_workload
+    w = KW("graph_kda", 2, 2, 128, 128, 8, 12, seed=205)
+    dev = "cuda"
+    recs = [I.kda_step_inputs(w, t, dev) for t in range(w.steps)]
+    sa, _, _, _ = kda_from_workload(w, dev)
+    sb, _, _, _ = kda_from_workload(w, dev)
+    oa = [sa.new_output() for _ in range(w.steps)]
+    ob = [sb.new_output() for _ in range(w.steps)]
+    for t in range(w.steps):
+        sa.step(recs[t], oa[t])
+    torch.cuda.synchronize()
+
+    def steps():
+        for t in range(w.steps):
+            sb.step(recs[t], ob[t])
+
+    _capture(steps)
+    for t in range(w.steps):
+        assert torch.equal(oa[t], ob[t]), t
+    for fa, fb in ((sa.S, sb.S), (sa.rg, sb.rg), (sa.re, sb.re), (sa.rk, sb.rk), (sa.cursors, sb.cursors)):
+        assert torch.equal(fa, fb)
+    assert H.status(sa) == 0 and H.status(sb) == 0
