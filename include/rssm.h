@@ -407,6 +407,13 @@ RSSM_API int rssm_kda_prime(const rssm_kda_desc* desc, const float* S, const rss
 RSSM_API const char* rssm_status_string(int code); /* text for RSSM_* and RSSM_DEV_* codes */
 RSSM_API int rssm_version(void);                   /* major * 10000 + minor * 100 + patch */
 
+/* Self-test of the kernels' bounded waits: launches one block that waits for
+ * a copy nothing delivers. The wait gives up after its limit (about one
+ * second; the block waits once more, bounded, before it leaves) and writes
+ * RSSM_DEV_TIMEOUT to dev_status (non-NULL, 16-byte aligned, caller-zeroed).
+ * The context stays usable. Takes about two seconds of one block. */
+RSSM_API int rssm_selftest_bounded_wait(int32_t* dev_status, rssm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,7 @@ rssm_kda_ring = rssm_gdn_ring   # same fields; g holds one log decay per key cha
 P = c_void_p
 _SIGNATURES = {
     "rssm_version": (c_int, []),
+    "rssm_selftest_bounded_wait": (c_int, [P, P]),
     "rssm_status_string": (c_char_p, [c_int]),
     "rssm_mamba2_ring_bytes": (c_int, [P, P]),
     "rssm_gdn_ring_bytes": (c_int, [P, P]),
@@ -164,6 +165,10 @@ def _ref(s):
 
 def rssm_version():
     return load().rssm_version()
+
+
+def rssm_selftest_bounded_wait(dev_status, stream=None):
+    return load().rssm_selftest_bounded_wait(ptr(dev_status), _stream(stream, dev_status))
 
 
 def rssm_mamba2_ring_bytes(desc):

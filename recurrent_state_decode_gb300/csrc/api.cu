@@ -119,6 +119,13 @@ extern "C" {
 
 int rssm_version(void) { return 200; }
 
+int rssm_selftest_bounded_wait(int32_t* dev_status, rssm_stream_t stream) {
+  int rc;
+  if (!dev_status) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_opt(dev_status))) return rc;
+  return cuda_rc(bounded_wait_selftest_launch(dev_status, (cudaStream_t)stream));
+}
+
 const char* rssm_status_string(int code) {
   switch (code) {
     case RSSM_OK: return "ok";

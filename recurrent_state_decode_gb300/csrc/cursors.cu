@@ -82,6 +82,23 @@ __global__ void downcast_f8_kernel(const float* __restrict__ src, uint8_t* __res
   store_f8_row(dst, reinterpret_cast<float*>(dst + rows * 128), row, v, lane);
 }
 
+// Self-test of the bounded wait every kernel uses for its bulk copies: one
+// thread arms an mbarrier for 16 bytes that no copy delivers, so its wait gives
+// up after the limit and reports RSSM_DEV_TIMEOUT. No copy is in flight, so
+// nothing writes into the block's shared memory after it leaves.
+__global__ void bounded_wait_selftest_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&bar, 16);
+  mbar_wait_or_report(&bar, 0, status);
+}
+
+cudaError_t bounded_wait_selftest_launch(int32_t* status, cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 1, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 cudaError_t cursor_launch(int mode, int32_t* cursors, const int32_t* kept, int batch, int L, int32_t* status,
                           cudaStream_t st, const int32_t* slots, int n_state) {
   if (batch <= 0) return cudaSuccess;

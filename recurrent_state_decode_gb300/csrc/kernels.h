@@ -73,6 +73,9 @@ cudaError_t gdn_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st
 bool gdn_step_fast_applies(const GdnArgs& a);
 cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
 
+// One block whose bulk-copy wait expires (cursors.cu): the timeout path's self-test.
+cudaError_t bounded_wait_selftest_launch(int32_t* status, cudaStream_t st);
+
 // Kimi Delta Attention (kda.cu, kda_step_fast.cu) takes GdnArgs with g, rg
 // holding one log decay per key channel: g [Bt, H, DK], rg [Bt, H, L, DK].
 // GDN_CONVENTIONAL, GDN_STEP, GDN_FLUSH and GDN_PRIME name its kernels too.

@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 23
+    assert len(declared) == 24
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -141,6 +141,8 @@ def test_cursor_call_validation(lib):
     assert lib.rssm_checkpoint_downcast(None, None, 0, bd.RSSM_BF16, None) == bd.RSSM_OK
     assert lib.rssm_checkpoint_downcast(ALIGNED, ALIGNED + 2, 8, bd.RSSM_F16, None) == bd.RSSM_ERR_MISALIGNED
     assert lib.rssm_checkpoint_downcast(ALIGNED, ALIGNED, 8, bd.RSSM_F32, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_selftest_bounded_wait(None, None) == bd.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_selftest_bounded_wait(ALIGNED + 4, None) == bd.RSSM_ERR_MISALIGNED
 
 
 def test_gdn_validation(lib):
