@@ -100,6 +100,16 @@ void set_ring(M2Args& a, const rssm_mamba2_ring* r) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA; }
 
+// The KDA ring: the GDN fields, g holding one log decay per key channel.
+void set_kda_ring(GdnArgs& a, const rssm_kda_ring* r) {
+  a.rq = r->q;
+  a.rk = r->k;
+  a.rv = r->v;
+  a.rg = r->g;
+  a.rbeta = r->beta;
+  a.re = r->e;
+}
+
 GdnArgs gdn_args(const rssm_gdn_desc* d) {
   GdnArgs a{};
   a.Bt = d->batch;
@@ -485,17 +495,6 @@ int rssm_kda_conventional_step(const rssm_kda_desc* d, float* S, const rssm_bf16
   a.o = o;
   return cuda_rc(kda_launch(GDN_CONVENTIONAL, a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
 }
-
-namespace {
-void set_kda_ring(GdnArgs& a, const rssm_kda_ring* r) {
-  a.rq = r->q;
-  a.rk = r->k;
-  a.rv = r->v;
-  a.rg = r->g;
-  a.rbeta = r->beta;
-  a.re = r->e;
-}
-}  // namespace
 
 int rssm_kda_step(const rssm_kda_desc* d, float* S, const rssm_kda_ring* ring, int32_t* cursors, const rssm_bf16* q,
                   const rssm_bf16* k, const rssm_bf16* v, const float* g, const float* beta, void* o,
