@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   float* tile = dsm;                 // the block's 64 rows
   float* vecs = dsm + FPB * GD;      // [0..3] new k_j, [4..7] new q_i (fp32)
   float* es = vecs + 2 * KMAX * GD;  // e of committed record t at es + t * ES
-  __shared__ float tbl[2 * KMAX][FW * EW];  // [n][e]: k_e . vec_n; vec 0..3 = new k_j, 4..7 = new q_i
+  __shared__ float tbl[2][2 * KMAX][FW * EW];  // [half][n][e]: k_e . vec_n over column half `half`;
+                                                // vec 0..3 = new k_j, 4..7 = new q_i
   __shared__ float cf[2 * KMAX][33];        // [n][t]: D(a_n, t) (k_t . vec_n) of committed record t (padded rows)
   __shared__ uint64_t bar[2];
   __shared__ int4 cur_s;
@@ -92,18 +93,19 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   __syncthreads();
   // dot tables tbl[n][e] = k_e . vec_n for entries e < 32 (ring slot e if e < L,
   // new record e - L if e < L + K, else 0): [32 x 128] . [128 x 8] on the
-  // tensor cores, warp w < 2 taking entries 16 w .. 16 w + 15 (bf16 inputs are
-  // exact in tf32, so one mma per k-step).
+  // tensor cores, warp w taking entries 16 (w & 1) .. 16 (w & 1) + 15 over the
+  // column half w >> 1 (bf16 inputs are exact in tf32, so one mma per k-step);
+  // readers add the two halves.
   const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
-  if (warp < 2) {
-    const int e0 = 16 * warp + qg, e1 = e0 + 8;
+  {
+    const int e0 = 16 * (warp & 1) + qg, e1 = e0 + 8, ch = warp >> 1;
     const uint16_t* g0 = e0 < L ? a.rk + (sh * L + e0) * GD : nullptr;
     const uint16_t* g1 = e1 < L ? a.rk + (sh * L + e1) * GD : nullptr;
     const float* s0 = (e0 >= L && e0 < L + K) ? vecs + (e0 - L) * GD : nullptr;
     const float* s1 = (e1 >= L && e1 < L + K) ? vecs + (e1 - L) * GD : nullptr;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int jb = 0; jb < GD / 16; jb++) {
+    for (int jb = ch * (GD / 32); jb < (ch + 1) * (GD / 32); jb++) {
       const int col = 16 * jb + 4 * qt;
       const float4 r0 = g0 ? load_bf4(g0 + col) : (s0 ? ld4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
       const float4 r1 = g1 ? load_bf4(g1 + col) : (s1 ? ld4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
@@ -113,10 +115,10 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
       mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w), __float_as_uint(r1.w),
                     __float_as_uint(bv.z), __float_as_uint(bv.w));
     }
-    tbl[2 * qt][e0] = acc[0];
-    tbl[2 * qt + 1][e0] = acc[1];
-    tbl[2 * qt][e1] = acc[2];
-    tbl[2 * qt + 1][e1] = acc[3];
+    tbl[ch][2 * qt][e0] = acc[0];
+    tbl[ch][2 * qt + 1][e0] = acc[1];
+    tbl[ch][2 * qt][e1] = acc[2];
+    tbl[ch][2 * qt + 1][e1] = acc[3];
   }
   // An invalid cursor (reported by the epilogue) runs as an empty window with
   // every store masked.
@@ -158,14 +160,15 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   if (threadIdx.x == 0 && !fold) ticket = cursor_ticket(a.cursors, sb);  // done with the ring's k and g
   if (warp == 0) {  // window coefficients of committed record `lane`, one row per vector
 #pragma unroll
-    for (int n = 0; n < 2 * KMAX; n++) cf[n][lane] = lane < count ? expf(Ga[n & (KMAX - 1)] - G) * tbl[n][sl] : 0.f;
+    for (int n = 0; n < 2 * KMAX; n++)
+      cf[n][lane] = lane < count ? expf(Ga[n & (KMAX - 1)] - G) * (tbl[0][n][sl] + tbl[1][n][sl]) : 0.f;
   }
   __syncthreads();  // the coefficient table
   float cpl = 0.f;
   if (lane < 16) {
-    if (cj2 < cj && cj < K) cpl = expf(Gx - Gy) * tbl[cj][L + cj2];
+    if (cj2 < cj && cj < K) cpl = expf(Gx - Gy) * (tbl[0][cj][L + cj2] + tbl[1][cj][L + cj2]);
   } else {
-    if (cj2 <= cj && cj < K) cpl = expf(Gx - Gy) * tbl[KMAX + cj][L + cj2];
+    if (cj2 <= cj && cj < K) cpl = expf(Gx - Gy) * (tbl[0][KMAX + cj][L + cj2] + tbl[1][KMAX + cj][L + cj2]);
   }
   const bool ok0 = mbar_wait(&bar[0], 0), ok1 = mbar_wait(&bar[1], 0);
   const bool landed = __all_sync(FULL, ok0 && ok1);  // uniform over the warp

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;                                                  // the block's rows (fp32, or bf16)
   uint16_t* xs = reinterpret_cast<uint16_t*>(dsm + FPB * FN);         // x of record k, row r: xs[k * FPB + r]
-  __shared__ float tbl[KMAX][FW * EW];                                // B_e . C_i
+  __shared__ float tbl[2][KMAX][FW * EW];                             // B_e . C_i over column half [0] / [1]
   __shared__ float cf[KMAX][33];                                      // window coefficient of record k, output i
   __shared__ uint64_t bar;
   __shared__ int last_flags;
@@ -186,9 +186,10 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   const uint16_t* cvec = qg < K ? a.C + (((size_t)b * K + qg) * G + g) * FN : nullptr;
   // dot table tbl[i][e] = B_e . C_i for entries e < 32 (ring slot e if e < L, new
   // record e - L if e < L + K, else 0): [32 x 128] . [128 x 8] on the tensor
-  // cores, warp w < 2 taking entries 16 w .. 16 w + 15 (bf16 inputs are exact in tf32)
-  if (warp < 2) {
-    const int e0 = 16 * warp + qg, e1 = e0 + 8;
+  // cores, warp w taking entries 16 (w & 1) .. 16 (w & 1) + 15 over the column
+  // half w >> 1 (bf16 inputs are exact in tf32); the reader adds the halves
+  {
+    const int e0 = 16 * (warp & 1) + qg, e1 = e0 + 8, ch = warp >> 1;
     auto row_of = [&](int e) -> const uint16_t* {
       if (e < L) return a.rB + ((size_t)sg * L + e) * FN;
       if (e < L + K) return a.B + (((size_t)b * K + (e - L)) * G + g) * FN;
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     const uint16_t* s1 = row_of(e1);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int jb = 0; jb < FN / 16; jb++) {
+    for (int jb = ch * (FN / 32); jb < (ch + 1) * (FN / 32); jb++) {
       const int col = 16 * jb + 4 * qt;
       const float4 r0 = s0 ? load_bf4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 r1 = s1 ? load_bf4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -209,10 +210,10 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
                     __float_as_uint(bv.z), __float_as_uint(bv.w));
     }
     if (qt < 2) {  // columns 2 qt, 2 qt + 1 are outputs 0..3
-      tbl[2 * qt][e0] = acc[0];
-      tbl[2 * qt + 1][e0] = acc[1];
-      tbl[2 * qt][e1] = acc[2];
-      tbl[2 * qt + 1][e1] = acc[3];
+      tbl[ch][2 * qt][e0] = acc[0];
+      tbl[ch][2 * qt + 1][e0] = acc[1];
+      tbl[ch][2 * qt][e1] = acc[2];
+      tbl[ch][2 * qt + 1][e1] = acc[3];
     }
   }
   // An invalid cursor (reported by the epilogue below) runs as an empty window
@@ -254,7 +255,8 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
 #pragma unroll
     for (int i = 0; i < KMAX; i++) {
       const float Sa = __shfl_sync(FULL, S, (count + i) & 31);
-      cf[i][lane] = (i < K && lane <= count + i) ? fmaf(dtk * expf(Sa - S), tbl[i][ek], lane == count + i ? Dh : 0.f)
+      cf[i][lane] = (i < K && lane <= count + i) ? fmaf(dtk * expf(Sa - S), tbl[0][i][ek] + tbl[1][i][ek],
+                                                      lane == count + i ? Dh : 0.f)
                                                  : 0.f;
     }
   }
