@@ -142,12 +142,6 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     const float v = __shfl_up_sync(FULL, G, o);
     if (lane >= o) G += v;
   }
-  float Ga[KMAX], gam[KMAX];  // G at record count + j; e^{G_a}
-#pragma unroll
-  for (int j = 0; j < KMAX; j++) {
-    Ga[j] = __shfl_sync(FULL, G, (count + j) & 31);
-    gam[j] = expf(Ga[j]);
-  }
   const float Gc = __shfl_sync(FULL, G, (count - 1) & 31);
   const float Pf = expf(Gc);                                 // fold: e^{G_{count-1}}
   const float wf = lane < count ? expf(Gc - G) : 0.f;        // fold weight of record `lane`
@@ -158,10 +152,11 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   __syncthreads();  // the dot tables
   int ticket = 0;
   if (threadIdx.x == 0 && !fold) ticket = cursor_ticket(a.cursors, sb);  // done with the ring's k and g
-  if (warp == 0) {  // window coefficients of committed record `lane`, one row per vector
-#pragma unroll
-    for (int n = 0; n < 2 * KMAX; n++)
-      cf[n][lane] = lane < count ? expf(Ga[n & (KMAX - 1)] - G) * (tbl[0][n][sl] + tbl[1][n][sl]) : 0.f;
+  {  // window coefficients of committed record `lane`: warp w builds rows w and w + 4 (vectors k_w, q_w)
+    const float Gw = __shfl_sync(FULL, G, (count + warp) & 31);
+    const float d = lane < count ? expf(Gw - G) : 0.f;
+    cf[warp][lane] = d * (tbl[0][warp][sl] + tbl[1][warp][sl]);
+    cf[warp + KMAX][lane] = d * (tbl[0][warp + KMAX][sl] + tbl[1][warp + KMAX][sl]);
   }
   __syncthreads();  // the coefficient table
   float cpl = 0.f;

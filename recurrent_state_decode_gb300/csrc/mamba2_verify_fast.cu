@@ -251,14 +251,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   // Outputs come from the checkpoint and every record since it (the fold only
   // writes the checkpoint): output i = e^{S_a} (h0 . C_i) + sum_{k<=a} cf[i][k] x_k,
   // a = count + i, cf = dt_k e^{S_a - S_k} (B_k . C_i) (+ D on record a).
-  if (warp == 0) {
-#pragma unroll
-    for (int i = 0; i < KMAX; i++) {
-      const float Sa = __shfl_sync(FULL, S, (count + i) & 31);
-      cf[i][lane] = (i < K && lane <= count + i) ? fmaf(dtk * expf(Sa - S), tbl[0][i][ek] + tbl[1][i][ek],
-                                                      lane == count + i ? Dh : 0.f)
-                                                 : 0.f;
-    }
+  {  // warp w builds row i = w (KMAX = 4 warps; every warp holds S, dtk and ek)
+    const int i = warp;
+    const float Sa = __shfl_sync(FULL, S, (count + i) & 31);
+    cf[i][lane] = (i < K && lane <= count + i) ? fmaf(dtk * expf(Sa - S), tbl[0][i][ek] + tbl[1][i][ek],
+                                                    lane == count + i ? Dh : 0.f)
+                                               : 0.f;
   }
   // Append the new records' x and z rows of this block now: its committed x
   // rows are in registers and shared memory already.
