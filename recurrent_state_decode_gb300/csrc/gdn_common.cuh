@@ -27,13 +27,29 @@ __device__ __forceinline__ void gdn_verify_epilogue(const GdnArgs& a, int b, int
     }
     return;
   }
-  const int nv = DK >> 3;
-  for (int q = tid; q < K * H * nv; q += nt) {
-    const int j = q / (H * nv), r = q - j * H * nv, h = r / nv, v = r - h * nv;
-    const size_t slot = ((size_t)sb * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
-    const size_t src = (((size_t)b * K + j) * H + h) * DK + v * 8;
-    *reinterpret_cast<uint4*>(a.rk + slot * DK + v * 8) = *reinterpret_cast<const uint4*>(a.k + src);
-    *reinterpret_cast<uint4*>(a.rq + slot * DK + v * 8) = *reinterpret_cast<const uint4*>(a.q + src);
+  const int nv = DK >> 3, pieces = K * H * nv;
+  constexpr int U = 4;  // pieces in flight per thread: all loads before the stores
+  for (int q0 = tid; q0 < pieces; q0 += U * nt) {
+    uint4 kv[U], qv[U];
+    size_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int q = q0 + u * nt;
+      if (q < pieces) {
+        const int j = q / (H * nv), r = q - j * H * nv, h = r / nv, v = r - h * nv;
+        dst[u] = (((size_t)sb * H + h) * L + wrap(wrap(c.x + c.y + j, L), L)) * DK + v * 8;
+        const size_t src = (((size_t)b * K + j) * H + h) * DK + v * 8;
+        kv[u] = *reinterpret_cast<const uint4*>(a.k + src);
+        qv[u] = *reinterpret_cast<const uint4*>(a.q + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      if (q0 + u * nt < pieces) {
+        *reinterpret_cast<uint4*>(a.rk + dst[u]) = kv[u];
+        *reinterpret_cast<uint4*>(a.rq + dst[u]) = qv[u];
+      }
+    }
   }
   for (int q = tid; q < K * H; q += nt) {
     const int j = q / H, h = q - j * H;

@@ -65,15 +65,30 @@ __device__ __forceinline__ void verify_epilogue(const M2Args& a, int b, int sb, 
     return;
   }
   constexpr int NV = FN / 8;  // 16-byte pieces per group row
-  for (int q = tid; q < K * G * NV; q += FT) {
-    const int i = q / (G * NV), r = q - i * G * NV, g = r / NV, v = r - g * NV;
-    int slot = c.x + c.y + i;
-    slot = slot < L ? slot : slot - L;
-    slot = slot < L ? slot : slot - L;
-    const size_t src = (((size_t)b * K + i) * G + g) * FN + v * 8;
-    const size_t dst = (((size_t)sb * G + g) * L + slot) * FN + v * 8;
-    *reinterpret_cast<uint4*>(a.rB + dst) = ldg16(a.B + src);
-    *reinterpret_cast<uint4*>(a.rC + dst) = ldg16(a.C + src);
+  constexpr int U = 4;        // pieces in flight per thread: all loads before the stores
+  const int pieces = K * G * NV;
+  for (int q0 = tid; q0 < pieces; q0 += U * FT) {
+    uint4 bv[U], cv[U];
+    size_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int q = q0 + u * FT;
+      if (q < pieces) {
+        const int i = q / (G * NV), r = q - i * G * NV, g = r / NV, v = r - g * NV;
+        const int slot = wrap(wrap(c.x + c.y + i, L), L);
+        const size_t src = (((size_t)b * K + i) * G + g) * FN + v * 8;
+        dst[u] = (((size_t)sb * G + g) * L + slot) * FN + v * 8;
+        bv[u] = ldg16(a.B + src);
+        cv[u] = ldg16(a.C + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      if (q0 + u * FT < pieces) {
+        *reinterpret_cast<uint4*>(a.rB + dst[u]) = bv[u];
+        *reinterpret_cast<uint4*>(a.rC + dst[u]) = cv[u];
+      }
+    }
   }
   for (int q = tid; q < K * H; q += FT) {
     const int i = q / H, h = q - i * H;
