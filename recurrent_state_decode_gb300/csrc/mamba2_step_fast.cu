@@ -38,10 +38,11 @@ using namespace fastrows;
 
 constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 
-// RD16: the block reads the bf16 read copy (16 KiB tiles, eight blocks per SM).
+// RD16: the block reads the 16-bit or fp8 read copy (16 KiB tiles, seven blocks
+// per SM: at eight the 64-register cap spilled, and seven measured 2% faster).
 // SLOTS: batch rows name their state rows through a slot table.
 template <bool OUT_BF16, bool RD16, bool SLOTS>
-__global__ void __launch_bounds__(FT, RD16 ? 8 : 6) m2_step_fast_kernel(M2Args a) {
+__global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
   __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
   extern __shared__ __align__(128) float tile_d[];
@@ -227,7 +228,7 @@ cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) 
   };
   auto k = a.slots ? pick(std::true_type{}) : pick(std::false_type{});
   const int smem = rd16 ? FPB * FN * 2 : 0;
-  // six 32 KiB (eight 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
+  // six 32 KiB (seven 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
