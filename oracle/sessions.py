@@ -181,7 +181,11 @@ def gdn_spec_session(S0, prefill, starts, counts, verifies, kepts, L):
     sequence's checkpoint must equal it); cursors_verify, cursors_commit
     [Bt,4]; state (the committed state after the commit).
     """
-    S = gdn_prefill(S0, prefill, counts)
+    return _delta_spec_session(_gdn_step, gdn_prefill(S0, prefill, counts), starts, counts, verifies, kepts, L)
+
+
+def _delta_spec_session(step, S, starts, counts, verifies, kepts, L):
+    """The speculative session of a delta-rule layer, from the committed state S."""
     cs = [(int(s), int(c), 0, 0) for s, c in zip(starts, counts)]
     for rec, kept in zip(verifies, kepts):
         K = rec["q"].shape[1]
@@ -196,7 +200,7 @@ def gdn_spec_session(S0, prefill, starts, counts, verifies, kepts, L):
         Ss, os_ = [], []
         Si = committed
         for i in range(K):
-            Si, oi = _gdn_step(Si, _take(rec, i))
+            Si, oi = step(Si, _take(rec, i))
             Ss.append(Si)
             os_.append(oi)
         o = np.stack(os_, axis=1)
@@ -245,3 +249,9 @@ def kda_ar_session(S0, prefill, starts, counts, steps, L):
             cs[b] = nc
             flushed[b] = fl
         yield {"o": o, "flushed": flushed, "state": S, "cursors": np.array(cs, np.int64)}
+
+
+def kda_spec_session(S0, prefill, starts, counts, verifies, kepts, L):
+    """Speculative decode for Kimi Delta Attention: as gdn_spec_session, with
+    g [Bt,K,H,dk] one log decay per key channel."""
+    return _delta_spec_session(_kda_step, kda_prefill(S0, prefill, counts), starts, counts, verifies, kepts, L)

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from oracle import cursors as cur
-from oracle import gdn, mamba2, sessions
+from oracle import gdn, kda, mamba2, sessions
 
 
 def test_ar_trace_by_hand():
@@ -189,3 +189,39 @@ def test_gdn_spec_session_folds_like_mamba2(rng):
         np.testing.assert_array_equal(a["cursors_verify"], c["cursors_verify"])
         np.testing.assert_array_equal(a["cursors_commit"], c["cursors_commit"])
     assert any(x["folded"].any() for x in g)
+
+
+def _kda_records(rng, Bt, H, dk, dv, n):
+    r = _gdn_records(rng, Bt, H, dk, dv, n)
+    r["g"] = -0.5 * np.log1p(np.exp(rng.standard_normal((Bt, n, H, dk))))  # one decay per key channel
+    return r
+
+
+@pytest.mark.parametrize("reject", [False, True])
+def test_kda_spec_session_matches_ar(rng, reject):
+    """KDA spec decode with kept drafts equals AR decode over exactly the kept
+    tokens (outputs, committed state), from prefilled windows; a rejected
+    draft's output is the continuation through it."""
+    Bt, H, dk, dv, L, K, V = 3, 2, 4, 3, 6, 3, 7
+    S0 = 0.1 * rng.standard_normal((Bt, H, dv, dk))
+    pre = _kda_records(rng, Bt, H, dk, dv, L - 1)
+    starts, counts = np.array([0, 2, 5]), np.array([0, 3, 5])
+    drafts = [_kda_records(rng, Bt, H, dk, dv, K) for _ in range(V)]
+    kepts = [rng.integers(1, K + 1, Bt) if reject else np.full(Bt, K) for _ in range(V)]
+    spec = list(sessions.kda_spec_session(S0, pre, starts, counts, drafts, kepts, L))
+    for b in range(Bt):
+        S = S0[b:b + 1]
+        for j in range(counts[b]):
+            r = {k: a[b:b + 1, j] for k, a in pre.items()}
+            S, _ = kda.conventional_step(S, r["q"], r["k"], r["v"], r["g"], r["beta"])
+        for v in range(V):
+            Sv = S
+            for i in range(K):
+                r = {k: a[b:b + 1, i] for k, a in drafts[v].items()}
+                Sv, o = kda.conventional_step(Sv, r["q"], r["k"], r["v"], r["g"], r["beta"])
+                np.testing.assert_allclose(spec[v]["o"][b, i], o[0], rtol=1e-12, atol=1e-14)
+                if i + 1 == kepts[v][b]:
+                    Snext = Sv
+            S = Snext
+            np.testing.assert_allclose(spec[v]["state"][b], S[0], rtol=1e-12, atol=1e-14)
+    assert any(x["folded"].any() for x in spec)
