@@ -2,7 +2,7 @@
 """Benchmark of the ReplaySSM decode path on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mamba2_serving|mamba2_spec|gdn_serving|gdn_spec|kda_serving|mamba2_bf16_read|mamba2_f16_read|mamba2_f8_read|mamba2_tiny]
+                    [--workload mamba2_serving|mamba2_spec|gdn_serving|gdn_spec|kda_serving|kda_spec|mamba2_bf16_read|mamba2_f16_read|mamba2_f8_read|mamba2_tiny]
     python bench.py --mode profile --steps 3 --warmup 1      # a few calls, no timing (for ncu)
 
 A step is one decode step of one layer over the whole batch: one
@@ -566,6 +566,43 @@ def other_workloads(args, dev, out, out_bytes, K, W_, dist, stream):
                    "bytes_ratio_vs_snapshot_spec": conv_spec_bytes / nbytes, "steps": K}
     del st, recs, kepts
     torch.cuda.empty_cache()
+
+    # Kimi Delta Attention speculative verify + commit, K = T + 1 records per sequence per step
+    w = I.WORKLOADS["kda_spec"]
+    st, _, _, counts0 = kda_from_workload(w, dev, out)
+    recs = [I.kda_verify_inputs(w, t, dev) for t in range(W_ + K)]
+    kepts = [I.accepted_kept(w, t, dev) for t in range(W_ + K)]
+    o = st.new_verify_output(w.n_new)
+
+    def kspec(i):
+        st.verify(recs[i], o)
+        st.commit(kepts[i])
+
+    for t in range(W_):
+        kspec(t)
+    torch.cuda.synchronize()
+    ms, _ = time_calls(lambda i: kspec(W_ + i), K, stream)
+    bd.check(int(st.status.item()), "device status")
+    counts = counts0.cpu().tolist()
+    kl = [k.cpu().tolist() for k in kepts]
+    nbytes = 0
+    accepted = 0
+    for t in range(W_ + K):
+        if t >= W_:
+            nbytes += bm.kda_verify_bytes(w.nheads, w.dk, w.dv, w.buf_len, w.n_new, counts, out_bytes)
+            accepted += sum(kl[t])
+        counts = [(0 if c + w.n_new > w.buf_len else c) + k for c, k in zip(counts, kl[t])]
+    nbytes /= K
+    us = ms * 1e3 / K
+    tile = w.nheads * w.dv * w.dk * 4
+    conv_spec_bytes = w.batch * tile * (1 + w.drafts)  # one state read + T snapshot writes per verify
+    res[w.name] = {"us_per_step": us, "accepted_tokens_per_s": accepted / (ms * 1e-3),
+                   "hbm_gbs": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                   "algorithmic_bytes_per_step": nbytes,
+                   "conventional_snapshot_bytes_per_step": conv_spec_bytes,
+                   "bytes_ratio_vs_snapshot_spec": conv_spec_bytes / nbytes, "steps": K}
+    del st, recs, kepts
+    torch.cuda.empty_cache()
     return res
 
 
@@ -644,6 +681,12 @@ def profile_other(args, dist):
         o = st.new_output()
         for t in range(n):
             st.step(I.kda_step_inputs(w, t, dev), o)
+    elif args.workload == "kda_spec":
+        st, _, _, _ = kda_from_workload(w, dev, out)
+        o = st.new_verify_output(w.n_new)
+        for t in range(n):
+            st.verify(I.kda_verify_inputs(w, t, dev), o)
+            st.commit(I.accepted_kept(w, t, dev))
     elif args.workload == "gdn_spec":
         st, _, _, _ = gdn_from_workload(w, dev, out)
         o = st.new_verify_output(w.n_new)
@@ -670,7 +713,7 @@ def main(argv=None):
         else:
             from recurrent_state_decode_gb300 import binding
             binding.load()
-            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec", "gdn_spec", "kda_serving"):
+            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec", "gdn_spec", "kda_serving", "kda_spec"):
                 res = profile_other(args, dist)
             elif args.workload.startswith("mamba2") and "spec" not in args.workload:
                 res = bench_mamba2_ar(args, dist)

@@ -396,6 +396,21 @@ RSSM_API int rssm_kda_step(const rssm_kda_desc* desc, float* S, const rssm_kda_r
 RSSM_API int rssm_kda_flush(const rssm_kda_desc* desc, float* S, const rssm_kda_ring* ring,
                    int32_t* cursors, int32_t* dev_status, rssm_stream_t stream);
 
+/* Speculative verify for KDA (as rssm_gdn_spec_verify: K = n_new records
+ * appended at ring slots (start + count + i) mod L with their corrections,
+ * outputs o_i after the committed records plus new records 0..i, the
+ * committed window folded into S first if count + K > L; pending = K, flags =
+ * folded; followed by one rssm_commit_cursors).
+ *  q, k [batch, K, nheads, dk], v [batch, K, nheads, dv] (bf16);
+ *  g [batch, K, nheads, dk], beta [batch, K, nheads] fp32;
+ *  o [batch, K, nheads, dv] of out_dtype.
+ *  1 <= n_new <= buf_len (else RSSM_ERR_INVALID_ARG); dk = dv = 128, n_new <= 4
+ *  and buf_len + n_new <= 32 (else RSSM_ERR_UNSUPPORTED). */
+RSSM_API int rssm_kda_spec_verify(const rssm_kda_desc* desc, int n_new, float* S, const rssm_kda_ring* ring,
+                         int32_t* cursors, const rssm_bf16* q, const rssm_bf16* k, const rssm_bf16* v,
+                         const float* g, const float* beta, void* o, int32_t* dev_status,
+                         rssm_stream_t stream);
+
 /* Fills ring->e for windows written into the ring directly (as
  * rssm_gdn_prime). Writes ring->e only. */
 RSSM_API int rssm_kda_prime(const rssm_kda_desc* desc, const float* S, const rssm_kda_ring* ring,

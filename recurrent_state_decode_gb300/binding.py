@@ -81,6 +81,7 @@ _SIGNATURES = {
     "rssm_kda_step": (c_int, [P] * 11 + [P]),
     "rssm_kda_flush": (c_int, [P] * 5 + [P]),
     "rssm_kda_prime": (c_int, [P] * 5 + [P]),
+    "rssm_kda_spec_verify": (c_int, [P, c_int] + [P] * 11),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -288,6 +289,12 @@ def rssm_kda_step(desc, S, ring, cursors, q, k, v, g, beta, o, dev_status=None, 
 
 def rssm_kda_flush(desc, S, ring, cursors, dev_status=None, stream=None):
     return load().rssm_kda_flush(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status), _stream(stream, S))
+
+
+def rssm_kda_spec_verify(desc, n_new, S, ring, cursors, q, k, v, g, beta, o, dev_status=None, stream=None):
+    return load().rssm_kda_spec_verify(
+        _ref(desc), int(n_new), ptr(S), _ref(ring), ptr(cursors), ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), ptr(o),
+        ptr(dev_status), _stream(stream, S))
 
 
 def rssm_kda_prime(desc, S, ring, cursors, dev_status=None, stream=None):

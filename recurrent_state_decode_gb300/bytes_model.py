@@ -123,6 +123,16 @@ def kda_step_bytes(H, DK, DV, L, counts, out_bytes=2):
     return total
 
 
+def kda_verify_bytes(H, DK, DV, L, K, counts, out_bytes=2):
+    """One verify + commit; counts = committed window counts before the verify."""
+    tile, rec, e, past, o = kda_parts(H, DK, DV, out_bytes)
+    total = 0
+    for c in counts:
+        total += 2 * tile if c + K > L else tile
+        total += K * (2 * rec + e) + c * past + K * o + 2 * CURSOR + 4
+    return total
+
+
 def kda_conventional_bytes(H, DK, DV, batch, out_bytes=2):
     tile, rec, e, past, o = kda_parts(H, DK, DV, out_bytes)
     return batch * (2 * tile + rec + o)

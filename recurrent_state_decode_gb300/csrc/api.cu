@@ -541,6 +541,34 @@ int rssm_kda_flush(const rssm_kda_desc* d, float* S, const rssm_kda_ring* ring, 
   return cuda_rc(cursor_launch(CUR_FLUSH, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
 }
 
+int rssm_kda_spec_verify(const rssm_kda_desc* d, int n_new, float* S, const rssm_kda_ring* ring, int32_t* cursors,
+                         const rssm_bf16* q, const rssm_bf16* k, const rssm_bf16* v, const float* g,
+                         const float* beta, void* o, int32_t* dev_status, rssm_stream_t stream) {
+  int rc = check_gdn(d);
+  if (rc) return rc;
+  if (n_new < 1 || n_new > d->buf_len) return RSSM_ERR_INVALID_ARG;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors, q, k, v, g, beta, o})))
+    return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  GdnArgs a = gdn_args(d);
+  a.K = n_new;
+  if (!kda_verify_applies(a)) return RSSM_ERR_UNSUPPORTED;  // dk = dv = 128, K <= 4, L + K <= 32
+  a.S = S;
+  set_kda_ring(a, ring);
+  a.cursors = cursors;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.o = o;
+  a.status = dev_status;
+  return cuda_rc(kda_verify_launch(a, d->out_dtype == RSSM_BF16, (cudaStream_t)stream));
+}
+
 int rssm_kda_prime(const rssm_kda_desc* d, const float* S, const rssm_kda_ring* ring, const int32_t* cursors,
                    int32_t* dev_status, rssm_stream_t stream) {
   int rc = check_gdn(d);

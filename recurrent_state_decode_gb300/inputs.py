@@ -94,6 +94,7 @@ WORKLOADS = {
     "mamba2_f8_read": Mamba2Workload("mamba2_f8_read", 256, 128, 64, 128, 8, 16, 4096, seed=1004, read_copy="f8"),
     "gdn_spec": GDNWorkload("gdn_spec", 512, 32, 128, 128, 16, 128, seed=1005, drafts=3),
     "kda_serving": KDAWorkload("kda_serving", 256, 32, 128, 128, 16, 256, seed=1006),
+    "kda_spec": KDAWorkload("kda_spec", 512, 32, 128, 128, 16, 128, seed=1007, drafts=3),
 }
 
 
@@ -218,6 +219,11 @@ def kda_records(w, stream, index, n, device):
 def kda_step_inputs(w, t, device):
     r = kda_records(w, "step", t, 1, device)
     return {k: v[:, 0].contiguous() for k, v in r.items()}
+
+
+def kda_verify_inputs(w, t, device):
+    """Records of verify step t: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g [Bt,K,H,dk], beta [Bt,K,H] fp32."""
+    return {k: v.contiguous() for k, v in kda_records(w, "step", t, w.n_new, device).items()}
 
 
 def kda_prefill(w, device):

@@ -184,7 +184,12 @@ class KDAState(GDNState):
                  "rssm_kda_prime")
 
     def verify(self, rec, o, stream=None, slots=None):
-        raise NotImplementedError("the KDA layer has no speculative verify in this library")
+        """rec: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g [Bt,K,H,dk], beta [Bt,K,H] fp32; o [Bt,K,H,dv]."""
+        if slots is not None:
+            raise ValueError("the KDA verify takes no state slots")
+        bd.check(bd.rssm_kda_spec_verify(self.desc, rec["q"].shape[1], self.S, self.ring, self.cursors, rec["q"],
+                                         rec["k"], rec["v"], rec["g"], rec["beta"], o, self.status, stream),
+                 "rssm_kda_spec_verify")
 
 
 def mamba2_from_workload(w, device="cuda", out_dtype=bd.RSSM_F32, read_copy=None):

@@ -78,3 +78,6 @@ def test_bytes_model_serving_cycle():
     kpast = 32 * (256 + 512) + e
     assert kd == pytest.approx(2097152 * 17 / 16 + (15 * (2 * krec + e) + krec) / 16 + 7.5 * kpast + 32 * 128 * 2 + 32)
     assert bm.kda_conventional_bytes(32, 128, 128, 2) == 2 * (2 * 2097152 + krec + 32 * 128 * 2)
+    kv = bm.kda_verify_bytes(32, 128, 128, 16, 4, [12, 13])
+    assert kv == (2097152 + 4 * (2 * krec + e) + 12 * kpast + 4 * 32 * 128 * 2 + 68) + \
+        (2 * 2097152 + 4 * (2 * krec + e) + 13 * kpast + 4 * 32 * 128 * 2 + 68)

@@ -220,3 +220,97 @@ def test_kda_step_with_slots_matches_the_plain_call():
     for f in fields:
         assert torch.equal(getattr(ss, f)[perm], getattr(sa, f)), f
     assert H.status(sa) == 0 and H.status(ss) == 0
+
+
+# ----------------------------------------------------------------------------- speculative verify
+
+def run_kda_spec(w, out_dtype=bd.RSSM_F32):
+    dev = "cuda"
+    st, pre, starts, counts = kda_from_workload(w, dev, out_dtype)
+    fv, fk = H.Feed(), H.Feed()
+    sess = sessions.kda_spec_session(H.F64(st.S), H.sub(pre, slice(None)), starts.cpu().numpy(),
+                                     counts.cpu().numpy(), fv, fk, w.buf_len)
+    o = st.new_verify_output(w.n_new)
+    folds = 0
+    for t in range(w.steps):
+        rec = I.kda_verify_inputs(w, t, dev)
+        kept = I.accepted_kept(w, t, dev)
+        fv.rec = H.sub(rec, slice(None))
+        fk.rec = kept.cpu().numpy()
+        st.verify(rec, o)
+        cv = st.cursors.cpu().numpy()
+        st.commit(kept)
+        exp = next(sess)
+        og_ = H.F64(o)
+        if out_dtype == bd.RSSM_F32:
+            assert H.rel_l2(og_, exp["o"]) <= TOL_Y32, t
+        else:
+            assert H.bf16_excess(og_, exp["o"]) <= TOL_BF16_EXCESS, t
+        np.testing.assert_array_equal(cv, exp["cursors_verify"])
+        np.testing.assert_array_equal(st.cursors.cpu().numpy(), exp["cursors_commit"])
+        for b in range(w.batch):
+            if exp["folded"][b]:
+                folds += 1
+                assert H.rel_l2(H.F64(st.S[b]), exp["committed_state"][b]) <= TOL_CKPT, (t, b)
+    assert H.status(st) == 0
+    # the ring's cached corrections of the committed window agree with the
+    # checkpoint and the window's records (what the AR step relies on)
+    S, cur = H.F64(st.S), st.cursors.cpu().numpy()
+    ring = {f: H.F64(getattr(st, n)) for f, n in (("k", "rk"), ("v", "rv"), ("g", "rg"), ("e", "re"))}
+    beta = H.F64(st.rbeta)
+    for b in range(w.batch):
+        s0, c = int(cur[b, 0]), int(cur[b, 1])
+        if c == 0:
+            continue
+        slots = [(s0 + t) % w.buf_len for t in range(c)]
+        e = ok.replay_corrections(S[b], ring["k"][b][:, slots], ring["v"][b][:, slots], ring["g"][b][:, slots],
+                                  beta[b][:, slots])
+        assert H.rel_l2(ring["e"][b][:, slots], e) <= 1e-5, b
+    return folds
+
+
+KSPEC = [
+    KW("kspec_128", 3, 4, 128, 128, 16, 24, seed=420, drafts=3),     # the serving tile
+    KW("kspec_L5", 2, 2, 128, 128, 5, 14, seed=421, drafts=3),       # folds often
+    KW("kspec_K1", 2, 2, 128, 128, 8, 12, seed=422, drafts=0),       # one record per verify
+    KW("kspec_K2", 3, 2, 128, 128, 8, 12, seed=423, drafts=1),
+    KW("kspec_L28", 2, 2, 128, 128, 28, 24, seed=424, drafts=3),     # L + K = 32, the longest view
+    KW("kspec_K_eq_L", 3, 2, 128, 128, 4, 8, seed=425, drafts=3),    # K = L: every verify with count > 0 folds
+]
+
+
+@pytest.mark.parametrize("w", KSPEC, ids=lambda w: w.name)
+def test_kda_spec(w):
+    assert run_kda_spec(w) > 0 or w.name == "kspec_K1"
+
+
+def test_kda_spec_bf16_out():
+    run_kda_spec(KSPEC[0], out_dtype=bd.RSSM_BF16)
+
+
+def test_kda_spec_unsupported_and_invalid():
+    st = KDAState(2, 2, 128, 128, 30)
+    rec = {k: torch.zeros(1, device="cuda") for k in ("q", "k", "v", "g", "beta")}
+    args = (st.S, st.ring, st.cursors, rec["q"], rec["k"], rec["v"], rec["g"], rec["beta"], st.S)
+    assert bd.rssm_kda_spec_verify(st.desc, 3, *args) == bd.RSSM_ERR_UNSUPPORTED   # L + K > 32
+    st8 = KDAState(2, 2, 128, 128, 8)
+    args8 = (st8.S, st8.ring, st8.cursors, rec["q"], rec["k"], rec["v"], rec["g"], rec["beta"], st8.S)
+    assert bd.rssm_kda_spec_verify(st8.desc, 5, *args8) == bd.RSSM_ERR_UNSUPPORTED  # K > 4
+    assert bd.rssm_kda_spec_verify(st8.desc, 0, *args8) == bd.RSSM_ERR_INVALID_ARG
+    assert bd.rssm_kda_spec_verify(st8.desc, 9, *args8) == bd.RSSM_ERR_INVALID_ARG  # K > L
+
+
+def test_kda_verify_over_pending_is_reported():
+    """A second verify before the commit is reported and changes nothing."""
+    w = KW("kpend", 2, 2, 128, 128, 8, 1, seed=426, drafts=1, prefill=False)
+    st, _, _, _ = kda_from_workload(w, "cuda")
+    o = st.new_verify_output(w.n_new)
+    rec = I.kda_verify_inputs(w, 0, "cuda")
+    st.verify(rec, o)
+    torch.cuda.synchronize()
+    before = (st.S.clone(), st.cursors.clone(), st.re.clone(), st.rk.clone())
+    st.verify(rec, o)
+    torch.cuda.synchronize()
+    assert H.status(st) == bd.RSSM_DEV_PENDING
+    for x, y in zip(before, (st.S, st.cursors, st.re, st.rk)):
+        assert torch.equal(x, y)
