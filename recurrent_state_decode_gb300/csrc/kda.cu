@@ -248,25 +248,21 @@ __global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
     mbar_arrive_expect_tx(&s.bar, FPB * KD * 4);
     bulk_load(s.tile, a.S + tbase, FPB * KD * 4, &s.bar);
   }
-  {  // thread c: channel c of every record's key and decay prefix sum, and of the new queries
+  {  // thread c: channel c of every record's g and key (independent loads), then the prefix sums
     const int c = tid;
-    float acc = 0.f;
+#pragma unroll 4
     for (int t = 0; t < total; t++) {
-      float g, k;
-      if (t < count) {
-        const size_t row = rec_row(t);
-        g = a.rg[row * KD + c];
-        k = bf_to_f(a.rk[row * KD + c]);
-      } else {
-        const size_t row = new_row(t - count);
-        g = a.g[row * KD + c];
-        k = bf_to_f(a.k[row * KD + c]);
-      }
-      acc += g;
-      s.G[t * KD + c] = acc;
-      s.kw[t * KD + c] = k;
+      const bool ring = t < count;
+      const size_t row = ring ? rec_row(t) : new_row(t - count);
+      s.G[t * KD + c] = ring ? a.rg[row * KD + c] : a.g[row * KD + c];
+      s.kw[t * KD + c] = bf_to_f(ring ? a.rk[row * KD + c] : a.k[row * KD + c]);
     }
     for (int j = 0; j < K; j++) s.qw[j * KD + c] = bf_to_f(a.q[new_row(j) * KD + c]);
+    float acc = 0.f;
+    for (int t = 0; t < total; t++) {
+      acc += s.G[t * KD + c];
+      s.G[t * KD + c] = acc;
+    }
   }
   for (int i = tid; i < count * FPB; i += FT) {  // the committed records' e at the block's rows
     const int t = i / FPB, r = i - t * FPB;
@@ -354,26 +350,38 @@ __global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
   }
 }
 
-// One block per sequence, after the verify in stream order: on a cursor with
-// 0 <= start < L, 0 <= count <= L and pending == 0, append the new records'
-// k, q, g rows and beta at slots (start + count + j) mod L and set pending = K,
-// flags = folded; otherwise report as the cursor checks do and leave it.
+// One block per (sequence, head), after the verify in stream order: on a
+// cursor with 0 <= start < L, 0 <= count <= L and pending == 0, append the
+// head's new records' k, q, g rows and beta at slots (start + count + j) mod L.
+// The last of the sequence's blocks to have read the cursor (an arrival count
+// in the high half of its flags word) sets pending = K, flags = folded, or
+// reports as the cursor checks do and leaves it as it was.
 __global__ void __launch_bounds__(FT) kda_verify_epilogue_kernel(GdnArgs a) {
-  const int b = blockIdx.x, tid = threadIdx.x, L = a.L, K = a.K, H = a.H;
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, L = a.L, K = a.K, H = a.H;
   int4 c = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
   int err = 0;
   if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L))
     err = RSSM_DEV_BAD_CURSOR;
   else if (c.z != 0)
     err = RSSM_DEV_PENDING;
-  if (err) {
-    if (tid == 0) report(a.status, err);
-    return;
+  __syncthreads();  // every thread has read the cursor
+  if (tid == 0) {
+    const int ticket = cursor_ticket(a.cursors, b);
+    if (last_ticket(ticket, H)) {
+      if (err) {
+        report(a.status, err);
+        c.w = ticket & 0xffff;  // the flags as they were, the arrival count cleared
+      } else {
+        c.w = (c.y + K > L) ? 1 : 0;
+        c.z = K;
+      }
+      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
+    }
   }
+  if (err) return;
   constexpr int NB = KD / 8, NG = KD / 4;  // 16-byte pieces of a bf16 row, of an fp32 row
-  for (int q = tid; q < K * H * (2 * NB + NG); q += FT) {
-    const int j = q / (H * (2 * NB + NG)), rem = q - j * H * (2 * NB + NG), h = rem / (2 * NB + NG);
-    const int piece = rem - h * (2 * NB + NG);
+  for (int q = tid; q < K * (2 * NB + NG); q += FT) {
+    const int j = q / (2 * NB + NG), piece = q - j * (2 * NB + NG);
     const size_t ring = ((size_t)b * H + h) * L + (c.x + c.y + j) % L, rec = ((size_t)b * K + j) * H + h;
     if (piece < NB) {
       reinterpret_cast<uint4*>(a.rk + ring * KD)[piece] = reinterpret_cast<const uint4*>(a.k + rec * KD)[piece];
@@ -384,15 +392,7 @@ __global__ void __launch_bounds__(FT) kda_verify_epilogue_kernel(GdnArgs a) {
           reinterpret_cast<const float4*>(a.g + rec * KD)[piece - 2 * NB];
     }
   }
-  for (int q = tid; q < K * H; q += FT) {
-    const int j = q / H, h = q - j * H;
-    a.rbeta[((size_t)b * H + h) * pad4(L) + (c.x + c.y + j) % L] = a.beta[((size_t)b * K + j) * H + h];
-  }
-  if (tid == 0) {
-    c.w = (c.y + K > L) ? 1 : 0;
-    c.z = K;
-    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
-  }
+  if (tid < K) a.rbeta[((size_t)b * H + h) * pad4(L) + (c.x + c.y + tid) % L] = a.beta[((size_t)b * K + tid) * H + h];
 }
 
 template <typename Kern>
@@ -409,7 +409,9 @@ cudaError_t launch_smem(Kern k, dim3 grid, int threads, size_t smem, cudaStream_
 
 bool kda_window_applies(const GdnArgs& a) { return a.DK == KD && a.DV == KD && a.Bt <= 65535 && a.H <= 65535; }
 
-bool kda_verify_applies(const GdnArgs& a) { return kda_window_applies(a) && a.K <= VK && a.L + a.K <= WMAX; }
+bool kda_verify_applies(const GdnArgs& a) {
+  return kda_window_applies(a) && a.K <= VK && a.L + a.K <= WMAX && a.H < (1 << 15);  // H arrivals in 15 bits
+}
 
 cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
@@ -417,7 +419,7 @@ cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   cudaError_t e = out_bf16 ? launch_smem(kda_verify_kernel<true>, grid, FT, sizeof(KdaVerSmem), st, a)
                            : launch_smem(kda_verify_kernel<false>, grid, FT, sizeof(KdaVerSmem), st, a);
   if (e != cudaSuccess) return e;
-  kda_verify_epilogue_kernel<<<a.Bt, FT, 0, st>>>(a);
+  kda_verify_epilogue_kernel<<<dim3(a.Bt, a.H), FT, 0, st>>>(a);
   return cudaGetLastError();
 }
 
