@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(FT) kda_window_kernel(GdnArgs a) {
 constexpr int VK = 4;  // new records per verify on this kernel
 
 struct KdaVerSmem {
-  float tile[FPB * KD];      // the block's 64 state rows
   float kw[WMAX * KD];       // keys of records 0 .. total - 1 (fp32)
   float G[WMAX * KD];        // channel prefix sums of g over the same records
   float qw[VK * KD];         // the new records' queries
@@ -212,7 +211,6 @@ struct KdaVerSmem {
   float us[2 * VK * FPB];    // S0 . vecs[v] at the block's rows
   float M[VK * WMAX];        // M[j][s] = (exp(G_t - G_s) * k_s) . k_t, t = count + j, s < t
   float Q[VK * WMAX];        // Q[i][s] = (exp(G_a - G_s) * k_s) . q_i, a = count + i, s <= a
-  uint64_t bar;
 };
 
 // One CTA of four warps per (sequence, head, 64 state rows). Records t of the
@@ -226,6 +224,9 @@ struct KdaVerSmem {
 // are the same whether taken from S0 with every record or after the fold. The
 // new records' e and v rows of this block go to the ring here; their shared
 // fields (k, q, g, beta) and the cursor follow in kda_verify_epilogue_kernel.
+// The checkpoint rows are read from global memory by the warp that owns them
+// (coalesced float4 per lane), which keeps shared memory to 51 KiB: four blocks
+// per SM.
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -242,12 +243,7 @@ __global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
   auto rec_row = [&](int t) { return sh * L + (start + t) % L; };          // ring row of committed record t
   auto new_row = [&](int j) { return ((size_t)b * K + j) * H + h; };       // record row of new record j
   const size_t tbase = (sh * KD + p0) * KD;
-  if (tid == 0) {
-    mbar_init(&s.bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(&s.bar, FPB * KD * 4);
-    bulk_load(s.tile, a.S + tbase, FPB * KD * 4, &s.bar);
-  }
+  const float* srow = a.S + tbase;  // the block's 64 checkpoint rows
   {  // thread c: channel c of every record's g and key (independent loads), then the prefix sums
     const int c = tid;
 #pragma unroll 4
@@ -285,20 +281,14 @@ __global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
     const float p = warp_sum(dot4(kd, y));
     if (lane == 0) (table == 0 ? s.M : s.Q)[j * WMAX + sidx] = p;
   }
-  if (!__syncthreads_and(mbar_wait(&s.bar, 0))) {  // uniform over the block
-    if (tid == 0) {
-      report(a.status, RSSM_DEV_TIMEOUT);
-      mbar_wait(&s.bar, 0);  // the copy lands before the block leaves
-    }
-    return;
-  }
+  __syncthreads();  // the vectors and the tables
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;
 #pragma unroll
   for (int half = 0; half < 2; half++) {  // S0 . vecs for the warp's rows
     const int rl = half ? rl1 : rl0;
     float4 hv[8];
 #pragma unroll
-    for (int rr = 0; rr < 8; rr++) hv[rr] = ld4(s.tile + (rl + rr) * KD + 4 * lane);
+    for (int rr = 0; rr < 8; rr++) hv[rr] = ld4(srow + (size_t)(rl + rr) * KD + 4 * lane);
     for (int v = 0; v < 2 * K; v++) {
       const float4 x = ld4(s.vecs + (v < K ? v : VK + v - K) * KD + 4 * lane);
       float d[8];
@@ -337,7 +327,7 @@ __global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
       const int rl = half ? rl1 : rl0;
       float4 hv[8];
 #pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = mul4(gl, ld4(s.tile + (rl + rr) * KD + 4 * lane));
+      for (int rr = 0; rr < 8; rr++) hv[rr] = mul4(gl, ld4(srow + (size_t)(rl + rr) * KD + 4 * lane));
       for (int t = 0; t < count; t++) {
         const float4 kt = mul4(exp4(sub4(Gl, ld4(s.G + t * KD + 4 * lane))), ld4(s.kw + t * KD + 4 * lane));
 #pragma unroll
