@@ -11,11 +11,12 @@
 // lane s ring slot s (g); lane j new record j (g, beta); lane 8j + r the v of
 // new record j at row r of each group; the new records' k and q into shared
 // memory (fp32). Entry e of the dot tables is ring slot e (e < L) or new
-// record e - L; (k_e . k_j) and (k_e . q_i) for all 32 entries come from two
-// warps' tensor-core products [32 x 128] . [128 x 8]. After the cursor: the
+// record e - L; (k_e . k_j) and (k_e . q_i) for all 32 entries come from
+// tensor-core products [32 x 128] . [128 x 8], warp w taking entries
+// 16 (w & 1) .. + 15 over column half w >> 1 (readers add the halves). After the cursor: the
 // window records' e rows by one 256-byte bulk copy each (second mbarrier), one
 // inclusive warp scan of g, and a per-block table of the committed records'
-// coefficients D (k_t . vec). Each warp then forms S0 . [k_0..k_3, q_0..q_3] for
+// coefficients D (k_t . vec), warp w building rows w and w + 4. Each warp then forms S0 . [k_0..k_3, q_0..q_3] for
 // its 16 rows as m16n8k8 tf32 mma (the fp32 state split into two tf32 parts),
 // adds the committed window's terms, solves the new records' e in order within
 // each quad and completes the outputs. If count + K > L the

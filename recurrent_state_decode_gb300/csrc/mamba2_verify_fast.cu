@@ -13,18 +13,21 @@
 // gate z of new record i at row r, and every lane its column chunk of the new
 // records' C. Records are indexed k in [0, count + K): k < count the committed
 // window (ring slot (start + k) mod L), then the K new ones. Entry e of the
-// B.C table is ring slot e (e < L) or new record e - L; warp w forms the dots
-// of entries w, w+4, ... against all four C_i (two batches of 16 partials per
-// lane, one transposed reduction each), shared through shared memory.
+// B.C table is ring slot e (e < L) or new record e - L; the table [32 x 128] .
+// [128 x 4] is a tensor-core product (m16n8k8 tf32, the bf16 inputs exact),
+// warp w taking entries 16 (w & 1) .. + 15 over column half w >> 1, and the
+// readers add the halves. Warp w then builds row w of the coefficient table.
 //
 // Once the cursor is known lane k takes record k by a shuffle and one
 // inclusive warp scan gives S_k = A sum_{j<=k} dt_j. If count + K > L the
 // committed window is folded first, h' = e^{S_{count-1}} h0 + sum_{k<count}
-// dt_k e^{S_{count-1}-S_k} x_k B_k^T, written once (with the bf16 read copy),
+// dt_k e^{S_{count-1}-S_k} x_k B_k^T, written once (with the read copy),
 // and output i covers records [count, count+i]; otherwise h' = h0 and output i
 // covers [0, count+i]. Output i: y_i[r] = (e^{S_last - S_first-1} (h' . C_i)[r]
 // + sum_k dt_k e^{S_last - S_k} (B_k . C_i) x_k[r] + D x_last[r]) silu(z_i[r]),
-// last = count + i, one transposed 8-row reduction per output and row group.
+// last = count + i; h0 . [C_0..C_3] is an m16n8k8 tf32 product per warp (the
+// fp32 state split in two tf32 parts, a 16-bit read copy exact in tf32, an fp8
+// one scaled by its row scales after the product).
 // The new records' x and z rows go to the ring here (these rows are read by
 // this block alone); their B, C and dt rows, which other blocks read, are
 // appended by the last of the sequence's blocks to finish (an arrival count in
