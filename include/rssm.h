@@ -37,11 +37,11 @@
  *    touched). Any other slot outside [0, n_slots) is reported as
  *    RSSM_DEV_BAD_SLOT and its row skipped. Two rows of one call must not
  *    name the same slot (their state updates would race). State slots are
- *    honoured by the decode calls (step, spec_verify) on the shape-specialised
- *    kernels -- Mamba-2 dstate 128, headdim a multiple of 64, a power-of-two
- *    nheads / ngroups; Gated DeltaNet and KDA dk = dv = 128 -- and by
- *    rssm_commit_cursors_slots; elsewhere a non-NULL state_slots returns
- *    RSSM_ERR_UNSUPPORTED. Calls on whole state arrays (flush, prime,
+ *    honoured by the decode calls on the shape-specialised kernels -- the
+ *    Mamba-2 step and spec_verify (dstate 128, headdim a multiple of 64, a
+ *    power-of-two nheads / ngroups), the Gated DeltaNet step and spec_verify
+ *    and the KDA step (dk = dv = 128) -- and by rssm_commit_cursors_slots;
+ *    elsewhere a non-NULL state_slots returns RSSM_ERR_UNSUPPORTED. Calls on whole state arrays (flush, prime,
  *    downcast, conventional steps) take state_slots = NULL with batch = the
  *    number of state rows.
  *
