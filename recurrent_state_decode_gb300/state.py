@@ -9,6 +9,13 @@ import torch
 from . import binding as bd
 
 
+def _check_slots(slots, like):
+    """A slot table is a contiguous int32 tensor on the state's device."""
+    if slots.dtype != torch.int32 or slots.device != like.device or not slots.is_contiguous():
+        raise ValueError(f"state slots must be a contiguous int32 tensor on {like.device}, "
+                         f"got {slots.dtype} on {slots.device}")
+
+
 class Mamba2State:
     """Checkpoint (+ optional read copy: read_copy True or "bf16" for bf16,
     "f16" for fp16, "f8" for e4m3 with one fp32 scale per state row), ring
@@ -57,6 +64,7 @@ class Mamba2State:
 
     def slot_desc(self, slots):
         """The descriptor of a call whose batch rows use state rows ``slots``."""
+        _check_slots(slots, self.ckpt)
         d = self.desc
         return bd.mamba2_desc(slots.numel(), d.nheads, d.headdim, d.dstate, d.ngroups, d.buf_len, d.out_dtype,
                               d.read_dtype, state_slots=slots, n_slots=self.batch)
@@ -90,6 +98,8 @@ class Mamba2State:
 
 
 def _commit(st, kept, stream, slots):
+    if slots is not None:
+        _check_slots(slots, st.cursors)
     if slots is None:
         bd.check(bd.rssm_commit_cursors(st.cursors, kept, st.batch, st.buf_len, st.status, stream),
                  "rssm_commit_cursors")
@@ -127,6 +137,7 @@ class GDNState:
         return torch.empty((rows, self.nheads, self.dv), dtype=self.o_dtype, device=self.S.device)
 
     def slot_desc(self, slots):
+        _check_slots(slots, self.S)
         d = self.desc
         return bd.gdn_desc(slots.numel(), d.nheads, d.dk, d.dv, d.buf_len, d.out_dtype, state_slots=slots,
                            n_slots=self.batch)

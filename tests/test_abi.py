@@ -260,3 +260,22 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bd, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         bd.load()
+
+
+def test_slot_tables_are_checked_before_any_call():
+    """The state layer refuses a slot table the kernels would misread (not
+    int32, not on the state's device, not contiguous); nothing is launched."""
+    import torch
+
+    from recurrent_state_decode_gb300.state import GDNState, Mamba2State
+    m = Mamba2State(2, 4, 64, 128, 2, 8, device="cpu")
+    g = GDNState(2, 2, 128, 128, 8, device="cpu")
+    for st in (m, g):
+        with pytest.raises(ValueError):
+            st.slot_desc(torch.zeros(3, dtype=torch.int64))
+        with pytest.raises(ValueError):
+            st.slot_desc(torch.zeros(6, dtype=torch.int32)[::2])
+        d = st.slot_desc(torch.tensor([1, -1, 0], dtype=torch.int32))
+        assert d.batch == 3 and d.n_slots == 2
+    with pytest.raises(ValueError):
+        m.commit(torch.zeros(3, dtype=torch.int32), slots=torch.zeros(3, dtype=torch.int64))
