@@ -2,6 +2,8 @@
 // caller's stream. Nothing here allocates, synchronises or reads device data.
 #include <climits>
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "kernels.h"
 #include "rssm.h"
@@ -588,3 +590,41 @@ int rssm_kda_prime(const rssm_kda_desc* d, const float* S, const rssm_kda_ring* 
 }
 
 }  // extern "C"
+
+namespace rssm {
+
+cudaError_t prepare_kernel(const void* fn, size_t dyn_smem, bool max_carveout) {
+  struct Entry {
+    const void* fn;
+    int device;
+    size_t smem;  // dynamic shared-memory limit set so far (0: the default)
+    bool carveout;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t need = dyn_smem > 48 * 1024 ? dyn_smem : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry* ent = nullptr;
+  for (Entry& d : done)
+    if (d.fn == fn && d.device == dev) ent = &d;
+  if (!ent) {
+    done.push_back(Entry{fn, dev, 0, false});
+    ent = &done.back();
+  }
+  if (max_carveout && !ent->carveout) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    ent->carveout = true;
+  }
+  if (need > ent->smem) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+    if (e != cudaSuccess) return e;
+    ent->smem = need;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace rssm

@@ -322,10 +322,8 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_replay_kernel(GdnArgs a) {
 namespace {
 template <typename Kern>
 cudaError_t launch_gdn(Kern k, int grid, size_t smem, cudaStream_t st, const GdnArgs& a) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = prepare(k, smem, false);
+  if (e != cudaSuccess) return e;
   k<<<grid, GDN_THREADS, smem, st>>>(a);
   return cudaGetLastError();
 }

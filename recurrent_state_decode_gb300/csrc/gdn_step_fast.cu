@@ -229,9 +229,7 @@ cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st
   auto k = a.slots ? (out_bf16 ? gdn_step_fast_kernel<true, true> : gdn_step_fast_kernel<false, true>)
                    : (out_bf16 ? gdn_step_fast_kernel<true, false> : gdn_step_fast_kernel<false, false>);
   const int smem = (FPB * GD + a.L * ES) * 4;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<dim3(2, a.H, a.Bt), FT, smem, st>>>(a);
   return cudaGetLastError();

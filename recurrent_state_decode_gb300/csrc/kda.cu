@@ -387,10 +387,8 @@ __global__ void __launch_bounds__(FT) kda_verify_epilogue_kernel(GdnArgs a) {
 
 template <typename Kern>
 cudaError_t launch_smem(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t st, const GdnArgs& a) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = prepare(k, smem, false);
+  if (e != cudaSuccess) return e;
   k<<<grid, threads, smem, st>>>(a);
   return cudaGetLastError();
 }

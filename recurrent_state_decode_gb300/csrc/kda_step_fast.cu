@@ -252,9 +252,7 @@ cudaError_t kda_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st
   };
   auto k = a.slots ? pick(std::true_type{}) : pick(std::false_type{});
   const int smem = (FPB * GD + (a.L - 1) * (ES + GD)) * 4;  // five blocks per SM at L = 16
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<dim3(2, a.H, a.Bt), FT, smem, st>>>(a);
   return cudaGetLastError();

@@ -100,6 +100,17 @@ cudaError_t downcast_launch(const float* src, uint16_t* dst, size_t n, bool f16,
 // fp8 read copy of `rows` rows of 128 fp32 values, with one scale per row after the bytes.
 cudaError_t downcast_f8_launch(const float* src, uint8_t* dst, size_t rows, cudaStream_t st);
 
+// Launch attributes of a kernel on the current device, set the first time a
+// launch needs them rather than on every launch: the largest shared-memory
+// carveout of the unified L1 (when max_carveout) and a dynamic shared-memory
+// limit of at least dyn_smem bytes (when above the 48 KiB default). Later
+// calls that need no more are a table lookup under a mutex.
+cudaError_t prepare_kernel(const void* fn, size_t dyn_smem, bool max_carveout);
+template <typename Kern>
+inline cudaError_t prepare(Kern* k, size_t dyn_smem, bool max_carveout) {
+  return prepare_kernel(reinterpret_cast<const void*>(k), dyn_smem, max_carveout);
+}
+
 // Row stride of the per-record scalar rings (dt; g, beta): L rounded up to a
 // multiple of 4 slots, so that a row is a whole number of 16-byte units.
 inline __host__ __device__ int pad4(int L) { return (L + 3) & ~3; }

@@ -376,10 +376,8 @@ namespace {
 
 template <typename Kern>
 cudaError_t launch(Kern k, int grid, size_t smem, cudaStream_t st, const M2Args& a) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = prepare(k, smem, false);
+  if (e != cudaSuccess) return e;
   k<<<grid, 128, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -229,8 +229,7 @@ cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) 
   auto k = a.slots ? pick(std::true_type{}) : pick(std::false_type{});
   const int smem = rd16 ? FPB * FN * 2 : 0;
   // six 32 KiB (seven 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<grid, FT, smem, st>>>(a);
   return cudaGetLastError();

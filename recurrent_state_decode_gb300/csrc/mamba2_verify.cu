@@ -406,7 +406,7 @@ cudaError_t launch_verify(const M2Args& a, cudaStream_t st) {
   const int ntiles = a.Bt * a.H * a.nPB;
   const int grid = ntiles < di.sms ? ntiles : di.sms;
   auto k = m2_verify_kernel<LM, NCH, OUT_BF16>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = prepare(k, smem, false);
   if (e != cudaSuccess) return e;
   k<<<grid, THREADS, smem, st>>>(a, lay, S, ntiles);
   return cudaGetLastError();

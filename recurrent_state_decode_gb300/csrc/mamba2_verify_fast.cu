@@ -435,9 +435,7 @@ cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st
   auto k = a.slots ? (out_bf16 ? m2_verify_fast_kernel<true, true> : m2_verify_fast_kernel<false, true>)
                    : (out_bf16 ? m2_verify_fast_kernel<true, false> : m2_verify_fast_kernel<false, false>);
   const int smem = FPB * FN * 4 + (a.L + a.K) * FPB * 2;  // tile + the records' x rows
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<grid, FT, smem, st>>>(a);
   return cudaGetLastError();
