@@ -62,13 +62,21 @@ def status(st):
     return int(st.status.item())
 
 
-def ref_f8(x):
-    """Reference fp8 read copy of fp32 rows x [..., 128]: (e4m3 bytes, fp32 row
-    scales) with scale = max|row| / 448 and values x * (448 / max|row|) rounded
-    to nearest even, as the arithmetic of the format fixes them."""
-    import torch
-    m = x.abs().amax(dim=-1, keepdim=True)
-    c448 = torch.full_like(m, 448.0)  # tensor / tensor: IEEE fp32 division, as the format's definition reads
-    inv = torch.where(m > 0, c448 / m, torch.zeros_like(m))
-    q = (x * inv).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
-    return q, (m / c448).squeeze(-1)
+def bits16(t):
+    """The 16-bit codes of a bf16 / fp16 tensor, as uint16 numpy."""
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_read_copy(st, b):
+    """State row b's read copy equals the oracle's rounding of its fp32
+    checkpoint bit for bit (bf16 / fp16 codes; e4m3 codes and row scales)."""
+    from oracle import readcopy as rc
+    ck = st.ckpt[b].cpu().numpy()
+    if getattr(st, "read_q", None) is not None:
+        q, sc = rc.e4m3_rows(ck)
+        np.testing.assert_array_equal(st.read_q[b].cpu().numpy(), q)
+        np.testing.assert_array_equal(st.read_scale[b].cpu().numpy(), sc)
+    elif st.ckpt_read.dtype == torch.float16:
+        np.testing.assert_array_equal(bits16(st.ckpt_read[b]), rc.fp16_bits(rc.to_fp16(ck)))
+    else:
+        np.testing.assert_array_equal(bits16(st.ckpt_read[b]), rc.bf16_bits(rc.to_bf16(ck)))

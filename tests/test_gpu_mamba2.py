@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import harness as H
+from oracle import readcopy as rc
 from oracle import sessions
 from recurrent_state_decode_gb300 import binding as bd
 from recurrent_state_decode_gb300 import inputs as I
@@ -64,11 +65,8 @@ def run_ar(w, out_dtype=bd.RSSM_F32, seqs=None, read_copy=None, steps=None, trac
                 flushes += 1
                 e = H.rel_l2(H.F64(st.ckpt[b]), exp["state"][i])
                 assert e <= TOL_CKPT, (t, b, e)
-                if read_copy and rc_f8:  # the fp8 read copy is the scaled RNE downcast of the new checkpoint
-                    q, sc = H.ref_f8(st.ckpt[b])
-                    assert torch.equal(st.read_q[b], q) and torch.equal(st.read_scale[b], sc)
-                elif read_copy:  # the read copy is the RNE downcast of the new checkpoint
-                    assert torch.equal(st.ckpt_read[b], st.ckpt[b].to(st.ckpt_read.dtype))
+                if read_copy:  # the read copy is the oracle's rounding of the new checkpoint, bit for bit
+                    H.assert_read_copy(st, b)
     assert H.status(st) == 0
     return flushes
 
@@ -324,12 +322,14 @@ def test_downcast_rne():
     x[:5] = torch.tensor([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -0.0, float("inf"), 1e-40])  # ties to even, signed zero, inf, subnormal
     out = torch.empty(1001, dtype=torch.bfloat16, device=dev)
     bd.check(bd.rssm_checkpoint_downcast(x, out, 1001, bd.RSSM_BF16))
-    assert torch.equal(out.view(torch.int16), x.to(torch.bfloat16).view(torch.int16))
+    xs = x.cpu().numpy()
+    np.testing.assert_array_equal(H.bits16(out), rc.bf16_bits(rc.to_bf16(xs)))
     # fp16: ties to even at 1 + 2^-11 and 1 + 3 * 2^-11, overflow to inf, fp16 subnormals
     x[:5] = torch.tensor([1.0 + 2 ** -11, 1.0 + 3 * 2 ** -11, 70000.0, -3e-6, 2 ** -25])
     h = torch.empty(1001, dtype=torch.float16, device=dev)
     bd.check(bd.rssm_checkpoint_downcast(x, h, 1001, bd.RSSM_F16))
-    assert torch.equal(h.view(torch.int16), x.to(torch.float16).view(torch.int16))
+    xs = x.cpu().numpy()
+    np.testing.assert_array_equal(H.bits16(h), rc.fp16_bits(rc.to_fp16(xs)))
 
 
 def test_downcast_f8_rows():
@@ -343,8 +343,9 @@ def test_downcast_f8_rows():
     st.ckpt[0, 0, 1] = -torch.rand(128, device="cuda") - 1.0
     st.ckpt[0, 1, 2] = 3.25
     st.downcast()
-    q, sc = H.ref_f8(st.ckpt)
-    assert torch.equal(st.read_q, q) and torch.equal(st.read_scale, sc)
+    q, sc = rc.e4m3_rows(st.ckpt.cpu().numpy())
+    np.testing.assert_array_equal(st.read_q.cpu().numpy(), q)
+    np.testing.assert_array_equal(st.read_scale.cpu().numpy(), sc)
     assert st.read_scale[0, 0, 0].item() == 0.0
 
 

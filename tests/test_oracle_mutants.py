@@ -27,6 +27,8 @@ def _run_pins(module):
         cases = [{}]
         if "m" in params:
             cases = [{"m": m} for m in (1, 5, 16)]
+        if "fmt" in params:
+            cases = [{"fmt": f} for f in ("bf16", "fp16")]
         for kw in cases:
             if "rng" in params:
                 kw = dict(kw, rng=np.random.default_rng(99))
@@ -165,3 +167,62 @@ def test_kda_replay_mutant_caught(monkeypatch):
     monkeypatch.setattr(kda, "_window_terms", _kda_undecayed_keys)
     with pytest.raises(AssertionError):
         pins_kda.test_replay_equals_conventional(np.random.default_rng(3), 5)
+
+
+# ----------------------------------------------------------------------------- read-copy rounding
+
+import oracle.readcopy as readcopy  # noqa: E402
+import test_oracle_readcopy as pins_rc  # noqa: E402
+
+
+def _round_mutant(variant):
+    real = readcopy.round_rne
+
+    def rnd(x, fmt, saturate=False):
+        p, emin, vmax = fmt
+        if variant == "half_away":       # ties away from zero instead of to even
+            x = np.asarray(x, np.float64)
+            r = real(x, fmt, saturate)
+            a = np.abs(x)
+            e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+            sp = np.ldexp(1.0, (np.maximum(e, emin) - p + 1).astype(np.int64))
+            tie = np.abs(np.abs(x) / sp - np.floor(np.abs(x) / sp) - 0.5) == 0
+            return np.where(tie & (a > 0), np.copysign(np.abs(r) + np.where(np.abs(r) < a, sp, 0), x), r)
+        if variant == "truncate":        # drops the low bits instead of rounding
+            x = np.asarray(x, np.float64)
+            r = real(x, fmt, saturate)
+            a = np.abs(x)
+            e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+            sp = np.ldexp(1.0, (np.maximum(e, emin) - p + 1).astype(np.int64))
+            t = np.copysign(np.floor(a / sp) * sp, x)
+            return np.where(np.isfinite(r) & (np.abs(r) <= vmax), t, r)
+        if variant == "no_subnormals":   # flushes below the smallest normal to zero
+            r = real(x, fmt, saturate)
+            return np.where(np.abs(r) < 2.0 ** emin, 0.0 * r, r)
+        if variant == "one_bit_short":   # one significant bit too few
+            return real(x, (p - 1, emin, vmax), saturate)
+        if variant == "no_saturation":   # e4m3 overflow to inf
+            return real(x, fmt, False)
+        raise AssertionError(variant)
+    return rnd
+
+
+@pytest.mark.parametrize("variant", ["half_away", "truncate", "no_subnormals", "one_bit_short", "no_saturation"])
+def test_readcopy_pins_catch(monkeypatch, variant):
+    monkeypatch.setattr(readcopy, "round_rne", _round_mutant(variant))
+    with np.errstate(all="ignore"):
+        failed = _run_pins(pins_rc)
+    assert failed, f"mutant {variant} passed every read-copy pin"
+
+
+def test_readcopy_row_scale_mutant_caught(monkeypatch):
+    """Scale by the row's mean magnitude instead of its maximum."""
+    def rows(x):
+        x = np.asarray(x, np.float32)
+        m = np.mean(np.abs(x), axis=-1, keepdims=True).astype(np.float32)
+        inv = np.where(m > 0, np.float32(448) / m, np.float32(0)).astype(np.float32)
+        codes = readcopy.e4m3_bits(readcopy.to_e4m3((x * inv).astype(np.float64)))
+        return codes, (m / np.float32(448)).astype(np.float32)[..., 0]
+    monkeypatch.setattr(readcopy, "e4m3_rows", rows)
+    failed = _run_pins(pins_rc)
+    assert failed
