@@ -49,14 +49,15 @@ def round_rne(x, fmt, saturate=False):
     p, emin, vmax = fmt
     x = np.asarray(x, np.float64)
     a = np.abs(x)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    fin = np.isfinite(x) & (a > 0)            # zeros, infinities and NaN are settled below
+    a1 = np.where(fin, a, 1.0)
+    e = np.floor(np.log2(a1))
     # log2 of a value just below a power of two can round up to the exponent;
     # settle e so that 2^e <= a < 2^(e + 1) holds exactly
-    e = np.where(np.ldexp(1.0, e.astype(np.int64)) > a, e - 1, e)
-    e = np.where(np.ldexp(1.0, (e + 1).astype(np.int64)) <= a, e + 1, e)
+    e = np.where(np.ldexp(1.0, e.astype(np.int64)) > a1, e - 1, e)
+    e = np.where(np.ldexp(1.0, (e + 1).astype(np.int64)) <= a1, e + 1, e)
     spacing_exp = (np.maximum(e, emin) - p + 1).astype(np.int64)
-    q = np.round(np.ldexp(x, -spacing_exp))          # exact scaling; half to even
+    q = np.round(np.ldexp(np.where(fin, x, 0.0), -spacing_exp))   # exact scaling; half to even
     r = np.ldexp(q, spacing_exp)
     over = np.abs(r) > vmax
     if saturate:
