@@ -16,6 +16,33 @@ def _check_slots(slots, like):
                          f"got {slots.dtype} on {slots.device}")
 
 
+def _check_tensor(name, t, dtype, shape, device):
+    """A tensor argument is a contiguous tensor of the given dtype and shape on
+    the state's device: the C ABI reads it by its base pointer alone."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch tensor, got {type(t).__name__}")
+    shape = tuple(int(v) for v in shape)
+    if t.dtype != dtype or t.device != device or tuple(t.shape) != shape or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape} on {device}, got {t.dtype} "
+                         f"{tuple(t.shape)} on {t.device}{'' if t.is_contiguous() else ' (not contiguous)'}")
+
+
+def _check_records(rec, spec, rows, device, n_new=None):
+    """Record fields against their (dtype, per-row shape); n_new adds the draft axis."""
+    lead = (rows,) if n_new is None else (rows, n_new)
+    for name, (dtype, tail) in spec.items():
+        if name not in rec:
+            raise ValueError(f"record field {name} is missing")
+        _check_tensor(name, rec[name], dtype, lead + tail, device)
+
+
+def _draft_count(rec, field):
+    t = rec.get(field)
+    if not isinstance(t, torch.Tensor) or t.dim() < 2 or t.shape[1] < 1:
+        raise ValueError(f"{field} of a verify must have a draft axis [rows, K, ...] with K >= 1")
+    return int(t.shape[1])
+
+
 class Mamba2State:
     """Checkpoint (+ optional read copy: read_copy True or "bf16" for bf16,
     "f16" for fp16, "f8" for e4m3 with one fp32 scale per state row), ring
@@ -72,19 +99,39 @@ class Mamba2State:
     def downcast(self, stream=None):
         bd.check(bd.rssm_mamba2_downcast(self.desc, self.ckpt, self.ckpt_read, stream), "rssm_mamba2_downcast")
 
+    def _record_spec(self):
+        H, P, N, G = self.nheads, self.headdim, self.dstate, self.ngroups
+        bf, f32 = torch.bfloat16, torch.float32
+        return {"x": (bf, (H, P)), "z": (bf, (H, P)), "B": (bf, (G, N)), "C": (bf, (G, N)), "dt": (f32, (H,))}
+
+    def _check_params(self, A, D=None):
+        dev = self.ckpt.device
+        _check_tensor("A", A, torch.float32, (self.nheads,), dev)
+        if D is not None:
+            _check_tensor("D", D, torch.float32, (self.nheads,), dev)
+
     def step(self, rec, A, D, y, stream=None, slots=None):
         desc = self.desc if slots is None else self.slot_desc(slots)
+        dev = self.ckpt.device
+        _check_records(rec, self._record_spec(), desc.batch, dev)
+        self._check_params(A, D)
+        _check_tensor("y", y, self.y_dtype, (desc.batch, self.nheads, self.headdim), dev)
         bd.check(bd.rssm_mamba2_step(desc, self.ckpt, self.ckpt_read, self.ring, self.cursors,
                                      rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
                                      self.status, stream), "rssm_mamba2_step")
 
     def flush(self, A, stream=None):
+        self._check_params(A)
         bd.check(bd.rssm_mamba2_flush(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors, A,
                                       self.status, stream), "rssm_mamba2_flush")
 
     def verify(self, rec, A, D, y, stream=None, slots=None):
-        n_new = rec["x"].shape[1]
+        n_new = _draft_count(rec, "x")
         desc = self.desc if slots is None else self.slot_desc(slots)
+        dev = self.ckpt.device
+        _check_records(rec, self._record_spec(), desc.batch, dev, n_new)
+        self._check_params(A, D)
+        _check_tensor("y", y, self.y_dtype, (desc.batch, n_new, self.nheads, self.headdim), dev)
         bd.check(bd.rssm_mamba2_spec_verify(desc, n_new, self.ckpt, self.ckpt_read, self.ring, self.cursors,
                                             rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
                                             self.status, stream), "rssm_mamba2_spec_verify")
@@ -93,6 +140,7 @@ class Mamba2State:
         _commit(self, kept, stream, slots)
 
     def reset(self, slots, stream=None):
+        _check_slots(slots, self.cursors)
         bd.check(bd.rssm_reset_cursors(self.cursors, slots, slots.numel(), self.batch, self.status, stream),
                  "rssm_reset_cursors")
 
@@ -100,6 +148,7 @@ class Mamba2State:
 def _commit(st, kept, stream, slots):
     if slots is not None:
         _check_slots(slots, st.cursors)
+    _check_tensor("kept", kept, torch.int32, (st.batch if slots is None else slots.numel(),), st.cursors.device)
     if slots is None:
         bd.check(bd.rssm_commit_cursors(st.cursors, kept, st.batch, st.buf_len, st.status, stream),
                  "rssm_commit_cursors")
@@ -142,8 +191,20 @@ class GDNState:
         return bd.gdn_desc(slots.numel(), d.nheads, d.dk, d.dv, d.buf_len, d.out_dtype, state_slots=slots,
                            n_slots=self.batch)
 
+    def _record_spec(self):
+        H, bf, f32 = self.nheads, torch.bfloat16, torch.float32
+        return {"q": (bf, (H, self.dk)), "k": (bf, (H, self.dk)), "v": (bf, (H, self.dv)), "g": (f32, (H,)),
+                "beta": (f32, (H,))}
+
+    def _check_call(self, rec, o, desc, n_new=None):
+        dev = self.S.device
+        _check_records(rec, self._record_spec(), desc.batch, dev, n_new)
+        lead = (desc.batch,) if n_new is None else (desc.batch, n_new)
+        _check_tensor("o", o, self.o_dtype, lead + (self.nheads, self.dv), dev)
+
     def step(self, rec, o, stream=None, slots=None):
         desc = self.desc if slots is None else self.slot_desc(slots)
+        self._check_call(rec, o, desc)
         bd.check(bd.rssm_gdn_step(desc, self.S, self.ring, self.cursors, rec["q"], rec["k"], rec["v"],
                                   rec["g"], rec["beta"], o, self.status, stream), "rssm_gdn_step")
 
@@ -158,7 +219,9 @@ class GDNState:
     def verify(self, rec, o, stream=None, slots=None):
         """rec: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g,beta [Bt,K,H] fp32; o [Bt,K,H,dv]."""
         desc = self.desc if slots is None else self.slot_desc(slots)
-        bd.check(bd.rssm_gdn_spec_verify(desc, rec["q"].shape[1], self.S, self.ring, self.cursors, rec["q"],
+        n_new = _draft_count(rec, "q")
+        self._check_call(rec, o, desc, n_new)
+        bd.check(bd.rssm_gdn_spec_verify(desc, n_new, self.S, self.ring, self.cursors, rec["q"],
                                          rec["k"], rec["v"], rec["g"], rec["beta"], o, self.status, stream),
                  "rssm_gdn_spec_verify")
 
@@ -180,8 +243,14 @@ class KDAState(GDNState):
         self.rg = torch.zeros((batch, nheads, buf_len, dk), dtype=torch.float32, device=self.S.device)
         self.ring = bd.kda_ring(self.rq, self.rk, self.rv, self.rg, self.rbeta, self.re)
 
+    def _record_spec(self):
+        spec = super()._record_spec()
+        spec["g"] = (torch.float32, (self.nheads, self.dk))
+        return spec
+
     def step(self, rec, o, stream=None, slots=None):
         desc = self.desc if slots is None else self.slot_desc(slots)
+        self._check_call(rec, o, desc)
         bd.check(bd.rssm_kda_step(desc, self.S, self.ring, self.cursors, rec["q"], rec["k"], rec["v"],
                                   rec["g"], rec["beta"], o, self.status, stream), "rssm_kda_step")
 
@@ -198,7 +267,9 @@ class KDAState(GDNState):
         """rec: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g [Bt,K,H,dk], beta [Bt,K,H] fp32; o [Bt,K,H,dv]."""
         if slots is not None:
             raise ValueError("the KDA verify takes no state slots")
-        bd.check(bd.rssm_kda_spec_verify(self.desc, rec["q"].shape[1], self.S, self.ring, self.cursors, rec["q"],
+        n_new = _draft_count(rec, "q")
+        self._check_call(rec, o, self.desc, n_new)
+        bd.check(bd.rssm_kda_spec_verify(self.desc, n_new, self.S, self.ring, self.cursors, rec["q"],
                                          rec["k"], rec["v"], rec["g"], rec["beta"], o, self.status, stream),
                  "rssm_kda_spec_verify")
 

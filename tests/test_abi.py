@@ -279,3 +279,57 @@ def test_slot_tables_are_checked_before_any_call():
         assert d.batch == 3 and d.n_slots == 2
     with pytest.raises(ValueError):
         m.commit(torch.zeros(3, dtype=torch.int32), slots=torch.zeros(3, dtype=torch.int64))
+
+
+def test_record_tensors_are_checked_before_any_call():
+    """The state layer refuses record, output and kept tensors the kernels
+    would misread: a wrong dtype, device, row count or shape, or a
+    non-contiguous view raises ValueError before the C ABI is reached."""
+    import torch
+
+    from recurrent_state_decode_gb300.state import GDNState, KDAState, Mamba2State
+    m = Mamba2State(2, 4, 64, 128, 2, 8, device="cpu")
+    bf, f32 = torch.bfloat16, torch.float32
+    rec = {"x": torch.zeros(2, 4, 64, dtype=bf), "z": torch.zeros(2, 4, 64, dtype=bf),
+           "B": torch.zeros(2, 2, 128, dtype=bf), "C": torch.zeros(2, 2, 128, dtype=bf),
+           "dt": torch.zeros(2, 4, dtype=f32)}
+    A, D, y = torch.zeros(4), torch.zeros(4), torch.zeros(2, 4, 64)
+    bad = [dict(rec, dt=torch.zeros(2, 4, dtype=bf)),                      # dt not fp32
+           dict(rec, x=torch.zeros(2, 4, 128, dtype=bf)[..., ::2]),        # a strided view of x
+           dict(rec, B=torch.zeros(1, 2, 128, dtype=bf)),                  # too few rows
+           dict(rec, C=torch.zeros(2, 2, 64, dtype=bf)),                   # wrong dstate
+           {k: v for k, v in rec.items() if k != "z"}]                     # a missing field
+    if torch.cuda.is_available():
+        bad.append(dict(rec, x=rec["x"].cuda()))                           # another device
+    for r in bad:
+        with pytest.raises(ValueError):
+            m.step(r, A, D, y)
+    with pytest.raises(ValueError):
+        m.step(rec, A, D, torch.zeros(2, 4, 64, dtype=bf))                 # y of the wrong dtype
+    with pytest.raises(ValueError):
+        m.step(rec, A.double(), D, y)                                      # A not fp32
+    with pytest.raises(ValueError):
+        m.step(rec, A, D, y, slots=torch.tensor([1, -1, 0], dtype=torch.int32))  # 2 record rows for 3 slot rows
+    vrec = {k: torch.stack([v, v], 1) for k, v in rec.items()}
+    with pytest.raises(ValueError):
+        m.verify(vrec, A, D, torch.zeros(2, 3, 4, 64))                     # y with 3 drafts for 2
+    with pytest.raises(ValueError):
+        m.verify(rec, A, D, y)                                             # no draft axis
+    with pytest.raises(ValueError):
+        m.commit(torch.zeros(2, dtype=torch.int64))                        # kept not int32
+    with pytest.raises(ValueError):
+        m.commit(torch.zeros(3, dtype=torch.int32))                        # kept of the wrong length
+    with pytest.raises(ValueError):
+        m.flush(torch.zeros(3))
+    g = GDNState(2, 2, 128, 128, 8, device="cpu")
+    grec = {"q": torch.zeros(2, 2, 128, dtype=bf), "k": torch.zeros(2, 2, 128, dtype=bf),
+            "v": torch.zeros(2, 2, 128, dtype=bf), "g": torch.zeros(2, 2), "beta": torch.zeros(2, 2)}
+    with pytest.raises(ValueError):
+        g.step(dict(grec, v=torch.zeros(2, 2, 64, dtype=bf)), torch.zeros(2, 2, 128))
+    with pytest.raises(ValueError):
+        g.step(grec, torch.zeros(2, 2, 128, dtype=bf))                     # o of the wrong dtype
+    k = KDAState(2, 2, 128, 128, 8, device="cpu")
+    with pytest.raises(ValueError):
+        k.step(grec, torch.zeros(2, 2, 128))                               # KDA g is per key channel
+    with pytest.raises(ValueError):
+        k.verify({f: torch.stack([v, v], 1) for f, v in grec.items()}, torch.zeros(2, 2, 2, 128))
