@@ -81,3 +81,31 @@ def test_bytes_model_serving_cycle():
     kv = bm.kda_verify_bytes(32, 128, 128, 16, 4, [12, 13])
     assert kv == (2097152 + 4 * (2 * krec + e) + 12 * kpast + 4 * 32 * 128 * 2 + 68) + \
         (2 * 2097152 + 4 * (2 * krec + e) + 13 * kpast + 4 * 32 * 128 * 2 + 68)
+
+
+def test_oracle_baseline_runs_on_several_cores():
+    """The CPU baseline's worker pool (spawned processes, one chunk of
+    sequences each) times the oracle on the tiny configuration."""
+    v, sample, used = bench.oracle_baseline("mamba2_tiny", 0.2, 2)
+    assert v > 0 and used == 2
+    assert "4 of 4 sequences on 2 worker processes" in sample
+
+
+def test_printed_line_keeps_the_claims_in_its_tail():
+    """The contract's keys come first; the comparison with the conventional
+    kernel closes the line, which stays short enough to be read whole."""
+    wl = {n: {"us_per_step": 123.456789, "frac": 0.612345, "speedup_vs_conventional": 1.3456,
+              "conventional_us_per_step": 188.0123, "accepted_tokens_per_s": 3.0e6, "hbm_gbs": 4600.1,
+              "algorithmic_bytes_per_step": 6.4e8, "steps": 20}
+          for n in ("mamba2_bf16_read", "mamba2_f16_read", "mamba2_f8_read", "mamba2_spec", "gdn_serving",
+                    "kda_serving", "gdn_spec", "kda_spec", "mamba2_emu_e4m3")}
+    res = {"metric": bench.METRIC, "value": 209.1234567, "unit": bench.UNIT, "n_gpus": 1, "steps": 20, "warmup": 5,
+           "ms_per_step": 0.2091234, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f32", "data": "synthetic", "config": {"workload": "mamba2_serving"}, "workloads": wl,
+           "speedup_vs_conventional": 1.5432, "conventional_us_per_step": 322.8, "tokens_per_s": 1.2e6,
+           "cpu_baseline": {"value": 1.0, "per_config": {c: {"value": 1.0, "cores": 16} for c in bench.CPU_CONFIGS}}}
+    line = __import__("json").dumps(bench.compact(res))
+    keys = list(bench.compact(res))
+    assert keys[:3] == ["metric", "value", "unit"] and keys[-1] == "speedup_vs_conventional"
+    assert line.index('"cpu_baseline"') < line.index('"workloads"')
+    assert len(line[line.index('"workloads"'):]) < 1500
