@@ -153,3 +153,76 @@ def e4m3_rows(x):
 def e4m3_rows_value(codes, scales):
     """Values an fp8 read copy stands for: e4m3 value * its row's scale."""
     return e4m3_value(codes) * np.asarray(scales, np.float64)[..., None]
+
+
+# ----------------------------------------------------------------------------- emulated read precisions
+
+# "ReplaySSM" (the paper's code repository), introduction: the emulation
+# kernels implement separate read and recurrence precision and expose their
+# quantization behavior. Reading taken: the non-flush read of the fp32
+# checkpoint goes through a quantise-dequantise in a chosen format (nothing
+# low-precision is stored), flushes read the fp32 checkpoint exactly, and
+# the call reports the quantisation error of what it read.
+#
+# Formats: (significant bits p, smallest normal exponent emin, largest finite
+# value); every format saturates at its largest value. INT8 is symmetric
+# 8-bit fixed point: RNE to an integer, clamped to [-127, 127].
+EMU_FORMATS = {
+    "bf16": BF16,
+    "fp16": FP16,
+    "e4m3": E4M3,
+    "e5m2": (3, -14, 57344.0),
+    "int8": None,
+}
+# Scaled formats (a scale per state row of dstate values, or per 64-row tile)
+# store value / s with s = max|group| / qmax; bf16 and fp16 take no scale.
+EMU_QMAX = {"e4m3": 448.0, "e5m2": 57344.0, "int8": 127.0}
+
+
+def emulate_quantise(t, fmt):
+    """t (already divided by its scale) rounded into format fmt, saturating."""
+    t = np.asarray(t, np.float64)
+    if fmt == "int8":
+        return np.clip(np.round(t), -127.0, 127.0)     # half to even
+    return round_rne(t, EMU_FORMATS[fmt], saturate=True)
+
+
+def emulate_read(h, fmt, scale):
+    """The emulated read of fp32 checkpoint rows h [..., rows, n]: the value
+    each element reads as. scale: "none", "row" (one scale per row of n
+    values) or "tile64" (one per 64-row block of a (sequence, head) tile).
+    The scale s = max|group| / qmax and its reciprocal qmax / max|group| are
+    fp32 divisions, the scaled value x * (qmax / max|group|) an fp32 product
+    (a code is decided in the precision the kernel computes in), and the read
+    value code * s an fp32 product; a group of zeros reads as zeros."""
+    h = np.asarray(h, np.float32)
+    if scale == "none":
+        if fmt not in ("bf16", "fp16"):
+            raise ValueError("e4m3, e5m2 and int8 are emulated with a scale")
+        return emulate_quantise(h.astype(np.float64), fmt)
+    if fmt not in EMU_QMAX:
+        raise ValueError("bf16 and fp16 are emulated without a scale")
+    qmax = np.float32(EMU_QMAX[fmt])
+    if scale == "row":
+        m = np.max(np.abs(h), axis=-1, keepdims=True)
+    elif scale == "tile64":
+        rows = h.shape[-2]
+        blocks = h.reshape(h.shape[:-2] + (rows // 64, 64, h.shape[-1]))
+        m = np.max(np.abs(blocks), axis=(-2, -1), keepdims=True)
+        m = np.broadcast_to(m, blocks.shape[:-1] + (1,)).reshape(h.shape[:-1] + (1,))
+    else:
+        raise ValueError(scale)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv = np.where(m > 0, qmax / m, np.float32(0)).astype(np.float32)
+    s = (m / qmax).astype(np.float32)
+    t = (h * inv).astype(np.float32)
+    q = emulate_quantise(t.astype(np.float64), fmt).astype(np.float32)
+    return (q * s).astype(np.float32).astype(np.float64)
+
+
+def emulation_error(h, fmt, scale):
+    """The quantisation behaviour of one emulated read: (sum of squared
+    errors, sum of squares of the exact values) over h."""
+    h64 = np.asarray(h, np.float32).astype(np.float64)
+    d = emulate_read(h, fmt, scale) - h64
+    return float(np.sum(d * d)), float(np.sum(h64 * h64))

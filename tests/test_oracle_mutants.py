@@ -27,8 +27,10 @@ def _run_pins(module):
         cases = [{}]
         if "m" in params:
             cases = [{"m": m} for m in (1, 5, 16)]
-        if "fmt" in params:
-            cases = [{"fmt": f} for f in ("bf16", "fp16")]
+        for mark in getattr(fn, "pytestmark", []):   # a pin's own parametrize cases
+            if mark.name == "parametrize":
+                names = [n.strip() for n in mark.args[0].split(",")]
+                cases = [dict(zip(names, v if len(names) > 1 else (v,))) for v in mark.args[1]]
         for kw in cases:
             if "rng" in params:
                 kw = dict(kw, rng=np.random.default_rng(99))
@@ -226,3 +228,36 @@ def test_readcopy_row_scale_mutant_caught(monkeypatch):
     monkeypatch.setattr(readcopy, "e4m3_rows", rows)
     failed = _run_pins(pins_rc)
     assert failed
+
+
+def test_emulation_mutants_caught(monkeypatch):
+    """int8 codes rounded half away from zero; a tile scale over 32 rows
+    instead of 64; the scale's reciprocal taken after the product."""
+    real = readcopy.emulate_quantise
+
+    def half_away(t, fmt):
+        if fmt == "int8":
+            t = np.asarray(t, np.float64)
+            return np.clip(np.sign(t) * np.floor(np.abs(t) + 0.5), -127.0, 127.0)
+        return real(t, fmt)
+    monkeypatch.setattr(readcopy, "emulate_quantise", half_away)
+    assert _run_pins(pins_rc)
+    monkeypatch.setattr(readcopy, "emulate_quantise", real)
+
+    real_read = readcopy.emulate_read
+
+    def tile32(h, fmt, scale):
+        if scale != "tile64":
+            return real_read(h, fmt, scale)
+        h = np.asarray(h, np.float32)
+        out = np.empty(h.shape)
+        for i in range(0, h.shape[-2], 32):          # one scale per 32 rows
+            blk = h[..., i:i + 32, :]
+            m = np.max(np.abs(blk), axis=(-2, -1), keepdims=True)
+            qmax = np.float32(readcopy.EMU_QMAX[fmt])
+            inv = np.where(m > 0, qmax / m, np.float32(0)).astype(np.float32)
+            q = readcopy.emulate_quantise((blk * inv).astype(np.float32).astype(np.float64), fmt)
+            out[..., i:i + 32, :] = (q.astype(np.float32) * (m / qmax).astype(np.float32)).astype(np.float32)
+        return out
+    monkeypatch.setattr(readcopy, "emulate_read", tile32)
+    assert _run_pins(pins_rc)

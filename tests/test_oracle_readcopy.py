@@ -157,3 +157,80 @@ def test_rounding_is_idempotent_and_monotone(fmt):
     r = f(x)
     np.testing.assert_array_equal(f(r.astype(np.float32)), r)
     assert (np.diff(r) >= 0).all()
+
+
+# ----------------------------------------------------------------------------- emulated read precisions
+
+def test_emulated_bf16_fp16_are_the_read_copies():
+    """Emulated without a scale, bf16 and fp16 read exactly what the stored
+    read copies hold (within range: the emulated formats saturate)."""
+    g = np.random.default_rng(8)
+    h = (g.standard_normal((2, 64, 128)) * 0.1).astype(np.float32)
+    np.testing.assert_array_equal(rc.emulate_read(h, "bf16", "none"), rc.to_bf16(h))
+    np.testing.assert_array_equal(rc.emulate_read(h, "fp16", "none"), rc.to_fp16(h))
+    assert rc.emulate_read(np.float32([1e6]), "fp16", "none")[0] == 65504.0   # saturates
+
+
+def test_emulated_e4m3_row_scale_is_the_fp8_read_copy():
+    g = np.random.default_rng(9)
+    h = (g.standard_normal((3, 64, 128)) * 10.0 ** g.uniform(-3, 1, (3, 64, 1))).astype(np.float32)
+    h[0, 5] = 0.0
+    codes, scales = rc.e4m3_rows(h)
+    want = (rc.e4m3_value(codes).astype(np.float32) * scales[..., None]).astype(np.float32)
+    np.testing.assert_array_equal(rc.emulate_read(h, "e4m3", "row"), want.astype(np.float64))
+
+
+def test_emulated_tile_scale_groups_64_rows():
+    """One scale per 64-row block: scaling one block leaves the other's reads
+    unchanged, and each block's largest element reads back exactly."""
+    g = np.random.default_rng(10)
+    h = (g.standard_normal((128, 128)) * 0.1).astype(np.float32)
+    r1 = rc.emulate_read(h, "int8", "tile64")
+    h2 = h.copy()
+    h2[64:] *= 8
+    r2 = rc.emulate_read(h2, "int8", "tile64")
+    np.testing.assert_array_equal(r1[:64], r2[:64])
+    h3 = h.copy()
+    h3[32:64] *= 8                        # same block as rows 0..31: their scale grows with it
+    assert not np.array_equal(rc.emulate_read(h3, "int8", "tile64")[:32], r1[:32])
+    for blk in (h[:64], h[64:]):
+        i = np.unravel_index(np.argmax(np.abs(blk)), blk.shape)
+        assert rc.emulate_read(blk, "int8", "tile64")[i] == pytest.approx(float(blk[i]), rel=1e-6)
+
+
+def test_emulated_int8_closed_form():
+    """A row with max 127/128 has scale 1/128 and reciprocal 128 (both exact):
+    the codes are 128 v rounded half to even -- 2^-8 -> 0.5 -> 0,
+    1.5/128 -> 2, -2.5/128 -> -2, 100.5/128 -> 100 -- and read back as
+    code / 128; the largest element reads back exactly."""
+    row = np.zeros((1, 128), np.float32)
+    row[0, :5] = [127 / 128, 2.0 ** -8, 1.5 / 128, -2.5 / 128, 100.5 / 128]
+    r = rc.emulate_read(row, "int8", "row")[0, :5]
+    np.testing.assert_array_equal(r, [127 / 128, 0.0, 2 / 128, -2 / 128, 100 / 128])
+    assert np.all(rc.emulate_read(row, "int8", "row")[0, 5:] == 0)
+
+
+@pytest.mark.parametrize("fmt,scale,bound", [("bf16", "none", 2.0 ** -8), ("fp16", "none", 2.0 ** -11),
+                                             ("e4m3", "row", 2.0 ** -4), ("e5m2", "row", 2.0 ** -3),
+                                             ("e4m3", "tile64", 2.0 ** -4)])
+def test_emulated_error_bounds(fmt, scale, bound):
+    """Relative error of an emulated read of normal-range values is at most
+    half a spacing of the format: 2^-p."""
+    g = np.random.default_rng(11)
+    h = (g.standard_normal((2, 64, 128)) * 0.1).astype(np.float32)
+    r = rc.emulate_read(h, fmt, scale)
+    big = np.abs(h) > 0.05 * np.abs(h).max()
+    rel = np.abs(r - h)[big] / np.abs(h)[big]
+    assert rel.max() <= bound * (1 + 1e-6)
+    e, n = rc.emulation_error(h, fmt, scale)
+    assert 0 < e < (bound ** 2) * n
+
+
+def test_emulated_formats_need_their_scales():
+    h = np.ones((64, 128), np.float32)
+    for fmt in ("e4m3", "e5m2", "int8"):
+        with pytest.raises(ValueError):
+            rc.emulate_read(h, fmt, "none")
+    for fmt in ("bf16", "fp16"):
+        with pytest.raises(ValueError):
+            rc.emulate_read(h, fmt, "row")
