@@ -213,6 +213,61 @@ RSSM_API int rssm_mamba2_spec_verify(const rssm_mamba2_desc* desc, int n_new,
                             void* y, int32_t* dev_status,
                             rssm_stream_t stream);
 
+/* Emulated read precision ("ReplaySSM", code repository, introduction: the
+ * emulation kernels implement separate read and recurrence precision and
+ * expose their quantization behavior). Nothing low-precision is stored: a
+ * non-flush step reads each checkpoint element through a quantise-dequantise
+ * in the chosen format, computed in fp32 registers, while a flushing step
+ * reads and folds the exact fp32 checkpoint. Formats saturate at their
+ * largest finite value; rounding is to nearest, ties to even:
+ *   RSSM_EMU_BF16, RSSM_EMU_F16   8 / 11 significant bits (IEEE exponent
+ *                                 ranges), no scale;
+ *   RSSM_EMU_E4M3, RSSM_EMU_E5M2  OCP FP8 (4 / 3 significant bits, largest
+ *                                 448 / 57344, subnormals), with a scale;
+ *   RSSM_EMU_INT8                 symmetric 8-bit integers in [-127, 127],
+ *                                 with a scale.
+ * A scale s = max|group| / qmax (qmax = 448, 57344 or 127) covers one state
+ * row of dstate values (RSSM_EMU_SCALE_ROW) or one 64-row block of a
+ * (sequence, head) tile (RSSM_EMU_SCALE_TILE64); an element x reads as
+ * Q(x * (qmax / max|group|)) * s, both quotients and both products in fp32. */
+enum { RSSM_EMU_BF16 = 1, RSSM_EMU_F16 = 2, RSSM_EMU_E4M3 = 3, RSSM_EMU_E5M2 = 4, RSSM_EMU_INT8 = 5 };
+enum { RSSM_EMU_SCALE_NONE = 0, RSSM_EMU_SCALE_ROW = 1, RSSM_EMU_SCALE_TILE64 = 2 };
+typedef struct {
+  int format; /* RSSM_EMU_* */
+  int scale;  /* RSSM_EMU_SCALE_NONE for bf16 / fp16; ROW or TILE64 for e4m3, e5m2, int8 */
+} rssm_emulation;
+
+/* Bytes of device workspace rssm_mamba2_step_emulated needs for desc: one
+ * pair of fp32 partial sums per warp of the launch (desc->batch * nheads *
+ * headdim / 16 pairs). 0 with RSSM_ERR_INVALID_ARG or _UNSUPPORTED in *rc
+ * (if rc is non-NULL) for a descriptor the call rejects. */
+RSSM_API size_t rssm_mamba2_emulated_workspace_bytes(const rssm_mamba2_desc* desc, int* rc);
+
+/* rssm_mamba2_step with an emulated read precision (see rssm_emulation):
+ * the same protocol (append, output-only non-flush steps, the fused flush
+ * on the L-th step from the exact checkpoint, cursors advanced within the
+ * call), and the quantisation behaviour of what the call read:
+ *  err        [2] double, device, written: the sum over every element that a
+ *             non-flush step of this call read of (read value - fp32 value)^2,
+ *             and of (fp32 value)^2 -- so sqrt(err[0] / err[1]) is the
+ *             relative L2 error of the emulated read. Summed in a fixed order
+ *             (fp32 within each warp's 2048 elements, then fp64): the same
+ *             inputs give the same bits.
+ *  workspace  device scratch of at least
+ *             rssm_mamba2_emulated_workspace_bytes(desc) bytes (else
+ *             RSSM_ERR_INVALID_ARG), 16-byte aligned, owned by the caller;
+ *             its contents need no initialisation and are overwritten.
+ * Needs the shape-specialised kernel's shapes (dstate 128, headdim a
+ * multiple of 64, buf_len <= 31, a power-of-two nheads / ngroups) and no
+ * state slots (else RSSM_ERR_UNSUPPORTED); desc->read_dtype is ignored.
+ * A format / scale pair other than those listed: RSSM_ERR_INVALID_ARG. */
+RSSM_API int rssm_mamba2_step_emulated(const rssm_mamba2_desc* desc, const rssm_emulation* emu, float* ckpt,
+                                       const rssm_mamba2_ring* ring, int32_t* cursors, const rssm_bf16* x,
+                                       const rssm_bf16* z, const rssm_bf16* B, const rssm_bf16* C,
+                                       const float* dt, const float* A, const float* D, void* y, double* err,
+                                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                       rssm_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * Cursors (shared by Mamba-2, Gated DeltaNet and KDA)
  */

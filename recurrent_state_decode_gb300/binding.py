@@ -29,6 +29,14 @@ RSSM_F32 = 0
 RSSM_BF16 = 1
 RSSM_F16 = 2
 RSSM_FP8_E4M3 = 3
+RSSM_EMU_BF16 = 1
+RSSM_EMU_F16 = 2
+RSSM_EMU_E4M3 = 3
+RSSM_EMU_E5M2 = 4
+RSSM_EMU_INT8 = 5
+RSSM_EMU_SCALE_NONE = 0
+RSSM_EMU_SCALE_ROW = 1
+RSSM_EMU_SCALE_TILE64 = 2
 
 c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
 
@@ -49,6 +57,10 @@ class rssm_gdn_desc(ctypes.Structure):
 
 class rssm_gdn_ring(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("q", "k", "v", "g", "beta", "e")]
+
+
+class rssm_emulation(ctypes.Structure):
+    _fields_ = [("format", c_int), ("scale", c_int)]
 
 
 rssm_kda_desc = rssm_gdn_desc   # the same struct in rssm.h
@@ -82,6 +94,8 @@ _SIGNATURES = {
     "rssm_kda_flush": (c_int, [P] * 5 + [P]),
     "rssm_kda_prime": (c_int, [P] * 5 + [P]),
     "rssm_kda_spec_verify": (c_int, [P, c_int] + [P] * 11),
+    "rssm_mamba2_emulated_workspace_bytes": (c_size_t, [P, P]),
+    "rssm_mamba2_step_emulated": (c_int, [P] * 15 + [c_size_t, P, P]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -299,3 +313,22 @@ def rssm_kda_spec_verify(desc, n_new, S, ring, cursors, q, k, v, g, beta, o, dev
 
 def rssm_kda_prime(desc, S, ring, cursors, dev_status=None, stream=None):
     return load().rssm_kda_prime(_ref(desc), ptr(S), _ref(ring), ptr(cursors), ptr(dev_status), _stream(stream, S))
+
+
+def emulation(fmt, scale):
+    """An emulated read precision: fmt an RSSM_EMU_* format, scale an RSSM_EMU_SCALE_* mode."""
+    return rssm_emulation(int(fmt), int(scale))
+
+
+def rssm_mamba2_emulated_workspace_bytes(desc):
+    rc = ctypes.c_int(0)
+    n = load().rssm_mamba2_emulated_workspace_bytes(_ref(desc), ctypes.byref(rc))
+    check(rc.value, "rssm_mamba2_emulated_workspace_bytes")
+    return int(n)
+
+
+def rssm_mamba2_step_emulated(desc, emu, ckpt, ring, cursors, x, z, B, C, dt, A, D, y, err, workspace,
+                              workspace_bytes, dev_status=None, stream=None):
+    return load().rssm_mamba2_step_emulated(
+        _ref(desc), _ref(emu), ptr(ckpt), _ref(ring), ptr(cursors), ptr(x), ptr(z), ptr(B), ptr(C), ptr(dt), ptr(A),
+        ptr(D), ptr(y), ptr(err), ptr(workspace), int(workspace_bytes), ptr(dev_status), _stream(stream, ckpt))

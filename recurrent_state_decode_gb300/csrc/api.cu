@@ -231,6 +231,64 @@ int rssm_mamba2_step(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_rea
   return cuda_rc(cursor_launch(CUR_AR, cursors, nullptr, d->batch, d->buf_len, dev_status, st));
 }
 
+// An emulated step's descriptor and format: the shape-specialised kernel's shapes, no slots, a listed
+// format / scale pair. Fills the launch arguments' shape fields.
+static int check_emulated(const rssm_mamba2_desc* d, const rssm_emulation* emu, M2Args& a) {
+  int rc = check_m2(d);
+  if (rc) return rc;
+  if (!emu) return RSSM_ERR_INVALID_ARG;
+  const bool unscaled = emu->format == RSSM_EMU_BF16 || emu->format == RSSM_EMU_F16;
+  const bool scaled = emu->format == RSSM_EMU_E4M3 || emu->format == RSSM_EMU_E5M2 || emu->format == RSSM_EMU_INT8;
+  if (!(unscaled && emu->scale == RSSM_EMU_SCALE_NONE) &&
+      !(scaled && (emu->scale == RSSM_EMU_SCALE_ROW || emu->scale == RSSM_EMU_SCALE_TILE64)))
+    return RSSM_ERR_INVALID_ARG;
+  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
+  a = m2_args(d);
+  a.emu_fmt = emu->format;
+  a.emu_scale = emu->scale;
+  return m2_step_fast_applies(a) ? RSSM_OK : RSSM_ERR_UNSUPPORTED;
+}
+
+size_t rssm_mamba2_emulated_workspace_bytes(const rssm_mamba2_desc* d, int* rc_out) {
+  // any listed format: the workspace depends on the shape alone
+  const rssm_emulation probe = {RSSM_EMU_BF16, RSSM_EMU_SCALE_NONE};
+  M2Args a{};
+  const int rc = check_emulated(d, &probe, a);
+  if (rc_out) *rc_out = rc;
+  return rc ? 0 : m2_emulated_partials(a) * sizeof(float2);
+}
+
+int rssm_mamba2_step_emulated(const rssm_mamba2_desc* d, const rssm_emulation* emu, float* ckpt,
+                              const rssm_mamba2_ring* ring, int32_t* cursors, const rssm_bf16* x, const rssm_bf16* z,
+                              const rssm_bf16* B, const rssm_bf16* C, const float* dt, const float* A, const float* D,
+                              void* y, double* err, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              rssm_stream_t stream) {
+  M2Args a{};
+  int rc = check_emulated(d, emu, a);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({ckpt, ring->x, ring->z, ring->B, ring->C, ring->dt, cursors, x, z, B, C, dt, A, D, y, err,
+                        workspace})))
+    return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  if (workspace_bytes < m2_emulated_partials(a) * sizeof(float2)) return RSSM_ERR_INVALID_ARG;
+  a.ckpt = ckpt;
+  set_ring(a, ring);
+  a.cursors = cursors;
+  a.x = x;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.dt = dt;
+  a.A = A;
+  a.D = D;
+  a.y = y;
+  a.status = dev_status;
+  a.emu_part = static_cast<float2*>(workspace);
+  return cuda_rc(m2_step_emulated_launch(a, d->out_dtype == RSSM_BF16, err, (cudaStream_t)stream));
+}
+
 int rssm_mamba2_flush(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
                       int32_t* cursors, const float* A, int32_t* dev_status, rssm_stream_t stream) {
   int rc = check_m2(d);

@@ -219,6 +219,68 @@ __device__ __forceinline__ void store_f8_row(uint8_t* q, float* scales, size_t r
   if (lane == 0) scales[row] = m / E4M3_MAX;
 }
 
+// ---------------------------------------------------------------- emulated read precisions
+
+// Largest code magnitude of a scaled emulated format (RSSM_EMU_E4M3, _E5M2,
+// _INT8); 1 for the unscaled ones.
+__device__ __forceinline__ float emu_qmax(int fmt) {
+  return fmt == RSSM_EMU_E4M3 ? 448.f : fmt == RSSM_EMU_E5M2 ? 57344.f : fmt == RSSM_EMU_INT8 ? 127.f : 1.f;
+}
+
+// t rounded to nearest, ties to even, into emulated format fmt, saturating
+// at its largest finite value. A binary format with p significant bits and
+// smallest normal exponent emin: at or above 2^emin the fp32 pattern is
+// rounded at bit 24 - p (adding half an ulp minus one plus the kept lowest
+// bit, then clearing the dropped bits; a carry moves into the exponent);
+// below it the spacing is fixed at 2^k, k = emin - p + 1, and adding then
+// subtracting c = 1.5 * 2^(k + 23) rounds t to a multiple of 2^k (the sum
+// lies in [2^(k+23), 2^(k+24)), whose ulp is 2^k). int8: rintf (half to
+// even), clamped to [-127, 127].
+__device__ __forceinline__ float emu_quantise(float t, int fmt) {
+  if (fmt == RSSM_EMU_INT8) return fminf(fmaxf(rintf(t), -127.f), 127.f);
+  int sh;
+  float lo, c, vmax;  // 2^emin, the magic constant, the largest value
+  switch (fmt) {
+    case RSSM_EMU_BF16: sh = 16; lo = 0x1p-126f; c = 0x1.8p-110f; vmax = 0x1.fep127f; break;
+    case RSSM_EMU_F16: sh = 13; lo = 0x1p-14f; c = 0x1.8p-1f; vmax = 65504.f; break;
+    case RSSM_EMU_E4M3: sh = 20; lo = 0x1p-6f; c = 0x1.8p14f; vmax = 448.f; break;
+    default: sh = 21; lo = 0x1p-14f; c = 0x1.8p7f; vmax = 57344.f; break;  // RSSM_EMU_E5M2
+  }
+  uint32_t u = __float_as_uint(t);
+  u += (1u << (sh - 1)) - 1u + ((u >> sh) & 1u);
+  u &= ~((1u << sh) - 1u);
+  const float sub = __fsub_rn(__fadd_rn(t, c), c);
+  const float r = fabsf(t) < lo ? sub : __uint_as_float(u);
+  return fminf(fmaxf(r, -vmax), vmax);
+}
+
+// Maxima of V per-lane values over the warp, transposed like
+// reduce_transpose: afterwards m[0] of lane l is the maximum of index idx(l).
+template <int V>
+__device__ __forceinline__ float max_transpose(float (&m)[V], int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 5; lvl++) {
+    const int off = 16 >> lvl;
+    const int n = V >> lvl;
+    if (n > 1) {
+      const bool hi = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; i++) {
+        const float send = hi ? m[i] : m[i + n / 2];
+        const float keep = hi ? m[i + n / 2] : m[i];
+        m[i] = fmaxf(keep, __shfl_xor_sync(FULL, send, off));
+      }
+    } else {
+      m[0] = fmaxf(m[0], __shfl_xor_sync(FULL, m[0], off));
+    }
+  }
+  return m[0];
+}
+
+__device__ __forceinline__ float abs_max4(float4 v) {
+  return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+
 // ---------------------------------------------------------------- warp-level tensor-core pieces
 
 // Four 8x8 bf16 matrices from shared memory; lane l gives the address of row

@@ -38,10 +38,56 @@ using namespace fastrows;
 
 constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 
+// Emulated read of 8 rows (a non-flush step of the emulated instantiation):
+// every element x becomes Q(x * inv) * s for its row's (or its tile's)
+// scale, Q the format's rounding; err and nrm gather (read - x)^2 and x^2.
+// With a row scale the rows' maxima come from one transposed max reduction,
+// lane row_src(rr) computing row rr's quotients. Every lane must call this.
+__device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, float tinv, float ts, int lane,
+                                          float& err, float& nrm) {
+  float inv[8], sc[8];
+  const bool scaled = a.emu_scale != RSSM_EMU_SCALE_NONE;
+  if (a.emu_scale == RSSM_EMU_SCALE_ROW) {
+    float m[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) m[rr] = abs_max4(hv[rr]);
+    const float mm = max_transpose<8>(m, lane);  // the max of row reduce8_row(lane)
+    const float qmax = emu_qmax(a.emu_fmt);
+    const float my_inv = mm > 0.f ? qmax / mm : 0.f, my_s = mm / qmax;
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) {
+      inv[rr] = __shfl_sync(FULL, my_inv, row_src(rr));
+      sc[rr] = __shfl_sync(FULL, my_s, row_src(rr));
+    }
+  } else {
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) {
+      inv[rr] = tinv;
+      sc[rr] = ts;
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < 8; rr++) {
+    float* v = reinterpret_cast<float*>(&hv[rr]);
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float x = v[j];
+      const float q = emu_quantise(scaled ? __fmul_rn(x, inv[rr]) : x, a.emu_fmt);
+      const float r = scaled ? __fmul_rn(q, sc[rr]) : q;
+      const float d = r - x;
+      err = fmaf(d, d, err);
+      nrm = fmaf(x, x, nrm);
+      v[j] = r;
+    }
+  }
+}
+
 // RD16: the block reads the 16-bit or fp8 read copy (16 KiB tiles, seven blocks
 // per SM: at eight the 64-register cap spilled, and seven measured 2% faster).
 // SLOTS: batch rows name their state rows through a slot table.
-template <bool OUT_BF16, bool RD16, bool SLOTS>
+// EMU: non-flush steps read the fp32 tile through an emulated precision and
+// each warp writes its (error, norm) sums to a.emu_part (fp32 tiles, no slots).
+template <bool OUT_BF16, bool RD16, bool SLOTS, bool EMU = false>
 __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
   __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
@@ -113,6 +159,9 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
   }
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
   const int nblocks = a.H * a.nPB;  // blocks of this sequence
+  // this warp's slot of the emulated read's error sums (every path writes it)
+  float2* const emu_slot = EMU ? a.emu_part + ((size_t)(bh * a.nPB + pb) * FW + warp) : nullptr;
+  if (EMU && !valid && lane == 0) *emu_slot = make_float2(0.f, 0.f);
   if (!valid) {  // uniform over the block; the last block of the sequence reports it
     if (threadIdx.x == 0) {
       const int ticket = cursor_ticket(a.cursors, sb);
@@ -169,9 +218,23 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
   }
   if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
+    if (EMU && lane == 0) *emu_slot = make_float2(0.f, 0.f);
     mbar_wait(&bar, 0);
     if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
     return;
+  }
+  // Emulated read with one scale per 64-row tile: each warp takes the whole
+  // tile's maximum from shared memory itself (no block barrier after the wait).
+  float emu_tinv = 1.f, emu_ts = 1.f, emu_err = 0.f, emu_nrm = 0.f;
+  if (EMU && !flush && a.emu_scale == RSSM_EMU_SCALE_TILE64) {
+    float m = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < FPB; r++) m = fmaxf(m, abs_max4(reinterpret_cast<const float4*>(tile + r * FN)[lane]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    const float qmax = emu_qmax(a.emu_fmt);
+    emu_tinv = m > 0.f ? qmax / m : 0.f;
+    emu_ts = m / qmax;
   }
   // A block that reads the bf16 copy folds from the fp32 rows in global memory.
   const bool from_tile = !(copy && flush);
@@ -197,6 +260,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
     } else {
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
+      if (EMU && !flush) emu_read8(hv, a, emu_tinv, emu_ts, lane, emu_err, emu_nrm);
     }
     float xl[8], tx[8];
     unpack8(xq[half], xl);
@@ -208,7 +272,37 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
     }
   }
 
+  if (EMU) {
+    const float e = warp_sum(emu_err), n = warp_sum(emu_nrm);
+    if (lane == 0) *emu_slot = make_float2(e, n);
+  }
   if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
+}
+
+// The emulated step's error sums: the per-warp pairs added in a fixed order
+// (each thread a strided share in fp64, then a tree over the block).
+__global__ void __launch_bounds__(256) emu_reduce_kernel(const float2* __restrict__ part, size_t n, double* err) {
+  __shared__ double se[256], sn[256];
+  double e = 0.0, q = 0.0;
+  for (size_t i = threadIdx.x; i < n; i += 256) {
+    const float2 v = part[i];
+    e += v.x;
+    q += v.y;
+  }
+  se[threadIdx.x] = e;
+  sn[threadIdx.x] = q;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      se[threadIdx.x] += se[threadIdx.x + o];
+      sn[threadIdx.x] += sn[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    err[0] = se[0];
+    err[1] = sn[0];
+  }
 }
 
 }  // namespace
@@ -232,6 +326,18 @@ cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) 
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<grid, FT, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, cudaStream_t st) {
+  if (a.Bt == 0) return cudaSuccess;
+  const dim3 grid(a.nPB, a.H, a.Bt);
+  auto k = out_bf16 ? m2_step_fast_kernel<true, false, false, true> : m2_step_fast_kernel<false, false, false, true>;
+  cudaError_t e = prepare(k, 0, true);
+  if (e != cudaSuccess) return e;
+  k<<<grid, FT, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  emu_reduce_kernel<<<1, 256, 0, st>>>(a.emu_part, m2_emulated_partials(a), err);
   return cudaGetLastError();
 }
 

@@ -120,6 +120,23 @@ class Mamba2State:
                                      rec["x"], rec["z"], rec["B"], rec["C"], rec["dt"], A, D, y,
                                      self.status, stream), "rssm_mamba2_step")
 
+    def step_emulated(self, rec, A, D, y, emu, err, workspace, stream=None):
+        """rssm_mamba2_step with an emulated read precision: emu from
+        ``binding.emulation``; err float64 [2] and workspace (uint8, at least
+        ``binding.rssm_mamba2_emulated_workspace_bytes(self.desc)`` bytes) on
+        the device."""
+        dev = self.ckpt.device
+        _check_records(rec, self._record_spec(), self.batch, dev)
+        self._check_params(A, D)
+        _check_tensor("y", y, self.y_dtype, (self.batch, self.nheads, self.headdim), dev)
+        _check_tensor("err", err, torch.float64, (2,), dev)
+        if not isinstance(workspace, torch.Tensor) or workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError(f"workspace must be a contiguous tensor on {dev}")
+        nbytes = workspace.numel() * workspace.element_size()
+        bd.check(bd.rssm_mamba2_step_emulated(self.desc, emu, self.ckpt, self.ring, self.cursors, rec["x"], rec["z"],
+                                              rec["B"], rec["C"], rec["dt"], A, D, y, err, workspace, nbytes,
+                                              self.status, stream), "rssm_mamba2_step_emulated")
+
     def flush(self, A, stream=None):
         self._check_params(A)
         bd.check(bd.rssm_mamba2_flush(self.desc, self.ckpt, self.ckpt_read, self.ring, self.cursors, A,

@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 25
+    assert len(declared) == 27
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -333,3 +333,37 @@ def test_record_tensors_are_checked_before_any_call():
         k.step(grec, torch.zeros(2, 2, 128))                               # KDA g is per key channel
     with pytest.raises(ValueError):
         k.verify({f: torch.stack([v, v], 1) for f, v in grec.items()}, torch.zeros(2, 2, 2, 128))
+
+
+def test_emulated_step_host_checks(lib):
+    """rssm_mamba2_step_emulated: the workspace size query, the format / scale
+    pairs it takes, the shapes and the workspace size it needs."""
+    d = bd.mamba2_desc(4, 8, 64, 128, 2, 16)
+    n = bd.rssm_mamba2_emulated_workspace_bytes(d)
+    assert n == 4 * 8 * 1 * 4 * 8            # one (error, norm) fp32 pair per warp: 4 warps per block
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    args = [ALIGNED] * 9                     # x, z, B, C, dt, A, D, y, err
+
+    def call(desc, emu, nbytes=n, ws=ALIGNED):
+        return lib.rssm_mamba2_step_emulated(ctypes.byref(desc), None if emu is None else ctypes.byref(emu), ALIGNED,
+                                             ctypes.byref(ring), ALIGNED, *args[:8], args[8], ws, nbytes, None, None)
+    ok = [(bd.RSSM_EMU_BF16, 0), (bd.RSSM_EMU_F16, 0), (bd.RSSM_EMU_E4M3, 1), (bd.RSSM_EMU_E5M2, 2),
+          (bd.RSSM_EMU_INT8, 1), (bd.RSSM_EMU_INT8, 2)]
+    bad = [(bd.RSSM_EMU_BF16, 1), (bd.RSSM_EMU_F16, 2), (bd.RSSM_EMU_E4M3, 0), (bd.RSSM_EMU_INT8, 0), (0, 0),
+           (6, 1), (bd.RSSM_EMU_E4M3, 3)]
+    for f, sc in bad:
+        assert call(d, bd.emulation(f, sc)) == bd.RSSM_ERR_INVALID_ARG, (f, sc)
+    assert call(d, None) == bd.RSSM_ERR_INVALID_ARG
+    for f, sc in ok:   # valid pairs pass every host check; an empty batch launches nothing
+        assert call(bd.mamba2_desc(0, 8, 64, 128, 2, 16), bd.emulation(f, sc)) == bd.RSSM_OK
+    emu = bd.emulation(bd.RSSM_EMU_E4M3, bd.RSSM_EMU_SCALE_ROW)
+    assert call(d, emu, nbytes=n - 1) == bd.RSSM_ERR_INVALID_ARG
+    assert call(d, emu, ws=None) == bd.RSSM_ERR_INVALID_ARG
+    assert call(d, emu, ws=ALIGNED + 8) == bd.RSSM_ERR_MISALIGNED
+    for shape in ((4, 8, 64, 64, 2, 16), (4, 8, 48, 128, 2, 16), (4, 8, 64, 128, 2, 32), (4, 6, 64, 128, 2, 16)):
+        ds = bd.mamba2_desc(*shape)
+        assert call(ds, emu) == bd.RSSM_ERR_UNSUPPORTED, shape
+        with pytest.raises(bd.RssmError):
+            bd.rssm_mamba2_emulated_workspace_bytes(ds)
+    slots = bd.mamba2_desc(4, 8, 64, 128, 2, 16, state_slots=ALIGNED, n_slots=4)
+    assert call(slots, emu) == bd.RSSM_ERR_UNSUPPORTED

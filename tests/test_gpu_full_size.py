@@ -85,10 +85,15 @@ def check_checkpoints(ck, ckpt, ckpt0, batch):
     return len(ck)
 
 
-def run_mamba2_ar(w, out_dtype, steps, read_copy=None, compare_steps=None, sample=None):
+def run_mamba2_ar(w, out_dtype, steps, read_copy=None, compare_steps=None, sample=None, emu=None, reports=None):
     """AR decode of workload w on the GPU beside the oracle pool; returns
-    (per-step rel-L2, bf16 excess, finite flags, checkpoint errors, state)."""
-    st, A, D, pre, starts, counts = mamba2_from_workload(w, DEV, out_dtype, read_copy)
+    (per-step rel-L2, bf16 excess, finite flags, checkpoint errors, state).
+    emu: an emulated read precision (rssm_mamba2_step_emulated), whose
+    per-step error reports are appended to ``reports``."""
+    st, A, D, pre, starts, counts = mamba2_from_workload(w, DEV, out_dtype, False if emu else read_copy)
+    if emu is not None:
+        err = torch.zeros(2, dtype=torch.float64, device=DEV)
+        ws = torch.empty(bd.rssm_mamba2_emulated_workspace_bytes(st.desc), dtype=torch.uint8, device=DEV)
     ckpt0 = st.ckpt.clone()
     seqs = np.arange(w.batch) if sample is None else np.asarray(sample)
     chunks = OW.chunks_of(len(seqs)) if sample is None else [np.array([i]) for i in range(len(seqs))]
@@ -102,7 +107,11 @@ def run_mamba2_ar(w, out_dtype, steps, read_copy=None, compare_steps=None, sampl
         for t in range(steps):
             rec = I.mamba2_step_inputs(w, t, DEV)
             prev = st.ckpt.clone()
-            st.step(rec, A, D, y)
+            if emu is None:
+                st.step(rec, A, D, y)
+            else:
+                st.step_emulated(rec, A, D, y, emu, err, ws)
+                reports.append(err.tolist())
             model_next = [oc.ar_step(c, w.buf_len) for c in model]
             np.testing.assert_array_equal(st.cursors.cpu().numpy(), np.array([m[0] for m in model_next]))
             quiet = [b for b, m in enumerate(model_next) if not m[2]]
@@ -292,3 +301,28 @@ def test_read_copy_4096_steps(name):
     slope = np.polyfit(np.arange(len(trace)), trace, 1)[0]
     assert slope < 1e-7, slope
     assert all(e <= TOL_CKPT for e in ck.values())
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "int8"])
+def test_emulated_read_4096_steps(fmt):
+    """The serving layer with an emulated read precision (one scale per 64-row
+    tile: e4m3, or int8), 4096 steps, 16 sequences spanning the initial window
+    counts: the output error against the fp64 conventional decode stays within
+    the read's own bound (e4m3: 2^-4; int8: 2^-6, half an int8 step of a tile
+    whose largest element is about 4 of its RMS) and does not grow, and the
+    error each call reports stays at a constant level."""
+    w = I.WORKLOADS["mamba2_serving"]
+    w = type(w)(**{**w.__dict__, "name": "mamba2_emu", "steps": 4096})
+    emu = bd.emulation(bd.RSSM_EMU_E4M3 if fmt == "e4m3" else bd.RSSM_EMU_INT8, bd.RSSM_EMU_SCALE_TILE64)
+    sample = spread(I.initial_cursors(w, DEV)[1], 16)
+    reports = []
+    rel, excess, finite, ck, st, ckpt0 = run_mamba2_ar(w, bd.RSSM_F32, w.steps, sample=sample, emu=emu,
+                                                      reports=reports)
+    trace = np.array(rel)
+    assert all(finite)
+    assert trace.max() <= (2.0 ** -4 if fmt == "e4m3" else 2.0 ** -6), trace.max()
+    assert trace[-512:].max() <= 1.25 * trace[:512].max()
+    assert np.polyfit(np.arange(len(trace)), trace, 1)[0] < 1e-7
+    assert all(e <= TOL_CKPT for e in ck.values())
+    q = np.sqrt([e / n for e, n in reports])     # relative L2 error of each call's emulated read
+    assert q[-512:].max() <= 1.25 * q[:512].max() and q.min() > 0
