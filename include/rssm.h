@@ -268,6 +268,36 @@ RSSM_API int rssm_mamba2_step_emulated(const rssm_mamba2_desc* desc, const rssm_
                                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                        rssm_stream_t stream);
 
+/* rssm_mamba2_step_emulated for callers that cannot allocate device memory
+ * when they decode. The pages have no counterpart of this call. Some hosts
+ * reserve nearly all of the GPU's memory for their own pools before decoding
+ * starts, or hand a kernel library a stream but no allocator, and cudaMalloc
+ * itself may synchronise the device in the middle of a decode loop. This
+ * variant takes no workspace: its per-warp error sums go to a static device
+ * array inside librssm of RSSM_NOALLOC_MAX_WARPS (error, norm) fp32 pairs --
+ * 2 MiB on every GPU that loads the library, held until the process exits --
+ * and it never calls cudaMalloc, cudaFree or any routine that allocates.
+ *  - Arguments, protocol, limits and results are those of
+ *    rssm_mamba2_step_emulated, without workspace and workspace_bytes.
+ *  - A launch of more than RSSM_NOALLOC_MAX_WARPS warps (batch * nheads *
+ *    headdim / 16; the serving layer of batch 256, 128 heads of 64 rows has
+ *    131072) returns RSSM_ERR_UNSUPPORTED and launches nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *    first call before any stream capture. Devices 0..RSSM_NOALLOC_MAX_DEVICES-1.
+ *  - Every call on a device uses the same array, which keeps the last call's
+ *    sums. Nothing in it needs clearing (each call writes every entry it reads
+ *    before reading it), but two calls whose kernels overlap on the GPU --
+ *    on different streams without an ordering between them -- race on it:
+ *    order them (one stream, or events). */
+#define RSSM_NOALLOC_MAX_WARPS 262144
+#define RSSM_NOALLOC_MAX_DEVICES 64
+RSSM_API int rssm_mamba2_step_emulated_noalloc(const rssm_mamba2_desc* desc, const rssm_emulation* emu, float* ckpt,
+                                               const rssm_mamba2_ring* ring, int32_t* cursors, const rssm_bf16* x,
+                                               const rssm_bf16* z, const rssm_bf16* B, const rssm_bf16* C,
+                                               const float* dt, const float* A, const float* D, void* y,
+                                               double* err, int32_t* dev_status, rssm_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * Cursors (shared by Mamba-2, Gated DeltaNet and KDA)
  */

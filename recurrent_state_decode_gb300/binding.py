@@ -96,6 +96,7 @@ _SIGNATURES = {
     "rssm_kda_spec_verify": (c_int, [P, c_int] + [P] * 11),
     "rssm_mamba2_emulated_workspace_bytes": (c_size_t, [P, P]),
     "rssm_mamba2_step_emulated": (c_int, [P] * 15 + [c_size_t, P, P]),
+    "rssm_mamba2_step_emulated_noalloc": (c_int, [P] * 16),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -332,3 +333,13 @@ def rssm_mamba2_step_emulated(desc, emu, ckpt, ring, cursors, x, z, B, C, dt, A,
     return load().rssm_mamba2_step_emulated(
         _ref(desc), _ref(emu), ptr(ckpt), _ref(ring), ptr(cursors), ptr(x), ptr(z), ptr(B), ptr(C), ptr(dt), ptr(A),
         ptr(D), ptr(y), ptr(err), ptr(workspace), int(workspace_bytes), ptr(dev_status), _stream(stream, ckpt))
+
+
+RSSM_NOALLOC_MAX_WARPS = 262144
+
+
+def rssm_mamba2_step_emulated_noalloc(desc, emu, ckpt, ring, cursors, x, z, B, C, dt, A, D, y, err, dev_status=None,
+                                      stream=None):
+    return load().rssm_mamba2_step_emulated_noalloc(
+        _ref(desc), _ref(emu), ptr(ckpt), _ref(ring), ptr(cursors), ptr(x), ptr(z), ptr(B), ptr(C), ptr(dt), ptr(A),
+        ptr(D), ptr(y), ptr(err), ptr(dev_status), _stream(stream, ckpt))

@@ -289,6 +289,35 @@ int rssm_mamba2_step_emulated(const rssm_mamba2_desc* d, const rssm_emulation* e
   return cuda_rc(m2_step_emulated_launch(a, d->out_dtype == RSSM_BF16, err, (cudaStream_t)stream));
 }
 
+int rssm_mamba2_step_emulated_noalloc(const rssm_mamba2_desc* d, const rssm_emulation* emu, float* ckpt,
+                                      const rssm_mamba2_ring* ring, int32_t* cursors, const rssm_bf16* x,
+                                      const rssm_bf16* z, const rssm_bf16* B, const rssm_bf16* C, const float* dt,
+                                      const float* A, const float* D, void* y, double* err, int32_t* dev_status,
+                                      rssm_stream_t stream) {
+  M2Args a{};
+  int rc = check_emulated(d, emu, a);
+  if (rc) return rc;
+  if (d->batch == 0) return RSSM_OK;
+  if (!ring) return RSSM_ERR_INVALID_ARG;
+  if ((rc = check_ptrs({ckpt, ring->x, ring->z, ring->B, ring->C, ring->dt, cursors, x, z, B, C, dt, A, D, y, err})))
+    return rc;
+  if ((rc = check_opt(dev_status))) return rc;
+  if (m2_emulated_partials(a) > (size_t)M2_NOALLOC_PARTIALS) return RSSM_ERR_UNSUPPORTED;  // beyond the static array
+  a.ckpt = ckpt;
+  set_ring(a, ring);
+  a.cursors = cursors;
+  a.x = x;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.dt = dt;
+  a.A = A;
+  a.D = D;
+  a.y = y;
+  a.status = dev_status;
+  return cuda_rc(m2_step_emulated_noalloc_launch(a, d->out_dtype == RSSM_BF16, err, (cudaStream_t)stream));
+}
+
 int rssm_mamba2_flush(const rssm_mamba2_desc* d, float* ckpt, rssm_bf16* ckpt_read, const rssm_mamba2_ring* ring,
                       int32_t* cursors, const float* A, int32_t* dev_status, rssm_stream_t stream) {
   int rc = check_m2(d);

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "rssm.h"
+
 namespace rssm {
 
 // Mamba-2 launch arguments (device pointers, dense row-major layouts of rssm.h).
@@ -43,6 +45,10 @@ cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, cudaStream_t st);
 // Entries of a.emu_part an emulated step of these arguments writes.
 inline size_t m2_emulated_partials(const M2Args& a) { return (size_t)a.Bt * a.H * a.nPB * 4; }
+// The same step with its error sums in the library's static device array (mamba2_step_fast.cu), which holds
+// M2_NOALLOC_PARTIALS pairs: a.emu_part is ignored; a larger launch returns cudaErrorInvalidValue.
+constexpr int M2_NOALLOC_PARTIALS = RSSM_NOALLOC_MAX_WARPS;
+cudaError_t m2_step_emulated_noalloc_launch(M2Args a, int out_bf16, double* err, cudaStream_t st);
 // The persistent speculative verify (mamba2_verify.cu); its epilogue kernel is in mamba2.cu.
 cudaError_t m2_verify_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // Shape-specialised verify (dstate 128, headdim a multiple of 64, K <= 4; mamba2_verify_fast.cu).

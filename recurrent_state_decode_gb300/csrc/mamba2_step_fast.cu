@@ -25,6 +25,7 @@
 // ring slot. The last of a sequence's blocks to have read its cursor advances
 // it (an arrival count in the high half of the cursor's flags word), so the
 // step needs no second kernel.
+#include <mutex>
 #include <type_traits>
 
 #include "fast_rows.cuh"
@@ -339,6 +340,41 @@ cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   emu_reduce_kernel<<<1, 256, 0, st>>>(a.emu_part, m2_emulated_partials(a), err);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- the no-allocation variant's scratch
+
+// The emulated step's per-warp error sums for callers that cannot hand the
+// library a workspace: a static device array, present on every GPU that
+// loads the library until the process exits.
+static __device__ __align__(256) float2 g_emu_scratch[M2_NOALLOC_PARTIALS];
+
+// Device address of g_emu_scratch on the current device. In host code the
+// array's name stands for a host-side shadow, not device memory, so the
+// address is looked up once per device with that device current, and kept.
+static cudaError_t emu_scratch_address(float2** out) {
+  static std::mutex mu;
+  static float2* addr[RSSM_NOALLOC_MAX_DEVICES] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= RSSM_NOALLOC_MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_emu_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float2*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t m2_step_emulated_noalloc_launch(M2Args a, int out_bf16, double* err, cudaStream_t st) {
+  if (m2_emulated_partials(a) > (size_t)M2_NOALLOC_PARTIALS) return cudaErrorInvalidValue;  // checked by the caller
+  cudaError_t e = emu_scratch_address(&a.emu_part);
+  if (e != cudaSuccess) return e;
+  return m2_step_emulated_launch(a, out_bf16, err, st);
 }
 
 }  // namespace rssm

@@ -28,7 +28,7 @@ def header_functions():
 
 def test_exports_match_header(lib):
     declared = header_functions()
-    assert len(declared) == 27
+    assert len(declared) == 28
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == declared
@@ -367,3 +367,21 @@ def test_emulated_step_host_checks(lib):
             bd.rssm_mamba2_emulated_workspace_bytes(ds)
     slots = bd.mamba2_desc(4, 8, 64, 128, 2, 16, state_slots=ALIGNED, n_slots=4)
     assert call(slots, emu) == bd.RSSM_ERR_UNSUPPORTED
+
+
+def test_noalloc_step_host_checks(lib):
+    """The no-allocation emulated step takes the emulated step's checks, and a
+    launch beyond its static scratch (more than RSSM_NOALLOC_MAX_WARPS warps)
+    is refused on the host with RSSM_ERR_UNSUPPORTED."""
+    ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
+    emu = bd.emulation(bd.RSSM_EMU_E4M3, bd.RSSM_EMU_SCALE_TILE64)
+
+    def call(desc, e=emu):
+        return lib.rssm_mamba2_step_emulated_noalloc(ctypes.byref(desc), ctypes.byref(e), ALIGNED, ctypes.byref(ring),
+                                                     *([ALIGNED] * 10), None, None)
+    assert bd.RSSM_NOALLOC_MAX_WARPS == 262144
+    big = bd.mamba2_desc(513, 128, 64, 128, 8, 16)          # 513 * 128 * 4 warps > 262144
+    assert call(big) == bd.RSSM_ERR_UNSUPPORTED
+    assert call(bd.mamba2_desc(4, 8, 64, 128, 2, 16), bd.emulation(bd.RSSM_EMU_E4M3, 0)) == bd.RSSM_ERR_INVALID_ARG
+    assert call(bd.mamba2_desc(4, 8, 64, 64, 2, 16)) == bd.RSSM_ERR_UNSUPPORTED
+    assert call(bd.mamba2_desc(0, 8, 64, 128, 2, 16)) == bd.RSSM_OK
