@@ -227,8 +227,31 @@ __device__ __forceinline__ float emu_qmax(int fmt) {
   return fmt == RSSM_EMU_E4M3 ? 448.f : fmt == RSSM_EMU_E5M2 ? 57344.f : fmt == RSSM_EMU_INT8 ? 127.f : 1.f;
 }
 
-// t rounded to nearest, ties to even, into emulated format fmt, saturating
-// at its largest finite value. A binary format with p significant bits and
+// The constants of an emulated format's rounding (see emu_quantise), taken
+// once per thread.
+struct EmuQ {
+  uint32_t half, mask;  // half an ulp at the kept precision minus one; the dropped bits
+  int sh;               // dropped bits of the fp32 significand (24 - p)
+  float lo, c, vmax;    // 2^emin; the magic constant 1.5 * 2^(k + 23); the largest value
+  bool int8;
+};
+
+__device__ __forceinline__ EmuQ emu_params(int fmt) {
+  EmuQ q;
+  q.int8 = fmt == RSSM_EMU_INT8;
+  switch (fmt) {
+    case RSSM_EMU_BF16: q.sh = 16; q.lo = 0x1p-126f; q.c = 0x1.8p-110f; q.vmax = 0x1.fep127f; break;
+    case RSSM_EMU_F16: q.sh = 13; q.lo = 0x1p-14f; q.c = 0x1.8p-1f; q.vmax = 65504.f; break;
+    case RSSM_EMU_E4M3: q.sh = 20; q.lo = 0x1p-6f; q.c = 0x1.8p14f; q.vmax = 448.f; break;
+    default: q.sh = 21; q.lo = 0x1p-14f; q.c = 0x1.8p7f; q.vmax = 57344.f; break;  // E5M2 (unused for int8)
+  }
+  q.half = (1u << (q.sh - 1)) - 1u;
+  q.mask = ~((1u << q.sh) - 1u);
+  return q;
+}
+
+// t rounded to nearest, ties to even, into an emulated format, saturating at
+// its largest finite value. A binary format with p significant bits and
 // smallest normal exponent emin: at or above 2^emin the fp32 pattern is
 // rounded at bit 24 - p (adding half an ulp minus one plus the kept lowest
 // bit, then clearing the dropped bits; a carry moves into the exponent);
@@ -236,22 +259,13 @@ __device__ __forceinline__ float emu_qmax(int fmt) {
 // subtracting c = 1.5 * 2^(k + 23) rounds t to a multiple of 2^k (the sum
 // lies in [2^(k+23), 2^(k+24)), whose ulp is 2^k). int8: rintf (half to
 // even), clamped to [-127, 127].
-__device__ __forceinline__ float emu_quantise(float t, int fmt) {
-  if (fmt == RSSM_EMU_INT8) return fminf(fmaxf(rintf(t), -127.f), 127.f);
-  int sh;
-  float lo, c, vmax;  // 2^emin, the magic constant, the largest value
-  switch (fmt) {
-    case RSSM_EMU_BF16: sh = 16; lo = 0x1p-126f; c = 0x1.8p-110f; vmax = 0x1.fep127f; break;
-    case RSSM_EMU_F16: sh = 13; lo = 0x1p-14f; c = 0x1.8p-1f; vmax = 65504.f; break;
-    case RSSM_EMU_E4M3: sh = 20; lo = 0x1p-6f; c = 0x1.8p14f; vmax = 448.f; break;
-    default: sh = 21; lo = 0x1p-14f; c = 0x1.8p7f; vmax = 57344.f; break;  // RSSM_EMU_E5M2
-  }
+__device__ __forceinline__ float emu_quantise(float t, const EmuQ& q) {
+  if (q.int8) return fminf(fmaxf(rintf(t), -127.f), 127.f);
   uint32_t u = __float_as_uint(t);
-  u += (1u << (sh - 1)) - 1u + ((u >> sh) & 1u);
-  u &= ~((1u << sh) - 1u);
-  const float sub = __fsub_rn(__fadd_rn(t, c), c);
-  const float r = fabsf(t) < lo ? sub : __uint_as_float(u);
-  return fminf(fmaxf(r, -vmax), vmax);
+  u = (u + q.half + ((u >> q.sh) & 1u)) & q.mask;
+  const float sub = __fsub_rn(__fadd_rn(t, q.c), q.c);
+  const float r = fabsf(t) < q.lo ? sub : __uint_as_float(u);
+  return fminf(fmaxf(r, -q.vmax), q.vmax);
 }
 
 // Maxima of V per-lane values over the warp, transposed like

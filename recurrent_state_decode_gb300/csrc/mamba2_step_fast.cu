@@ -44,8 +44,8 @@ constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
 // scale, Q the format's rounding; err and nrm gather (read - x)^2 and x^2.
 // With a row scale the rows' maxima come from one transposed max reduction,
 // lane row_src(rr) computing row rr's quotients. Every lane must call this.
-__device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, float tinv, float ts, int lane,
-                                          float& err, float& nrm) {
+__device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, const EmuQ& fq, float tinv, float ts,
+                                          int lane, float& err, float& nrm) {
   float inv[8], sc[8];
   const bool scaled = a.emu_scale != RSSM_EMU_SCALE_NONE;
   if (a.emu_scale == RSSM_EMU_SCALE_ROW) {
@@ -73,7 +73,7 @@ __device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, floa
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       const float x = v[j];
-      const float q = emu_quantise(scaled ? __fmul_rn(x, inv[rr]) : x, a.emu_fmt);
+      const float q = emu_quantise(scaled ? __fmul_rn(x, inv[rr]) : x, fq);
       const float r = scaled ? __fmul_rn(q, sc[rr]) : q;
       const float d = r - x;
       err = fmaf(d, d, err);
@@ -89,7 +89,7 @@ __device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, floa
 // EMU: non-flush steps read the fp32 tile through an emulated precision and
 // each warp writes its (error, norm) sums to a.emu_part (fp32 tiles, no slots).
 template <bool OUT_BF16, bool RD16, bool SLOTS, bool EMU = false>
-__global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a) {
+__global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
   __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
   extern __shared__ __align__(128) float tile_d[];
@@ -217,22 +217,31 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
       }
     }
   }
-  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
+  // (the emulated instantiation makes the outcome block-uniform: it meets a block barrier after the wait)
+  if (!(EMU ? __syncthreads_and(mbar_wait(&bar, 0)) : __all_sync(FULL, mbar_wait(&bar, 0)))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
     if (EMU && lane == 0) *emu_slot = make_float2(0.f, 0.f);
     mbar_wait(&bar, 0);
     if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
     return;
   }
-  // Emulated read with one scale per 64-row tile: each warp takes the whole
-  // tile's maximum from shared memory itself (no block barrier after the wait).
+  // Emulated read with one scale per 64-row tile: the maxima of the warps'
+  // rows meet in shared memory (the dot table's first entries, consumed by now).
   float emu_tinv = 1.f, emu_ts = 1.f, emu_err = 0.f, emu_nrm = 0.f;
+  EmuQ emu_q{};
+  if (EMU) emu_q = emu_params(a.emu_fmt);
   if (EMU && !flush && a.emu_scale == RSSM_EMU_SCALE_TILE64) {
     float m = 0.f;
-#pragma unroll 8
-    for (int r = 0; r < FPB; r++) m = fmaxf(m, abs_max4(reinterpret_cast<const float4*>(tile + r * FN)[lane]));
+#pragma unroll
+    for (int rr = 0; rr < 8; rr++) {
+      m = fmaxf(m, abs_max4(reinterpret_cast<const float4*>(tile + (rl0 + rr) * FN)[lane]));
+      m = fmaxf(m, abs_max4(reinterpret_cast<const float4*>(tile + (rl1 + rr) * FN)[lane]));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    if (lane == 0) sc[warp] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
     const float qmax = emu_qmax(a.emu_fmt);
     emu_tinv = m > 0.f ? qmax / m : 0.f;
     emu_ts = m / qmax;
@@ -261,7 +270,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
     } else {
 #pragma unroll
       for (int rr = 0; rr < 8; rr++) hv[rr] = reinterpret_cast<const float4*>(tile + (rl + rr) * FN)[lane];
-      if (EMU && !flush) emu_read8(hv, a, emu_tinv, emu_ts, lane, emu_err, emu_nrm);
+      if (EMU && !flush) emu_read8(hv, a, emu_q, emu_tinv, emu_ts, lane, emu_err, emu_nrm);
     }
     float xl[8], tx[8];
     unpack8(xq[half], xl);
@@ -282,10 +291,12 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a
 
 // The emulated step's error sums: the per-warp pairs added in a fixed order
 // (each thread a strided share in fp64, then a tree over the block).
-__global__ void __launch_bounds__(256) emu_reduce_kernel(const float2* __restrict__ part, size_t n, double* err) {
-  __shared__ double se[256], sn[256];
+constexpr int EMU_RT = 1024;  // threads of the reduction
+
+__global__ void __launch_bounds__(EMU_RT) emu_reduce_kernel(const float2* __restrict__ part, size_t n, double* err) {
+  __shared__ double se[EMU_RT], sn[EMU_RT];
   double e = 0.0, q = 0.0;
-  for (size_t i = threadIdx.x; i < n; i += 256) {
+  for (size_t i = threadIdx.x; i < n; i += EMU_RT) {
     const float2 v = part[i];
     e += v.x;
     q += v.y;
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(256) emu_reduce_kernel(const float2* __restric
   se[threadIdx.x] = e;
   sn[threadIdx.x] = q;
   __syncthreads();
-  for (int o = 128; o > 0; o >>= 1) {
+  for (int o = EMU_RT / 2; o > 0; o >>= 1) {
     if (threadIdx.x < o) {
       se[threadIdx.x] += se[threadIdx.x + o];
       sn[threadIdx.x] += sn[threadIdx.x + o];
@@ -314,8 +325,8 @@ bool m2_step_fast_applies(const M2Args& a) {
 }
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
-  const dim3 grid(a.nPB, a.H, a.Bt);
   const bool rd16 = a.ckpt_read != nullptr;
+  const dim3 grid(a.nPB, a.H, a.Bt);
   auto pick = [&](auto slots) {
     constexpr bool S = decltype(slots)::value;
     return rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true, S> : m2_step_fast_kernel<false, true, S>)
@@ -338,7 +349,7 @@ cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, 
   if (e != cudaSuccess) return e;
   k<<<grid, FT, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  emu_reduce_kernel<<<1, 256, 0, st>>>(a.emu_part, m2_emulated_partials(a), err);
+  emu_reduce_kernel<<<1, EMU_RT, 0, st>>>(a.emu_part, m2_emulated_partials(a), err);
   return cudaGetLastError();
 }
 
