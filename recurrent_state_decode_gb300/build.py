@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "librssm.so")
-SOURCES = ["api.cu", "mamba2.cu", "mamba2_step.cu", "mamba2_step_fast.cu", "mamba2_verify.cu", "mamba2_verify_fast.cu", "gdn.cu", "gdn_step_fast.cu", "gdn_verify.cu", "gdn_verify_fast.cu", "kda.cu", "kda_step_fast.cu", "cursors.cu"]
+SOURCES = ["api.cu", "mamba2.cu", "mamba2_step.cu", "mamba2_step_fast.cu", "mamba2_verify.cu", "mamba2_verify_fast.cu", "gdn.cu", "gdn_step_fast.cu", "gdn_verify.cu", "gdn_verify_fast.cu", "kda.cu", "kda_step_fast.cu", "kda_verify_fast.cu", "cursors.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

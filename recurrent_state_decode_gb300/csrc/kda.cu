@@ -198,193 +198,6 @@ __global__ void __launch_bounds__(FT) kda_window_kernel(GdnArgs a) {
   }
 }
 
-// ------------------------------------------------------------------ speculative verify
-
-constexpr int VK = 4;  // new records per verify on this kernel
-
-struct KdaVerSmem {
-  float kw[WMAX * KD];       // keys of records 0 .. total - 1 (fp32)
-  float G[WMAX * KD];        // channel prefix sums of g over the same records
-  float qw[VK * KD];         // the new records' queries
-  float vecs[2 * VK * KD];   // exp(G_t) * k_t of new record j at [j], exp(G_a) * q_i at [VK + i]
-  float es[WMAX * FPB];      // e of every record at the block's rows (committed from the ring, new solved)
-  float us[2 * VK * FPB];    // S0 . vecs[v] at the block's rows
-  float M[VK * WMAX];        // M[j][s] = (exp(G_t - G_s) * k_s) . k_t, t = count + j, s < t
-  float Q[VK * WMAX];        // Q[i][s] = (exp(G_a - G_s) * k_s) . q_i, a = count + i, s <= a
-};
-
-// One CTA of four warps per (sequence, head, 64 state rows). Records t of the
-// view run over [0, count + K): t < count the committed window (ring slot
-// (start + t) mod L), then the K new ones. With G_t the channel-wise prefix
-// sums of g:
-//   e_t = beta_t (v_t - S0 (exp(G_t) * k_t) - sum_{s<t} ((exp(G_t - G_s) * k_s) . k_t) e_s)    (new t)
-//   o_i = S0 (exp(G_a) * q_i) + sum_{s<=a} ((exp(G_a - G_s) * k_s) . q_i) e_s,  a = count + i
-// The committed records' e come from the ring. If count + K > L the committed
-// window is first folded into S (as the flush does), written once; the outputs
-// are the same whether taken from S0 with every record or after the fold. The
-// new records' e and v rows of this block go to the ring here; their shared
-// fields (k, q, g, beta) and the cursor follow in kda_verify_epilogue_kernel.
-// The checkpoint rows are read from global memory by the warp that owns them
-// (coalesced float4 per lane), which keeps shared memory to 51 KiB: four blocks
-// per SM.
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(FT) kda_verify_kernel(GdnArgs a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  KdaVerSmem& s = *reinterpret_cast<KdaVerSmem*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int L = a.L, K = a.K, H = a.H, pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const size_t sh = (size_t)b * H + h;
-  const int p0 = pb * FPB;
-  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
-  // uniform over the block; a bad cursor is reported by the epilogue kernel
-  if (!(cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0)) return;
-  const int start = cur.x, count = cur.y, total = count + K;
-  const bool fold = total > L;
-  auto rec_row = [&](int t) { return sh * L + (start + t) % L; };          // ring row of committed record t
-  auto new_row = [&](int j) { return ((size_t)b * K + j) * H + h; };       // record row of new record j
-  const size_t tbase = (sh * KD + p0) * KD;
-  const float* srow = a.S + tbase;  // the block's 64 checkpoint rows
-  {  // thread c: channel c of every record's g and key (independent loads), then the prefix sums
-    const int c = tid;
-#pragma unroll 4
-    for (int t = 0; t < total; t++) {
-      const bool ring = t < count;
-      const size_t row = ring ? rec_row(t) : new_row(t - count);
-      s.G[t * KD + c] = ring ? a.rg[row * KD + c] : a.g[row * KD + c];
-      s.kw[t * KD + c] = bf_to_f(ring ? a.rk[row * KD + c] : a.k[row * KD + c]);
-    }
-    for (int j = 0; j < K; j++) s.qw[j * KD + c] = bf_to_f(a.q[new_row(j) * KD + c]);
-    float acc = 0.f;
-    for (int t = 0; t < total; t++) {
-      acc += s.G[t * KD + c];
-      s.G[t * KD + c] = acc;
-    }
-  }
-  for (int i = tid; i < count * FPB; i += FT) {  // the committed records' e at the block's rows
-    const int t = i / FPB, r = i - t * FPB;
-    s.es[i] = a.re[rec_row(t) * KD + p0 + r];
-  }
-  __syncthreads();
-  // the S0 vectors and the dot tables (one warp per entry, lanes over channel chunks)
-  for (int v = warp; v < 2 * K; v += FW) {
-    const int j = v < K ? v : v - K, t = count + j;
-    const float4 x = v < K ? ld4(s.kw + t * KD + 4 * lane) : ld4(s.qw + j * KD + 4 * lane);
-    reinterpret_cast<float4*>(s.vecs + (v < K ? j : VK + j) * KD)[lane] = mul4(exp4(ld4(s.G + t * KD + 4 * lane)), x);
-  }
-  for (int it = warp; it < 2 * K * total; it += FW) {
-    const int table = it / (K * total), rem = it - table * K * total, j = rem / total, sidx = rem - j * total;
-    const int t = count + j;                   // the new record (table 0) or the output's last record (table 1)
-    if (table == 0 ? sidx >= t : sidx > t) continue;  // uniform over the warp
-    const float4 kd = mul4(exp4(sub4(ld4(s.G + t * KD + 4 * lane), ld4(s.G + sidx * KD + 4 * lane))),
-                           ld4(s.kw + sidx * KD + 4 * lane));
-    const float4 y = table == 0 ? ld4(s.kw + t * KD + 4 * lane) : ld4(s.qw + j * KD + 4 * lane);
-    const float p = warp_sum(dot4(kd, y));
-    if (lane == 0) (table == 0 ? s.M : s.Q)[j * WMAX + sidx] = p;
-  }
-  __syncthreads();  // the vectors and the tables
-  const int rl0 = warp * 8, rl1 = HALF + warp * 8;
-#pragma unroll
-  for (int half = 0; half < 2; half++) {  // S0 . vecs for the warp's rows
-    const int rl = half ? rl1 : rl0;
-    float4 hv[8];
-#pragma unroll
-    for (int rr = 0; rr < 8; rr++) hv[rr] = ld4(srow + (size_t)(rl + rr) * KD + 4 * lane);
-    for (int v = 0; v < 2 * K; v++) {
-      const float4 x = ld4(s.vecs + (v < K ? v : VK + v - K) * KD + 4 * lane);
-      float d[8];
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++) d[rr] = dot4(hv[rr], x);
-      reduce8(d, lane);
-      if ((lane & 3) == 0) s.us[v * FPB + rl + reduce8_row(lane)] = d[0];
-    }
-  }
-  __syncthreads();
-  if (tid < FPB) {  // thread r: row p0 + r; the new records' e in order, then the outputs
-    const int r = tid;
-    for (int j = 0; j < K; j++) {
-      const int t = count + j;
-      const size_t nr = new_row(j);
-      float rhs = bf_to_f(a.v[nr * KD + p0 + r]) - s.us[j * FPB + r];
-      for (int sidx = 0; sidx < t; sidx++) rhs = fmaf(-s.M[j * WMAX + sidx], s.es[sidx * FPB + r], rhs);
-      const float e = a.beta[nr] * rhs;
-      s.es[t * FPB + r] = e;
-      const size_t ring = sh * L + (start + t) % L;  // the new record's slot: (start + count + j) mod L
-      a.re[ring * KD + p0 + r] = e;
-      a.rv[ring * KD + p0 + r] = a.v[nr * KD + p0 + r];
-    }
-    for (int i = 0; i < K; i++) {
-      const int t = count + i;
-      float o = s.us[(K + i) * FPB + r];
-      for (int sidx = 0; sidx <= t; sidx++) o = fmaf(s.Q[i * WMAX + sidx], s.es[sidx * FPB + r], o);
-      store_out<OUT_BF16>(a.o, new_row(i) * KD + p0 + r, o);
-    }
-  }
-  if (fold) {  // S0' = S0 Diag(exp(G_{c-1})) + sum_{s<c} e_s (exp(G_{c-1} - G_s) * k_s)^T, c = count, written once
-    const float4 Gl = ld4(s.G + (count - 1) * KD + 4 * lane);
-    const float4 gl = exp4(Gl);
-#pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int rl = half ? rl1 : rl0;
-      float4 hv[8];
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++) hv[rr] = mul4(gl, ld4(srow + (size_t)(rl + rr) * KD + 4 * lane));
-      for (int t = 0; t < count; t++) {
-        const float4 kt = mul4(exp4(sub4(Gl, ld4(s.G + t * KD + 4 * lane))), ld4(s.kw + t * KD + 4 * lane));
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(s.es[t * FPB + rl + rr], kt, hv[rr]);
-      }
-#pragma unroll
-      for (int rr = 0; rr < 8; rr++)
-        __stcs(reinterpret_cast<float4*>(a.S + tbase + (size_t)(rl + rr) * KD) + lane, hv[rr]);
-    }
-  }
-}
-
-// One block per (sequence, head), after the verify in stream order: on a
-// cursor with 0 <= start < L, 0 <= count <= L and pending == 0, append the
-// head's new records' k, q, g rows and beta at slots (start + count + j) mod L.
-// The last of the sequence's blocks to have read the cursor (an arrival count
-// in the high half of its flags word) sets pending = K, flags = folded, or
-// reports as the cursor checks do and leaves it as it was.
-__global__ void __launch_bounds__(FT) kda_verify_epilogue_kernel(GdnArgs a) {
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, L = a.L, K = a.K, H = a.H;
-  int4 c = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
-  int err = 0;
-  if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L))
-    err = RSSM_DEV_BAD_CURSOR;
-  else if (c.z != 0)
-    err = RSSM_DEV_PENDING;
-  __syncthreads();  // every thread has read the cursor
-  if (tid == 0) {
-    const int ticket = cursor_ticket(a.cursors, b);
-    if (last_ticket(ticket, H)) {
-      if (err) {
-        report(a.status, err);
-        c.w = ticket & 0xffff;  // the flags as they were, the arrival count cleared
-      } else {
-        c.w = (c.y + K > L) ? 1 : 0;
-        c.z = K;
-      }
-      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)b) = c;
-    }
-  }
-  if (err) return;
-  constexpr int NB = KD / 8, NG = KD / 4;  // 16-byte pieces of a bf16 row, of an fp32 row
-  for (int q = tid; q < K * (2 * NB + NG); q += FT) {
-    const int j = q / (2 * NB + NG), piece = q - j * (2 * NB + NG);
-    const size_t ring = ((size_t)b * H + h) * L + (c.x + c.y + j) % L, rec = ((size_t)b * K + j) * H + h;
-    if (piece < NB) {
-      reinterpret_cast<uint4*>(a.rk + ring * KD)[piece] = reinterpret_cast<const uint4*>(a.k + rec * KD)[piece];
-    } else if (piece < 2 * NB) {
-      reinterpret_cast<uint4*>(a.rq + ring * KD)[piece - NB] = reinterpret_cast<const uint4*>(a.q + rec * KD)[piece - NB];
-    } else {
-      reinterpret_cast<float4*>(a.rg + ring * KD)[piece - 2 * NB] =
-          reinterpret_cast<const float4*>(a.g + rec * KD)[piece - 2 * NB];
-    }
-  }
-  if (tid < K) a.rbeta[((size_t)b * H + h) * pad4(L) + (c.x + c.y + tid) % L] = a.beta[((size_t)b * K + tid) * H + h];
-}
-
 template <typename Kern>
 cudaError_t launch_smem(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t st, const GdnArgs& a) {
   cudaError_t e = prepare(k, smem, false);
@@ -396,20 +209,6 @@ cudaError_t launch_smem(Kern k, dim3 grid, int threads, size_t smem, cudaStream_
 }  // namespace
 
 bool kda_window_applies(const GdnArgs& a) { return a.DK == KD && a.DV == KD && a.Bt <= 65535 && a.H <= 65535; }
-
-bool kda_verify_applies(const GdnArgs& a) {
-  return kda_window_applies(a) && a.K <= VK && a.L + a.K <= WMAX && a.H < (1 << 15);  // H arrivals in 15 bits
-}
-
-cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
-  if (a.Bt == 0) return cudaSuccess;
-  const dim3 grid(2, a.H, a.Bt);
-  cudaError_t e = out_bf16 ? launch_smem(kda_verify_kernel<true>, grid, FT, sizeof(KdaVerSmem), st, a)
-                           : launch_smem(kda_verify_kernel<false>, grid, FT, sizeof(KdaVerSmem), st, a);
-  if (e != cudaSuccess) return e;
-  kda_verify_epilogue_kernel<<<dim3(a.Bt, a.H), FT, 0, st>>>(a);
-  return cudaGetLastError();
-}
 
 cudaError_t kda_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;

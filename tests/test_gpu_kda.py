@@ -288,6 +288,37 @@ def test_kda_spec_bf16_out():
     run_kda_spec(KSPEC[0], out_dtype=bd.RSSM_BF16)
 
 
+def test_kda_spec_strong_decays():
+    """Speculative decode with per-token decays down to about exp(-12) per
+    channel (the window, the new records and the fold): every decay factor is
+    an exponential of a later-minus-earlier sum, so nothing overflows and the
+    outputs, corrections and folded checkpoints stay at the fp32 tolerances."""
+    w = KW("kspec_strong", 3, 2, 128, 128, 8, 16, seed=427, drafts=3)
+    dev = "cuda"
+    st, pre, starts, counts = kda_from_workload(w, dev)
+    fv, fk = H.Feed(), H.Feed()
+    sess = sessions.kda_spec_session(H.F64(st.S), H.sub(pre, slice(None)), starts.cpu().numpy(),
+                                     counts.cpu().numpy(), fv, fk, w.buf_len)
+    o = st.new_verify_output(w.n_new)
+    folds = 0
+    for t in range(w.steps):
+        rec = I.kda_verify_inputs(w, t, dev)
+        rec["g"] = (rec["g"] * 4.0).contiguous()
+        kept = I.accepted_kept(w, t, dev)
+        fv.rec, fk.rec = H.sub(rec, slice(None)), kept.cpu().numpy()
+        st.verify(rec, o)
+        st.commit(kept)
+        exp = next(sess)
+        assert torch.isfinite(o).all()
+        assert H.rel_l2(H.F64(o), exp["o"]) <= TOL_Y32, t
+        for b in range(w.batch):
+            if exp["folded"][b]:
+                folds += 1
+                assert H.rel_l2(H.F64(st.S[b]), exp["committed_state"][b]) <= TOL_CKPT, (t, b)
+    assert folds > 0
+    assert H.status(st) == 0
+
+
 def test_kda_spec_unsupported_and_invalid():
     st = KDAState(2, 2, 128, 128, 30)
     rec = {k: torch.zeros(1, device="cuda") for k in ("q", "k", "v", "g", "beta")}
