@@ -20,23 +20,27 @@
 // and a fold (count + K > L) writes S0 Diag(E) + sum_{t<count} e_t (f_t * k_t)^T.
 // The committed records' e come from the ring (fixed from their append).
 //
-// One CTA of four warps per (sequence, head, 64 state rows); warp w owns rows
-// 8w..8w+7 and 32+8w..32+8w+7. At launch: the 64 rows by one bulk copy (TMA,
-// non-tensor; never multicast) into shared memory; thread c takes channel c of
-// the new records (g, k, q), forms w_j, k~_j, q~_i into shared memory and its
-// channel's share of the sixteen couplings among new records (one transposed
-// reduction per warp, summed over the warps in shared memory); lane j the new
-// record j's beta, lane 4 j + t the v of new record t at the lane's rows, as
-// the Gated DeltaNet verify. After the cursor: the window's e rows (this block's) and g rows by bulk copy (second
-// mbarrier); thread c turns its channel of the g rows into f_t in place and E;
-// each warp forms the dots (f_t * k_t) . [k~, q~] of four committed records
-// per round (one 32-value transposed reduction). The S0 product with the
-// eight vectors E * k~_j, E * q~_i is an m16n8k8 tf32 mma per warp with both
-// operands split into two tf32 parts (three products per k-step); the new
-// records' e are solved within each quad, the outputs completed, the new e and
-// v rows appended, the fold written if any. The new records' k, q, g and beta
-// (read by the head's other block) are appended by the sequence's last block
-// to arrive, which also marks the cursor pending.
+// One CTA of eight warps per (sequence, head), so that the work per head --
+// the couplings, the decays, the dot table -- is done once: warp w owns state
+// rows 8w..8w+7 and 64+8w..64+8w+7. At launch: the head's 128 rows by two
+// bulk copies (TMA, non-tensor; never multicast) into shared memory; threads
+// c < 128 take channel c of the new records (g, k, q), form w_j, k~_j, q~_i
+// into shared memory and their channel's share of the sixteen couplings among
+// new records (one transposed reduction per warp, summed over the warps in
+// shared memory); lane j the new record j's beta, lane 4 j + t the v of new
+// record t at the lane's rows, as in the Gated DeltaNet verify. As soon as
+// the cursor is read, the last warp (idle in the channel phase) stages the
+// window's e and g rows by bulk copies, one record per lane (second
+// mbarrier). Then thread c
+// turns its channel of the g rows into f_t in place and E; each warp forms the
+// dots (f_t * k_t) . [k~, q~] of two committed records per round (one 16-value
+// transposed reduction). The S0 product with the eight vectors E * k~_j,
+// E * q~_i is an m16n8k8 tf32 mma per warp with both operands split into two
+// tf32 parts (three products per k-step); the new records' e are solved within
+// each quad, the outputs completed, the new e and v rows appended, the fold
+// written if any. The block then appends its head's new k, q, g rows and beta
+// (no other block reads them), and the sequence's last block to arrive marks
+// the cursor pending.
 #include "fast_rows.cuh"
 #include "kernels.h"
 
@@ -49,118 +53,113 @@ using namespace fastrows;
 constexpr int GD = 128;      // dk = dv
 constexpr int KMAX = 4;      // new records per verify on this path
 constexpr int WMAX = 32;     // records since the checkpoint: L + K <= 32
-constexpr int ES = FPB + 4;  // floats per staged e row (padded; 16-byte multiple)
+constexpr int VW = 8;        // warps per block: one block per (sequence, head), warp w rows 8w.. and 64 + 8w..
+constexpr int VT = 32 * VW;  // threads per block
+constexpr int VHALF = 64;    // a warp's second row group starts here
+constexpr int ES = GD + 4;   // floats per staged e row (padded; 16-byte multiple)
 
-// Epilogue of a KDA verify for sequence b (state slot sb), run by the whole
-// block once no block of the sequence reads the ring rows it overwrites: on a
-// cursor with 0 <= start < L, 0 <= count <= L and pending == 0, append the K
-// new records' k, q, g rows and beta at slots (start + count + j) mod L and
-// set pending = K, flags = folded; otherwise report as the cursor checks do
-// and leave the cursor with its flags word set to `flags`.
-__device__ __forceinline__ void kda_verify_epilogue(const GdnArgs& a, int b, int sb, int4 c, int flags) {
+// The new records' k, q, g rows and beta of head h at ring slots (start +
+// count + j) mod L (cursor c, already checked), by the whole block. One block
+// per (sequence, head) reads that head's ring rows, so it appends them itself
+// once it is done reading.
+__device__ __forceinline__ void append_head(const GdnArgs& a, int b, int h, int4 c) {
   const int L = a.L, K = a.K, H = a.H, tid = threadIdx.x;
-  c.w = flags;
-  int err = 0;
-  if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L))
-    err = RSSM_DEV_BAD_CURSOR;
-  else if (c.z != 0)
-    err = RSSM_DEV_PENDING;
-  if (err) {
-    if (tid == 0) {
-      report(a.status, err);
-      *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)sb) = c;
-    }
-    return;
-  }
   constexpr int NB = GD / 8, NG = GD / 4;  // 16-byte pieces of a bf16 row, of an fp32 row
-  constexpr int PER = 2 * NB + NG;         // pieces of one (record, head): k, q, g
-  const int pieces = K * H * PER;
-  constexpr int U = 4;  // pieces in flight per thread: all loads before the stores
-  for (int q0 = tid; q0 < pieces; q0 += U * FT) {
-    uint4 val[U];
-    size_t dst[U];
-    int kind[U];
-#pragma unroll
-    for (int u = 0; u < U; u++) {
-      const int q = q0 + u * FT;
-      kind[u] = -1;
-      if (q < pieces) {
-        const int j = q / (H * PER), r = q - j * H * PER, h = r / PER, piece = r - h * PER;
-        const size_t ring = ((size_t)sb * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
-        const size_t rec = ((size_t)b * K + j) * H + h;
-        if (piece < NB) {
-          kind[u] = 0;
-          dst[u] = ring * GD + piece * 8;
-          val[u] = *reinterpret_cast<const uint4*>(a.k + rec * GD + piece * 8);
-        } else if (piece < 2 * NB) {
-          kind[u] = 1;
-          dst[u] = ring * GD + (piece - NB) * 8;
-          val[u] = *reinterpret_cast<const uint4*>(a.q + rec * GD + (piece - NB) * 8);
-        } else {
-          kind[u] = 2;
-          dst[u] = ring * GD + (piece - 2 * NB) * 4;
-          val[u] = *reinterpret_cast<const uint4*>(a.g + rec * GD + (piece - 2 * NB) * 4);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; u++) {
-      if (kind[u] == 0) *reinterpret_cast<uint4*>(a.rk + dst[u]) = val[u];
-      if (kind[u] == 1) *reinterpret_cast<uint4*>(a.rq + dst[u]) = val[u];
-      if (kind[u] == 2) *reinterpret_cast<uint4*>(a.rg + dst[u]) = val[u];
+  constexpr int PER = 2 * NB + NG;         // pieces of one record: k, q, g
+  for (int q = tid; q < K * PER; q += VT) {
+    const int j = q / PER, piece = q - j * PER;
+    const size_t ring = ((size_t)b * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
+    const size_t rec = ((size_t)b * K + j) * H + h;
+    if (piece < NB) {
+      *reinterpret_cast<uint4*>(a.rk + ring * GD + piece * 8) = *reinterpret_cast<const uint4*>(a.k + rec * GD + piece * 8);
+    } else if (piece < 2 * NB) {
+      const int v = piece - NB;
+      *reinterpret_cast<uint4*>(a.rq + ring * GD + v * 8) = *reinterpret_cast<const uint4*>(a.q + rec * GD + v * 8);
+    } else {
+      const int v = piece - 2 * NB;
+      *reinterpret_cast<uint4*>(a.rg + ring * GD + v * 4) = *reinterpret_cast<const uint4*>(a.g + rec * GD + v * 4);
     }
   }
-  for (int q = tid; q < K * H; q += FT) {
-    const int j = q / H, h = q - j * H;
-    a.rbeta[((size_t)sb * H + h) * pad4(L) + wrap(wrap(c.x + c.y + j, L), L)] = a.beta[((size_t)b * K + j) * H + h];
-  }
-  if (tid == 0) {
+  if (tid < K)
+    a.rbeta[((size_t)b * H + h) * pad4(L) + wrap(wrap(c.x + c.y + tid, L), L)] = a.beta[((size_t)b * K + tid) * H + h];
+}
+
+// The cursor rule of a verify, applied by the sequence's last block to arrive
+// (one thread): on a cursor with 0 <= start < L, 0 <= count <= L and pending
+// == 0, pending = K and flags = folded; otherwise the same report as the
+// cursor checks and no move. The arrival count is cleared.
+__device__ __forceinline__ void finish_verify_cursor(int32_t* cursors, int b, int4 c, int ticket, int nblocks, int L,
+                                                     int K, int32_t* status) {
+  if (!last_ticket(ticket, nblocks)) return;
+  c.w = ticket & 0xffff;
+  if (!(c.x >= 0 && c.x < L && c.y >= 0 && c.y <= L)) {
+    report(status, RSSM_DEV_BAD_CURSOR);
+  } else if (c.z != 0) {
+    report(status, RSSM_DEV_PENDING);
+  } else {
     c.z = K;
     c.w = (c.y + K > L) ? 1 : 0;
-    *reinterpret_cast<int4*>(a.cursors + 4 * (size_t)sb) = c;
   }
+  *reinterpret_cast<int4*>(cursors + 4 * (size_t)b) = c;
 }
 
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
+__global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   const int L = a.L, H = a.H, K = a.K;
-  float* tile = dsm;                 // the block's 64 rows
-  float* vt = tile + FPB * GD;       // [0..3] k~_j, [4..7] q~_i (fp32, all channels)
+  float* tile = dsm;                 // the head's 128 rows
+  float* vt = tile + GD * GD;        // [0..3] k~_j, [4..7] q~_i (fp32, all channels)
   float* ew = vt + 2 * KMAX * GD;    // E by channel
   float* fd = ew + GD;               // g, then f, of committed record t at fd + t * GD
-  float* es = fd + L * GD;           // e of committed record t at es + t * ES (the block's rows)
+  float* es = fd + L * GD;           // e of committed record t at es + t * ES (all rows)
   __shared__ float cf[2 * KMAX][WMAX + 1];  // [n][t]: (f_t * k_t) . vec_n
-  __shared__ float cred[FW][32];            // the couplings' per-warp sums (lane layout of cpl)
+  __shared__ float cred[4][32];             // the couplings' per-warp sums (warps 0..3; lane layout of cpl)
   __shared__ uint64_t bar[2];               // [0] the rows, [1] the window's e and g rows
   __shared__ int4 cur_s;
-  __shared__ int last_flags;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, c = threadIdx.x;
-  const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.y, b = blockIdx.z;
   const size_t sh = (size_t)b * H + h;
-  const int p0 = pb * FPB;
-  const size_t tbase = (sh * GD + p0) * GD;
+  const size_t tbase = sh * GD * GD;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar[0], FPB * GD * 4);
-    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
+    mbar_arrive_expect_tx(&bar[0], GD * GD * 4);
+    bulk_load(tile, a.S + tbase, GD * GD * 2, &bar[0]);
+    bulk_load(tile + GD * GD / 2, a.S + tbase + GD * GD / 2, GD * GD * 2, &bar[0]);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
-  const int rl0 = warp * 8, rl1 = HALF + warp * 8;
+  // An invalid cursor (reported by the sequence's last block) runs as an empty
+  // window with every store masked.
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
+  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, total = count + K;
+  const bool fold = valid && total > L;
+  if (warp == VW - 1) {  // the last warp (idle in the channel phase below) stages the window's e and g rows
+    if (lane == 0) {
+      cur_s = cur;
+      mbar_init(&bar[1], 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&bar[1], (uint32_t)count * 2 * GD * 4);
+    }
+    __syncwarp();
+    if (lane < count) {  // lane t: committed record t, in record order
+      const size_t row = sh * L + wrap(start + lane, L);
+      bulk_load(es + lane * ES, a.re + row * GD, GD * 4, &bar[1]);
+      bulk_load(fd + lane * GD, a.rg + row * GD, GD * 4, &bar[1]);
+    }
+  }
+  const int rl0 = warp * 8, rl1 = VHALF + warp * 8;
   const int qg = lane >> 2, qt = lane & 3;  // tensor-core fragment coordinates
   const int rA = rl0 + qg, rB = rl1 + qg;   // the rows of this lane's accumulator fragments
   float bn = 0.f;
   if (lane < K) bn = a.beta[((size_t)b * K + lane) * H + h];
   uint32_t vtA = 0, vtB = 0;  // v of new record qt at rows rA, rB (bf16 bits)
   if (qt < K) {
-    const size_t vrow = (((size_t)b * K + qt) * H + h) * GD + p0;
+    const size_t vrow = (((size_t)b * K + qt) * H + h) * GD;
     vtA = a.v[vrow + rA];
     vtB = a.v[vrow + rB];
   }
-  {  // thread c: channel c of the new records -> w_j, k~_j, q~_i and the couplings among them
+  if (warp < 4) {  // thread c: channel c of the new records -> w_j, k~_j, q~_i and the couplings among them
     float gn[KMAX], kn[KMAX], qn[KMAX], Gn[KMAX];
     float acc = 0.f;
 #pragma unroll
@@ -192,20 +191,6 @@ __global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
     }
     cred[warp][lane] = reduce_transpose<32>(p, lane);  // lane l: this warp's sum of index l
   }
-  // An invalid cursor (reported by the epilogue) runs as an empty window with
-  // every store masked.
-  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
-  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, total = count + K;
-  const bool fold = valid && total > L;
-  if (threadIdx.x == 0) {  // the committed records' e rows of this block and their g rows, in record order
-    cur_s = cur;
-    mbar_arrive_expect_tx(&bar[1], (uint32_t)count * (FPB + GD) * 4);
-    for (int t = 0; t < count; t++) {
-      const size_t row = sh * L + wrap(start + t, L);
-      bulk_load(es + t * ES, a.re + row * GD + p0, FPB * 4, &bar[1]);
-      bulk_load(fd + t * GD, a.rg + row * GD, GD * 4, &bar[1]);
-    }
-  }
   __syncthreads();  // k~, q~ and the couplings' partial sums; the barriers' initialisation
   const float cpl = cred[0][lane] + cred[1][lane] + cred[2][lane] + cred[3][lane];
   const bool staged = __syncthreads_and(mbar_wait(&bar[1], 0));
@@ -216,7 +201,7 @@ __global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
   }
   const bool live = valid && staged;
   const int cnt = staged ? count : 0;
-  {  // channel c: f_t = exp(G_W - G_t) in place of g_t, backwards over the window, then E = exp(G_W)
+  if (c < GD) {  // channel c: f_t = exp(G_W - G_t) in place of g_t, backwards over the window, then E = exp(G_W)
     float s = 0.f;
     for (int t = cnt - 1; t >= 0; t--) {
       const float x = fd[t * GD + c];
@@ -226,22 +211,27 @@ __global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
     ew[c] = expf(s);
   }
   __syncthreads();  // f_t and E
-  if (threadIdx.x == 0 && !fold) ticket = cursor_ticket(a.cursors, b);  // done with the ring's k and g rows
-  // window coefficients cf[n][t] = (f_t * k_t) . vec_n: warp w takes records 16 r + 4 w + i (i < 4)
+  if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);  // every thread has read the cursor
+  // window coefficients cf[n][t] = (f_t * k_t) . vec_n: warp w takes records 16 r + 2 w + i (i < 2)
   const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
-  for (int base = 0; base < cnt; base += 4 * FW) {  // uniform
-    float pk[32];
+  for (int base = 0; base < cnt; base += 2 * VW) {  // uniform
+    float4 kh[2];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const int t = base + 4 * warp + i;
-      float4 kh = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < cnt) kh = mul4(ld4(fd + t * GD + lane * 4), load_bf4(rkp + wrap(start + t, L) * GD));
-#pragma unroll
-      for (int n = 0; n < 2 * KMAX; n++) pk[8 * i + n] = dot4(kh, ld4(vt + n * GD + lane * 4));
+    for (int i = 0; i < 2; i++) {
+      const int t = base + 2 * warp + i;
+      kh[i] = t < cnt ? mul4(ld4(fd + t * GD + lane * 4), load_bf4(rkp + wrap(start + t, L) * GD))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float red = reduce_transpose<32>(pk, lane);  // lane l: record base + 4 w + (l >> 3), vector l & 7
-    const int t = base + 4 * warp + (lane >> 3);
-    if (t < cnt) cf[lane & 7][t] = red;
+    float pk[16];
+#pragma unroll
+    for (int n = 0; n < 2 * KMAX; n++) {
+      const float4 v = ld4(vt + n * GD + lane * 4);
+      pk[n] = dot4(kh[0], v);
+      pk[8 + n] = dot4(kh[1], v);
+    }
+    const float red = reduce_transpose<16>(pk, lane);  // lane l: index l >> 1 = record 2 w + (l >> 4), vector (l >> 1) & 7
+    const int t = base + 2 * warp + (lane >> 4);
+    if ((lane & 1) == 0 && t < cnt) cf[(lane >> 1) & 7][t] = red;
   }
   __syncthreads();  // the coefficient table
   const bool landed = __all_sync(FULL, mbar_wait(&bar[0], 0));  // uniform over the warp
@@ -329,7 +319,7 @@ __global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
       oB1 = fmaf(c1, eB[j], oB1);
     }
     if (live && qt >= 2) {
-      const size_t o0 = (((size_t)b * K + i0) * H + h) * GD + p0;
+      const size_t o0 = (((size_t)b * K + i0) * H + h) * GD;
       if (i0 < K) {
         store_out<OUT_BF16>(a.o, o0 + rA, oA0);
         store_out<OUT_BF16>(a.o, o0 + rB, oB0);
@@ -347,10 +337,10 @@ __global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
         mb = qt == j ? eB[j] : mb;
       }
       const size_t slot = sh * L + wrap(wrap(start + count + qt, L), L);
-      a.re[slot * GD + p0 + rA] = ma;
-      a.re[slot * GD + p0 + rB] = mb;
-      a.rv[slot * GD + p0 + rA] = (uint16_t)vtA;
-      a.rv[slot * GD + p0 + rB] = (uint16_t)vtB;
+      a.re[slot * GD + rA] = ma;
+      a.re[slot * GD + rB] = mb;
+      a.rv[slot * GD + rA] = (uint16_t)vtA;
+      a.rv[slot * GD + rB] = (uint16_t)vtB;
     }
     if (fold && staged) {  // S0 Diag(E) + sum_{t<count} e_t (f_t * k_t)^T, written once
       const float4 e4 = ld4(ew + lane * 4);
@@ -385,24 +375,20 @@ __global__ void __launch_bounds__(FT, 4) kda_verify_fast_kernel(GdnArgs a) {
       }
     }
   }
-  if (fold) {  // uniform: the fold read the ring's k rows until here
-    __syncthreads();
-    if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);
-  }
+  // this head's new k, q, g rows and beta, after every warp is done with the ring rows they may overwrite
   __syncthreads();
-  if (threadIdx.x == 0) last_flags = last_ticket(ticket, 2 * H) ? (ticket & 0xffff) : -1;
-  __syncthreads();
-  if (last_flags >= 0) kda_verify_epilogue(a, b, b, cur_s, last_flags);
+  if (live) append_head(a, b, h, cur_s);
+  if (threadIdx.x == 0) finish_verify_cursor(a.cursors, b, cur_s, ticket, H, L, K, a.status);
 }
 
 }  // namespace
 
 bool kda_verify_applies(const GdnArgs& a) {
-  return a.DK == GD && a.DV == GD && a.K <= KMAX && a.L + a.K <= WMAX && 2 * a.H < (1 << 15) && a.H <= 65535 &&
+  return a.DK == GD && a.DV == GD && a.K <= KMAX && a.L + a.K <= WMAX && a.H < (1 << 15) && a.H <= 65535 &&
          a.Bt <= 65535 && !a.slots;
 }
 
-size_t kda_verify_fast_smem(int L) { return (size_t)(FPB * GD + 2 * KMAX * GD + GD + L * GD + L * ES) * 4; }
+size_t kda_verify_fast_smem(int L) { return (size_t)(GD * GD + 2 * KMAX * GD + GD + L * GD + L * ES) * 4; }
 
 cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
@@ -410,7 +396,7 @@ cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   const size_t smem = kda_verify_fast_smem(a.L);
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
-  k<<<dim3(2, a.H, a.Bt), FT, smem, st>>>(a);
+  k<<<dim3(1, a.H, a.Bt), VT, smem, st>>>(a);
   return cudaGetLastError();
 }
 
