@@ -18,9 +18,9 @@
 // Gated DeltaNet step: warp w owns rows 8w..8w+7 and 32+8w..32+8w+7, lane l
 // the column chunk 4l..4l+3. At launch: the 64 rows by one bulk copy (TMA,
 // non-tensor; never multicast) into shared memory, the current record, and
-// the ring keys of the slots whose dots the warp forms. Once the cursor is
-// known thread 0 copies, in record order, the window records' e rows of this
-// block and their g rows (bulk copies on a second mbarrier); thread c then
+// the ring keys of the slots whose dots the warp forms. As soon as the cursor
+// arrives, warp 0's lane t copies window record t's e rows of this block and
+// its g row (bulk copies on a second mbarrier); thread c then
 // runs the suffix sums of channel c backwards over the window, leaving f_t in
 // place of g_t, and Gamma. Warp w forms (f_s * k_s) . k and (f_s * k_s) . q
 // for ring slots w, w+4, ... (slot L: the current k), one transposed
@@ -73,6 +73,19 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
     bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
+  // An invalid cursor (reported by the sequence's last block) runs as an empty
+  // window with every store masked, so that no thread leaves before a barrier.
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
+  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0;
+  if (warp == 0) {  // the window's e rows (this block's) and g rows, in record order, as soon as the cursor is known
+    if (lane == 0) mbar_arrive_expect_tx(&bar[1], (uint32_t)count * (FPB + GD) * 4);
+    __syncwarp();
+    if (lane < count) {
+      const size_t row = sh * L + wrap(start + lane, L);
+      bulk_load(es + lane * ES, a.re + row * GD + p0, FPB * 4, &bar[1]);
+      bulk_load(fd + lane * GD, a.rg + row * GD, GD * 4, &bar[1]);
+    }
+  }
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's row groups (within the block)
   // the current record; thread c holds channel c of its log decay
   const uint2 kraw = *reinterpret_cast<const uint2*>(a.k + bh * GD + lane * 4);
@@ -86,18 +99,6 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   for (int j = 0; j < KW; j++) {
     const int s = warp + FW * j;
     kr[j] = s < L ? *reinterpret_cast<const uint2*>(a.rk + (sh * L + s) * GD + lane * 4) : make_uint2(0, 0);
-  }
-  // An invalid cursor (reported by the sequence's last block) runs as an empty
-  // window with every store masked, so that no thread leaves before a barrier.
-  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
-  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0;
-  if (threadIdx.x == 0) {  // the window's e rows (this block's) and g rows, in record order
-    mbar_arrive_expect_tx(&bar[1], (uint32_t)count * (FPB + GD) * 4);
-    for (int t = 0; t < count; t++) {
-      const size_t row = sh * L + wrap(start + t, L);
-      bulk_load(es + t * ES, a.re + row * GD + p0, FPB * 4, &bar[1]);
-      bulk_load(fd + t * GD, a.rg + row * GD, GD * 4, &bar[1]);
-    }
   }
   int ticket = 0;
   __syncthreads();  // the barriers' initialisation is visible; every thread has read the cursor
