@@ -51,6 +51,8 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=2.0,
                     help="wall-clock seconds of oracle decoding per configuration for cpu_baseline (all host cores)")
     ap.add_argument("--detail", default=None, help="also write the full result, every workload's figures, here")
+    ap.add_argument("--bytes-out", default=None,
+                    help="profile mode: write the algorithmic bytes of every call it makes (JSON) here")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -442,6 +444,10 @@ def bench_mamba2_ar(args, dist):
         for t in range(W_ + K):
             st.step(recs[t], A, D, y)
         torch.cuda.synchronize()
+        c0 = counts0.cpu().tolist()
+        write_bytes(args, [bm.mamba2_step_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len,
+                                                [(c + t) % w.buf_len for c in c0], w.read_copy, out_bytes)
+                           for t in range(W_ + K)])
         return None
 
     # --- ReplaySSM step
@@ -815,8 +821,26 @@ def e2e_mamba2(st, A, D, w, dev, K, W_, y_dtype):
             "how": "wall clock, K pipelined steps: H2D of the record (pinned), rssm_mamba2_step, D2H of y"}
 
 
+def write_bytes(args, per_call):
+    """Profile mode: the algorithmic bytes of each call, in call order, for the ncu summaries."""
+    if args.bytes_out:
+        with open(args.bytes_out, "w") as f:
+            json.dump({"workload": args.workload, "bytes_per_call": per_call}, f)
+
+
+def spec_bytes(fn, w, counts0, kepts, out_bytes, n):
+    """Algorithmic bytes of n verifies from initial counts (fold when count + K > L)."""
+    counts = counts0.cpu().tolist()
+    out = []
+    for t in range(n):
+        out.append(fn(counts))
+        kl = kepts[t].cpu().tolist()
+        counts = [(0 if c + w.n_new > w.buf_len else c) + k for c, k in zip(counts, kl)]
+    return out
+
+
 def profile_other(args, dist):
-    """A few calls of the speculative or GDN workload, untimed (for ncu)."""
+    """A few calls of the speculative, delta-rule or emulated-read workload, untimed (for ncu)."""
     import torch
 
     from recurrent_state_decode_gb300 import binding as bd
@@ -825,38 +849,65 @@ def profile_other(args, dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     out = bd.RSSM_BF16 if args.out_dtype == "bf16" else bd.RSSM_F32
-    w = I.WORKLOADS[args.workload]
+    w = I.WORKLOADS["mamba2_serving" if args.workload == "mamba2_emu_e4m3_tile64" else args.workload]
     n = args.warmup + args.steps
-    if args.workload == "gdn_serving":
-        st, _, _, _ = gdn_from_workload(w, dev, out)
+    from recurrent_state_decode_gb300 import bytes_model as bm
+    ob = 2 if out == bd.RSSM_BF16 else 4
+    kepts = [I.accepted_kept(w, t, dev) for t in range(n)] if getattr(w, "drafts", 0) else None
+    if args.workload == "mamba2_emu_e4m3_tile64":
+        st, A, D, _, _, counts0 = mamba2_from_workload(w, dev, out)
+        y = st.new_output()
+        err = torch.zeros(2, dtype=torch.float64, device=dev)
+        ws = torch.empty(bd.rssm_mamba2_emulated_workspace_bytes(st.desc), dtype=torch.uint8, device=dev)
+        emu = bd.emulation(bd.RSSM_EMU_E4M3, bd.RSSM_EMU_SCALE_TILE64)
+        for t in range(n):
+            st.step_emulated(I.mamba2_step_inputs(w, t, dev), A, D, y, emu, err, ws)
+        c0 = counts0.cpu().tolist()
+        per = [bm.mamba2_step_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len,
+                                    [(c + t) % w.buf_len for c in c0], False, ob) for t in range(n)]
+    elif args.workload == "gdn_serving":
+        st, _, _, counts0 = gdn_from_workload(w, dev, out)
         o = st.new_output()
         for t in range(n):
             st.step(I.gdn_step_inputs(w, t, dev), o)
+        c0 = counts0.cpu().tolist()
+        per = [bm.gdn_step_bytes(w.nheads, w.dk, w.dv, w.buf_len, [(c + t) % w.buf_len for c in c0], ob)
+               for t in range(n)]
     elif args.workload == "kda_serving":
-        st, _, _, _ = kda_from_workload(w, dev, out)
+        st, _, _, counts0 = kda_from_workload(w, dev, out)
         o = st.new_output()
         for t in range(n):
             st.step(I.kda_step_inputs(w, t, dev), o)
+        c0 = counts0.cpu().tolist()
+        per = [bm.kda_step_bytes(w.nheads, w.dk, w.dv, w.buf_len, [(c + t) % w.buf_len for c in c0], ob)
+               for t in range(n)]
     elif args.workload == "kda_spec":
-        st, _, _, _ = kda_from_workload(w, dev, out)
+        st, _, _, counts0 = kda_from_workload(w, dev, out)
         o = st.new_verify_output(w.n_new)
         for t in range(n):
             st.verify(I.kda_verify_inputs(w, t, dev), o)
-            st.commit(I.accepted_kept(w, t, dev))
+            st.commit(kepts[t])
+        per = spec_bytes(lambda c: bm.kda_verify_bytes(w.nheads, w.dk, w.dv, w.buf_len, w.n_new, c, ob),
+                         w, counts0, kepts, ob, n)
     elif args.workload == "gdn_spec":
-        st, _, _, _ = gdn_from_workload(w, dev, out)
+        st, _, _, counts0 = gdn_from_workload(w, dev, out)
         o = st.new_verify_output(w.n_new)
         for t in range(n):
             st.verify(I.gdn_verify_inputs(w, t, dev), o)
-            st.commit(I.accepted_kept(w, t, dev))
+            st.commit(kepts[t])
+        per = spec_bytes(lambda c: bm.gdn_verify_bytes(w.nheads, w.dk, w.dv, w.buf_len, w.n_new, c, ob),
+                         w, counts0, kepts, ob, n)
     else:
-        st, A, D, _, _, _ = mamba2_from_workload(w, dev, out)
+        st, A, D, _, _, counts0 = mamba2_from_workload(w, dev, out)
         y = st.new_output(w.n_new)
         for t in range(n):
             st.verify(I.mamba2_verify_inputs(w, t, dev), A, D, y)
-            st.commit(I.accepted_kept(w, t, dev))
+            st.commit(kepts[t])
+        per = spec_bytes(lambda c: bm.mamba2_verify_bytes(w.nheads, w.headdim, w.dstate, w.ngroups, w.buf_len,
+                                                          w.n_new, c, False, ob), w, counts0, kepts, ob, n)
     torch.cuda.synchronize()
     bd.check(int(st.status.item()), "device status")
+    write_bytes(args, per)
     return None
 
 
@@ -917,7 +968,8 @@ def main(argv=None):
         else:
             from recurrent_state_decode_gb300 import binding
             binding.load()
-            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec", "gdn_spec", "kda_serving", "kda_spec"):
+            if args.mode == "profile" and args.workload in ("gdn_serving", "mamba2_spec", "gdn_spec", "kda_serving",
+                                                            "kda_spec", "mamba2_emu_e4m3_tile64"):
                 res = profile_other(args, dist)
             elif args.workload.startswith("mamba2") and "spec" not in args.workload:
                 res = bench_mamba2_ar(args, dist)

@@ -238,8 +238,8 @@ typedef struct {
 } rssm_emulation;
 
 /* Bytes of device workspace rssm_mamba2_step_emulated needs for desc: one
- * pair of fp32 partial sums per warp of the launch (desc->batch * nheads *
- * headdim / 16 pairs). 0 with RSSM_ERR_INVALID_ARG or _UNSUPPORTED in *rc
+ * pair of fp32 partial sums per block of the launch (desc->batch * nheads *
+ * headdim / 64 pairs of 8 bytes). 0 with RSSM_ERR_INVALID_ARG or _UNSUPPORTED in *rc
  * (if rc is non-NULL) for a descriptor the call rejects. */
 RSSM_API size_t rssm_mamba2_emulated_workspace_bytes(const rssm_mamba2_desc* desc, int* rc);
 
@@ -251,7 +251,7 @@ RSSM_API size_t rssm_mamba2_emulated_workspace_bytes(const rssm_mamba2_desc* des
  *             non-flush step of this call read of (read value - fp32 value)^2,
  *             and of (fp32 value)^2 -- so sqrt(err[0] / err[1]) is the
  *             relative L2 error of the emulated read. Summed in a fixed order
- *             (fp32 within each warp's 2048 elements, then fp64): the same
+ *             (fp32 within each block's 8192 elements, then fp64): the same
  *             inputs give the same bits.
  *  workspace  device scratch of at least
  *             rssm_mamba2_emulated_workspace_bytes(desc) bytes (else
@@ -273,10 +273,11 @@ RSSM_API int rssm_mamba2_step_emulated(const rssm_mamba2_desc* desc, const rssm_
  * reserve nearly all of the GPU's memory for their own pools before decoding
  * starts, or hand a kernel library a stream but no allocator, and cudaMalloc
  * itself may synchronise the device in the middle of a decode loop. This
- * variant takes no workspace: its per-warp error sums go to a static device
- * array inside librssm of RSSM_NOALLOC_MAX_WARPS (error, norm) fp32 pairs --
- * 2 MiB on every GPU that loads the library, held until the process exits --
- * and it never calls cudaMalloc, cudaFree or any routine that allocates.
+ * variant takes no workspace: its per-block error sums go to a static device
+ * array inside librssm of RSSM_NOALLOC_MAX_WARPS / 4 (error, norm) fp32
+ * pairs -- 512 KiB on every GPU that loads the library, held until the
+ * process exits -- and it never calls cudaMalloc, cudaFree or any routine
+ * that allocates.
  *  - Arguments, protocol, limits and results are those of
  *    rssm_mamba2_step_emulated, without workspace and workspace_bytes.
  *  - A launch of more than RSSM_NOALLOC_MAX_WARPS warps (batch * nheads *

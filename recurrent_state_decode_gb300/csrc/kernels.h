@@ -29,7 +29,7 @@ struct M2Args {
   const int32_t* slots;  // [Bt] state row of each batch row (-1: padding), or null: row b uses state row b
   int Sn;                // state rows (the leading dimension of ckpt, ckpt_read, the ring and the cursors)
   int emu_fmt, emu_scale;  // emulated read precision (RSSM_EMU_*; 0: none)
-  float2* emu_part;        // [blocks * 4] per-warp (sum of squared read errors, sum of squares)
+  float2* emu_part;        // [blocks] per-block (sum of squared read errors, sum of squares)
 };
 
 enum { M2_CONVENTIONAL = 0, M2_STEP = 1, M2_FLUSH = 2, M2_VERIFY = 3 };
@@ -40,14 +40,14 @@ cudaError_t m2_step_launch(const M2Args& a, int out_bf16, cudaStream_t st);
 // Shape-specialised AR step (dstate 128, headdim a multiple of 64; mamba2_step_fast.cu).
 bool m2_step_fast_applies(const M2Args& a);
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st);
-// The same kernel with an emulated read precision (a.emu_fmt, a.emu_scale), writing per-warp error
+// The same kernel with an emulated read precision (a.emu_fmt, a.emu_scale), writing per-block error
 // sums to a.emu_part, then their fixed-order reduction into err[2].
 cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, cudaStream_t st);
 // Entries of a.emu_part an emulated step of these arguments writes.
-inline size_t m2_emulated_partials(const M2Args& a) { return (size_t)a.Bt * a.H * a.nPB * 4; }
+inline size_t m2_emulated_partials(const M2Args& a) { return (size_t)a.Bt * a.H * a.nPB; }
 // The same step with its error sums in the library's static device array (mamba2_step_fast.cu), which holds
 // M2_NOALLOC_PARTIALS pairs: a.emu_part is ignored; a larger launch returns cudaErrorInvalidValue.
-constexpr int M2_NOALLOC_PARTIALS = RSSM_NOALLOC_MAX_WARPS;
+constexpr int M2_NOALLOC_PARTIALS = RSSM_NOALLOC_MAX_WARPS / 4;  // one pair per block of four warps
 cudaError_t m2_step_emulated_noalloc_launch(M2Args a, int out_bf16, double* err, cudaStream_t st);
 // The persistent speculative verify (mamba2_verify.cu); its epilogue kernel is in mamba2.cu.
 cudaError_t m2_verify_launch(const M2Args& a, int out_bf16, cudaStream_t st);

@@ -87,7 +87,7 @@ __device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, cons
 // per SM: at eight the 64-register cap spilled, and seven measured 2% faster).
 // SLOTS: batch rows name their state rows through a slot table.
 // EMU: non-flush steps read the fp32 tile through an emulated precision and
-// each warp writes its (error, norm) sums to a.emu_part (fp32 tiles, no slots).
+// each block writes its (error, norm) sums to a.emu_part (fp32 tiles, no slots).
 template <bool OUT_BF16, bool RD16, bool SLOTS, bool EMU = false>
 __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
@@ -160,9 +160,9 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
   }
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
   const int nblocks = a.H * a.nPB;  // blocks of this sequence
-  // this warp's slot of the emulated read's error sums (every path writes it)
-  float2* const emu_slot = EMU ? a.emu_part + ((size_t)(bh * a.nPB + pb) * FW + warp) : nullptr;
-  if (EMU && !valid && lane == 0) *emu_slot = make_float2(0.f, 0.f);
+  // this block's entry of the emulated read's error sums (every path writes it)
+  float2* const emu_slot = EMU ? a.emu_part + ((size_t)bh * a.nPB + pb) : nullptr;
+  if (EMU && !valid && threadIdx.x == 0) *emu_slot = make_float2(0.f, 0.f);
   if (!valid) {  // uniform over the block; the last block of the sequence reports it
     if (threadIdx.x == 0) {
       const int ticket = cursor_ticket(a.cursors, sb);
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
   // (the emulated instantiation makes the outcome block-uniform: it meets a block barrier after the wait)
   if (!(EMU ? __syncthreads_and(mbar_wait(&bar, 0)) : __all_sync(FULL, mbar_wait(&bar, 0)))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
-    if (EMU && lane == 0) *emu_slot = make_float2(0.f, 0.f);
+    if (EMU && threadIdx.x == 0) *emu_slot = make_float2(0.f, 0.f);
     mbar_wait(&bar, 0);
     if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
     return;
@@ -282,9 +282,14 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
     }
   }
 
-  if (EMU) {
+  if (EMU) {  // the block's sums, warps 0..3 added in order (the outcome of the wait is block-uniform here);
+             // entries 16.. of the dot table, apart from the tile maxima's 0..3
     const float e = warp_sum(emu_err), n = warp_sum(emu_nrm);
-    if (lane == 0) *emu_slot = make_float2(e, n);
+    float* const red = sc + 16;
+    if (lane == 0) red[warp] = e, red[FW + warp] = n;
+    __syncthreads();
+    if (threadIdx.x == 0)
+      *emu_slot = make_float2(((red[0] + red[1]) + red[2]) + red[3], ((red[FW] + red[FW + 1]) + red[FW + 2]) + red[FW + 3]);
   }
   if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
 }
@@ -292,14 +297,23 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
 // The emulated step's error sums: the per-warp pairs added in a fixed order
 // (each thread a strided share in fp64, then a tree over the block).
 constexpr int EMU_RT = 1024;  // threads of the reduction
+constexpr int EMU_U = 16;     // loads in flight per thread
 
 __global__ void __launch_bounds__(EMU_RT) emu_reduce_kernel(const float2* __restrict__ part, size_t n, double* err) {
   __shared__ double se[EMU_RT], sn[EMU_RT];
   double e = 0.0, q = 0.0;
-  for (size_t i = threadIdx.x; i < n; i += EMU_RT) {
-    const float2 v = part[i];
-    e += v.x;
-    q += v.y;
+  for (size_t i0 = threadIdx.x; i0 < n; i0 += (size_t)EMU_U * EMU_RT) {  // EMU_U loads issued, then added in order
+    float2 v[EMU_U];
+#pragma unroll
+    for (int u = 0; u < EMU_U; u++) {
+      const size_t i = i0 + (size_t)u * EMU_RT;
+      v[u] = i < n ? part[i] : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < EMU_U; u++) {
+      e += v[u].x;
+      q += v[u].y;
+    }
   }
   se[threadIdx.x] = e;
   sn[threadIdx.x] = q;

@@ -340,7 +340,7 @@ def test_emulated_step_host_checks(lib):
     pairs it takes, the shapes and the workspace size it needs."""
     d = bd.mamba2_desc(4, 8, 64, 128, 2, 16)
     n = bd.rssm_mamba2_emulated_workspace_bytes(d)
-    assert n == 4 * 8 * 1 * 4 * 8            # one (error, norm) fp32 pair per warp: 4 warps per block
+    assert n == 4 * 8 * 1 * 8                # one (error, norm) fp32 pair per block (sequence, head, 64 rows)
     ring = bd.rssm_mamba2_ring(*([ALIGNED] * 5))
     args = [ALIGNED] * 9                     # x, z, B, C, dt, A, D, y, err
 

@@ -22,8 +22,19 @@ def _fields(path):
 
 def test_there_are_kernel_summaries():
     names = {os.path.basename(p) for p in SUMMARIES}
-    assert {"mamba2_step_serving.txt", "mamba2_verify_spec.txt", "gdn_step_serving.txt",
-            "gdn_verify_spec.txt", "kda_step_serving.txt"} <= names
+    assert {"mamba2_step_serving.txt", "mamba2_step_bf16_read.txt", "mamba2_step_emulated_e4m3.txt",
+            "mamba2_verify_spec.txt", "gdn_step_serving.txt", "gdn_verify_spec.txt", "kda_step_serving.txt",
+            "kda_verify_spec.txt"} <= names
+
+
+@pytest.mark.parametrize("path", SUMMARIES, ids=os.path.basename)
+def test_summary_was_taken_on_the_committed_sources(path):
+    """A summary's source hash is that of the kernel sources as they are now
+    (the hash bench.py checks before quoting a summary's DRAM traffic): a
+    change to a kernel makes its summary stale until it is captured again."""
+    import bench
+    f = _fields(path)
+    assert f["source_sha256"] == bench.source_hash(f["source_files"].split()), "recapture this summary"
 
 
 @pytest.mark.parametrize("path", SUMMARIES, ids=os.path.basename)

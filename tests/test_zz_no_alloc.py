@@ -1,7 +1,7 @@
 """rssm_mamba2_step_emulated_noalloc: the emulated-precision decode step for
 callers that cannot allocate device memory while they decode -- a host that
 has already reserved the GPU's memory for its own pools, or that hands the
-library a stream but no allocator. It keeps its scratch (the per-warp error
+library a stream but no allocator. It keeps its scratch (the per-block error
 sums) in a static device array inside the library instead of a workspace
 argument.
 
