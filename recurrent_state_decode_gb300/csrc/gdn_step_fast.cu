@@ -29,6 +29,8 @@
 // window terms are each lane's partials, added before the reduction). The last
 // of a sequence's blocks to have read its cursor advances it (an arrival count
 // in the high half of the cursor's flags word), so the step is one kernel.
+#include <type_traits>
+
 #include "fast_rows.cuh"
 #include "kernels.h"
 
@@ -40,10 +42,14 @@ using namespace fastrows;
 
 constexpr int GD = 128;  // dk = dv
 constexpr int KW = 8;    // dot entries per warp: 4 x 8 >= L + 1
+// With L <= 16 four ring slots per warp cover the window, and the current
+// record's k . q is one warp sum instead: half the dot work, an 8-wide reduction.
+constexpr int KW_SHORT = 4;
 constexpr int ES = FPB + 4;  // floats per staged e row (padded against bank conflicts; 16-byte multiple)
 
 // SLOTS: batch rows name their state rows through a slot table.
-template <bool OUT_BF16, bool SLOTS>
+// KWT: ring slots per warp in the dot table (KW, or KW_SHORT when L <= 16).
+template <bool OUT_BF16, bool SLOTS, int KWT = KW>
 __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;               // the block's 64 rows
@@ -70,6 +76,10 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
     bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
+  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
+  // An invalid cursor (reported by the cursor kernel) runs as an empty window
+  // with every store masked, so that no lane leaves before the shuffles below.
+  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, m = count + 1;
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's row groups (within the block)
   // ring slot `lane`: g
   const float gs = lane < L ? a.rg[sh * pad4(L) + lane] : 0.f;
@@ -79,23 +89,28 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const float gm = a.g[bh], bm = a.beta[bh];
   const int vr = (lane >> 1) & 7;  // the row this lane finishes (lanes 0..15)
   const uint16_t vbA = a.v[bh * GD + p0 + rl0 + vr], vbB = a.v[bh * GD + p0 + rl1 + vr];
-  {  // k_s . k and k_s . q for ring slots s = warp + 4 j (s == L: the current k)
+  float kq_cur;  // k . q of the current record
+  {  // k_s . k and k_s . q for ring slots s = warp + 4 j (s == L: the current k, with KW slots per warp)
     const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
-    float pk[2 * KW];
+    float pk[2 * KWT];
 #pragma unroll
-    for (int j = 0; j < KW; j++) {
+    for (int j = 0; j < KWT; j++) {
       const int s = warp + FW * j;
-      const float4 ks = s < L ? load_bf4(rkp + s * GD) : (s == L ? bf4_to_f4(kraw) : make_float4(0.f, 0.f, 0.f, 0.f));
+      const float4 ks = s < L ? load_bf4(rkp + s * GD)
+                              : (KWT == KW && s == L ? bf4_to_f4(kraw) : make_float4(0.f, 0.f, 0.f, 0.f));
       pk[2 * j] = dot4(ks, bf4_to_f4(kraw));
       pk[2 * j + 1] = dot4(ks, bf4_to_f4(qraw));
     }
-    const float red = reduce_transpose<2 * KW>(pk, lane);  // lane l: partial l >> 1 = (slot j = l >> 2, k or q)
-    if ((lane & 1) == 0) ((lane & 2) ? skq : skk)[warp + FW * (lane >> 2)] = red;
+    const float red = reduce_transpose<2 * KWT>(pk, lane);
+    if (KWT == KW) {  // lane l: partial l >> 1 = (slot j = l >> 2, k or q)
+      if ((lane & 1) == 0) ((lane & 2) ? skq : skk)[warp + FW * (lane >> 2)] = red;
+      kq_cur = 0.f;
+    } else {  // lane l: partial reduce8_row(l) = (slot j = index >> 1, k or q)
+      const int idx = reduce8_row(lane);
+      if ((lane & 3) == 0) ((idx & 1) ? skq : skk)[warp + FW * (idx >> 1)] = red;
+      kq_cur = warp_sum(dot4(bf4_to_f4(kraw), bf4_to_f4(qraw)));
+    }
   }
-  const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
-  // An invalid cursor (reported by the cursor kernel) runs as an empty window
-  // with every store masked, so that no lane leaves before the shuffles below.
-  const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, m = count + 1;
   if (threadIdx.x == 0) {  // the window's e rows of this block, in record order
     mbar_arrive_expect_tx(&bar[1], (uint32_t)count * FPB * 4);
     for (int t = 0; t < count; t++) {
@@ -129,7 +144,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const int ent = lane < count ? sl : L;
   const float cK = lane < count ? Dt * skk[ent] : 0.f;
   const float cQ = lane < count ? Dt * skq[ent] : 0.f;
-  const float kq_cur = skq[L];
+  if (KWT == KW) kq_cur = skq[L];
   const float4 ka = scale4(gamma, bf4_to_f4(kraw)), qa = scale4(gamma, bf4_to_f4(qraw));
   // Append the current record now (its e follows below): its slot is outside
   // the window, so no block reads it for a result.
@@ -226,8 +241,12 @@ bool gdn_step_fast_applies(const GdnArgs& a) {
 
 cudaError_t gdn_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
-  auto k = a.slots ? (out_bf16 ? gdn_step_fast_kernel<true, true> : gdn_step_fast_kernel<false, true>)
-                   : (out_bf16 ? gdn_step_fast_kernel<true, false> : gdn_step_fast_kernel<false, false>);
+  auto pick = [&](auto kwt) {
+    constexpr int W = decltype(kwt)::value;
+    return a.slots ? (out_bf16 ? gdn_step_fast_kernel<true, true, W> : gdn_step_fast_kernel<false, true, W>)
+                   : (out_bf16 ? gdn_step_fast_kernel<true, false, W> : gdn_step_fast_kernel<false, false, W>);
+  };
+  auto k = a.L <= FW * KW_SHORT ? pick(std::integral_constant<int, KW_SHORT>{}) : pick(std::integral_constant<int, KW>{});
   const int smem = (FPB * GD + a.L * ES) * 4;
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;

@@ -40,10 +40,14 @@ using namespace fastrows;
 
 constexpr int GD = 128;      // dk = dv
 constexpr int KW = 8;        // dot entries per warp: 4 x 8 >= L + 1
+// With L <= 16 four ring slots per warp cover the window, and the current
+// record's k . q is one warp sum instead: half the dot work, an 8-wide reduction.
+constexpr int KW_SHORT = 4;
 constexpr int ES = FPB + 4;  // floats per staged e row (padded against bank conflicts; 16-byte multiple)
 
 // SLOTS: batch rows name their state rows through a slot table.
-template <bool OUT_BF16, bool SLOTS>
+// KWT: ring slots per warp in the dot table (KW, or KW_SHORT when L <= 16).
+template <bool OUT_BF16, bool SLOTS, int KWT = KW>
 __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   const int L = a.L, H = a.H;
@@ -94,9 +98,9 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   const int vr = (lane >> 1) & 7;  // the row this lane finishes (lanes 0..15)
   const uint16_t vbA = a.v[bh * GD + p0 + rl0 + vr], vbB = a.v[bh * GD + p0 + rl1 + vr];
   // ring keys of slots s = warp + 4 j (their decays are known once the cursor is)
-  uint2 kr[KW];
+  uint2 kr[KWT];
 #pragma unroll
-  for (int j = 0; j < KW; j++) {
+  for (int j = 0; j < KWT; j++) {
     const int s = warp + FW * j;
     kr[j] = s < L ? *reinterpret_cast<const uint2*>(a.rk + (sh * L + s) * GD + lane * 4) : make_uint2(0, 0);
   }
@@ -129,30 +133,38 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   }
   __syncthreads();
   const float4 kc = bf4_to_f4(kraw), qc = bf4_to_f4(qraw);
-  {  // (f_s * k_s) . k and (f_s * k_s) . q for ring slots s = warp + 4 j (s == L: the current k)
-    float pk[2 * KW];
+  float kq_cur;  // k . q of the current record
+  {  // (f_s * k_s) . k and (f_s * k_s) . q for ring slots s = warp + 4 j (s == L: the current k, with KW slots per warp)
+    float pk[2 * KWT];
 #pragma unroll
-    for (int j = 0; j < KW; j++) {
+    for (int j = 0; j < KWT; j++) {
       const int s = warp + FW * j;
       int pos = s - start;
       pos = pos < 0 ? pos + L : pos;  // the slot's record index in the window
       float4 ks = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s < L && pos < cnt)
         ks = mul4(bf4_to_f4(kr[j]), ld4(fd + pos * GD + lane * 4));
-      else if (s == L)
+      else if (KWT == KW && s == L)
         ks = kc;
       pk[2 * j] = dot4(ks, kc);
       pk[2 * j + 1] = dot4(ks, qc);
     }
-    const float red = reduce_transpose<2 * KW>(pk, lane);  // lane l: partial l >> 1 = (slot j = l >> 2, k or q)
-    if ((lane & 1) == 0) ((lane & 2) ? skq : skk)[warp + FW * (lane >> 2)] = red;
+    const float red = reduce_transpose<2 * KWT>(pk, lane);
+    if (KWT == KW) {  // lane l: partial l >> 1 = (slot j = l >> 2, k or q)
+      if ((lane & 1) == 0) ((lane & 2) ? skq : skk)[warp + FW * (lane >> 2)] = red;
+      kq_cur = 0.f;
+    } else {  // lane l: partial reduce8_row(l) = (slot j = index >> 1, k or q)
+      const int idx = reduce8_row(lane);
+      if ((lane & 3) == 0) ((idx & 1) ? skq : skk)[warp + FW * (idx >> 1)] = red;
+      kq_cur = warp_sum(dot4(kc, qc));
+    }
   }
   __syncthreads();
   int sl = start + lane;
   sl = sl < L ? sl : sl - L;
   const float cK = lane < cnt ? skk[sl] : 0.f;  // lane t: record t's coefficients
   const float cQ = lane < cnt ? skq[sl] : 0.f;
-  const float kq_cur = skq[L];
+  if (KWT == KW) kq_cur = skq[L];
   const float4 gm4 = ld4(gam + lane * 4);
   const float4 ka = mul4(gm4, kc), qa = mul4(gm4, qc);
   // Append the current record now (its e follows below): its slot is outside
@@ -247,11 +259,16 @@ bool kda_step_fast_applies(const GdnArgs& a) {
 
 cudaError_t kda_step_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
-  auto pick = [&](auto slots) {
+  auto pick = [&](auto slots, auto kwt) {
     constexpr bool S = decltype(slots)::value;
-    return out_bf16 ? kda_step_fast_kernel<true, S> : kda_step_fast_kernel<false, S>;
+    constexpr int W = decltype(kwt)::value;
+    return out_bf16 ? kda_step_fast_kernel<true, S, W> : kda_step_fast_kernel<false, S, W>;
   };
-  auto k = a.slots ? pick(std::true_type{}) : pick(std::false_type{});
+  const bool short_window = a.L <= FW * KW_SHORT;
+  auto k = a.slots ? (short_window ? pick(std::true_type{}, std::integral_constant<int, KW_SHORT>{})
+                                   : pick(std::true_type{}, std::integral_constant<int, KW>{}))
+                   : (short_window ? pick(std::false_type{}, std::integral_constant<int, KW_SHORT>{})
+                                   : pick(std::false_type{}, std::integral_constant<int, KW>{}));
   const int smem = (FPB * GD + (a.L - 1) * (ES + GD)) * 4;  // five blocks per SM at L = 16
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;

@@ -38,6 +38,9 @@ namespace {
 using namespace fastrows;
 
 constexpr int KW = 8;  // 4 warps x 8 >= L + 1 dots for L <= 31
+// With L <= 16 four slots per warp cover the ring, and the current record's
+// dot is one warp sum instead: half the dot work and a 4-wide reduction.
+constexpr int KW_SHORT = 4;
 
 // Emulated read of 8 rows (a non-flush step of the emulated instantiation):
 // every element x becomes Q(x * inv) * s for its row's (or its tile's)
@@ -88,7 +91,8 @@ __device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, cons
 // SLOTS: batch rows name their state rows through a slot table.
 // EMU: non-flush steps read the fp32 tile through an emulated precision and
 // each block writes its (error, norm) sums to a.emu_part (fp32 tiles, no slots).
-template <bool OUT_BF16, bool RD16, bool SLOTS, bool EMU = false>
+// KWT: dot slots per warp (KW, or KW_SHORT when L <= 16).
+template <bool OUT_BF16, bool RD16, bool SLOTS, bool EMU = false, int KWT = KW>
 __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
   __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
@@ -146,17 +150,23 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
   const uint2 craw = *reinterpret_cast<const uint2*>(a.C + (size_t)bg * FN + lane * 4);
   const uint2 braw = *reinterpret_cast<const uint2*>(a.B + (size_t)bg * FN + lane * 4);
   const float4 cm = bf4_to_f4(craw);
-  {  // c_s = B_s . C for slots s = warp + 4 i (s == L: the current record)
+  float cdot = 0.f;  // B . C of the current record (with KW_SHORT slots per warp)
+  {  // c_s = B_s . C for slots s = warp + 4 i (s == L: the current record, with KW slots per warp)
     const uint16_t* rBp = a.rB + (size_t)sg * L * FN + lane * 4;
     const float4 bc = bf4_to_f4(braw);
-    float pk[KW];
+    float pk[KWT];
 #pragma unroll
-    for (int i = 0; i < KW; i++) {
+    for (int i = 0; i < KWT; i++) {
       const int s = warp + FW * i;
-      pk[i] = s < L ? dot4(load_bf4(rBp + s * FN), cm) : (s == L ? dot4(bc, cm) : 0.f);
+      pk[i] = s < L ? dot4(load_bf4(rBp + s * FN), cm) : (KWT == KW && s == L ? dot4(bc, cm) : 0.f);
     }
-    const float red = reduce_transpose<KW>(pk, lane);
-    if ((lane & 3) == 0) sc[warp + FW * reduce8_row(lane)] = red;
+    const float red = reduce_transpose<KWT>(pk, lane);
+    if (KWT == KW) {
+      if ((lane & 3) == 0) sc[warp + FW * reduce8_row(lane)] = red;
+    } else {  // 4-wide: lane l holds slot index 2 (l >> 4 & 1) + (l >> 3 & 1)
+      if ((lane & 7) == 0) sc[warp + FW * (((lane >> 4) & 1) * 2 + ((lane >> 3) & 1))] = red;
+      cdot = warp_sum(dot4(bc, cm));
+    }
   }
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
   const int nblocks = a.H * a.nPB;  // blocks of this sequence
@@ -196,7 +206,8 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
     ticket = cursor_ticket(a.cursors, sb);
     scur = cur;
   }
-  const float coef = lane < m ? fmaf(wk, sc[lane < count ? sl : L], lane == count ? Dh : 0.f) : 0.f;
+  const float cs = lane < count ? sc[sl] : (KWT == KW ? sc[L] : cdot);
+  const float coef = lane < m ? fmaf(wk, cs, lane == count ? Dh : 0.f) : 0.f;
   // the gates do not need the checkpoint rows: computed before waiting for them
   const uint4 xq[2] = {lane < count ? xrA : xcA, lane < count ? xrB : xcB};  // lane k: x_k, both groups
   const float gA = silu_fast(zA), gB = silu_fast(zB);
@@ -339,14 +350,18 @@ bool m2_step_fast_applies(const M2Args& a) {
 }
 
 cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) {
-  const bool rd16 = a.ckpt_read != nullptr;
   const dim3 grid(a.nPB, a.H, a.Bt);
-  auto pick = [&](auto slots) {
+  const bool rd16 = a.ckpt_read != nullptr, short_window = a.L <= FW * KW_SHORT;
+  auto pick = [&](auto slots, auto kwt) {
     constexpr bool S = decltype(slots)::value;
-    return rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true, S> : m2_step_fast_kernel<false, true, S>)
-                : (out_bf16 ? m2_step_fast_kernel<true, false, S> : m2_step_fast_kernel<false, false, S>);
+    constexpr int W = decltype(kwt)::value;
+    return rd16 ? (out_bf16 ? m2_step_fast_kernel<true, true, S, false, W> : m2_step_fast_kernel<false, true, S, false, W>)
+                : (out_bf16 ? m2_step_fast_kernel<true, false, S, false, W> : m2_step_fast_kernel<false, false, S, false, W>);
   };
-  auto k = a.slots ? pick(std::true_type{}) : pick(std::false_type{});
+  using KS = std::integral_constant<int, KW_SHORT>;
+  using KL = std::integral_constant<int, KW>;
+  auto k = a.slots ? (short_window ? pick(std::true_type{}, KS{}) : pick(std::true_type{}, KL{}))
+                   : (short_window ? pick(std::false_type{}, KS{}) : pick(std::false_type{}, KL{}));
   const int smem = rd16 ? FPB * FN * 2 : 0;
   // six 32 KiB (seven 16 KiB) tiles per SM need the largest shared-memory split of the unified L1
   cudaError_t e = prepare(k, smem, true);
@@ -358,7 +373,11 @@ cudaError_t m2_step_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st) 
 cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
   const dim3 grid(a.nPB, a.H, a.Bt);
-  auto k = out_bf16 ? m2_step_fast_kernel<true, false, false, true> : m2_step_fast_kernel<false, false, false, true>;
+  const bool short_window = a.L <= FW * KW_SHORT;
+  auto k = out_bf16 ? (short_window ? m2_step_fast_kernel<true, false, false, true, KW_SHORT>
+                                    : m2_step_fast_kernel<true, false, false, true, KW>)
+                    : (short_window ? m2_step_fast_kernel<false, false, false, true, KW_SHORT>
+                                    : m2_step_fast_kernel<false, false, false, true, KW>);
   cudaError_t e = prepare(k, 0, true);
   if (e != cudaSuccess) return e;
   k<<<grid, FT, 0, st>>>(a);
