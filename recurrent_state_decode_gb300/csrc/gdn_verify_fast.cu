@@ -7,24 +7,28 @@
 //
 // One CTA of four warps per (sequence, head, 64 state rows); warp w owns rows
 // 8w..8w+7 and 32+8w..32+8w+7, lane l the float4 column chunk 4l..4l+3. At
-// launch: one bulk copy (TMA, non-tensor; never multicast) of the 64 rows;
-// lane s ring slot s (g); lane j new record j (g, beta); lane 8j + r the v of
-// new record j at row r of each group; the new records' k and q into shared
-// memory (fp32). Entry e of the dot tables is ring slot e (e < L) or new
-// record e - L; (k_e . k_j) and (k_e . q_i) for all 32 entries come from
-// tensor-core products [32 x 128] . [128 x 8], warp w taking entries
-// 16 (w & 1) .. + 15 over column half w >> 1 (readers add the halves). After the cursor: the
-// window records' e rows by one 256-byte bulk copy each (second mbarrier), one
-// inclusive warp scan of g, and a per-block table of the committed records'
-// coefficients D (k_t . vec), warp w building rows w and w + 4. Each warp then forms S0 . [k_0..k_3, q_0..q_3] for
-// its 16 rows as m16n8k8 tf32 mma (the fp32 state split into two tf32 parts),
-// adds the committed window's terms, solves the new records' e in order within
-// each quad and completes the outputs. If count + K > L the
-// committed window is folded into the rows, written once. The new records'
-// v and e rows go to the ring here; their k, q, g, beta (read by the other
-// block of the head) are appended by the sequence's last block to arrive,
-// which also marks the cursor pending.
+// launch, none of it waiting on another: one bulk copy (TMA, non-tensor; never
+// multicast) of the 64 rows; lane s ring slot s (g); lane j new record j (g,
+// beta); lane 4g + t the v of new record t at rows 8w + g and 32 + 8w + g; each
+// lane its fragments of the dot tables' operands and of the new records' k and
+// q (bf16, in registers). Entry e of the dot tables is ring slot e (e < L) or
+// new record e - L; (k_e . k_j) and (k_e . q_i) for all 32 entries come from
+// tensor-core products [32 x 128] . [128 x 8], warp w taking entries 16 (w & 1)
+// .. + 15 over column half w >> 1 (readers add the halves), taken once thread
+// 0 has requested the window records' e rows (one 256-byte bulk copy each,
+// second mbarrier), which it does as soon as the cursor arrives. Then one
+// inclusive warp scan of g and a per-block table of the committed records'
+// coefficients D (k_t . vec), warp w building rows w and w + 4. Each warp then
+// forms S0 . [k_0..k_3, q_0..q_3] for its 16 rows as m16n8k8 tf32 mma (the fp32
+// state split into two tf32 parts, two independent accumulator chains), adds
+// the committed window's terms, solves the new records' e in order within each
+// quad and completes the outputs. If count + K > L the committed window is
+// folded into the rows on the tensor cores, written once. The new records' v
+// and e rows go to the ring here; their k, q, g, beta (read by the other block
+// of the head) are appended by the sequence's last block to arrive, which also
+// marks the cursor pending.
 #include "fast_rows.cuh"
+#include "fold_mma.cuh"
 #include "gdn_common.cuh"
 
 namespace rssm {
@@ -43,8 +47,7 @@ template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;                 // the block's 64 rows
-  float* vecs = dsm + FPB * GD;      // [0..3] new k_j, [4..7] new q_i (fp32)
-  float* es = vecs + 2 * KMAX * GD;  // e of committed record t at es + t * ES
+  float* es = dsm + FPB * GD;        // e of committed record t at es + t * ES
   __shared__ float tbl[2][2 * KMAX][FW * EW];  // [half][n][e]: k_e . vec_n over column half `half`;
                                                 // vec 0..3 = new k_j, 4..7 = new q_i
   __shared__ float cf[2 * KMAX][33];        // [n][t]: D(a_n, t) (k_t . vec_n) of committed record t (padded rows)
@@ -84,42 +87,38 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     vtA = a.v[vrow + rA];
     vtB = a.v[vrow + rB];
   }
-  // the new records' k and q, fp32, in shared memory (each warp its own rows of the table)
-  for (int v = warp; v < 2 * KMAX; v += FW) {
-    const int j = v & (KMAX - 1);
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < K) f = load_bf4((v < KMAX ? a.k : a.q) + (((size_t)b * K + j) * H + h) * GD + lane * 4);
-    reinterpret_cast<float4*>(vecs + v * GD)[lane] = f;
+  // the products' B fragments: vector n = qg (new k_n for n < 4, new q_{n-4} from 4 on) at
+  // columns 16 jb + 4 qt .. + 3, bf16 (exact in tf32), zero past the K new records
+  uint2 cv[GD / 16];
+  {
+    const int j = qg & (KMAX - 1);
+    const uint16_t* vp = (qg < KMAX ? a.k : a.q) + (((size_t)b * K + j) * H + h) * GD + 4 * qt;
+#pragma unroll
+    for (int jb = 0; jb < GD / 16; jb++)
+      cv[jb] = j < K ? *reinterpret_cast<const uint2*>(vp + 16 * jb) : make_uint2(0, 0);
   }
-  __syncthreads();
   // dot tables tbl[n][e] = k_e . vec_n for entries e < 32 (ring slot e if e < L,
   // new record e - L if e < L + K, else 0): [32 x 128] . [128 x 8] on the
   // tensor cores, warp w taking entries 16 (w & 1) .. 16 (w & 1) + 15 over the
   // column half w >> 1 (bf16 inputs are exact in tf32, so one mma per k-step);
-  // readers add the two halves.
-  const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
+  // readers add the two halves. The rows are requested here, the products
+  // taken once the e rows are on their way.
+  const int e0 = 16 * (warp & 1) + qg, e1 = e0 + 8, ch = warp >> 1;
+  uint2 da[GD / 32], db[GD / 32];
   {
-    const int e0 = 16 * (warp & 1) + qg, e1 = e0 + 8, ch = warp >> 1;
-    const uint16_t* g0 = e0 < L ? a.rk + (sh * L + e0) * GD : nullptr;
-    const uint16_t* g1 = e1 < L ? a.rk + (sh * L + e1) * GD : nullptr;
-    const float* s0 = (e0 >= L && e0 < L + K) ? vecs + (e0 - L) * GD : nullptr;
-    const float* s1 = (e1 >= L && e1 < L + K) ? vecs + (e1 - L) * GD : nullptr;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    auto row_of = [&](int e) -> const uint16_t* {
+      if (e < L) return a.rk + (sh * L + e) * GD;
+      if (e < L + K) return a.k + (((size_t)b * K + (e - L)) * H + h) * GD;
+      return nullptr;
+    };
+    const uint16_t* g0 = row_of(e0);
+    const uint16_t* g1 = row_of(e1);
 #pragma unroll
-    for (int jb = ch * (GD / 32); jb < (ch + 1) * (GD / 32); jb++) {
-      const int col = 16 * jb + 4 * qt;
-      const float4 r0 = g0 ? load_bf4(g0 + col) : (s0 ? ld4(s0 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
-      const float4 r1 = g1 ? load_bf4(g1 + col) : (s1 ? ld4(s1 + col) : make_float4(0.f, 0.f, 0.f, 0.f));
-      const float4 bv = ld4(vecs + qg * GD + col);
-      mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y), __float_as_uint(r1.y),
-                    __float_as_uint(bv.x), __float_as_uint(bv.y));
-      mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w), __float_as_uint(r1.w),
-                    __float_as_uint(bv.z), __float_as_uint(bv.w));
+    for (int j = 0; j < GD / 32; j++) {
+      const int col = 16 * (ch * (GD / 32) + j) + 4 * qt;
+      da[j] = g0 ? *reinterpret_cast<const uint2*>(g0 + col) : make_uint2(0, 0);
+      db[j] = g1 ? *reinterpret_cast<const uint2*>(g1 + col) : make_uint2(0, 0);
     }
-    tbl[ch][2 * qt][e0] = acc[0];
-    tbl[ch][2 * qt + 1][e0] = acc[1];
-    tbl[ch][2 * qt][e1] = acc[2];
-    tbl[ch][2 * qt + 1][e1] = acc[3];
   }
   // An invalid cursor (reported by the epilogue) runs as an empty window with
   // every store masked.
@@ -131,6 +130,22 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     mbar_arrive_expect_tx(&bar[1], (uint32_t)count * FPB * 4);
     for (int t = 0; t < count; t++)
       bulk_load(es + t * ES, a.re + (sh * L + wrap(start + t, L)) * GD + p0, FPB * 4, &bar[1]);
+  }
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < GD / 32; j++) {
+      const float4 r0 = bf4_to_f4(da[j]), r1 = bf4_to_f4(db[j]);
+      const float4 bv = bf4_to_f4(ch ? cv[GD / 32 + j] : cv[j]);
+      mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y), __float_as_uint(r1.y),
+                    __float_as_uint(bv.x), __float_as_uint(bv.y));
+      mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w), __float_as_uint(r1.w),
+                    __float_as_uint(bv.z), __float_as_uint(bv.w));
+    }
+    tbl[ch][2 * qt][e0] = acc[0];
+    tbl[ch][2 * qt + 1][e0] = acc[1];
+    tbl[ch][2 * qt][e1] = acc[2];
+    tbl[ch][2 * qt + 1][e1] = acc[3];
   }
   // record t on lane t: committed (ring slot sl) or new (record jn)
   int sl = start + lane;
@@ -177,26 +192,28 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
     // S0 . [k_0..k_3, q_0..q_3] for rows (rA, rB) on the tensor cores: per 16
     // columns two k-steps of m16n8k8 (lane t takes the float4 at column 4t, so
     // the k order is permuted alike in A and B), S0 split into two tf32 parts.
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4], ch[2][4] = {};  // the hi and lo parts' products, two independent chains
 #pragma unroll
     for (int jb = 0; jb < GD / 16; jb++) {
       const int col = 16 * jb + 4 * qt;
       const float4 r0 = ld4(tile + rA * GD + col), r1 = ld4(tile + rB * GD + col);
-      const float4 bv = ld4(vecs + qg * GD + col);
+      const float4 bv = bf4_to_f4(cv[jb]);
       uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
       split_tf32(r0.x, h0, l0);
       split_tf32(r1.x, h1, l1);
       split_tf32(r0.y, h2, l2);
       split_tf32(r1.y, h3, l3);
-      mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.x), __float_as_uint(bv.y));
-      mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+      mma_tf32_1688(ch[0], h0, h1, h2, h3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+      mma_tf32_1688(ch[1], l0, l1, l2, l3, __float_as_uint(bv.x), __float_as_uint(bv.y));
       split_tf32(r0.z, h0, l0);
       split_tf32(r1.z, h1, l1);
       split_tf32(r0.w, h2, l2);
       split_tf32(r1.w, h3, l3);
-      mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
-      mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+      mma_tf32_1688(ch[0], h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+      mma_tf32_1688(ch[1], l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
     }
+#pragma unroll
+    for (int q = 0; q < 4; q++) acc[q] = ch[0][q] + ch[1][q];
     // + the committed window: sum_t D(a_n, t) (k_t . vec_n) e_t[row]
     const int n0 = 2 * qt, n1 = n0 + 1;
     float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
@@ -273,34 +290,11 @@ __global__ void __launch_bounds__(FT, 5) gdn_verify_fast_kernel(GdnArgs a) {
       a.rv[slot * GD + p0 + rA] = (uint16_t)vtA;
       a.rv[slot * GD + p0 + rB] = (uint16_t)vtB;
     }
-    if (fold) {  // S0' = e^{G_{c-1}} S0 + sum_{t<c} D(c-1, t) e_t k_t^T, written once
-#pragma unroll
-      for (int half = 0; half < 2; half++) {
-        const int rl = half ? rl1 : rl0;
-        float4 hv[8];
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++) hv[rr] = scale4(Pf, ld4(tile + (rl + rr) * GD + lane * 4));
-        for (int t0 = 0; t0 < count; t0 += 2) {
-          float4 kt[2];
-#pragma unroll
-          for (int u = 0; u < 2; u++)
-            kt[u] = t0 + u < count ? load_bf4(rkp + wrap(start + t0 + u, L) * GD) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int u = 0; u < 2; u++) {
-            const int t = t0 + u;
-            const float c = __shfl_sync(FULL, wf, t & 31);
-            if (t < count) {  // uniform
-              const float4 ea2 = ld4(es + t * ES + rl), eb2 = ld4(es + t * ES + rl + 4);
-              const float et[8] = {ea2.x, ea2.y, ea2.z, ea2.w, eb2.x, eb2.y, eb2.z, eb2.w};
-#pragma unroll
-              for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(c * et[rr], kt[u], hv[rr]);
-            }
-          }
-        }
-#pragma unroll
-        for (int rr = 0; rr < 8; rr++)
-          __stcs(reinterpret_cast<float4*>(a.S + tbase + (size_t)(rl + rr) * GD) + lane, hv[rr]);
-      }
+    if (fold) {  // S0' = e^{G_{c-1}} S0 + sum_{t<c} D(c-1, t) e_t k_t^T, written once (tensor cores)
+      const uint16_t* rk0 = a.rk + sh * L * GD;
+      fold_rows_mma(
+          tile, a.S + tbase, [&](int t) { return rk0 + wrap(start + t, L) * GD; },
+          [&](int t, int r) { return es[t * ES + r]; }, count, Pf, wf, rl0, rl1, lane);
     }
   }
   if (fold) {  // uniform: the fold read the ring's k rows until here
@@ -324,7 +318,7 @@ cudaError_t gdn_verify_fast_launch(const GdnArgs& a, int out_bf16, cudaStream_t 
   if (a.Bt == 0) return cudaSuccess;
   auto k = a.slots ? (out_bf16 ? gdn_verify_fast_kernel<true, true> : gdn_verify_fast_kernel<false, true>)
                    : (out_bf16 ? gdn_verify_fast_kernel<true, false> : gdn_verify_fast_kernel<false, false>);
-  const int smem = (FPB * GD + 2 * KMAX * GD + a.L * ES) * 4;
+  const int smem = (FPB * GD + a.L * ES) * 4;
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<dim3(2, a.H, a.Bt), FT, smem, st>>>(a);

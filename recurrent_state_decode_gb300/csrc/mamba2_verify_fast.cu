@@ -26,14 +26,19 @@
 // covers [0, count+i]. Output i: y_i[r] = (e^{S_last - S_first-1} (h' . C_i)[r]
 // + sum_k dt_k e^{S_last - S_k} (B_k . C_i) x_k[r] + D x_last[r]) silu(z_i[r]),
 // last = count + i; h0 . [C_0..C_3] is an m16n8k8 tf32 product per warp (the
-// fp32 state split in two tf32 parts, a 16-bit read copy exact in tf32, an fp8
-// one scaled by its row scales after the product).
+// fp32 state split in two tf32 parts on two independent accumulator chains, a
+// 16-bit read copy exact in tf32, an fp8 one scaled by its row scales after the
+// product), and so is the window term [x_k] . [coefficients] (x bf16, the
+// coefficients in two tf32 parts). The fold of an fp32 checkpoint is a
+// tensor-core product too; with a read copy it runs in the row layout, from
+// the fp32 rows in global memory.
 // The new records' x and z rows go to the ring here (these rows are read by
 // this block alone); their B, C and dt rows, which other blocks read, are
 // appended by the last of the sequence's blocks to finish (an arrival count in
 // the high half of the cursor's flags word), which also marks the cursor
 // pending: a verify is one kernel.
 #include "fast_rows.cuh"
+#include "fold_mma.cuh"
 #include "kernels.h"
 
 namespace rssm {
@@ -44,6 +49,7 @@ using namespace fastrows;
 
 constexpr int KMAX = 4;  // new records per verify on this path
 constexpr int EW = 8;    // B.C entries per warp: 4 warps x 8 = 32 >= L + K
+constexpr int XS = FPB + 8;  // x table row stride (bf16): a record's rows start 16 bytes apart in bank terms
 
 // Epilogue of a verify, run by all threads of the sequence's last block: on a
 // cursor with 0 <= start < L, 0 <= count <= L and pending == 0, append the K
@@ -134,7 +140,7 @@ template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   extern __shared__ __align__(128) float dsm[];
   float* tile = dsm;                                                  // the block's rows (fp32, or bf16)
-  uint16_t* xs = reinterpret_cast<uint16_t*>(dsm + FPB * FN);         // x of record k, row r: xs[k * FPB + r]
+  uint16_t* xs = reinterpret_cast<uint16_t*>(dsm + FPB * FN);         // x of record k, row r: xs[k * XS + r]
   __shared__ float tbl[2][KMAX][FW * EW];                             // B_e . C_i over column half [0] / [1]
   __shared__ float cf[KMAX][33];                                      // window coefficient of record k, output i
   __shared__ uint64_t bar;
@@ -258,8 +264,8 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   const uint4 xar = shfl_u4(xsA, sl), xbr = shfl_u4(xsB, sl), xan = shfl_u4(xnA, jn), xbn = shfl_u4(xnB, jn);
   const uint4 xq[2] = {lane < count ? xar : xan, lane < count ? xbr : xbn};
   if (lane < total) {  // this warp's rows of every record's x, in record order
-    *reinterpret_cast<uint4*>(xs + lane * FPB + rl0) = xq[0];
-    *reinterpret_cast<uint4*>(xs + lane * FPB + rl1) = xq[1];
+    *reinterpret_cast<uint4*>(xs + lane * XS + rl0) = xq[0];
+    *reinterpret_cast<uint4*>(xs + lane * XS + rl1) = xq[1];
   }
   __syncthreads();  // the dot table (and each warp's x rows)
   // Without a fold the epilogue writes free ring slots only: this block is done
@@ -295,6 +301,11 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   }
   const float Pn0 = expf(__shfl_sync(FULL, S, (count + 2 * qt) & 31));
   const float Pn1 = expf(__shfl_sync(FULL, S, (count + 2 * qt + 1) & 31));
+  // this lane's columns of C_qg (the mma's B fragments), requested before the wait
+  uint2 cv[FN / 16];
+#pragma unroll
+  for (int jb = 0; jb < FN / 16; jb++)
+    cv[jb] = cvec ? *reinterpret_cast<const uint2*>(cvec + 16 * jb + 4 * qt) : make_uint2(0, 0);
   __syncthreads();  // the coefficient table
   const bool landed = __all_sync(FULL, mbar_wait(&bar, 0));  // uniform over the warp
   if (!landed) {
@@ -309,16 +320,17 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     // h0 . [C_0..C_3] for rows (rA, rB) as m16n8k8 tf32 mma; an fp32 state is
     // split into two tf32 parts, the bf16 or fp16 read copy is exact in tf32
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float ch[2][4] = {};
 #pragma unroll
     for (int jb = 0; jb < FN / 16; jb++) {
       const int col = 16 * jb + 4 * qt;
       float4 r0, r1;
       state_rows(tile, gstate, t16, a.read_f16, a.read_f8, rA, rB, col, r0, r1);
-      const float4 bv = cvec ? load_bf4(cvec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 bv = bf4_to_f4(cv[jb]);
       if (t16) {  // uniform
-        mma_tf32_1688(acc, __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y),
+        mma_tf32_1688(ch[0], __float_as_uint(r0.x), __float_as_uint(r1.x), __float_as_uint(r0.y),
                       __float_as_uint(r1.y), __float_as_uint(bv.x), __float_as_uint(bv.y));
-        mma_tf32_1688(acc, __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w),
+        mma_tf32_1688(ch[1], __float_as_uint(r0.z), __float_as_uint(r1.z), __float_as_uint(r0.w),
                       __float_as_uint(r1.w), __float_as_uint(bv.z), __float_as_uint(bv.w));
       } else {
         uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
@@ -326,16 +338,18 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
         split_tf32(r1.x, h1, l1);
         split_tf32(r0.y, h2, l2);
         split_tf32(r1.y, h3, l3);
-        mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.x), __float_as_uint(bv.y));
-        mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+        mma_tf32_1688(ch[0], h0, h1, h2, h3, __float_as_uint(bv.x), __float_as_uint(bv.y));
+        mma_tf32_1688(ch[1], l0, l1, l2, l3, __float_as_uint(bv.x), __float_as_uint(bv.y));
         split_tf32(r0.z, h0, l0);
         split_tf32(r1.z, h1, l1);
         split_tf32(r0.w, h2, l2);
         split_tf32(r1.w, h3, l3);
-        mma_tf32_1688(acc, h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
-        mma_tf32_1688(acc, l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+        mma_tf32_1688(ch[0], h0, h1, h2, h3, __float_as_uint(bv.z), __float_as_uint(bv.w));
+        mma_tf32_1688(ch[1], l0, l1, l2, l3, __float_as_uint(bv.z), __float_as_uint(bv.w));
       }
     }
+#pragma unroll
+    for (int q = 0; q < 4; q++) acc[q] = ch[0][q] + ch[1][q];
     if (t16 && a.read_f8) {  // e4m3 rows times their scales (the scale of a row factors out of its dots)
       const float* scales = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(a.ckpt_read) +
                                                            (size_t)a.Sn * H * P * FN);
@@ -345,17 +359,28 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
       acc[2] *= sB;
       acc[3] *= sB;
     }
+    // window term W[r][n] = sum_k x_k[r] cf[n][k] at rows (rA, rB), outputs n < 4: m16n8k8
+    // tf32 products over blocks of 8 records in acc's fragment layout (x is bf16, exact
+    // in tf32; cf enters as two tf32 parts; records past the window enter as 0)
+    float wd[2][4] = {};
+    for (int k0 = 0; k0 < total; k0 += 8) {
+      const int ka = k0 + qt, kb = ka + 4;
+      const uint32_t a0 = ka < total ? (uint32_t)xs[ka * XS + rA] << 16 : 0u;
+      const uint32_t a1 = ka < total ? (uint32_t)xs[ka * XS + rB] << 16 : 0u;
+      const uint32_t a2 = kb < total ? (uint32_t)xs[kb * XS + rA] << 16 : 0u;
+      const uint32_t a3 = kb < total ? (uint32_t)xs[kb * XS + rB] << 16 : 0u;
+      uint32_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+      if (qg < KMAX) {  // cf[n][k] = 0 past output n's window
+        split_tf32(cf[qg][ka], h0, l0);
+        split_tf32(cf[qg][kb], h1, l1);
+      }
+      mma_tf32_1688(wd[0], a0, a1, a2, a3, h0, h1);
+      mma_tf32_1688(wd[1], a0, a1, a2, a3, l0, l1);
+    }
     if (qt < 2) {  // outputs n0 = 2 qt, n1 = n0 + 1 at rows rA, rB
       const int n0 = 2 * qt, n1 = n0 + 1;
-      float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
-      for (int k = 0; k < total; k++) {
-        const float c0 = cf[n0][k], c1 = cf[n1][k];
-        const float xa = bf_to_f(xs[k * FPB + rA]), xb = bf_to_f(xs[k * FPB + rB]);
-        w00 = fmaf(c0, xa, w00);
-        w01 = fmaf(c1, xa, w01);
-        w10 = fmaf(c0, xb, w10);
-        w11 = fmaf(c1, xb, w11);
-      }
+      const float w00 = wd[0][0] + wd[1][0], w01 = wd[0][1] + wd[1][1];
+      const float w10 = wd[0][2] + wd[1][2], w11 = wd[0][3] + wd[1][3];
       if (valid) {
         const size_t y0 = (((size_t)b * K + n0) * H + h) * P + p0;
         if (n0 < K) {
@@ -368,7 +393,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
         }
       }
     }
-    if (fold) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, written once (with the bf16 copy)
+    if (fold && !copy) {  // h' = Pf h0 + sum_{k<count} wf_k x_k[r] B_k, written once (tensor cores)
+      const uint16_t* rBg = a.rB + (size_t)sg * L * FN;
+      fold_rows_mma(
+          tile, a.ckpt + tbase, [&](int k) { return rBg + wrap(start + k, L) * FN; },
+          [&](int k, int r) { return bf_to_f(xs[k * XS + r]); }, count, Pf, wf, rl0, rl1, lane);
+    } else if (fold) {  // the read copy: row layout, from the fp32 rows in global memory (with the copy)
 #pragma unroll
       for (int half = 0; half < 2; half++) {
         const int rl = half ? rl1 : rl0;
@@ -434,7 +464,7 @@ cudaError_t m2_verify_fast_launch(const M2Args& a, int out_bf16, cudaStream_t st
   const dim3 grid(a.nPB, a.H, a.Bt);
   auto k = a.slots ? (out_bf16 ? m2_verify_fast_kernel<true, true> : m2_verify_fast_kernel<false, true>)
                    : (out_bf16 ? m2_verify_fast_kernel<true, false> : m2_verify_fast_kernel<false, false>);
-  const int smem = FPB * FN * 4 + (a.L + a.K) * FPB * 2;  // tile + the records' x rows
+  const int smem = FPB * FN * 4 + (a.L + a.K) * XS * 2;  // tile + the records' x rows
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;
   k<<<grid, FT, smem, st>>>(a);
