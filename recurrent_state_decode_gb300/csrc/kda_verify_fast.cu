@@ -28,11 +28,11 @@
 // into shared memory and their channel's share of the sixteen couplings among
 // new records (one transposed reduction per warp, summed over the warps in
 // shared memory); lane j the new record j's beta, lane 4 j + t the v of new
-// record t at the lane's rows, as in the Gated DeltaNet verify. As soon as
-// the cursor is read, the last warp (idle in the channel phase) stages the
-// window's e and g rows by bulk copies, one record per lane (second
-// mbarrier). Then thread c
-// turns its channel of the g rows into f_t in place and E; each warp forms the
+// record t at the lane's rows, as in the Gated DeltaNet verify. The last warp
+// (idle in the channel phase) requests the rows and, before the cursor is
+// known, every ring slot's e, g and k rows (one slot per lane, second
+// mbarrier), so that nothing later waits on global memory. Then thread c
+// turns its channel of the window's g rows into f_t in place and E; each warp forms the
 // dots (f_t * k_t) . [k~, q~] of two committed records per round (one 16-value
 // transposed reduction). The S0 product with the eight vectors E * k~_j,
 // E * q~_i is an m16n8k8 tf32 mma per warp with both operands split into two
@@ -110,8 +110,9 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   float* tile = dsm;                 // the head's 128 rows
   float* vt = tile + GD * GD;        // [0..3] k~_j, [4..7] q~_i (fp32, all channels)
   float* ew = vt + 2 * KMAX * GD;    // E by channel
-  float* fd = ew + GD;               // g, then f, of committed record t at fd + t * GD
-  float* es = fd + L * GD;           // e of committed record t at es + t * ES (all rows)
+  float* fd = ew + GD;               // g, then f, of ring slot s at fd + s * GD
+  float* es = fd + L * GD;           // e of ring slot s at es + s * ES (all rows)
+  uint16_t* ks = reinterpret_cast<uint16_t*>(es + L * ES);  // k of ring slot s at ks + s * GD
   __shared__ float cf[2 * KMAX][WMAX + 1];  // [n][t]: (f_t * k_t) . vec_n
   __shared__ float cred[4][32];             // the couplings' per-warp sums (warps 0..3; lane layout of cpl)
   __shared__ uint64_t bar[2];               // [0] the rows, [1] the window's e and g rows
@@ -121,33 +122,31 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   const size_t sh = (size_t)b * H + h;
   const size_t tbase = sh * GD * GD;
 
-  if (threadIdx.x == 0) {
-    mbar_init(&bar[0], 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(&bar[0], GD * GD * 4);
-    bulk_load(tile, a.S + tbase, GD * GD * 2, &bar[0]);
-    bulk_load(tile + GD * GD / 2, a.S + tbase + GD * GD / 2, GD * GD * 2, &bar[0]);
+  if (warp == VW - 1) {  // the last warp (idle in the channel phase below): the rows, and every ring slot's e, g, k
+    if (lane == 0) {
+      mbar_init(&bar[0], 1);
+      mbar_init(&bar[1], 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&bar[0], GD * GD * 4);
+      bulk_load(tile, a.S + tbase, GD * GD * 2, &bar[0]);
+      bulk_load(tile + GD * GD / 2, a.S + tbase + GD * GD / 2, GD * GD * 2, &bar[0]);
+      mbar_arrive_expect_tx(&bar[1], (uint32_t)L * (2 * GD * 4 + GD * 2));
+    }
+    __syncwarp();
+    if (lane < L) {  // lane s: ring slot s, requested before the cursor is known
+      const size_t row = sh * L + lane;
+      bulk_load(es + lane * ES, a.re + row * GD, GD * 4, &bar[1]);
+      bulk_load(fd + lane * GD, a.rg + row * GD, GD * 4, &bar[1]);
+      bulk_load(ks + lane * GD, a.rk + row * GD, GD * 2, &bar[1]);
+    }
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
+  if (threadIdx.x == 0) cur_s = cur;
   // An invalid cursor (reported by the sequence's last block) runs as an empty
   // window with every store masked.
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y <= L && cur.z == 0;
   const int start = valid ? cur.x : 0, count = valid ? cur.y : 0, total = count + K;
   const bool fold = valid && total > L;
-  if (warp == VW - 1) {  // the last warp (idle in the channel phase below) stages the window's e and g rows
-    if (lane == 0) {
-      cur_s = cur;
-      mbar_init(&bar[1], 1);
-      fence_mbar_init();
-      mbar_arrive_expect_tx(&bar[1], (uint32_t)count * 2 * GD * 4);
-    }
-    __syncwarp();
-    if (lane < count) {  // lane t: committed record t, in record order
-      const size_t row = sh * L + wrap(start + lane, L);
-      bulk_load(es + lane * ES, a.re + row * GD, GD * 4, &bar[1]);
-      bulk_load(fd + lane * GD, a.rg + row * GD, GD * 4, &bar[1]);
-    }
-  }
   const int rl0 = warp * 8, rl1 = VHALF + warp * 8;
   const int qg = lane >> 2, qt = lane & 3;  // tensor-core fragment coordinates
   const int rA = rl0 + qg, rB = rl1 + qg;   // the rows of this lane's accumulator fragments
@@ -204,8 +203,9 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   if (c < GD) {  // channel c: f_t = exp(G_W - G_t) in place of g_t, backwards over the window, then E = exp(G_W)
     float s = 0.f;
     for (int t = cnt - 1; t >= 0; t--) {
-      const float x = fd[t * GD + c];
-      fd[t * GD + c] = expf(s);
+      const int sl = wrap(start + t, L);
+      const float x = fd[sl * GD + c];
+      fd[sl * GD + c] = expf(s);
       s += x;
     }
     ew[c] = expf(s);
@@ -213,13 +213,13 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   __syncthreads();  // f_t and E
   if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);  // every thread has read the cursor
   // window coefficients cf[n][t] = (f_t * k_t) . vec_n: warp w takes records 16 r + 2 w + i (i < 2)
-  const uint16_t* rkp = a.rk + sh * L * GD + lane * 4;
   for (int base = 0; base < cnt; base += 2 * VW) {  // uniform
     float4 kh[2];
 #pragma unroll
     for (int i = 0; i < 2; i++) {
       const int t = base + 2 * warp + i;
-      kh[i] = t < cnt ? mul4(ld4(fd + t * GD + lane * 4), load_bf4(rkp + wrap(start + t, L) * GD))
+      const int sl = wrap(start + t, L);
+      kh[i] = t < cnt ? mul4(ld4(fd + sl * GD + lane * 4), load_bf4(ks + sl * GD + lane * 4))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float pk[16];
@@ -272,8 +272,9 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
     const int n0 = 2 * qt, n1 = n0 + 1;
     float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
     for (int t = 0; t < cnt; t++) {
+      const int sl = wrap(start + t, L);
       const float c0 = cf[n0][t], c1 = cf[n1][t];
-      const float eA = es[t * ES + rA], eB = es[t * ES + rB];
+      const float eA = es[sl * ES + rA], eB = es[sl * ES + rB];
       w00 = fmaf(c0, eA, w00);
       w01 = fmaf(c1, eA, w01);
       w10 = fmaf(c0, eB, w10);
@@ -354,15 +355,16 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
           float4 kt[2];
 #pragma unroll
           for (int u = 0; u < 2; u++) {
-            const int t = t0 + u;
-            kt[u] = t < cnt ? mul4(ld4(fd + t * GD + lane * 4), load_bf4(rkp + wrap(start + t, L) * GD))
+            const int t = t0 + u, sl = wrap(start + t, L);
+            kt[u] = t < cnt ? mul4(ld4(fd + sl * GD + lane * 4), load_bf4(ks + sl * GD + lane * 4))
                             : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
           for (int u = 0; u < 2; u++) {
             const int t = t0 + u;
             if (t < cnt) {  // uniform
-              const float4 ea2 = ld4(es + t * ES + rl), eb2 = ld4(es + t * ES + rl + 4);
+              const int sl = wrap(start + t, L);
+              const float4 ea2 = ld4(es + sl * ES + rl), eb2 = ld4(es + sl * ES + rl + 4);
               const float et[8] = {ea2.x, ea2.y, ea2.z, ea2.w, eb2.x, eb2.y, eb2.z, eb2.w};
 #pragma unroll
               for (int rr = 0; rr < 8; rr++) hv[rr] = fma4(et[rr], kt[u], hv[rr]);
@@ -388,7 +390,7 @@ bool kda_verify_applies(const GdnArgs& a) {
          a.Bt <= 65535 && !a.slots;
 }
 
-size_t kda_verify_fast_smem(int L) { return (size_t)(GD * GD + 2 * KMAX * GD + GD + L * GD + L * ES) * 4; }
+size_t kda_verify_fast_smem(int L) { return (size_t)(GD * GD + 2 * KMAX * GD + GD + L * GD + L * ES) * 4 + (size_t)L * GD * 2; }
 
 cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;

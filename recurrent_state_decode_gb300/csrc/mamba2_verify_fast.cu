@@ -299,6 +299,11 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     a.rz[rrow + rl0 + gr] = zbA;
     a.rz[rrow + rl1 + gr] = zbB;
   }
+#pragma unroll
+  for (int u = 0; u < 2; u++) {  // the gates, silu(z)
+    zg[u][0] = silu_fast(zg[u][0]);
+    zg[u][1] = silu_fast(zg[u][1]);
+  }
   const float Pn0 = expf(__shfl_sync(FULL, S, (count + 2 * qt) & 31));
   const float Pn1 = expf(__shfl_sync(FULL, S, (count + 2 * qt + 1) & 31));
   // this lane's columns of C_qg (the mma's B fragments), requested before the wait
@@ -307,6 +312,24 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
   for (int jb = 0; jb < FN / 16; jb++)
     cv[jb] = cvec ? *reinterpret_cast<const uint2*>(cvec + 16 * jb + 4 * qt) : make_uint2(0, 0);
   __syncthreads();  // the coefficient table
+  // window term W[r][n] = sum_k x_k[r] cf[n][k] at rows (rA, rB), outputs n < 4: m16n8k8
+  // tf32 products over blocks of 8 records in acc's fragment layout (x is bf16, exact
+  // in tf32; cf enters as two tf32 parts; records past the window enter as 0), before the rows land
+  float wd[2][4] = {};
+  for (int k0 = 0; k0 < total; k0 += 8) {
+    const int ka = k0 + qt, kb = ka + 4;
+    const uint32_t a0 = ka < total ? (uint32_t)xs[ka * XS + rA] << 16 : 0u;
+    const uint32_t a1 = ka < total ? (uint32_t)xs[ka * XS + rB] << 16 : 0u;
+    const uint32_t a2 = kb < total ? (uint32_t)xs[kb * XS + rA] << 16 : 0u;
+    const uint32_t a3 = kb < total ? (uint32_t)xs[kb * XS + rB] << 16 : 0u;
+    uint32_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+    if (qg < KMAX) {  // cf[n][k] = 0 past output n's window
+      split_tf32(cf[qg][ka], h0, l0);
+      split_tf32(cf[qg][kb], h1, l1);
+    }
+    mma_tf32_1688(wd[0], a0, a1, a2, a3, h0, h1);
+    mma_tf32_1688(wd[1], a0, a1, a2, a3, l0, l1);
+  }
   const bool landed = __all_sync(FULL, mbar_wait(&bar, 0));  // uniform over the warp
   if (!landed) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
@@ -359,24 +382,6 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
       acc[2] *= sB;
       acc[3] *= sB;
     }
-    // window term W[r][n] = sum_k x_k[r] cf[n][k] at rows (rA, rB), outputs n < 4: m16n8k8
-    // tf32 products over blocks of 8 records in acc's fragment layout (x is bf16, exact
-    // in tf32; cf enters as two tf32 parts; records past the window enter as 0)
-    float wd[2][4] = {};
-    for (int k0 = 0; k0 < total; k0 += 8) {
-      const int ka = k0 + qt, kb = ka + 4;
-      const uint32_t a0 = ka < total ? (uint32_t)xs[ka * XS + rA] << 16 : 0u;
-      const uint32_t a1 = ka < total ? (uint32_t)xs[ka * XS + rB] << 16 : 0u;
-      const uint32_t a2 = kb < total ? (uint32_t)xs[kb * XS + rA] << 16 : 0u;
-      const uint32_t a3 = kb < total ? (uint32_t)xs[kb * XS + rB] << 16 : 0u;
-      uint32_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
-      if (qg < KMAX) {  // cf[n][k] = 0 past output n's window
-        split_tf32(cf[qg][ka], h0, l0);
-        split_tf32(cf[qg][kb], h1, l1);
-      }
-      mma_tf32_1688(wd[0], a0, a1, a2, a3, h0, h1);
-      mma_tf32_1688(wd[1], a0, a1, a2, a3, l0, l1);
-    }
     if (qt < 2) {  // outputs n0 = 2 qt, n1 = n0 + 1 at rows rA, rB
       const int n0 = 2 * qt, n1 = n0 + 1;
       const float w00 = wd[0][0] + wd[1][0], w01 = wd[0][1] + wd[1][1];
@@ -384,12 +389,12 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
       if (valid) {
         const size_t y0 = (((size_t)b * K + n0) * H + h) * P + p0;
         if (n0 < K) {
-          store_out<OUT_BF16>(a.y, y0 + rA, fmaf(Pn0, acc[0], w00) * silu_fast(zg[0][0]));
-          store_out<OUT_BF16>(a.y, y0 + rB, fmaf(Pn0, acc[2], w10) * silu_fast(zg[0][1]));
+          store_out<OUT_BF16>(a.y, y0 + rA, fmaf(Pn0, acc[0], w00) * zg[0][0]);
+          store_out<OUT_BF16>(a.y, y0 + rB, fmaf(Pn0, acc[2], w10) * zg[0][1]);
         }
         if (n1 < K) {
-          store_out<OUT_BF16>(a.y, y0 + (size_t)H * P + rA, fmaf(Pn1, acc[1], w01) * silu_fast(zg[1][0]));
-          store_out<OUT_BF16>(a.y, y0 + (size_t)H * P + rB, fmaf(Pn1, acc[3], w11) * silu_fast(zg[1][1]));
+          store_out<OUT_BF16>(a.y, y0 + (size_t)H * P + rA, fmaf(Pn1, acc[1], w01) * zg[1][0]);
+          store_out<OUT_BF16>(a.y, y0 + (size_t)H * P + rB, fmaf(Pn1, acc[3], w11) * zg[1][1]);
         }
       }
     }
@@ -446,9 +451,8 @@ __global__ void __launch_bounds__(FT, 6) m2_verify_fast_kernel(M2Args a) {
     __syncthreads();
     if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, sb);
   }
-  __syncthreads();
   if (threadIdx.x == 0) last_flags = last_ticket(ticket, a.H * a.nPB) ? (ticket & 0xffff) : -1;
-  __syncthreads();
+  __syncthreads();  // every thread is done; last_flags is visible
   if (last_flags >= 0) verify_epilogue(a, b, sb, cur, last_flags);
 }
 
