@@ -305,25 +305,57 @@ __global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_ker
   if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, scur, ticket, nblocks, L, a.status);
 }
 
-// The emulated step's error sums: the per-warp pairs added in a fixed order
-// (each thread a strided share in fp64, then a tree over the block).
-constexpr int EMU_RT = 1024;  // threads of the reduction
-constexpr int EMU_U = 16;     // loads in flight per thread
+// The emulated step's error sums, added in a fixed order in two stages. A
+// single block of the whole reduction spent most of its time in fp64 adds on
+// one SM (this GPU's fp64 rate is low); spread over one block per 256 pairs
+// the adds take a few microseconds.
+constexpr int EMU_C = 256;    // pairs per first-stage block (its threads)
+constexpr int EMU_RT = 1024;  // threads of the second stage
 
-__global__ void __launch_bounds__(EMU_RT) emu_reduce_kernel(const float2* __restrict__ part, size_t n, double* err) {
+// (a, b) summed over a warp by a fixed butterfly; every lane ends with the total.
+__device__ __forceinline__ void warp_sum2(double& a, double& b) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(FULL, a, o);
+    b += __shfl_xor_sync(FULL, b, o);
+  }
+}
+
+// Stage 1: block j adds pairs [256 j, 256 j + 256) in fp64 (a butterfly per
+// warp, then the eight warps in order) and writes the total over the chunk's
+// first two pairs (one double2, which needs 16 bytes: a chunk of one pair is
+// left as it is and read as a pair by stage 2).
+__global__ void __launch_bounds__(EMU_C) emu_reduce1_kernel(float2* part, size_t n) {
+  __shared__ double2 w[EMU_C / 32];
+  const size_t base = (size_t)blockIdx.x * EMU_C, i = base + threadIdx.x;
+  const float2 v = i < n ? part[i] : make_float2(0.f, 0.f);
+  double e = v.x, q = v.y;
+  warp_sum2(e, q);
+  if ((threadIdx.x & 31) == 0) w[threadIdx.x >> 5] = make_double2(e, q);
+  __syncthreads();  // every pair of the chunk is read before its first two are overwritten
+  if (threadIdx.x == 0 && n - base >= 2) {
+    double2 t = w[0];
+#pragma unroll
+    for (int k = 1; k < EMU_C / 32; k++) t.x += w[k].x, t.y += w[k].y;
+    *reinterpret_cast<double2*>(part + base) = t;
+  }
+}
+
+// Stage 2: one block adds the chunks' totals (thread t chunks t, t + 1024, ...
+// in order, then a tree over the block) into err[0..1].
+__global__ void __launch_bounds__(EMU_RT) emu_reduce2_kernel(const float2* __restrict__ part, size_t n, double* err) {
   __shared__ double se[EMU_RT], sn[EMU_RT];
+  const size_t chunks = (n + EMU_C - 1) / EMU_C;
   double e = 0.0, q = 0.0;
-  for (size_t i0 = threadIdx.x; i0 < n; i0 += (size_t)EMU_U * EMU_RT) {  // EMU_U loads issued, then added in order
-    float2 v[EMU_U];
-#pragma unroll
-    for (int u = 0; u < EMU_U; u++) {
-      const size_t i = i0 + (size_t)u * EMU_RT;
-      v[u] = i < n ? part[i] : make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < EMU_U; u++) {
-      e += v[u].x;
-      q += v[u].y;
+  for (size_t j = threadIdx.x; j < chunks; j += EMU_RT) {
+    const size_t base = j * EMU_C;
+    if (n - base >= 2) {
+      const double2 t = *reinterpret_cast<const double2*>(part + base);
+      e += t.x;
+      q += t.y;
+    } else {
+      e += part[base].x;
+      q += part[base].y;
     }
   }
   se[threadIdx.x] = e;
@@ -382,7 +414,10 @@ cudaError_t m2_step_emulated_launch(const M2Args& a, int out_bf16, double* err, 
   if (e != cudaSuccess) return e;
   k<<<grid, FT, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  emu_reduce_kernel<<<1, EMU_RT, 0, st>>>(a.emu_part, m2_emulated_partials(a), err);
+  const size_t n = m2_emulated_partials(a);
+  emu_reduce1_kernel<<<(unsigned)((n + EMU_C - 1) / EMU_C), EMU_C, 0, st>>>(a.emu_part, n);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  emu_reduce2_kernel<<<1, EMU_RT, 0, st>>>(a.emu_part, n, err);
   return cudaGetLastError();
 }
 
