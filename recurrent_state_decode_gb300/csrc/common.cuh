@@ -227,45 +227,55 @@ __device__ __forceinline__ float emu_qmax(int fmt) {
   return fmt == RSSM_EMU_E4M3 ? 448.f : fmt == RSSM_EMU_E5M2 ? 57344.f : fmt == RSSM_EMU_INT8 ? 127.f : 1.f;
 }
 
-// The constants of an emulated format's rounding (see emu_quantise), taken
-// once per thread.
+// An emulated format, taken once per thread (see emu_quantise4).
 struct EmuQ {
-  uint32_t half, mask;  // half an ulp at the kept precision minus one; the dropped bits
-  int sh;               // dropped bits of the fp32 significand (24 - p)
-  float lo, c, vmax;    // 2^emin; the magic constant 1.5 * 2^(k + 23); the largest value
-  bool int8;
+  int fmt;     // RSSM_EMU_*
+  float vmax;  // the largest finite value
 };
 
 __device__ __forceinline__ EmuQ emu_params(int fmt) {
   EmuQ q;
-  q.int8 = fmt == RSSM_EMU_INT8;
-  switch (fmt) {
-    case RSSM_EMU_BF16: q.sh = 16; q.lo = 0x1p-126f; q.c = 0x1.8p-110f; q.vmax = 0x1.fep127f; break;
-    case RSSM_EMU_F16: q.sh = 13; q.lo = 0x1p-14f; q.c = 0x1.8p-1f; q.vmax = 65504.f; break;
-    case RSSM_EMU_E4M3: q.sh = 20; q.lo = 0x1p-6f; q.c = 0x1.8p14f; q.vmax = 448.f; break;
-    default: q.sh = 21; q.lo = 0x1p-14f; q.c = 0x1.8p7f; q.vmax = 57344.f; break;  // E5M2 (unused for int8)
-  }
-  q.half = (1u << (q.sh - 1)) - 1u;
-  q.mask = ~((1u << q.sh) - 1u);
+  q.fmt = fmt;
+  q.vmax = fmt == RSSM_EMU_BF16 ? 0x1.fep127f : fmt == RSSM_EMU_F16 ? 65504.f : emu_qmax(fmt);
   return q;
 }
 
-// t rounded to nearest, ties to even, into an emulated format, saturating at
-// its largest finite value. A binary format with p significant bits and
-// smallest normal exponent emin: at or above 2^emin the fp32 pattern is
-// rounded at bit 24 - p (adding half an ulp minus one plus the kept lowest
-// bit, then clearing the dropped bits; a carry moves into the exponent);
-// below it the spacing is fixed at 2^k, k = emin - p + 1, and adding then
-// subtracting c = 1.5 * 2^(k + 23) rounds t to a multiple of 2^k (the sum
-// lies in [2^(k+23), 2^(k+24)), whose ulp is 2^k). int8: rintf (half to
-// even), clamped to [-127, 127].
-__device__ __forceinline__ float emu_quantise(float t, const EmuQ& q) {
-  if (q.int8) return fminf(fmaxf(rintf(t), -127.f), 127.f);
-  uint32_t u = __float_as_uint(t);
-  u = (u + q.half + ((u >> q.sh) & 1u)) & q.mask;
-  const float sub = __fsub_rn(__fadd_rn(t, q.c), q.c);
-  const float r = fabsf(t) < q.lo ? sub : __uint_as_float(u);
-  return fminf(fmaxf(r, -q.vmax), q.vmax);
+// Four values rounded to nearest, ties to even, into an emulated format and
+// back to fp32, saturating at the format's largest finite value, through
+// CUDA's conversions: e4m3 and e5m2 by the saturating fp8 conversion; bf16
+// and fp16 by the round-to-nearest conversions after a clamp to the largest
+// finite value (so that nothing rounds to infinity); int8 by rintf (half to
+// even), clamped to [-127, 127]. The format is uniform over the launch.
+__device__ __forceinline__ float4 emu_quantise4(float4 t, const EmuQ& q) {
+  auto clamp = [&](float x) { return fminf(fmaxf(x, -q.vmax), q.vmax); };
+  auto fp8 = [](float a, float b, __nv_fp8_interpretation_t k) {
+    const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, k);
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(p, k);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+  };
+  float2 lo, hi;
+  switch (q.fmt) {
+    case RSSM_EMU_BF16:
+      lo = __bfloat1622float2(__floats2bfloat162_rn(clamp(t.x), clamp(t.y)));
+      hi = __bfloat1622float2(__floats2bfloat162_rn(clamp(t.z), clamp(t.w)));
+      break;
+    case RSSM_EMU_F16:
+      lo = __half22float2(__floats2half2_rn(clamp(t.x), clamp(t.y)));
+      hi = __half22float2(__floats2half2_rn(clamp(t.z), clamp(t.w)));
+      break;
+    case RSSM_EMU_E4M3:
+      lo = fp8(t.x, t.y, __NV_E4M3);
+      hi = fp8(t.z, t.w, __NV_E4M3);
+      break;
+    case RSSM_EMU_E5M2:
+      lo = fp8(t.x, t.y, __NV_E5M2);
+      hi = fp8(t.z, t.w, __NV_E5M2);
+      break;
+    default:  // int8
+      lo = make_float2(fminf(fmaxf(rintf(t.x), -127.f), 127.f), fminf(fmaxf(rintf(t.y), -127.f), 127.f));
+      hi = make_float2(fminf(fmaxf(rintf(t.z), -127.f), 127.f), fminf(fmaxf(rintf(t.w), -127.f), 127.f));
+  }
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // Maxima of V per-lane values over the warp, transposed like

@@ -72,17 +72,24 @@ __device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, cons
   }
 #pragma unroll
   for (int rr = 0; rr < 8; rr++) {
-    float* v = reinterpret_cast<float*>(&hv[rr]);
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const float x = v[j];
-      const float q = emu_quantise(scaled ? __fmul_rn(x, inv[rr]) : x, fq);
-      const float r = scaled ? __fmul_rn(q, sc[rr]) : q;
-      const float d = r - x;
-      err = fmaf(d, d, err);
-      nrm = fmaf(x, x, nrm);
-      v[j] = r;
-    }
+    const float4 x = hv[rr];
+    const float4 t = scaled ? make_float4(__fmul_rn(x.x, inv[rr]), __fmul_rn(x.y, inv[rr]), __fmul_rn(x.z, inv[rr]),
+                                          __fmul_rn(x.w, inv[rr]))
+                            : x;
+    const float4 q = emu_quantise4(t, fq);
+    const float4 r = scaled ? make_float4(__fmul_rn(q.x, sc[rr]), __fmul_rn(q.y, sc[rr]), __fmul_rn(q.z, sc[rr]),
+                                          __fmul_rn(q.w, sc[rr]))
+                            : q;
+    const float d0 = r.x - x.x, d1 = r.y - x.y, d2 = r.z - x.z, d3 = r.w - x.w;
+    err = fmaf(d0, d0, err);
+    err = fmaf(d1, d1, err);
+    err = fmaf(d2, d2, err);
+    err = fmaf(d3, d3, err);
+    nrm = fmaf(x.x, x.x, nrm);
+    nrm = fmaf(x.y, x.y, nrm);
+    nrm = fmaf(x.z, x.z, nrm);
+    nrm = fmaf(x.w, x.w, nrm);
+    hv[rr] = r;
   }
 }
 
@@ -93,7 +100,7 @@ __device__ __forceinline__ void emu_read8(float4 (&hv)[8], const M2Args& a, cons
 // each block writes its (error, norm) sums to a.emu_part (fp32 tiles, no slots).
 // KWT: dot slots per warp (KW, or KW_SHORT when L <= 16).
 template <bool OUT_BF16, bool RD16, bool SLOTS, bool EMU = false, int KWT = KW>
-__global__ void __launch_bounds__(FT, RD16 ? 7 : (EMU ? 5 : 6)) m2_step_fast_kernel(M2Args a) {
+__global__ void __launch_bounds__(FT, RD16 ? 7 : 6) m2_step_fast_kernel(M2Args a) {
   // the block's rows: a static fp32 tile, or the dynamic 16 KiB of a bf16 one
   __shared__ __align__(128) float tile_s[RD16 ? 4 : FPB * FN];
   extern __shared__ __align__(128) float tile_d[];

@@ -10,9 +10,10 @@ both sides, so the reads agree exactly); its replay formula over the window
 gives the expected output (fp32 path: <= 1e-4 relative L2); its
 emulation_error gives the expected error report (<= 1e-5 relative). Flushed
 checkpoints are checked against the conventional session (<= 1e-5).
-The kernel's quantiser is also checked, bit for bit, against CUDA's own
-conversions: the emulated bf16 read against the stored bf16 read copy, and
-the emulated e4m3 read with a row scale against the stored fp8 read copy.
+The emulated reads are also checked, bit for bit, against the stored read
+copies: the emulated bf16 read against the stored bf16 copy, and the
+emulated e4m3 read with a row scale against the stored fp8 copy (the two
+paths scale, convert and read back separately).
 """
 import numpy as np
 import pytest
@@ -121,8 +122,9 @@ def test_emulated_step_against_the_oracle(fmt, scale):
 @pytest.mark.parametrize("fmt,read_copy", [("bf16", True), ("e4m3", "f8")])
 def test_emulated_read_equals_the_stored_read_copy(fmt, read_copy):
     """The emulated bf16 read (no scale) and e4m3 read (row scale) are the
-    stored bf16 and fp8 read copies of the same checkpoint: the kernel's own
-    quantiser against CUDA's conversions, bit for bit, through the outputs."""
+    stored bf16 and fp8 read copies of the same checkpoint: the emulated
+    path's scaling and conversion against the stored copies', bit for bit,
+    through the outputs."""
     w = W("emu_rc", 3, 8, 64, 128, 2, 8, 12, seed=602)
     se, A, D, _, _, _ = mamba2_from_workload(w, DEV, bd.RSSM_F32, read_copy=False)
     sr, _, _, _, _, _ = mamba2_from_workload(w, DEV, bd.RSSM_F32, read_copy=read_copy)
@@ -139,7 +141,7 @@ def test_emulated_read_equals_the_stored_read_copy(fmt, read_copy):
     assert H.status(se) == 0 and H.status(sr) == 0
 
 
-def test_emulated_quantiser_against_cuda_conversions():
+def test_emulated_quantiser_against_the_oracle_rounding():
     """A checkpoint of values chosen to hit every rounding case (ties, the
     format-subnormal ranges, saturation): a one-step emulated read of it
     (no window, so y = h . C with C a unit vector picks one column) equals
