@@ -174,3 +174,31 @@ def test_emulated_quantiser_against_the_oracle_rounding():
             st.step_emulated(rec, A, D, y, bd.emulation(FMT[fmt], SCALE[scale]), err, ws)
             got[:, col] = y[0, 0].double().cpu().numpy() / 30.0
         np.testing.assert_allclose(got, want, rtol=2e-7, atol=0, err_msg=f"{fmt}-{scale}")
+
+
+@pytest.mark.parametrize("batch", [257, 513])
+def test_error_report_with_a_ragged_last_chunk(batch):
+    """The error report's two-stage reduction over one (error, norm) pair per
+    block: a launch of 257 blocks leaves a last chunk of one pair (read as
+    the pair itself), 513 blocks a last chunk of one pair after two full
+    ones. The report equals the oracle's emulation_error summed over every
+    sequence whose step does not flush (<= 1e-5 relative)."""
+    w = W("emu_ragged", batch, 1, 64, 128, 1, 4, 3, seed=605)
+    st, A, D, _, _, _ = mamba2_from_workload(w, DEV, bd.RSSM_F32, read_copy=False)
+    err, ws = emu_buffers(st)
+    emu = bd.emulation(FMT["e4m3"], SCALE["tile64"])
+    y = st.new_output()
+    for t in range(w.steps):
+        rec = I.mamba2_step_inputs(w, t, DEV)
+        counts = st.cursors[:, 1].cpu().numpy()
+        h0 = st.ckpt.cpu().numpy()
+        e_exp = n_exp = 0.0
+        for b in range(w.batch):
+            if counts[b] + 1 != w.buf_len:  # a flushing step reads the exact checkpoint
+                e, n = rc.emulation_error(h0[b], "e4m3", "tile64")
+                e_exp, n_exp = e_exp + e, n_exp + n
+        st.step_emulated(rec, A, D, y, emu, err, ws)
+        e_gpu, n_gpu = err.tolist()
+        assert n_gpu == pytest.approx(n_exp, rel=TOL_ERR), t
+        assert e_gpu == pytest.approx(e_exp, rel=TOL_ERR, abs=1e-30), t
+    assert H.status(st) == 0
