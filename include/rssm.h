@@ -40,7 +40,8 @@
  *    honoured by the decode calls on the shape-specialised kernels -- the
  *    Mamba-2 step and spec_verify (dstate 128, headdim a multiple of 64, a
  *    power-of-two nheads / ngroups), the Gated DeltaNet step and spec_verify
- *    and the KDA step (dk = dv = 128) -- and by rssm_commit_cursors_slots;
+ *    and the KDA step and spec_verify (dk = dv = 128) -- and by
+ *    rssm_commit_cursors_slots;
  *    elsewhere a non-NULL state_slots returns RSSM_ERR_UNSUPPORTED. Calls on whole state arrays (flush, prime,
  *    downcast, conventional steps) take state_slots = NULL with batch = the
  *    number of state rows.
@@ -491,7 +492,8 @@ RSSM_API int rssm_kda_flush(const rssm_kda_desc* desc, float* S, const rssm_kda_
  *  g [batch, K, nheads, dk], beta [batch, K, nheads] fp32;
  *  o [batch, K, nheads, dv] of out_dtype.
  *  1 <= n_new <= buf_len (else RSSM_ERR_INVALID_ARG); dk = dv = 128, n_new <= 4
- *  and buf_len + n_new <= 32 (else RSSM_ERR_UNSUPPORTED). */
+ *  and buf_len + n_new <= 32 (else RSSM_ERR_UNSUPPORTED). State slots are
+ *  honoured (records and outputs by batch row, state rows by slot). */
 RSSM_API int rssm_kda_spec_verify(const rssm_kda_desc* desc, int n_new, float* S, const rssm_kda_ring* ring,
                          int32_t* cursors, const rssm_bf16* q, const rssm_bf16* k, const rssm_bf16* v,
                          const float* g, const float* beta, void* o, int32_t* dev_status,

@@ -636,7 +636,6 @@ int rssm_kda_spec_verify(const rssm_kda_desc* d, int n_new, float* S, const rssm
   int rc = check_gdn(d);
   if (rc) return rc;
   if (n_new < 1 || n_new > d->buf_len) return RSSM_ERR_INVALID_ARG;
-  if (d->state_slots) return RSSM_ERR_UNSUPPORTED;
   if (d->batch == 0) return RSSM_OK;
   if (!ring) return RSSM_ERR_INVALID_ARG;
   if ((rc = check_ptrs({S, ring->q, ring->k, ring->v, ring->g, ring->beta, ring->e, cursors, q, k, v, g, beta, o})))

@@ -62,13 +62,13 @@ constexpr int ES = GD + 4;   // floats per staged e row (padded; 16-byte multipl
 // count + j) mod L (cursor c, already checked), by the whole block. One block
 // per (sequence, head) reads that head's ring rows, so it appends them itself
 // once it is done reading.
-__device__ __forceinline__ void append_head(const GdnArgs& a, int b, int h, int4 c) {
+__device__ __forceinline__ void append_head(const GdnArgs& a, int b, int sb, int h, int4 c) {
   const int L = a.L, K = a.K, H = a.H, tid = threadIdx.x;
   constexpr int NB = GD / 8, NG = GD / 4;  // 16-byte pieces of a bf16 row, of an fp32 row
   constexpr int PER = 2 * NB + NG;         // pieces of one record: k, q, g
   for (int q = tid; q < K * PER; q += VT) {
     const int j = q / PER, piece = q - j * PER;
-    const size_t ring = ((size_t)b * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
+    const size_t ring = ((size_t)sb * H + h) * L + wrap(wrap(c.x + c.y + j, L), L);
     const size_t rec = ((size_t)b * K + j) * H + h;
     if (piece < NB) {
       *reinterpret_cast<uint4*>(a.rk + ring * GD + piece * 8) = *reinterpret_cast<const uint4*>(a.k + rec * GD + piece * 8);
@@ -81,7 +81,7 @@ __device__ __forceinline__ void append_head(const GdnArgs& a, int b, int h, int4
     }
   }
   if (tid < K)
-    a.rbeta[((size_t)b * H + h) * pad4(L) + wrap(wrap(c.x + c.y + tid, L), L)] = a.beta[((size_t)b * K + tid) * H + h];
+    a.rbeta[((size_t)sb * H + h) * pad4(L) + wrap(wrap(c.x + c.y + tid, L), L)] = a.beta[((size_t)b * K + tid) * H + h];
 }
 
 // The cursor rule of a verify, applied by the sequence's last block to arrive
@@ -103,7 +103,8 @@ __device__ __forceinline__ void finish_verify_cursor(int32_t* cursors, int b, in
   *reinterpret_cast<int4*>(cursors + 4 * (size_t)b) = c;
 }
 
-template <bool OUT_BF16>
+// SLOTS: batch rows name their state rows through a slot table.
+template <bool OUT_BF16, bool SLOTS>
 __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   extern __shared__ __align__(128) float dsm[];
   const int L = a.L, H = a.H, K = a.K;
@@ -119,7 +120,10 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   __shared__ int4 cur_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, c = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
-  const size_t sh = (size_t)b * H + h;
+  // the batch row's state slot; a padding row (or a reported bad slot) leaves at once
+  const int sb = SLOTS ? state_slot(a.slots, a.Sn, b, a.status, h == 0 && threadIdx.x == 0) : b;
+  if (SLOTS && sb < 0) return;
+  const size_t sh = (size_t)sb * H + h;  // the state's rows (S, ring, cursor); the records' are b's
   const size_t tbase = sh * GD * GD;
 
   if (warp == VW - 1) {  // the last warp (idle in the channel phase below): the rows, and every ring slot's e, g, k
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
       bulk_load(ks + lane * GD, a.rk + row * GD, GD * 2, &bar[1]);
     }
   }
-  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)b);
+  const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * (size_t)sb);
   if (threadIdx.x == 0) cur_s = cur;
   // An invalid cursor (reported by the sequence's last block) runs as an empty
   // window with every store masked.
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
     ew[c] = expf(s);
   }
   __syncthreads();  // f_t and E
-  if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, b);  // every thread has read the cursor
+  if (threadIdx.x == 0) ticket = cursor_ticket(a.cursors, sb);  // every thread has read the cursor
   // window coefficients cf[n][t] = (f_t * k_t) . vec_n: warp w takes records 16 r + 2 w + i (i < 2)
   for (int base = 0; base < cnt; base += 2 * VW) {  // uniform
     float4 kh[2];
@@ -379,22 +383,23 @@ __global__ void __launch_bounds__(VT, 2) kda_verify_fast_kernel(GdnArgs a) {
   }
   // this head's new k, q, g rows and beta, after every warp is done with the ring rows they may overwrite
   __syncthreads();
-  if (live) append_head(a, b, h, cur_s);
-  if (threadIdx.x == 0) finish_verify_cursor(a.cursors, b, cur_s, ticket, H, L, K, a.status);
+  if (live) append_head(a, b, sb, h, cur_s);
+  if (threadIdx.x == 0) finish_verify_cursor(a.cursors, sb, cur_s, ticket, H, L, K, a.status);
 }
 
 }  // namespace
 
 bool kda_verify_applies(const GdnArgs& a) {
   return a.DK == GD && a.DV == GD && a.K <= KMAX && a.L + a.K <= WMAX && a.H < (1 << 15) && a.H <= 65535 &&
-         a.Bt <= 65535 && !a.slots;
+         a.Bt <= 65535 && a.Sn <= 65535;
 }
 
 size_t kda_verify_fast_smem(int L) { return (size_t)(GD * GD + 2 * KMAX * GD + GD + L * GD + L * ES) * 4 + (size_t)L * GD * 2; }
 
 cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st) {
   if (a.Bt == 0) return cudaSuccess;
-  auto k = out_bf16 ? kda_verify_fast_kernel<true> : kda_verify_fast_kernel<false>;
+  auto k = a.slots ? (out_bf16 ? kda_verify_fast_kernel<true, true> : kda_verify_fast_kernel<false, true>)
+                   : (out_bf16 ? kda_verify_fast_kernel<true, false> : kda_verify_fast_kernel<false, false>);
   const size_t smem = kda_verify_fast_smem(a.L);
   cudaError_t e = prepare(k, smem, true);
   if (e != cudaSuccess) return e;

@@ -282,11 +282,10 @@ class KDAState(GDNState):
 
     def verify(self, rec, o, stream=None, slots=None):
         """rec: q,k [Bt,K,H,dk], v [Bt,K,H,dv] bf16; g [Bt,K,H,dk], beta [Bt,K,H] fp32; o [Bt,K,H,dv]."""
-        if slots is not None:
-            raise ValueError("the KDA verify takes no state slots")
+        desc = self.desc if slots is None else self.slot_desc(slots)
         n_new = _draft_count(rec, "q")
-        self._check_call(rec, o, self.desc, n_new)
-        bd.check(bd.rssm_kda_spec_verify(self.desc, n_new, self.S, self.ring, self.cursors, rec["q"],
+        self._check_call(rec, o, desc, n_new)
+        bd.check(bd.rssm_kda_spec_verify(desc, n_new, self.S, self.ring, self.cursors, rec["q"],
                                          rec["k"], rec["v"], rec["g"], rec["beta"], o, self.status, stream),
                  "rssm_kda_spec_verify")
 

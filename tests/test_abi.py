@@ -238,7 +238,8 @@ def test_kda_host_checks(lib):
     assert lib.rssm_kda_conventional_step(ctypes.byref(ds), *([ALIGNED] * 8), None) == bd.RSSM_ERR_UNSUPPORTED
     d0 = bd.kda_desc(0, 2, 128, 128, 16)
     assert lib.rssm_kda_step(ctypes.byref(d0), None, None, *([None] * 7), None, None) == bd.RSSM_OK
-    # the speculative verify: n_new in [1, L]; K <= 4, L + K <= 32 and dk = dv = 128 on its kernel; no slots
+    # the speculative verify: n_new in [1, L]; K <= 4, L + K <= 32 and dk = dv = 128 on its kernel (with or
+    # without state slots)
     args = (ALIGNED, rb, *([ALIGNED] * 8))
     for n_new in (0, 17, -1):
         assert lib.rssm_kda_spec_verify(ctypes.byref(d), n_new, *args, None, None) == bd.RSSM_ERR_INVALID_ARG
@@ -247,7 +248,8 @@ def test_kda_host_checks(lib):
     assert lib.rssm_kda_spec_verify(ctypes.byref(d30), 3, *args, None, None) == bd.RSSM_ERR_UNSUPPORTED
     d64 = bd.kda_desc(4, 2, 64, 128, 16)
     assert lib.rssm_kda_spec_verify(ctypes.byref(d64), 4, *args, None, None) == bd.RSSM_ERR_UNSUPPORTED
-    assert lib.rssm_kda_spec_verify(ctypes.byref(ds), 4, *args, None, None) == bd.RSSM_ERR_UNSUPPORTED
+    ds64 = bd.kda_desc(4, 2, 64, 128, 16, state_slots=ALIGNED, n_slots=8)
+    assert lib.rssm_kda_spec_verify(ctypes.byref(ds64), 4, *args, None, None) == bd.RSSM_ERR_UNSUPPORTED
     bad = (ALIGNED, rb, *([ALIGNED] * 7), ALIGNED + 4)  # misaligned o
     assert lib.rssm_kda_spec_verify(ctypes.byref(d), 4, *bad, None, None) == bd.RSSM_ERR_MISALIGNED
     assert lib.rssm_kda_spec_verify(ctypes.byref(d0), 4, *([None] * 10), None, None) == bd.RSSM_OK

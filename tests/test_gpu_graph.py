@@ -131,3 +131,45 @@ def test_kda_steps_replay_from_a_graph():
     for fa, fb in ((sa.S, sb.S), (sa.rg, sb.rg), (sa.re, sb.re), (sa.rk, sb.rk), (sa.cursors, sb.cursors)):
         assert torch.equal(fa, fb)
     assert H.status(sa) == 0 and H.status(sb) == 0
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["gdn", "kda"])
+def test_delta_verify_commit_replay_from_a_graph(kda):
+    """Speculative verifies and commits of the delta-rule layers, eager against
+    replayed from a graph, with state slots on the replayed side (a permuted
+    batch: the table is device data, read when the graph runs)."""
+    from recurrent_state_decode_gb300.inputs import KDAWorkload as KW
+    from recurrent_state_decode_gb300.state import GDNState, KDAState, gdn_from_workload, kda_from_workload
+    dev = "cuda"
+    if kda:
+        w = KW("graph_kda_spec", 3, 2, 128, 128, 8, 6, seed=206, drafts=3)
+        make, inputs, cls = kda_from_workload, I.kda_verify_inputs, KDAState
+    else:
+        w = GW("graph_gdn_spec", 3, 2, 128, 128, 8, 6, seed=207, drafts=3)
+        make, inputs, cls = gdn_from_workload, I.gdn_verify_inputs, GDNState
+    recs = [inputs(w, t, dev) for t in range(w.steps)]
+    kepts = [I.accepted_kept(w, t, dev) for t in range(w.steps)]
+    sa = make(w, dev)[0]
+    sb = cls(w.batch, w.nheads, w.dk, w.dv, w.buf_len, dev)
+    perm = torch.tensor([2, 0, 1], dtype=torch.int32, device=dev)  # batch row b uses state row perm[b]
+    fields = ("S", "rq", "rk", "rv", "rg", "rbeta", "re", "cursors")
+    for f in fields:
+        getattr(sb, f)[perm.long()] = getattr(sa, f)
+    oa = [sa.new_verify_output(w.n_new) for _ in range(w.steps)]
+    ob = [sb.new_verify_output(w.n_new) for _ in range(w.steps)]
+    for t in range(w.steps):
+        sa.verify(recs[t], oa[t])
+        sa.commit(kepts[t])
+    torch.cuda.synchronize()
+
+    def spec():
+        for t in range(w.steps):
+            sb.verify(recs[t], ob[t], slots=perm)
+            sb.commit(kepts[t], slots=perm)
+
+    _capture(spec)
+    for t in range(w.steps):
+        assert torch.equal(oa[t], ob[t]), t
+    for f in fields:
+        assert torch.equal(getattr(sb, f)[perm.long()], getattr(sa, f)), f
+    assert H.status(sa) == 0 and H.status(sb) == 0

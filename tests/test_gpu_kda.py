@@ -222,6 +222,42 @@ def test_kda_step_with_slots_matches_the_plain_call():
     assert H.status(sa) == 0 and H.status(ss) == 0
 
 
+def test_kda_verify_commit_with_slots_matches_the_plain_calls():
+    """The verify and commit through a slot table (a permuted batch with
+    padding rows) give the plain calls' outputs, states, rings and cursors bit
+    for bit; padding rows' outputs stay unwritten."""
+    w = KW("kslots_spec", 3, 2, 128, 128, 8, 8, seed=414, drafts=3)
+    dev = "cuda"
+    sa, _, _, _ = kda_from_workload(w, dev)
+    ss = KDAState(7, w.nheads, w.dk, w.dv, w.buf_len, dev)
+    perm, row_of, pad = [5, 0, 3], [2, 4, 1], [0, 3]
+    fields = ("S", "rq", "rk", "rv", "rg", "rbeta", "re", "cursors")
+    for f in fields:
+        getattr(ss, f)[perm] = getattr(sa, f)
+    slots = torch.full((5,), -1, dtype=torch.int32, device=dev)
+    slots[row_of] = torch.tensor(perm, dtype=torch.int32, device=dev)
+    for t in range(w.steps):
+        rec = I.kda_verify_inputs(w, t, dev)
+        kept = I.accepted_kept(w, t, dev)
+        oa = sa.new_verify_output(w.n_new)
+        sa.verify(rec, oa)
+        sa.commit(kept)
+        rows = {k: v[[0] * 5].clone() for k, v in rec.items()}
+        for k, v in rec.items():
+            rows[k][row_of] = v
+        os_ = torch.full((5, w.n_new, w.nheads, w.dv), float("nan"), device=dev)
+        ss.verify(rows, os_, slots=slots)
+        kept_rows = torch.full((5,), 999, dtype=torch.int32, device=dev)
+        kept_rows[row_of] = kept
+        ss.commit(kept_rows, slots=slots)
+        torch.cuda.synchronize()
+        assert torch.equal(os_[row_of], oa), t
+        assert torch.isnan(os_[pad]).all(), t
+    for f in fields:
+        assert torch.equal(getattr(ss, f)[perm], getattr(sa, f)), f
+    assert H.status(sa) == 0 and H.status(ss) == 0
+
+
 # ----------------------------------------------------------------------------- speculative verify
 
 def run_kda_spec(w, out_dtype=bd.RSSM_F32):

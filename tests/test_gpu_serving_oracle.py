@@ -222,19 +222,27 @@ def test_delta_step_with_slots_against_the_oracle(kda):
     assert H.status(ss) == 0
 
 
-def test_gdn_verify_commit_with_slots_against_the_oracle():
-    w = GW("so_gdn_spec", 3, 2, 128, 128, 8, 12, seed=505, drafts=3)
-    sa, pre, starts, counts = gdn_from_workload(w, DEV)
-    ss = GDNState(N_SLOTS, w.nheads, w.dk, w.dv, w.buf_len, DEV)
+@pytest.mark.parametrize("kda", [False, True], ids=["gdn", "kda"])
+def test_delta_verify_commit_with_slots_against_the_oracle(kda):
+    if kda:
+        w = KW("so_kda_spec", 3, 2, 128, 128, 8, 12, seed=506, drafts=3)
+        sa, pre, starts, counts = kda_from_workload(w, DEV)
+        ss = KDAState(N_SLOTS, w.nheads, w.dk, w.dv, w.buf_len, DEV)
+        session, verify_inputs = sessions.kda_spec_session, I.kda_verify_inputs
+    else:
+        w = GW("so_gdn_spec", 3, 2, 128, 128, 8, 12, seed=505, drafts=3)
+        sa, pre, starts, counts = gdn_from_workload(w, DEV)
+        ss = GDNState(N_SLOTS, w.nheads, w.dk, w.dv, w.buf_len, DEV)
+        session, verify_inputs = sessions.gdn_spec_session, I.gdn_verify_inputs
     unused, snap = place(sa, ss, GDN_FIELDS)
     fv, fk = H.Feed(), H.Feed()
-    sess = sessions.gdn_spec_session(H.F64(sa.S), H.sub(pre, slice(None)), starts.cpu().numpy(),
-                                     counts.cpu().numpy(), fv, fk, w.buf_len)
+    sess = session(H.F64(sa.S), H.sub(pre, slice(None)), starts.cpu().numpy(), counts.cpu().numpy(), fv, fk,
+                   w.buf_len)
     del sa
     slots = slot_table()
     folds = 0
     for t in range(w.steps):
-        rec = I.gdn_verify_inputs(w, t, DEV)
+        rec = verify_inputs(w, t, DEV)
         kept = I.accepted_kept(w, t, DEV)
         fv.rec, fk.rec = H.sub(rec, slice(None)), kept.cpu().numpy()
         o = torch.full((ROWS, w.n_new, w.nheads, w.dv), float("nan"), device=DEV)
