@@ -76,7 +76,7 @@ typedef uint16_t rssm_bf16;                /* bfloat16 bit pattern */
 enum {
   RSSM_OK = 0,
   RSSM_ERR_INVALID_ARG = -1, /* null pointer, bad dimension, bad n_new */
-  RSSM_ERR_UNSUPPORTED = -2, /* valid but outside this build's limits */
+  RSSM_ERR_UNSUPPORTED = -2, /* valid but outside the library's limits */
   RSSM_ERR_MISALIGNED = -3,  /* a base pointer is not 16-byte aligned */
   RSSM_ERR_CUDA = -4         /* a CUDA launch failed */
 };
@@ -97,7 +97,7 @@ enum {
  * read copy (RSSM_BF16, RSSM_F16, RSSM_FP8_E4M3). */
 enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2, RSSM_FP8_E4M3 = 3 };
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define RSSM_MAX_BUF_LEN 32 /* L in [1, 32] */
 #define RSSM_MAX_BATCH 65535 /* Mamba-2 batch (RSSM_ERR_UNSUPPORTED above) */
 #define RSSM_MAX_DIM 256    /* headdim, dstate, dk, dv: multiples of 8 in [8, 256] */

@@ -32,7 +32,7 @@ the replay (unrolled) forms follow from them by algebra. Modules:
 * ``kda``     -- the same for Kimi Delta Attention (the gated delta rule with
   a decay per key channel; the pages name the layer and give no equation).
 * ``cursors`` -- integer model of the ring-buffer cursors.
-* ``sessions`` -- drivers that run whole decode sessions (AR and speculative)
+* ``sessions`` -- runners of whole decode sessions (AR and speculative)
   with the conventional recurrence and the cursor model, producing every
   expected output, checkpoint and cursor.
 

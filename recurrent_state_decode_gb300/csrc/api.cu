@@ -142,7 +142,7 @@ const char* rssm_status_string(int code) {
   switch (code) {
     case RSSM_OK: return "ok";
     case RSSM_ERR_INVALID_ARG: return "invalid argument (null pointer, bad dimension or bad count)";
-    case RSSM_ERR_UNSUPPORTED: return "unsupported by this build (size limit)";
+    case RSSM_ERR_UNSUPPORTED: return "unsupported by the library (shape or size limit)";
     case RSSM_ERR_MISALIGNED: return "a base pointer is not 16-byte aligned";
     case RSSM_ERR_CUDA: return "CUDA launch error";
     case RSSM_DEV_BAD_CURSOR: return "device: cursor start/count out of range";

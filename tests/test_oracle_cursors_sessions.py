@@ -1,5 +1,5 @@
 """Pins for the cursor model (hand-derived traces, invariants) and for the
-session drivers (speculative decode with every draft kept equals AR decode;
+session runners (speculative decode with every draft kept equals AR decode;
 with drafts rejected it equals AR decode over the kept prefix)."""
 import numpy as np
 import pytest
