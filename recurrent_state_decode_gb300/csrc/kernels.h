@@ -96,7 +96,7 @@ cudaError_t kda_launch(int kind, const GdnArgs& a, int out_bf16, cudaStream_t st
 // The replay kernels' shapes: dk = dv = 128 (the step also L <= 31).
 bool kda_window_applies(const GdnArgs& a);
 bool kda_step_fast_applies(const GdnArgs& a);
-// Speculative verify (kda_verify_fast.cu: dk = dv = 128, K <= 4, L + K <= 32, no state slots); the
+// Speculative verify (kda_verify_fast.cu: dk = dv = 128, K <= 4, L + K <= 32, state slots honoured); the
 // sequence's last block appends the shared fields and marks the cursor, so a verify is one kernel.
 bool kda_verify_applies(const GdnArgs& a);
 cudaError_t kda_verify_launch(const GdnArgs& a, int out_bf16, cudaStream_t st);
