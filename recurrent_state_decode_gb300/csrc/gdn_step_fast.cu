@@ -18,9 +18,9 @@
 // 8w..8w+7 and 32+8w..32+8w+7, lane l the float4 column chunk 4l..4l+3. Every
 // load is issued at launch, none waiting on the cursor: the 64 rows by one bulk
 // copy (TMA, non-tensor; never multicast) into shared memory; lane s ring slot
-// s (g); the current record. Once the cursor is known thread 0 also copies the
-// window records' e rows of this block (one 256-byte bulk copy each, on a
-// second mbarrier), so that only the window's corrections are read. Warp w forms the dots
+// s (g); the current record. Once the cursor is known the block's threads also
+// copy the window records' e rows of this block (16-byte asynchronous copies,
+// spread over the threads), so that only the window's corrections are read. Warp w forms the dots
 // k_s . k and k_s . q of ring slots w, w+4, ... (slot L: the current k), one
 // transposed reduction, shared through shared memory. After the cursor, lane t
 // takes record t by a shuffle and one suffix scan gives every D(m-1, t). Per
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   float* tile = dsm;               // the block's 64 rows
   float* es = dsm + FPB * GD;      // e of window record t at es + t * ES (the block's rows)
   __shared__ float skk[FW * KW], skq[FW * KW];  // k_s . k, k_s . q by ring slot; [L] = current
-  __shared__ uint64_t bar[2];      // [0] the rows, [1] the window's e
+  __shared__ uint64_t bar;         // the rows
   __shared__ int4 cur_s;           // the cursor as read, for the sequence's last block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = a.L, H = a.H;
@@ -69,11 +69,10 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
   const size_t tbase = (sh * GD + p0) * GD;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar[0], FPB * GD * 4);
-    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
+    mbar_arrive_expect_tx(&bar, FPB * GD * 4);
+    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
@@ -111,13 +110,15 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
       kq_cur = warp_sum(dot4(bf4_to_f4(kraw), bf4_to_f4(qraw)));
     }
   }
-  if (threadIdx.x == 0) {  // the window's e rows of this block, in record order
-    mbar_arrive_expect_tx(&bar[1], (uint32_t)count * FPB * 4);
-    for (int t = 0; t < count; t++) {
-      const int s = start + t < L ? start + t : start + t - L;
-      bulk_load(es + t * ES, a.re + (sh * L + s) * GD + p0, FPB * 4, &bar[1]);
-    }
+  // the window's e rows of this block, in record order: 16-byte asynchronous copies spread over the threads
+  for (int c = threadIdx.x; c < count * (FPB / 4); c += FT) {
+    const int t = c / (FPB / 4), j = c - t * (FPB / 4);
+    const int s = start + t < L ? start + t : start + t - L;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(es + t * ES + 4 * j)),
+                 "l"(a.re + (sh * L + s) * GD + p0 + 4 * j)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   const bool flush = valid && m == L;
   const int scur = start + count < L ? start + count : start + count - L;  // the current record's slot
   // window, lane t = record t
@@ -164,11 +165,11 @@ __global__ void __launch_bounds__(FT, 6) gdn_step_fast_kernel(GdnArgs a) {
       }
     }
   }
-  const bool ok0 = mbar_wait(&bar[0], 0), ok1 = mbar_wait(&bar[1], 0);
-  if (!__all_sync(FULL, ok0 && ok1)) {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();  // every thread's e chunks
+  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
-    mbar_wait(&bar[0], 0);
-    mbar_wait(&bar[1], 0);
+    mbar_wait(&bar, 0);
     if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, cur_s, ticket, a.H * 2, L, a.status);
     return;
   }
