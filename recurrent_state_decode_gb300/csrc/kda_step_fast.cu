@@ -19,8 +19,8 @@
 // the column chunk 4l..4l+3. At launch: the 64 rows by one bulk copy (TMA,
 // non-tensor; never multicast) into shared memory, the current record, and
 // the ring keys of the slots whose dots the warp forms. As soon as the cursor
-// arrives, warp 0's lane t copies window record t's e rows of this block and
-// its g row (bulk copies on a second mbarrier); thread c then
+// arrives, the block's threads copy the window records' e rows of this block
+// and their g rows (16-byte asynchronous copies spread over the threads); thread c then
 // runs the suffix sums of channel c backwards over the window, leaving f_t in
 // place of g_t, and Gamma. Warp w forms (f_s * k_s) . k and (f_s * k_s) . q
 // for ring slots w, w+4, ... (slot L: the current k), one transposed
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   float* fd = es + (L - 1) * ES;     // g, then f, of window record t at fd + t * GD (all channels)
   __shared__ float skk[FW * KW], skq[FW * KW];  // (f_s * k_s) . k and . q by ring slot; [L] = current
   __shared__ __align__(16) float gam[GD];       // Gamma by channel
-  __shared__ uint64_t bar[2];                   // [0] the rows, [1] the window's e and g rows
+  __shared__ uint64_t bar;                      // the rows
   __shared__ int4 cur_s;                        // the cursor as read, for the sequence's last block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pb = blockIdx.x, b = blockIdx.z;
@@ -70,26 +70,26 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
   const size_t tbase = (sh * GD + p0) * GD;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar[0], FPB * GD * 4);
-    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar[0]);
+    mbar_arrive_expect_tx(&bar, FPB * GD * 4);
+    bulk_load(tile, a.S + tbase, FPB * GD * 4, &bar);
   }
   const int4 cur = *reinterpret_cast<const int4*>(a.cursors + 4 * sb);
   // An invalid cursor (reported by the sequence's last block) runs as an empty
   // window with every store masked, so that no thread leaves before a barrier.
   const bool valid = cur.x >= 0 && cur.x < L && cur.y >= 0 && cur.y < L && cur.z == 0;
   const int start = valid ? cur.x : 0, count = valid ? cur.y : 0;
-  if (warp == 0) {  // the window's e rows (this block's) and g rows, in record order, as soon as the cursor is known
-    if (lane == 0) mbar_arrive_expect_tx(&bar[1], (uint32_t)count * (FPB + GD) * 4);
-    __syncwarp();
-    if (lane < count) {
-      const size_t row = sh * L + wrap(start + lane, L);
-      bulk_load(es + lane * ES, a.re + row * GD + p0, FPB * 4, &bar[1]);
-      bulk_load(fd + lane * GD, a.rg + row * GD, GD * 4, &bar[1]);
-    }
+  // the window's e rows (this block's) and g rows, in record order, as soon as the cursor is known: 16-byte
+  // asynchronous copies spread over the threads
+  for (int c = threadIdx.x; c < count * ((FPB + GD) / 4); c += FT) {
+    const int t = c / ((FPB + GD) / 4), j = c - t * ((FPB + GD) / 4);
+    const size_t row = sh * L + wrap(start + t, L);
+    float* dst = j < FPB / 4 ? es + t * ES + 4 * j : fd + t * GD + 4 * (j - FPB / 4);
+    const float* src = j < FPB / 4 ? a.re + row * GD + p0 + 4 * j : a.rg + row * GD + 4 * (j - FPB / 4);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   const int rl0 = warp * 8, rl1 = HALF + warp * 8;  // the warp's row groups (within the block)
   // the current record; thread c holds channel c of its log decay
   const uint2 kraw = *reinterpret_cast<const uint2*>(a.k + bh * GD + lane * 4);
@@ -105,19 +105,14 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
     kr[j] = s < L ? *reinterpret_cast<const uint2*>(a.rk + (sh * L + s) * GD + lane * 4) : make_uint2(0, 0);
   }
   int ticket = 0;
-  __syncthreads();  // the barriers' initialisation is visible; every thread has read the cursor
-  // a copy that did not land leaves the window empty (reported, stores masked)
-  const bool landed = __syncthreads_and(mbar_wait(&bar[1], 0));
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();  // the barrier's initialisation is visible; every thread has read the cursor; the window's rows
   if (threadIdx.x == 0) {
     ticket = cursor_ticket(a.cursors, sb);
     cur_s = cur;
-    if (!landed) {
-      report(a.status, RSSM_DEV_TIMEOUT);
-      mbar_wait(&bar[1], 0);  // the copies land before the block can leave
-    }
   }
-  const int cnt = landed ? count : 0;
-  const bool live = valid && landed;
+  const int cnt = count;
+  const bool live = valid;
   const int m = cnt + 1;
   const bool flush = live && m == L;
   const int scur = wrap(start + count, L);  // the current record's slot
@@ -185,9 +180,9 @@ __global__ void __launch_bounds__(FT, 5) kda_step_fast_kernel(GdnArgs a) {
       }
     }
   }
-  if (!__all_sync(FULL, mbar_wait(&bar[0], 0))) {
+  if (!__all_sync(FULL, mbar_wait(&bar, 0))) {
     if (lane == 0) report(a.status, RSSM_DEV_TIMEOUT);
-    mbar_wait(&bar[0], 0);
+    mbar_wait(&bar, 0);
     if (threadIdx.x == 0) finish_ar_cursor(a.cursors, sb, cur_s, ticket, a.H * 2, L, a.status);
     return;
   }
